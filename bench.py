@@ -1,0 +1,465 @@
+"""Benchmark: GPT pre-LN layer forward + backward on GB300.
+
+Default workload: one layer of the 96-layer GPT (b1 s4096 h8192, 64 heads of
+128, ffn 32768) run as 8 tensor-parallel partitions on one GPU.  One step =
+mc_layer_forward + mc_layer_backward over one batch (every kernel of the hot
+path).  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload c1|c2|c3|c4|c4shard|c5] [--stage NAME]
+
+--impl reference times the fp64 CPU oracle on this host's cores, on a bounded
+sample of the same workload (a prefix of the sequence), with the same metric.
+--stage NAME times one kernel alone (for profiling); its line is a
+per-kernel measurement, not the step metric.
+Under torchrun each rank runs an independent replica (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "layer fwd+bwd tokens/s; BF16 TFLOP/s as % of GB300 dense tensor peak"
+NOMINAL_BF16_TFLOPS = 2250.0
+
+WORKLOADS = {
+    "c1": dict(micro_batch=1, seq_len=128, hidden=768, heads=12, ffn_hidden=3072, tp_parts=2, head_dim=0),
+    "c2": dict(micro_batch=4, seq_len=512, hidden=768, heads=12, ffn_hidden=3072, tp_parts=2, head_dim=0),
+    "c3": dict(micro_batch=8, seq_len=1024, hidden=2048, heads=16, ffn_hidden=8192, tp_parts=4, head_dim=0),
+    "c4": dict(micro_batch=1, seq_len=4096, hidden=8192, heads=64, ffn_hidden=32768, tp_parts=8, head_dim=0),
+    "c4shard": dict(micro_batch=1, seq_len=4096, hidden=8192, heads=8, ffn_hidden=4096, tp_parts=1, head_dim=128),
+    "c5": dict(micro_batch=1, seq_len=32768, hidden=4096, heads=32, ffn_hidden=16384, tp_parts=1, head_dim=0),
+}
+WORKLOAD_NAMES = {
+    "c1": "gpt-layer b1 s128 h768 H12 d64 f3072 tp2",
+    "c2": "gpt-layer b4 s512 h768 H12 d64 f3072 tp2",
+    "c3": "gpt-layer b8 s1024 h2048 H16 d128 f8192 tp4",
+    "c4": "gpt-layer b1 s4096 h8192 H64 d128 f32768 tp8 (one layer of the 96-layer GPT)",
+    "c4shard": "gpt-layer shard b1 s4096 h8192 H8 d128 a1024 f4096 tp1 (one TP=8 rank alone)",
+    "c5": "gpt-layer b1 s32768 h4096 H32 d128 f16384 tp1 (long sequence)",
+}
+
+# Kernels launched per step by mc_layer_forward + mc_layer_backward:
+# forward 7 (LN, QKV, attention, out-proj, LN, fc1, fc2); backward 21
+# (colsum x2 launches x3 sums, LN-backward x2 launches x2, 6 GEMMs,
+# attention backward 3).
+LAUNCHES_PER_STEP = 7 + 21
+
+
+def dims(w):
+    d = w["head_dim"] or w["hidden"] // w["heads"]
+    return dict(b=w["micro_batch"], s=w["seq_len"], T=w["micro_batch"] * w["seq_len"],
+                h=w["hidden"], H=w["heads"], d=d, a=w["heads"] * d, f=w["ffn_hidden"],
+                t=w["tp_parts"])
+
+
+def layer_flops(w) -> float:
+    """Algorithmic fwd+bwd flops: 3 x [2T(3ha + ah + 2hf) + 2 a b s (s+1)]."""
+    D = dims(w)
+    fwd = 2 * D["T"] * (3 * D["h"] * D["a"] + D["a"] * D["h"] + 2 * D["h"] * D["f"]) \
+        + 2 * D["a"] * D["b"] * D["s"] * (D["s"] + 1)
+    return 3.0 * fwd
+
+
+def measured_peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except Exception:
+        return {}
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- helpers
+def make_inputs(w, seed=0):
+    from layer_inputs import LayerShape, make_layer_inputs
+    shape = LayerShape(**w)
+    return make_layer_inputs(shape, seed=seed)
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- oracle timing
+def prepare_oracle(w, prefix_tokens: int):
+    """Inputs of a bounded sample of the workload for the fp64 oracle: the
+    first `prefix_tokens` tokens of the sequence (micro-batch 1), full
+    weights."""
+    from layer_inputs import LayerShape, make_layer_inputs
+
+    sample = dict(w)
+    sample["micro_batch"] = 1
+    sample["seq_len"] = min(prefix_tokens, w["seq_len"])
+    shape = LayerShape(**sample)
+    inp = make_layer_inputs(shape, seed=0)
+    return shape, inp.params_f64(), inp.f64("x"), inp.f64("dy")
+
+
+def oracle_step(prepared) -> float:
+    """One fp64 oracle forward + backward; returns its wall time in seconds."""
+    import oracle.layer as O
+
+    shape, P, x, dy = prepared
+    t0 = time.perf_counter()
+    O.layer_forward_backward(shape, P, x, dy)
+    return time.perf_counter() - t0
+
+
+def oracle_threads() -> int:
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS"):
+        if os.environ.get(var):
+            return int(os.environ[var])
+    return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------- arms
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    w = WORKLOADS[args.workload]
+    prepared = prepare_oracle(w, args.ref_prefix)
+    toks = prepared[0].seq_len
+    for _ in range(args.warmup):
+        oracle_step(prepared)
+    per = [oracle_step(prepared) for _ in range(args.steps)]
+    sec = sum(per) / len(per)
+    value = toks / sec
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD_NAMES[args.workload], **w},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle_threads(),
+                         "kind": "oracle",
+                         "sample": f"first {toks} tokens of the sequence (micro-batch 1), full "
+                                   f"weights, fp64 forward+backward per step"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_stage(args, w, device):
+    """Times one GEMM of the step alone (the fc1 forward product by default)."""
+    import torch
+
+    from megatron_transformer_layer_gb300 import _lib as L
+    D = dims(w)
+    T, h, f = D["T"], D["h"], D["f"]
+    g = torch.Generator(device=device).manual_seed(0)
+    A = torch.randn(T, h, device=device, generator=g).to(torch.bfloat16)
+    B = (torch.randn(f, h, device=device, generator=g) * 0.02).to(torch.bfloat16)
+    bias = torch.zeros(f, device=device, dtype=torch.bfloat16)
+    out = torch.empty(T, f, device=device, dtype=torch.bfloat16)
+    hp = torch.empty(T, f, device=device, dtype=torch.bfloat16)
+    st = torch.cuda.current_stream(device)
+
+    def launch():
+        rc = L.mc_gemm(T, f, h, A, h, 0, B, h, 0, out, f, L.MC_EPI_BIAS_GELU, bias=bias, aux=hp,
+                       ldaux=f, stream=st)
+        assert rc == 0, L.mc_strerror(rc)
+
+    for _ in range(args.warmup):
+        launch()
+    torch.cuda.synchronize(device)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
+    for i in range(args.steps):
+        ev[2 * i].record(st)
+        launch()
+        ev[2 * i + 1].record(st)
+    torch.cuda.synchronize(device)
+    ms = [ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(args.steps)]
+    flops = 2.0 * T * h * f
+    avg = sum(ms) / len(ms)
+    print(json.dumps({"stage": "gemm fc1 forward (bias+GeLU epilogue)", "M": T, "N": f, "K": h,
+                      "ms": avg, "tflops": flops / avg / 1e9}), flush=True)
+
+
+def run_ours(args, world, rank, local):
+    import numpy as np
+    import torch
+
+    from megatron_transformer_layer_gb300 import _lib as L
+    from megatron_transformer_layer_gb300.layer import TransformerLayer, bf16_tensor
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU for --impl ours")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    w = WORKLOADS[args.workload]
+    if args.stage:
+        run_stage(args, w, device)
+        return
+    D = dims(w)
+    inp = make_inputs(w)
+    params = {k: bf16_tensor(v, device) for k, v in inp.params.items()}
+    layer = TransformerLayer(**w, params=params, device=device)
+    x = torch.from_numpy(inp.f64("x").reshape(-1, D["h"]).astype(np.float32)).to(device)
+    dy = torch.from_numpy(inp.f64("dy").reshape(-1, D["h"]).astype(np.float32)).to(device)
+    y = torch.empty_like(x)
+    dx = torch.empty_like(x)
+    st = torch.cuda.current_stream(device)
+
+    def step():
+        layer.forward(x, y)
+        layer.backward(dy, dx)
+
+    for _ in range(max(args.warmup, 1)):
+        step()
+    torch.cuda.synchronize(device)
+    status = layer.device_status()
+    if status != 0:
+        raise SystemExit(f"device status {status}: {L.mc_strerror(status)}")
+
+    # ---- device-resident timing (inputs already in HBM)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    step_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    barrier(world)
+    torch.cuda.synchronize(device)
+    with ClockSampler(device.index if device.index is not None else 0) as clk:
+        e0.record(st)
+        step_ev[0].record(st)
+        for i in range(args.steps):
+            step()
+            step_ev[i + 1].record(st)
+        e1.record(st)
+        torch.cuda.synchronize(device)
+    barrier(world)
+    ms_total = e0.elapsed_time(e1)
+    per_step = [step_ev[i].elapsed_time(step_ev[i + 1]) for i in range(args.steps)]
+    ms_total = max_over_ranks(ms_total, world, device)
+    ms_step = ms_total / args.steps
+    tokens = D["T"]
+    value = world * tokens * args.steps / (ms_total / 1e3)
+    flops = layer_flops(w)
+    tflops = flops / (ms_step / 1e3) / 1e12
+    peaks = measured_peaks()
+    peak = peaks.get("bf16_tflops_sustained") or 1710.0
+    peak_burst = peaks.get("bf16_tflops") or 1900.0
+
+    # ---- end to end through the public API with host buffers
+    x_h = x.cpu().pin_memory()
+    dy_h = dy.cpu().pin_memory()
+    y_h = torch.empty_like(x_h).pin_memory()
+    dx_h = torch.empty_like(x_h).pin_memory()
+    x_d = torch.empty_like(x)
+    dy_d = torch.empty_like(dy)
+
+    def e2e_step():
+        x_d.copy_(x_h, non_blocking=True)
+        dy_d.copy_(dy_h, non_blocking=True)
+        layer.forward(x_d, y)
+        layer.backward(dy_d, dx, x=x_d)
+        y_h.copy_(y, non_blocking=True)
+        dx_h.copy_(dx, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(device)
+    barrier(world)
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record(st)
+    for _ in range(args.steps):
+        e2e_step()
+    a1.record(st)
+    torch.cuda.synchronize(device)
+    e2e_ms = max_over_ranks(a0.elapsed_time(a1), world, device)
+    e2e_value = world * tokens * args.steps / (e2e_ms / 1e3)
+    h2d = 2 * x.numel() * 4
+    d2h = 2 * x.numel() * 4
+
+    # ---- dominant kernel: the tcgen05 GEMM, fc1 forward product, timed alone
+    Dg = D
+    g_args = argparse.Namespace(steps=max(5, min(args.steps, 20)), warmup=2)
+    gemm = time_gemm_fc1(Dg, device, g_args, layer, params)
+    gemm_flops = 2.0 * Dg["T"] * Dg["h"] * Dg["f"]
+    achieved = gemm_flops / (gemm / 1e3) / 1e12
+    roofline = {"bound": "tensor", "kernel": "gemm_tcgen05 fc1 forward (bias+GeLU epilogue)",
+                "achieved": achieved, "peak": peak_burst, "unit": "TFLOP/s",
+                "frac": achieved / peak_burst, "peak_kind": "bf16 burst, of measured",
+                "flops_per_launch": gemm_flops, "ms_per_launch": gemm,
+                "traffic": TRAFFIC.get(args.workload)}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "ms_per_step_p50": statistics.median(per_step),
+        "ms_per_step_p95": sorted(per_step)[max(0, int(round(0.95 * len(per_step))) - 1)],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD_NAMES[args.workload], **w,
+                   "l2": "inputs larger than L2 (1.6 GB of bf16 weights plus activations read per step)"
+                   if args.workload == "c4" else "working set vs L2 not checked",
+                   "parallelism": f"tp{w['tp_parts']} virtual partitions on one GPU; "
+                                  f"{'replicas' if world > 1 else 'single GPU'}"},
+        "tflops": tflops,
+        "pct_of_peak": {"measured_sustained": tflops / peak, "nominal": tflops / NOMINAL_BF16_TFLOPS},
+        "clocks": clk.summary(),
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+        "roofline": roofline,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        prepared = prepare_oracle(w, args.ref_prefix)
+        toks = prepared[0].seq_len
+        sec = oracle_step(prepared)
+        line["cpu_baseline"] = {"value": toks / sec, "unit": "tokens/s", "cores": oracle_threads(),
+                                "kind": "oracle",
+                                "sample": f"first {toks} tokens of the sequence (micro-batch 1), "
+                                          f"full weights, one fp64 forward+backward"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# dram bytes read + written per launch of the timed GEMM, from an ncu capture
+# (None until captured for the current kernel build).
+TRAFFIC = {}
+
+
+def time_gemm_fc1(D, device, args, layer, params) -> float:
+    """Average duration (ms) of the fc1 forward GEMM launch, CUDA events on
+    the launching stream, inputs resident (layer's saved LN2 output)."""
+    import torch
+
+    from megatron_transformer_layer_gb300 import _lib as L
+    T, h, f = D["T"], D["h"], D["f"]
+    ln2 = torch.empty(T, h, device=device, dtype=torch.bfloat16).normal_()
+    out = torch.empty(T, f, device=device, dtype=torch.bfloat16)
+    hp = torch.empty(T, f, device=device, dtype=torch.bfloat16)
+    st = torch.cuda.current_stream(device)
+
+    def launch():
+        rc = L.mc_gemm(T, f, h, ln2, h, 0, params["w_fc1"], h, 0, out, f, L.MC_EPI_BIAS_GELU,
+                       bias=params["b_fc1"], aux=hp, ldaux=f, stream=st)
+        assert rc == 0, L.mc_strerror(rc)
+
+    for _ in range(args.warmup):
+        launch()
+    torch.cuda.synchronize(device)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
+    for i in range(args.steps):
+        ev[2 * i].record(st)
+        launch()
+        ev[2 * i + 1].record(st)
+    torch.cuda.synchronize(device)
+    ms = [ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(args.steps)]
+    del ln2, out, hp
+    return sum(ms) / len(ms)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="c4")
+    ap.add_argument("--stage", choices=["gemm_fc1"], default=None)
+    ap.add_argument("--ref-prefix", type=int, default=64,
+                    help="tokens of the sequence the CPU oracle processes per sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and not args.stage and args.impl == "ours":
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

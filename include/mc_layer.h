@@ -1,0 +1,217 @@
+/*
+ * mc_layer.h -- C ABI of a GB300 (sm_103a) library that runs one GPT pre-LN
+ * transformer layer, forward and backward, in BF16 with FP32 accumulation.
+ *
+ * What is computed
+ * ----------------
+ *   x1 = x + OutProj(CausalAttention(LN1(x)))        (attention sub-block)
+ *   y  = x1 + FC2(GeLU_tanh(FC1(LN2(x1))))            (MLP sub-block)
+ * and, for an upstream gradient dy, dx and the gradients of all twelve
+ * parameters.  LayerNorm uses the biased variance and eps = 1e-5; attention is
+ * softmax(q k^T / sqrt(d)) v with key j visible to query i iff j <= i; no
+ * dropout.
+ *
+ * Tensor-parallel split (Megatron tutorial cf-1.com/news/5344657, section 2.2
+ * "张量并行：把一个大矩阵劈开"): the QKV projection is split across tp_parts
+ * partitions by heads, the first MLP linear by columns and the second by
+ * rows, so the out-projection and fc2 each produce one partial product per
+ * partition that has to be summed (on a TP group of GPUs, an all-reduce).
+ * Here the partitions are virtual and live on one GPU: each partition's
+ * K-slice of a row-parallel GEMM accumulates into the same FP32 tensor-memory
+ * accumulator, in partition order, and the epilogue adds the bias once after
+ * the sum plus the residual.  The backward pass sums the column-parallel
+ * input gradients (QKV and fc1 dgrad) the same way.
+ * Divisibility (ai.lansai.wang/82226.html, section 并行度先做整数校验; tutorial
+ * section 2.2): hidden, heads and ffn_hidden must divide by tp_parts.
+ *
+ * Layouts (all row-major, all pointers are device pointers unless stated)
+ * -------------------------------------------------------------------------
+ *   T = micro_batch * seq_len tokens, h = hidden, H = heads,
+ *   d = head_dim (0 => h / H), a = H * d, f = ffn_hidden.
+ *   x, y, dy, dx      float32 [T, h]  (token-major; token = b * seq_len + s)
+ *   Weights (bf16 bit patterns, nn.Linear layout out x in, y = x W^T + b):
+ *     w_qkv [3a, h] = [Wq; Wk; Wv], each block head-major (head k owns rows
+ *     [k d, (k+1) d) of its block); b_qkv [3a]; w_o [h, a]; b_o [h];
+ *     w_fc1 [f, h]; b_fc1 [f]; w_fc2 [h, f]; b_fc2 [h];
+ *     ln{1,2}_g, ln{1,2}_b [h].
+ *   Gradients: float32, same shapes as the weights.
+ *
+ * Ownership and ordering
+ * ----------------------
+ *   All memory is owned by the caller.  The library never allocates, frees or
+ *   synchronises (except mc_layer_device_status, which synchronises `stream`).
+ *   Every call enqueues kernels on `stream` (a cudaStream_t; NULL = legacy
+ *   default stream) and returns without waiting.  `saved` is written by
+ *   mc_layer_forward and read by mc_layer_backward; `x` and `saved` must not
+ *   change in between.  `ws` is scratch; concurrent calls need distinct
+ *   `saved`/`ws` buffers.  All pointers must be 16-byte aligned; `saved` and
+ *   `ws` 256-byte aligned.
+ *
+ * Errors
+ * ------
+ *   Every entry point returns MC_OK (0) or a negative code.  Shape, pointer,
+ *   alignment and workspace-size errors are detected on the host before any
+ *   launch and nothing is enqueued.  MC_ERR_CUDA reports a launch error.
+ *   Device-side errors (a bounded wait that ran out, an out-of-range index
+ *   caught by a kernel's own check) are recorded in a status word inside `ws`
+ *   and read with mc_layer_device_status.
+ */
+#ifndef MC_LAYER_H_
+#define MC_LAYER_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ---------------------------------------------------- */
+#define MC_OK 0
+#define MC_ERR_SHAPE (-1)          /* a field <= 0, or a divisibility rule broken  */
+#define MC_ERR_UNSUPPORTED (-2)    /* legal shape this build does not run          */
+#define MC_ERR_NULLPTR (-3)        /* a required pointer is NULL                   */
+#define MC_ERR_ALIGN (-4)          /* a pointer is not aligned as documented       */
+#define MC_ERR_WORKSPACE (-5)      /* ws_bytes smaller than mc_layer_workspace_bytes */
+#define MC_ERR_CUDA (-6)           /* a CUDA runtime call or launch failed         */
+#define MC_ERR_DEVICE_TIMEOUT (-7) /* device: a bounded wait gave up               */
+#define MC_ERR_DEVICE_BOUNDS (-8)  /* device: an index check failed                */
+#define MC_ERR_ARGUMENT (-9)       /* another invalid argument (e.g. an enum)      */
+
+/* shape flags */
+#define MC_ACCUMULATE_GRADS 1u /* backward adds into the gradient buffers (+=)    */
+
+typedef struct mc_layer_shape {
+  int32_t micro_batch; /* b  (--micro-batch-size)               */
+  int32_t seq_len;     /* s  (--seq-length), any value >= 1      */
+  int32_t hidden;      /* h  (--hidden-size)                     */
+  int32_t heads;       /* H  (--num-attention-heads)             */
+  int32_t ffn_hidden;  /* f  (--ffn-hidden-size)                 */
+  int32_t tp_parts;    /* t  (--tensor-model-parallel-size)      */
+  int32_t head_dim;    /* 0 => hidden / heads; > 0 decouples a = heads * head_dim
+                          from hidden (one tensor-parallel rank's shard run alone) */
+  uint32_t flags;      /* MC_ACCUMULATE_GRADS or 0               */
+} mc_layer_shape;
+
+/* bf16 parameters (uint16_t bit patterns), device pointers. */
+typedef struct mc_layer_weights {
+  const uint16_t *ln1_g, *ln1_b, *w_qkv, *b_qkv, *w_o, *b_o;
+  const uint16_t *ln2_g, *ln2_b, *w_fc1, *b_fc1, *w_fc2, *b_fc2;
+} mc_layer_weights;
+
+/* fp32 parameter gradients, device pointers. */
+typedef struct mc_layer_grads {
+  float *ln1_g, *ln1_b, *w_qkv, *b_qkv, *w_o, *b_o;
+  float *ln2_g, *ln2_b, *w_fc1, *b_fc1, *w_fc2, *b_fc2;
+} mc_layer_grads;
+
+/* Returns MC_OK when the shape is legal and runnable, MC_ERR_SHAPE when a
+ * field is <= 0 or hidden/heads/ffn_hidden do not divide by tp_parts (or
+ * hidden by heads when head_dim = 0), MC_ERR_UNSUPPORTED when head_dim is not
+ * 64 or 128, or hidden, a / tp_parts or ffn_hidden / tp_parts is not a
+ * multiple of 64.  Pure host function; needs no GPU. */
+int mc_layer_check_shape(const mc_layer_shape* shape);
+
+/* Bytes of the `saved` buffer (activations kept from forward to backward):
+ * LN1/LN2 outputs and statistics, Q|K|V, attention output and log-sum-exp,
+ * x1, fc1 pre-activation and GeLU output.  0 for an illegal shape. */
+size_t mc_layer_saved_bytes(const mc_layer_shape* shape);
+
+/* Bytes of the `ws` scratch buffer, including the 256-byte device status
+ * block at its start.  0 for an illegal shape. */
+size_t mc_layer_workspace_bytes(const mc_layer_shape* shape);
+
+/* Forward pass.  x [T, h] fp32 in, y [T, h] fp32 out; fills `saved`.
+ * Clears the device status word in `ws` first. */
+int mc_layer_forward(const mc_layer_shape* shape, const mc_layer_weights* w, const float* x,
+                     float* y, void* saved, void* ws, size_t ws_bytes, void* stream);
+
+/* Backward pass.  dy [T, h] fp32 in; dx [T, h] fp32 out; parameter
+ * gradients written (or accumulated with MC_ACCUMULATE_GRADS) into `grads`.
+ * Reads `saved` from the matching forward call.  dx may alias dy. */
+int mc_layer_backward(const mc_layer_shape* shape, const mc_layer_weights* w, const float* x,
+                      const float* dy, const void* saved, float* dx, const mc_layer_grads* grads,
+                      void* ws, size_t ws_bytes, void* stream);
+
+/* Synchronises `stream` and returns the device status recorded in `ws` by
+ * the kernels since the last forward call: MC_OK, MC_ERR_DEVICE_TIMEOUT or
+ * MC_ERR_DEVICE_BOUNDS (or MC_ERR_CUDA if the synchronisation fails). */
+int mc_layer_device_status(const void* ws, void* stream);
+
+/* Static, human-readable text for a status code. */
+const char* mc_strerror(int code);
+
+/* ---- stage entry points ---------------------------------------------------
+ * The same kernels the layer calls use, exposed one stage at a time so each
+ * can be checked alone.  `status` is a device int[64] (256 bytes) that the
+ * kernels record device-side errors into; it may be NULL. */
+
+/* LayerNorm forward over rows of x [rows, h] fp32: out = (x - mean) * rstd *
+ * gamma + beta as bf16 [rows, h]; mean and rstd fp32 [rows] (may be NULL).
+ * Biased variance, eps = 1e-5.  h must be a multiple of 8 and <= 16384. */
+int mc_layernorm_forward(const float* x, const uint16_t* gamma, const uint16_t* beta,
+                         uint16_t* out, float* mean, float* rstd, int64_t rows, int32_t h,
+                         int* status, void* stream);
+
+/* LayerNorm backward: dx = resid + rstd * (g - mean(g) - xhat * mean(g * xhat))
+ * with g = dout * gamma and xhat = (x - mean) * rstd; dx fp32 [rows, h]
+ * (resid may be NULL, dx may alias resid).  If dx_bf16 is not NULL, a bf16
+ * copy of dx is written too.  Column sums over rows of dout * xhat, dout and
+ * (if colsum_dx is not NULL) dx are written to dgamma, dbeta, colsum_dx
+ * (fp32 [h]; added to their contents when `accumulate` is non-zero).
+ * `partials` is fp32 scratch of mc_layernorm_backward_scratch_floats(rows, h)
+ * floats. */
+int mc_layernorm_backward(const float* dout, const float* x, const float* mean, const float* rstd,
+                          const uint16_t* gamma, const float* resid, float* dx, uint16_t* dx_bf16,
+                          float* dgamma, float* dbeta, float* colsum_dx, int accumulate,
+                          float* partials, int64_t rows, int32_t h, int* status, void* stream);
+size_t mc_layernorm_backward_scratch_floats(int64_t rows, int32_t h);
+
+/* GEMM on the tcgen05 tensor cores: C[M, N] = sum_k A[m, k] B[n, k] (fp32
+ * accumulation), then an epilogue.
+ *   a_layout 0: A stored [M, K] (row stride lda); 1: A stored [K, M] (lda).
+ *   b_layout 0: B stored [N, K] (row stride ldb); 1: B stored [K, N] (ldb).
+ * Epilogues (out row stride ldc, aux row stride ldaux):
+ *   MC_EPI_STORE_F32        out fp32  = acc (+ out if accumulate)
+ *   MC_EPI_STORE_BF16       out bf16  = acc
+ *   MC_EPI_BIAS_BF16        out bf16  = acc + bias[n]
+ *   MC_EPI_BIAS_GELU        aux bf16  = acc + bias[n];  out bf16 = gelu_tanh(acc + bias[n])
+ *   MC_EPI_BIAS_RESID_F32   out fp32  = acc + bias[n] + resid[m, n] (resid fp32, ldaux)
+ *   MC_EPI_GELU_BWD         out bf16  = acc * gelu_tanh'(aux[m, n]) (aux bf16)
+ * `k_parts` > 1 marks the K range as k_parts equal partitions (a row-parallel
+ * product); they are summed in the accumulator in partition order.
+ * Requirements: M >= 1, N and K multiples of 64 (K >= 64 unless a_layout = 1,
+ * where K is the token count and may be any value >= 1), 16-byte aligned
+ * pointers and leading dimensions that are multiples of 8 elements. */
+#define MC_EPI_STORE_F32 0
+#define MC_EPI_STORE_BF16 1
+#define MC_EPI_BIAS_BF16 2
+#define MC_EPI_BIAS_GELU 3
+#define MC_EPI_BIAS_RESID_F32 4
+#define MC_EPI_GELU_BWD 5
+int mc_gemm(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda, int a_layout,
+            const uint16_t* B, int64_t ldb, int b_layout, void* out, int64_t ldc, int epilogue,
+            const uint16_t* bias, const void* aux, int64_t ldaux, int accumulate, int k_parts,
+            int* status, void* stream);
+
+/* Causal flash attention forward over a packed Q|K|V tensor qkv [T, 3a] bf16
+ * (token-major; head k of Q at columns [k d, (k+1) d), of K at a + k d, of V
+ * at 2a + k d).  Writes o [T, a] bf16 (heads in order) and lse [b, H, s]
+ * fp32 (natural log of the softmax denominator, scores scaled by 1/sqrt(d)).
+ * head_dim must be 64 or 128. */
+int mc_attention_forward(const uint16_t* qkv, uint16_t* o, float* lse, int32_t micro_batch,
+                         int32_t seq_len, int32_t heads, int32_t head_dim, int* status,
+                         void* stream);
+
+/* Causal flash attention backward: from qkv, o, lse and dO [T, a] bf16 writes
+ * dqkv [T, 3a] bf16 (dQ | dK | dV in the qkv layout).  `delta` is fp32
+ * scratch [b, H, s] (receives rowsum(dO * O)). */
+int mc_attention_backward(const uint16_t* qkv, const uint16_t* o, const float* lse,
+                          const uint16_t* dout, uint16_t* dqkv, float* delta, int32_t micro_batch,
+                          int32_t seq_len, int32_t heads, int32_t head_dim, int* status,
+                          void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MC_LAYER_H_ */

@@ -1,0 +1,205 @@
+"""ctypes binding of ``libmclayer.so`` (the C ABI in ``include/mc_layer.h``).
+
+Argument marshalling only: every function here has the name of the C entry
+point it calls and forwards plain integers (device pointers, sizes, a
+cudaStream_t handle).  Anything with a ``data_ptr()`` method (a torch tensor)
+is accepted where a pointer is expected.  No computation happens in Python.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+PKG_DIR = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG_DIR, "libmclayer.so")
+
+MC_OK = 0
+MC_ERR_SHAPE = -1
+MC_ERR_UNSUPPORTED = -2
+MC_ERR_NULLPTR = -3
+MC_ERR_ALIGN = -4
+MC_ERR_WORKSPACE = -5
+MC_ERR_CUDA = -6
+MC_ERR_DEVICE_TIMEOUT = -7
+MC_ERR_DEVICE_BOUNDS = -8
+MC_ERR_ARGUMENT = -9
+
+MC_ACCUMULATE_GRADS = 1
+
+MC_EPI_STORE_F32 = 0
+MC_EPI_STORE_BF16 = 1
+MC_EPI_BIAS_BF16 = 2
+MC_EPI_BIAS_GELU = 3
+MC_EPI_BIAS_RESID_F32 = 4
+MC_EPI_GELU_BWD = 5
+
+PARAM_ORDER = ("ln1_g", "ln1_b", "w_qkv", "b_qkv", "w_o", "b_o",
+               "ln2_g", "ln2_b", "w_fc1", "b_fc1", "w_fc2", "b_fc2")
+
+
+class McError(RuntimeError):
+    def __init__(self, code: int, where: str = ""):
+        self.code = code
+        super().__init__(f"{where}: {code} ({mc_strerror(code)})" if where else
+                         f"{code} ({mc_strerror(code)})")
+
+
+class mc_layer_shape(ctypes.Structure):  # noqa: N801 (C name)
+    _fields_ = [("micro_batch", ctypes.c_int32), ("seq_len", ctypes.c_int32),
+                ("hidden", ctypes.c_int32), ("heads", ctypes.c_int32),
+                ("ffn_hidden", ctypes.c_int32), ("tp_parts", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("flags", ctypes.c_uint32)]
+
+
+class mc_layer_weights(ctypes.Structure):  # noqa: N801
+    _fields_ = [(n, ctypes.c_void_p) for n in PARAM_ORDER]
+
+
+class mc_layer_grads(ctypes.Structure):  # noqa: N801
+    _fields_ = [(n, ctypes.c_void_p) for n in PARAM_ORDER]
+
+
+_lib = None
+
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_I64 = ctypes.c_int64
+_INT = ctypes.c_int
+_SZ = ctypes.c_size_t
+
+_SIGNATURES = {
+    "mc_layer_check_shape": (_INT, [ctypes.POINTER(mc_layer_shape)]),
+    "mc_layer_saved_bytes": (_SZ, [ctypes.POINTER(mc_layer_shape)]),
+    "mc_layer_workspace_bytes": (_SZ, [ctypes.POINTER(mc_layer_shape)]),
+    "mc_layer_forward": (_INT, [ctypes.POINTER(mc_layer_shape), ctypes.POINTER(mc_layer_weights),
+                                _P, _P, _P, _P, _SZ, _P]),
+    "mc_layer_backward": (_INT, [ctypes.POINTER(mc_layer_shape), ctypes.POINTER(mc_layer_weights),
+                                 _P, _P, _P, _P, ctypes.POINTER(mc_layer_grads), _P, _SZ, _P]),
+    "mc_layer_device_status": (_INT, [_P, _P]),
+    "mc_strerror": (ctypes.c_char_p, [_INT]),
+    "mc_layernorm_forward": (_INT, [_P, _P, _P, _P, _P, _P, _I64, _I32, _P, _P]),
+    "mc_layernorm_backward": (_INT, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _INT, _P,
+                                     _I64, _I32, _P, _P]),
+    "mc_layernorm_backward_scratch_floats": (_SZ, [_I64, _I32]),
+    "mc_gemm": (_INT, [_I64, _I64, _I64, _P, _I64, _INT, _P, _I64, _INT, _P, _I64, _INT, _P, _P,
+                       _I64, _INT, _INT, _P, _P]),
+    "mc_attention_forward": (_INT, [_P, _P, _P, _I32, _I32, _I32, _I32, _P, _P]),
+    "mc_attention_backward": (_INT, [_P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _P, _P]),
+}
+
+
+def lib() -> ctypes.CDLL:
+    """Loads libmclayer.so (built in-tree); raises if it is missing."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} not found: build it with "
+                               "`python -m megatron_transformer_layer_gb300.build`")
+        handle = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = handle
+    return _lib
+
+
+def _ptr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(s) -> int | None:
+    if s is None:
+        return None
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream  # torch.cuda.Stream
+
+
+def make_shape(micro_batch, seq_len, hidden, heads, ffn_hidden, tp_parts=1, head_dim=0, flags=0):
+    return mc_layer_shape(micro_batch, seq_len, hidden, heads, ffn_hidden, tp_parts, head_dim, flags)
+
+
+def make_weights(tensors: dict) -> mc_layer_weights:
+    return mc_layer_weights(*[_ptr(tensors[n]) for n in PARAM_ORDER])
+
+
+def make_grads(tensors: dict) -> mc_layer_grads:
+    return mc_layer_grads(*[_ptr(tensors[n]) for n in PARAM_ORDER])
+
+
+# ---- the C entry points, same names ----------------------------------------
+
+def mc_layer_check_shape(shape: mc_layer_shape) -> int:
+    return lib().mc_layer_check_shape(ctypes.byref(shape))
+
+
+def mc_layer_saved_bytes(shape: mc_layer_shape) -> int:
+    return lib().mc_layer_saved_bytes(ctypes.byref(shape))
+
+
+def mc_layer_workspace_bytes(shape: mc_layer_shape) -> int:
+    return lib().mc_layer_workspace_bytes(ctypes.byref(shape))
+
+
+def mc_layer_forward(shape, weights, x, y, saved, ws, ws_bytes, stream=None) -> int:
+    return lib().mc_layer_forward(ctypes.byref(shape), ctypes.byref(weights), _ptr(x), _ptr(y),
+                                  _ptr(saved), _ptr(ws), ws_bytes, _stream(stream))
+
+
+def mc_layer_backward(shape, weights, x, dy, saved, dx, grads, ws, ws_bytes, stream=None) -> int:
+    return lib().mc_layer_backward(ctypes.byref(shape), ctypes.byref(weights), _ptr(x), _ptr(dy),
+                                   _ptr(saved), _ptr(dx), ctypes.byref(grads), _ptr(ws), ws_bytes,
+                                   _stream(stream))
+
+
+def mc_layer_device_status(ws, stream=None) -> int:
+    return lib().mc_layer_device_status(_ptr(ws), _stream(stream))
+
+
+def mc_strerror(code: int) -> str:
+    try:
+        return lib().mc_strerror(code).decode()
+    except RuntimeError:
+        return "libmclayer.so not loaded"
+
+
+def mc_layernorm_forward(x, gamma, beta, out, mean, rstd, rows, h, status=None, stream=None) -> int:
+    return lib().mc_layernorm_forward(_ptr(x), _ptr(gamma), _ptr(beta), _ptr(out), _ptr(mean),
+                                      _ptr(rstd), rows, h, _ptr(status), _stream(stream))
+
+
+def mc_layernorm_backward(dout, x, mean, rstd, gamma, resid, dx, dx_bf16, dgamma, dbeta, colsum_dx,
+                          accumulate, partials, rows, h, status=None, stream=None) -> int:
+    return lib().mc_layernorm_backward(_ptr(dout), _ptr(x), _ptr(mean), _ptr(rstd), _ptr(gamma),
+                                       _ptr(resid), _ptr(dx), _ptr(dx_bf16), _ptr(dgamma),
+                                       _ptr(dbeta), _ptr(colsum_dx), accumulate, _ptr(partials),
+                                       rows, h, _ptr(status), _stream(stream))
+
+
+def mc_layernorm_backward_scratch_floats(rows: int, h: int) -> int:
+    return lib().mc_layernorm_backward_scratch_floats(rows, h)
+
+
+def mc_gemm(M, N, K, A, lda, a_layout, B, ldb, b_layout, out, ldc, epilogue, bias=None, aux=None,
+            ldaux=0, accumulate=0, k_parts=1, status=None, stream=None) -> int:
+    return lib().mc_gemm(M, N, K, _ptr(A), lda, a_layout, _ptr(B), ldb, b_layout, _ptr(out), ldc,
+                         epilogue, _ptr(bias), _ptr(aux), ldaux, accumulate, k_parts, _ptr(status),
+                         _stream(stream))
+
+
+def mc_attention_forward(qkv, o, lse, micro_batch, seq_len, heads, head_dim, status=None,
+                         stream=None) -> int:
+    return lib().mc_attention_forward(_ptr(qkv), _ptr(o), _ptr(lse), micro_batch, seq_len, heads,
+                                      head_dim, _ptr(status), _stream(stream))
+
+
+def mc_attention_backward(qkv, o, lse, dout, dqkv, delta, micro_batch, seq_len, heads, head_dim,
+                          status=None, stream=None) -> int:
+    return lib().mc_attention_backward(_ptr(qkv), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dqkv),
+                                       _ptr(delta), micro_batch, seq_len, heads, head_dim,
+                                       _ptr(status), _stream(stream))

@@ -1,0 +1,489 @@
+// Persistent, warp-specialised BF16 GEMM on the sm_103a tensor cores.
+//
+//   C[M, N] = sum_k A[m, k] * B[n, k]      (fp32 accumulation in TMEM)
+//
+// One CTA per SM walks a grouped sequence of 128 x BN output tiles.
+//   warp 0      TMA producer: 128B-swizzled A/B boxes -> STAGES-deep smem ring
+//   warp 1      allocates TMEM (2 accumulators of BN fp32 columns) and, from
+//               one thread, issues tcgen05.mma (M = 128, N = BN, K = 16)
+//   warps 2..5  epilogue: tcgen05.ld the accumulator, apply the fused
+//               epilogue, store to global memory; the second accumulator lets
+//               the next tile's main loop run underneath.
+//
+// Operands may be K-major ([rows, K] in memory) or MN-major ([K, rows] in
+// memory); the latter is how the dgrad (W used as [K, N]) and wgrad
+// (activations used transposed) products read their operands without any
+// transpose pass.  For a row-parallel product the K range is the
+// concatenation of the tp_parts partitions' K-slices, so each partition's
+// partial product is added into the same fp32 accumulator in partition order:
+// the cross-partition sum happens inside the accumulator and the epilogue
+// applies bias and residual once, after the sum.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "mc_layer_internal.h"
+#include "ptx.cuh"
+
+namespace mc {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;  // one 128-byte swizzle atom of bf16 along K
+constexpr int kThreads = 192;
+constexpr int kEpilogueThreads = 128;
+
+struct GemmArgs {
+  int M, N, K;
+  int num_kb;
+  int m_tiles, n_tiles, num_tiles;
+  void* out;
+  int64_t ldc;
+  const __nv_bfloat16* bias;
+  const void* aux;
+  int64_t ldaux;
+  int accumulate;
+  int* status;
+};
+
+template <int BN>
+struct GemmCfg {
+  static constexpr int kStages = BN == 256 ? 4 : 6;
+  static constexpr int kABytes = BM * BK * 2;
+  static constexpr int kBBytes = BN * BK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kTmemCols = 2 * BN;
+  // ring + barriers (full, empty, acc_full x2, acc_empty x2, drain) + tmem slot
+  static constexpr int kBarrierBytes = (2 * kStages + 5) * 8 + 8;
+  static constexpr int kSmemBytes = kStages * kStageBytes + kBarrierBytes + 1024;  // +align
+};
+
+__device__ __forceinline__ void tile_coords(int tile, int m_tiles, int n_tiles, int& mb, int& nb) {
+  constexpr int G = 8;  // M tiles per group; a group sweeps all N tiles
+  const int per_group = G * n_tiles;
+  const int group = tile / per_group;
+  const int first_m = group * G;
+  const int gsize = min(G, m_tiles - first_m);
+  const int r = tile - group * per_group;
+  mb = first_m + r % gsize;
+  nb = r / gsize;
+}
+
+__device__ __forceinline__ float gelu_tanh(float x) {
+  const float c = 0.7978845608028654f;  // sqrt(2/pi)
+  const float u = c * fmaf(0.044715f * x, x * x, x);
+  return 0.5f * x * (1.0f + tanhf(u));
+}
+
+__device__ __forceinline__ float gelu_tanh_grad(float x) {
+  const float c = 0.7978845608028654f;
+  const float x2 = x * x;
+  const float th = tanhf(c * fmaf(0.044715f * x, x2, x));
+  return 0.5f * (1.0f + th) + 0.5f * x * (1.0f - th * th) * c * fmaf(3.0f * 0.044715f, x2, 1.0f);
+}
+
+__device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* p, float (&v)[32]) {
+  const uint4* q = reinterpret_cast<const uint4*>(p);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint4 w = q[i];
+    v[8 * i + 0] = bf16_lo(w.x);
+    v[8 * i + 1] = bf16_hi(w.x);
+    v[8 * i + 2] = bf16_lo(w.y);
+    v[8 * i + 3] = bf16_hi(w.y);
+    v[8 * i + 4] = bf16_lo(w.z);
+    v[8 * i + 5] = bf16_hi(w.z);
+    v[8 * i + 6] = bf16_lo(w.w);
+    v[8 * i + 7] = bf16_hi(w.w);
+  }
+}
+
+__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* p, const float (&v)[32]) {
+  uint4* q = reinterpret_cast<uint4*>(p);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint4 w;
+    w.x = pack_bf16x2(v[8 * i + 0], v[8 * i + 1]);
+    w.y = pack_bf16x2(v[8 * i + 2], v[8 * i + 3]);
+    w.z = pack_bf16x2(v[8 * i + 4], v[8 * i + 5]);
+    w.w = pack_bf16x2(v[8 * i + 6], v[8 * i + 7]);
+    q[i] = w;
+  }
+}
+
+// Applies the epilogue to 32 consecutive columns [col0, col0 + 32) of `row`.
+template <int EPI>
+__device__ __forceinline__ void epilogue32(float (&v)[32], int row, int col0, const GemmArgs& g) {
+  if constexpr (EPI == MC_EPI_STORE_F32) {
+    float4* o = reinterpret_cast<float4*>(static_cast<float*>(g.out) + (int64_t)row * g.ldc + col0);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      float4 w = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+      if (g.accumulate) {
+        const float4 old = o[i];
+        w.x += old.x;
+        w.y += old.y;
+        w.z += old.z;
+        w.w += old.w;
+      }
+      o[i] = w;
+    }
+  } else if constexpr (EPI == MC_EPI_STORE_BF16) {
+    store_bf16x32(static_cast<__nv_bfloat16*>(g.out) + (int64_t)row * g.ldc + col0, v);
+  } else if constexpr (EPI == MC_EPI_BIAS_BF16) {
+    float b[32];
+    load_bf16x32(g.bias + col0, b);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] += b[i];
+    store_bf16x32(static_cast<__nv_bfloat16*>(g.out) + (int64_t)row * g.ldc + col0, v);
+  } else if constexpr (EPI == MC_EPI_BIAS_GELU) {
+    float b[32];
+    load_bf16x32(g.bias + col0, b);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] += b[i];
+    store_bf16x32(static_cast<__nv_bfloat16*>(const_cast<void*>(g.aux)) + (int64_t)row * g.ldaux +
+                      col0,
+                  v);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = gelu_tanh(v[i]);
+    store_bf16x32(static_cast<__nv_bfloat16*>(g.out) + (int64_t)row * g.ldc + col0, v);
+  } else if constexpr (EPI == MC_EPI_BIAS_RESID_F32) {
+    float b[32];
+    load_bf16x32(g.bias + col0, b);
+    const float4* r =
+        reinterpret_cast<const float4*>(static_cast<const float*>(g.aux) + (int64_t)row * g.ldaux + col0);
+    float4* o = reinterpret_cast<float4*>(static_cast<float*>(g.out) + (int64_t)row * g.ldc + col0);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float4 rr = r[i];
+      o[i] = make_float4(v[4 * i] + b[4 * i] + rr.x, v[4 * i + 1] + b[4 * i + 1] + rr.y,
+                         v[4 * i + 2] + b[4 * i + 2] + rr.z, v[4 * i + 3] + b[4 * i + 3] + rr.w);
+    }
+  } else if constexpr (EPI == MC_EPI_GELU_BWD) {
+    float hp[32];
+    load_bf16x32(static_cast<const __nv_bfloat16*>(g.aux) + (int64_t)row * g.ldaux + col0, hp);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] *= gelu_tanh_grad(hp[i]);
+    store_bf16x32(static_cast<__nv_bfloat16*>(g.out) + (int64_t)row * g.ldc + col0, v);
+  }
+}
+
+template <bool A_MN, bool B_MN, int BN, int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB, const GemmArgs g) {
+  using Cfg = GemmCfg<BN>;
+  constexpr int S = Cfg::kStages;
+  constexpr uint32_t kIdesc = idesc_bf16_f32(BM, BN, A_MN, B_MN);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + S * Cfg::kABytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * Cfg::kStageBytes);
+  uint64_t* empty = full + S;
+  uint64_t* acc_full = empty + S;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* drain = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], kEpilogueThreads);
+    }
+    mbar_init(drain, 1);
+    fence_mbar_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- producer
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < g.num_tiles; tile += gridDim.x) {
+        int mb, nb;
+        tile_coords(tile, g.m_tiles, g.n_tiles, mb, nb);
+        for (int kb = 0; kb < g.num_kb; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, g.status, kSiteGemmProducer)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[stage], Cfg::kStageBytes);
+          const int k0 = kb * BK;
+          uint8_t* a_dst = sA + stage * Cfg::kABytes;
+          uint8_t* b_dst = sB + stage * Cfg::kBBytes;
+          if constexpr (!A_MN) {
+            tma_load_2d(a_dst, &tmA, &full[stage], k0, mb * BM);
+          } else {
+            tma_load_2d(a_dst, &tmA, &full[stage], mb * BM, k0);
+            tma_load_2d(a_dst + 64 * BK * 2, &tmA, &full[stage], mb * BM + 64, k0);
+          }
+          if constexpr (!B_MN) {
+            tma_load_2d(b_dst, &tmB, &full[stage], k0, nb * BN);
+          } else {
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j)
+              tma_load_2d(b_dst + j * 64 * BK * 2, &tmB, &full[stage], nb * BN + j * 64, k0);
+          }
+          ++issued;
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Wait for this thread's copies still in flight (the last use of each
+      // stage) before the CTA may exit.
+      const int pending = issued < S ? issued : S;
+      for (int i = 0; i < pending; ++i) {
+        stage = stage == 0 ? S - 1 : stage - 1;
+        if (stage == S - 1) phase ^= 1u;
+        mbar_wait(&full[stage], phase, g.status, kSiteGemmDrain, 200000000ull, false);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- MMA issuer
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < g.num_tiles; tile += gridDim.x) {
+        if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, g.status, kSiteGemmMma)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        // The K loop runs over the partitions' K-slices in order; all of them
+        // accumulate into d_tmem.
+        for (int kb = 0; kb < g.num_kb; ++kb) {
+          if (!mbar_wait(&full[stage], phase, g.status, kSiteGemmMma)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(sA + stage * Cfg::kABytes);
+          const uint32_t b0 = smem_u32(sB + stage * Cfg::kBBytes);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            // K-major: a K step of 16 bf16 is 32 bytes inside the swizzled row.
+            // MN-major: a K step is 16 rows of 128 bytes; LBO = 64-wide MN chunk.
+            const uint64_t ad = A_MN ? smem_desc_sw128(a0 + k * 2048, 64 * BK * 2, 1024)
+                                     : smem_desc_sw128(a0 + k * 32, 16, 1024);
+            const uint64_t bd = B_MN ? smem_desc_sw128(b0 + k * 2048, 64 * BK * 2, 1024)
+                                     : smem_desc_sw128(b0 + k * 32, 16, 1024);
+            umma_bf16(d_tmem, ad, bd, kIdesc, (kb | k) != 0 ? 1u : 0u);
+          }
+          umma_commit(&empty[stage]);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&acc_full[acc]);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      // Every MMA issued by this thread must be complete before TMEM is freed.
+      umma_commit(drain);
+      mbar_wait(drain, 0, g.status, kSiteGemmDrain, 200000000ull, false);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;  // TMEM lanes [32 q, 32 q + 32)
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < g.num_tiles; tile += gridDim.x) {
+      int mb, nb;
+      tile_coords(tile, g.m_tiles, g.n_tiles, mb, nb);
+      if (!mbar_wait(&acc_full[acc], acc_phase, g.status, kSiteGemmEpilogue)) break;
+      tc_fence_after();
+      const int row = mb * BM + quarter * 32 + lane;
+      const uint32_t t_row = tmem_base + static_cast<uint32_t>(acc * BN) +
+                             (static_cast<uint32_t>(quarter * 32) << 16);
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        float v[32];
+        tmem_ld_32x32b_x32(t_row + c * 32, v);
+        const int col0 = nb * BN + c * 32;
+        if (row < g.M && col0 < g.N) epilogue32<EPI>(v, row, col0, g);
+      }
+      tc_fence_before();
+      mbar_arrive(&acc_empty[acc]);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, Cfg::kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2D bf16 tensor map over a row-major matrix [outer, inner] with row stride
+// `ld` elements, box [box_outer, box_inner], 128-byte swizzle, zero fill.
+bool make_tmap(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t ld,
+               uint32_t box_inner, uint32_t box_outer) {
+  auto enc = get_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {ld * 2};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <bool A_MN, bool B_MN, int BN, int EPI>
+int launch_variant(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& g,
+                   cudaStream_t stream) {
+  using Cfg = GemmCfg<BN>;
+  auto kern = gemm_tcgen05_kernel<A_MN, B_MN, BN, EPI>;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [&] {
+    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    Cfg::kSmemBytes);
+  });
+  if (attr_err != cudaSuccess) return MC_ERR_CUDA;
+  const int grid = g.num_tiles < num_sms() ? g.num_tiles : num_sms();
+  kern<<<grid, kThreads, Cfg::kSmemBytes, stream>>>(ta, tb, g);
+  return cudaGetLastError() == cudaSuccess ? MC_OK : MC_ERR_CUDA;
+}
+
+template <int BN, int EPI>
+int dispatch_layouts(int a_layout, int b_layout, const CUtensorMap& ta, const CUtensorMap& tb,
+                     const GemmArgs& g, cudaStream_t stream) {
+  if (!a_layout && !b_layout) return launch_variant<false, false, BN, EPI>(ta, tb, g, stream);
+  if (!a_layout && b_layout) return launch_variant<false, true, BN, EPI>(ta, tb, g, stream);
+  if (a_layout && b_layout) return launch_variant<true, true, BN, EPI>(ta, tb, g, stream);
+  return launch_variant<true, false, BN, EPI>(ta, tb, g, stream);
+}
+
+template <int BN>
+int dispatch_epilogue(int epi, int a_layout, int b_layout, const CUtensorMap& ta,
+                      const CUtensorMap& tb, const GemmArgs& g, cudaStream_t stream) {
+  switch (epi) {
+    case MC_EPI_STORE_F32:
+      return dispatch_layouts<BN, MC_EPI_STORE_F32>(a_layout, b_layout, ta, tb, g, stream);
+    case MC_EPI_STORE_BF16:
+      return dispatch_layouts<BN, MC_EPI_STORE_BF16>(a_layout, b_layout, ta, tb, g, stream);
+    case MC_EPI_BIAS_BF16:
+      return dispatch_layouts<BN, MC_EPI_BIAS_BF16>(a_layout, b_layout, ta, tb, g, stream);
+    case MC_EPI_BIAS_GELU:
+      return dispatch_layouts<BN, MC_EPI_BIAS_GELU>(a_layout, b_layout, ta, tb, g, stream);
+    case MC_EPI_BIAS_RESID_F32:
+      return dispatch_layouts<BN, MC_EPI_BIAS_RESID_F32>(a_layout, b_layout, ta, tb, g, stream);
+    case MC_EPI_GELU_BWD:
+      return dispatch_layouts<BN, MC_EPI_GELU_BWD>(a_layout, b_layout, ta, tb, g, stream);
+    default:
+      return MC_ERR_ARGUMENT;
+  }
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+int launch_gemm(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda, int a_layout,
+                const uint16_t* B, int64_t ldb, int b_layout, void* out, int64_t ldc, int epi,
+                const uint16_t* bias, const void* aux, int64_t ldaux, int accumulate, int k_parts,
+                int* status, cudaStream_t stream) {
+  if (M < 1 || N < 64 || K < 1 || N % 64 != 0) return MC_ERR_UNSUPPORTED;
+  if (M > (1 << 30) || N > (1 << 30) || K > (1 << 30)) return MC_ERR_UNSUPPORTED;
+  if (a_layout == 0 && (K % 64 != 0)) return MC_ERR_UNSUPPORTED;
+  if (k_parts < 1 || K % k_parts != 0) return MC_ERR_ARGUMENT;
+  if (a_layout < 0 || a_layout > 1 || b_layout < 0 || b_layout > 1) return MC_ERR_ARGUMENT;
+  if (epi < MC_EPI_STORE_F32 || epi > MC_EPI_GELU_BWD) return MC_ERR_ARGUMENT;
+  if (!A || !B || !out) return MC_ERR_NULLPTR;
+  const bool needs_bias =
+      epi == MC_EPI_BIAS_BF16 || epi == MC_EPI_BIAS_GELU || epi == MC_EPI_BIAS_RESID_F32;
+  const bool needs_aux =
+      epi == MC_EPI_BIAS_GELU || epi == MC_EPI_BIAS_RESID_F32 || epi == MC_EPI_GELU_BWD;
+  if ((needs_bias && !bias) || (needs_aux && !aux)) return MC_ERR_NULLPTR;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(out) || (bias && !aligned16(bias)) ||
+      (aux && !aligned16(aux)))
+    return MC_ERR_ALIGN;
+  if (lda % 8 || ldb % 8 || ldc % 8 || (needs_aux && ldaux % 8)) return MC_ERR_ALIGN;
+  // Leading dimensions must cover the rows they describe.
+  if ((a_layout == 0 ? lda < K : lda < M) || (b_layout == 0 ? ldb < K : ldb < N) || ldc < N ||
+      (needs_aux && ldaux < N))
+    return MC_ERR_ARGUMENT;
+
+  // Wide tiles when there are enough of them to fill the machine.
+  const int64_t m_tiles = (M + BM - 1) / BM;
+  const int bn = ((N % 256 == 0) && m_tiles * (N / 256) >= num_sms()) ? 256 : 128;
+
+  CUtensorMap ta, tb;
+  bool ok = a_layout == 0 ? make_tmap(&ta, A, K, M, lda, BK, BM)
+                          : make_tmap(&ta, A, M, K, lda, 64, BK);
+  ok = ok && (b_layout == 0 ? make_tmap(&tb, B, K, N, ldb, BK, bn)
+                            : make_tmap(&tb, B, N, K, ldb, 64, BK));
+  if (!ok) return MC_ERR_CUDA;
+
+  GemmArgs g;
+  g.M = static_cast<int>(M);
+  g.N = static_cast<int>(N);
+  g.K = static_cast<int>(K);
+  g.num_kb = static_cast<int>((K + BK - 1) / BK);
+  g.m_tiles = static_cast<int>(m_tiles);
+  g.n_tiles = static_cast<int>((N + bn - 1) / bn);
+  const int64_t tiles = m_tiles * g.n_tiles;
+  if (tiles > (1 << 30)) return MC_ERR_UNSUPPORTED;
+  g.num_tiles = static_cast<int>(tiles);
+  g.out = out;
+  g.ldc = ldc;
+  g.bias = reinterpret_cast<const __nv_bfloat16*>(bias);
+  g.aux = aux;
+  g.ldaux = ldaux;
+  g.accumulate = accumulate;
+  g.status = status;
+  return bn == 256 ? dispatch_epilogue<256>(epi, a_layout, b_layout, ta, tb, g, stream)
+                   : dispatch_epilogue<128>(epi, a_layout, b_layout, ta, tb, g, stream);
+}
+
+}  // namespace mc

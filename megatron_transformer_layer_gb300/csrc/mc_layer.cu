@@ -1,0 +1,357 @@
+// C ABI: shape checks, the `saved` / `ws` buffer plans and the launch
+// sequences of one layer's forward and backward pass.  All launches go to the
+// caller's stream; nothing here allocates or synchronises (except
+// mc_layer_device_status).
+#include <cuda_runtime.h>
+
+#include <mutex>
+#include <vector>
+
+#include "mc_layer_internal.h"
+
+namespace mc {
+
+int num_sms() {
+  static std::mutex mu;
+  static std::vector<int> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  std::lock_guard<std::mutex> lock(mu);
+  if (static_cast<int>(cache.size()) <= dev) cache.resize(dev + 1, 0);
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+      n = 1;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+namespace {
+
+struct Dims {
+  int64_t b, s, T, h, H, d, a, f, t;
+};
+
+Dims dims_of(const mc_layer_shape& sh) {
+  Dims D;
+  D.b = sh.micro_batch;
+  D.s = sh.seq_len;
+  D.T = D.b * D.s;
+  D.h = sh.hidden;
+  D.H = sh.heads;
+  D.d = sh.head_dim ? sh.head_dim : (sh.heads ? sh.hidden / sh.heads : 0);
+  D.a = D.H * D.d;
+  D.f = sh.ffn_hidden;
+  D.t = sh.tp_parts;
+  return D;
+}
+
+int check_shape(const mc_layer_shape* sh) {
+  if (!sh) return MC_ERR_NULLPTR;
+  if (sh->micro_batch <= 0 || sh->seq_len <= 0 || sh->hidden <= 0 || sh->heads <= 0 ||
+      sh->ffn_hidden <= 0 || sh->tp_parts <= 0 || sh->head_dim < 0)
+    return MC_ERR_SHAPE;
+  if ((sh->flags & ~MC_ACCUMULATE_GRADS) != 0) return MC_ERR_ARGUMENT;
+  const int t = sh->tp_parts;
+  // Divisibility: hidden size and heads (and the ffn slice of the column
+  // split) must divide by the tensor-parallel degree.
+  if (sh->hidden % t || sh->heads % t || sh->ffn_hidden % t) return MC_ERR_SHAPE;
+  if (sh->head_dim == 0 && sh->hidden % sh->heads) return MC_ERR_SHAPE;
+  const Dims D = dims_of(*sh);
+  if (D.d != 64 && D.d != 128) return MC_ERR_UNSUPPORTED;
+  if (D.h % 64 || (D.a / t) % 64 || (D.f / t) % 64) return MC_ERR_UNSUPPORTED;
+  if (D.h > kMaxLayerNormHidden) return MC_ERR_UNSUPPORTED;
+  if (D.T > (1 << 24) || D.f > (1 << 20) || 3 * D.a > (1 << 20) || D.H > 65535 || D.b > 65535)
+    return MC_ERR_UNSUPPORTED;
+  return MC_OK;
+}
+
+// Sequential 256-byte-aligned carving of a buffer.
+struct Carver {
+  uint8_t* base;
+  size_t off = 0;
+  explicit Carver(void* p) : base(static_cast<uint8_t*>(p)) {}
+  template <typename T>
+  T* take(size_t count) {
+    off = (off + 255) & ~static_cast<size_t>(255);
+    T* p = base ? reinterpret_cast<T*>(base + off) : nullptr;
+    off += count * sizeof(T);
+    return p;
+  }
+};
+
+struct Saved {
+  uint16_t *ln1, *qkv, *o, *ln2, *hp, *g;
+  float *mu1, *rs1, *lse, *x1, *mu2, *rs2;
+};
+
+Saved plan_saved(const Dims& D, void* p, size_t* bytes) {
+  Carver c(p);
+  Saved S;
+  S.ln1 = c.take<uint16_t>(D.T * D.h);
+  S.mu1 = c.take<float>(D.T);
+  S.rs1 = c.take<float>(D.T);
+  S.qkv = c.take<uint16_t>(D.T * 3 * D.a);
+  S.o = c.take<uint16_t>(D.T * D.a);
+  S.lse = c.take<float>(D.b * D.H * D.s);
+  S.x1 = c.take<float>(D.T * D.h);
+  S.ln2 = c.take<uint16_t>(D.T * D.h);
+  S.mu2 = c.take<float>(D.T);
+  S.rs2 = c.take<float>(D.T);
+  S.hp = c.take<uint16_t>(D.T * D.f);
+  S.g = c.take<uint16_t>(D.T * D.f);
+  if (bytes) *bytes = (c.off + 255) & ~static_cast<size_t>(255);
+  return S;
+}
+
+struct Work {
+  int* status;
+  uint16_t *dy16, *dhp, *dx1_16, *dO, *dqkv;
+  float *dln, *dx1, *delta, *partials;
+};
+
+Work plan_ws(const Dims& D, void* p, size_t* bytes) {
+  Carver c(p);
+  Work W;
+  W.status = c.take<int>(kStatusBytes / sizeof(int));
+  W.dy16 = c.take<uint16_t>(D.T * D.h);
+  W.dhp = c.take<uint16_t>(D.T * D.f);
+  W.dln = c.take<float>(D.T * D.h);
+  W.dx1 = c.take<float>(D.T * D.h);
+  W.dx1_16 = c.take<uint16_t>(D.T * D.h);
+  W.dO = c.take<uint16_t>(D.T * D.a);
+  W.delta = c.take<float>(D.b * D.H * D.s);
+  W.dqkv = c.take<uint16_t>(D.T * 3 * D.a);
+  const size_t ln_part = layernorm_backward_scratch_floats(D.T, static_cast<int>(D.h));
+  int64_t widest = D.f > 3 * D.a ? D.f : 3 * D.a;
+  if (D.h > widest) widest = D.h;
+  const size_t col_part = static_cast<size_t>(kColsumRowSplits) * widest;
+  W.partials = c.take<float>(ln_part > col_part ? ln_part : col_part);
+  if (bytes) *bytes = (c.off + 255) & ~static_cast<size_t>(255);
+  return W;
+}
+
+bool al(const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) & (n - 1)) == 0; }
+
+int check_weights(const mc_layer_weights* w) {
+  if (!w) return MC_ERR_NULLPTR;
+  const uint16_t* ptrs[12] = {w->ln1_g, w->ln1_b, w->w_qkv, w->b_qkv, w->w_o,   w->b_o,
+                              w->ln2_g, w->ln2_b, w->w_fc1, w->b_fc1, w->w_fc2, w->b_fc2};
+  for (auto p : ptrs) {
+    if (!p) return MC_ERR_NULLPTR;
+    if (!al(p, 16)) return MC_ERR_ALIGN;
+  }
+  return MC_OK;
+}
+
+int check_grads(const mc_layer_grads* g) {
+  if (!g) return MC_ERR_NULLPTR;
+  float* ptrs[12] = {g->ln1_g, g->ln1_b, g->w_qkv, g->b_qkv, g->w_o,   g->b_o,
+                     g->ln2_g, g->ln2_b, g->w_fc1, g->b_fc1, g->w_fc2, g->b_fc2};
+  for (auto p : ptrs) {
+    if (!p) return MC_ERR_NULLPTR;
+    if (!al(p, 16)) return MC_ERR_ALIGN;
+  }
+  return MC_OK;
+}
+
+#define MC_TRY(expr)           \
+  do {                         \
+    const int rc_ = (expr);    \
+    if (rc_ != MC_OK) return rc_; \
+  } while (0)
+
+}  // namespace
+}  // namespace mc
+
+using namespace mc;
+
+extern "C" {
+
+int mc_layer_check_shape(const mc_layer_shape* shape) { return check_shape(shape); }
+
+size_t mc_layer_saved_bytes(const mc_layer_shape* shape) {
+  if (check_shape(shape) != MC_OK) return 0;
+  size_t n = 0;
+  plan_saved(dims_of(*shape), nullptr, &n);
+  return n;
+}
+
+size_t mc_layer_workspace_bytes(const mc_layer_shape* shape) {
+  if (check_shape(shape) != MC_OK) return 0;
+  size_t n = 0;
+  plan_ws(dims_of(*shape), nullptr, &n);
+  return n;
+}
+
+int mc_layer_forward(const mc_layer_shape* shape, const mc_layer_weights* w, const float* x,
+                     float* y, void* saved, void* ws, size_t ws_bytes, void* stream) {
+  MC_TRY(check_shape(shape));
+  MC_TRY(check_weights(w));
+  if (!x || !y || !saved || !ws) return MC_ERR_NULLPTR;
+  if (!al(x, 16) || !al(y, 16) || !al(saved, 256) || !al(ws, 256)) return MC_ERR_ALIGN;
+  const Dims D = dims_of(*shape);
+  size_t need = 0;
+  plan_ws(D, nullptr, &need);
+  if (ws_bytes < need) return MC_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const Saved S = plan_saved(D, saved, nullptr);
+  const Work W = plan_ws(D, ws, nullptr);
+  const int t = static_cast<int>(D.t);
+  const int h = static_cast<int>(D.h);
+
+  if (cudaMemsetAsync(W.status, 0, kStatusBytes, st) != cudaSuccess) return MC_ERR_CUDA;
+  // F1  LN1
+  MC_TRY(launch_layernorm_forward(x, w->ln1_g, w->ln1_b, S.ln1, S.mu1, S.rs1, D.T, h, W.status, st));
+  // F2  QKV (column-parallel: every partition's heads are output columns)
+  MC_TRY(launch_gemm(D.T, 3 * D.a, D.h, S.ln1, D.h, 0, w->w_qkv, D.h, 0, S.qkv, 3 * D.a,
+                     MC_EPI_BIAS_BF16, w->b_qkv, nullptr, 0, 0, 1, W.status, st));
+  // F3  causal attention, local per head
+  MC_TRY(launch_attention_forward(S.qkv, S.o, S.lse, static_cast<int>(D.b), static_cast<int>(D.s),
+                                  static_cast<int>(D.H), static_cast<int>(D.d), W.status, st));
+  // F4  out-projection, row-parallel: partition partials summed in the
+  //     accumulator, then + b_o + x
+  MC_TRY(launch_gemm(D.T, D.h, D.a, S.o, D.a, 0, w->w_o, D.a, 0, S.x1, D.h, MC_EPI_BIAS_RESID_F32,
+                     w->b_o, x, D.h, 0, t, W.status, st));
+  // F5  LN2
+  MC_TRY(launch_layernorm_forward(S.x1, w->ln2_g, w->ln2_b, S.ln2, S.mu2, S.rs2, D.T, h, W.status, st));
+  // F6  fc1 + bias + GeLU (column-parallel)
+  MC_TRY(launch_gemm(D.T, D.f, D.h, S.ln2, D.h, 0, w->w_fc1, D.h, 0, S.g, D.f, MC_EPI_BIAS_GELU,
+                     w->b_fc1, S.hp, D.f, 0, 1, W.status, st));
+  // F7  fc2, row-parallel: partials summed, + b_fc2 + x1
+  MC_TRY(launch_gemm(D.T, D.h, D.f, S.g, D.f, 0, w->w_fc2, D.f, 0, y, D.h, MC_EPI_BIAS_RESID_F32,
+                     w->b_fc2, S.x1, D.h, 0, t, W.status, st));
+  return MC_OK;
+}
+
+int mc_layer_backward(const mc_layer_shape* shape, const mc_layer_weights* w, const float* x,
+                      const float* dy, const void* saved, float* dx, const mc_layer_grads* grads,
+                      void* ws, size_t ws_bytes, void* stream) {
+  MC_TRY(check_shape(shape));
+  MC_TRY(check_weights(w));
+  MC_TRY(check_grads(grads));
+  if (!x || !dy || !saved || !dx || !ws) return MC_ERR_NULLPTR;
+  if (!al(x, 16) || !al(dy, 16) || !al(dx, 16) || !al(saved, 256) || !al(ws, 256))
+    return MC_ERR_ALIGN;
+  const Dims D = dims_of(*shape);
+  size_t need = 0;
+  plan_ws(D, nullptr, &need);
+  if (ws_bytes < need) return MC_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const Saved S = plan_saved(D, const_cast<void*>(saved), nullptr);
+  const Work W = plan_ws(D, ws, nullptr);
+  const int acc = (shape->flags & MC_ACCUMULATE_GRADS) ? 1 : 0;
+  const int t = static_cast<int>(D.t);
+  const int h = static_cast<int>(D.h);
+  const mc_layer_grads& G = *grads;
+
+  // B1  fc2: db2 = colsum(dy) (+ bf16 copy of dy as a GEMM operand),
+  //     dW2 = dy^T g, dhp = (dy W2) * gelu'(hp)
+  MC_TRY(launch_colsum(dy, false, D.T, D.h, G.b_fc2, acc, W.dy16, W.partials, W.status, st));
+  MC_TRY(launch_gemm(D.h, D.f, D.T, W.dy16, D.h, 1, S.g, D.f, 1, G.w_fc2, D.f, MC_EPI_STORE_F32,
+                     nullptr, nullptr, 0, acc, 1, W.status, st));
+  MC_TRY(launch_gemm(D.T, D.f, D.h, W.dy16, D.h, 0, w->w_fc2, D.f, 1, W.dhp, D.f, MC_EPI_GELU_BWD,
+                     nullptr, S.hp, D.f, 0, 1, W.status, st));
+  // B2  fc1: db1, dW1 = dhp^T ln2, dln2 = sum_p dhp_p W1_p (partition sum in
+  //     the accumulator)
+  MC_TRY(launch_colsum(W.dhp, true, D.T, D.f, G.b_fc1, acc, nullptr, W.partials, W.status, st));
+  MC_TRY(launch_gemm(D.f, D.h, D.T, W.dhp, D.f, 1, S.ln2, D.h, 1, G.w_fc1, D.h, MC_EPI_STORE_F32,
+                     nullptr, nullptr, 0, acc, 1, W.status, st));
+  MC_TRY(launch_gemm(D.T, D.h, D.f, W.dhp, D.f, 0, w->w_fc1, D.h, 1, W.dln, D.h, MC_EPI_STORE_F32,
+                     nullptr, nullptr, 0, 0, t, W.status, st));
+  // B3  LN2 backward: dx1 = dy + LN2^T(dln2); dgamma2, dbeta2; db_o = colsum(dx1)
+  MC_TRY(launch_layernorm_backward(W.dln, S.x1, S.mu2, S.rs2, w->ln2_g, dy, W.dx1, W.dx1_16,
+                                   G.ln2_g, G.ln2_b, G.b_o, acc, W.partials, D.T, h, W.status, st));
+  // B4  out-projection: dWo = dx1^T O, dO = dx1 Wo
+  MC_TRY(launch_gemm(D.h, D.a, D.T, W.dx1_16, D.h, 1, S.o, D.a, 1, G.w_o, D.a, MC_EPI_STORE_F32,
+                     nullptr, nullptr, 0, acc, 1, W.status, st));
+  MC_TRY(launch_gemm(D.T, D.a, D.h, W.dx1_16, D.h, 0, w->w_o, D.a, 1, W.dO, D.a, MC_EPI_STORE_BF16,
+                     nullptr, nullptr, 0, 0, 1, W.status, st));
+  // B5  attention backward -> dQ | dK | dV
+  MC_TRY(launch_attention_backward(S.qkv, S.o, S.lse, W.dO, W.dqkv, W.delta, static_cast<int>(D.b),
+                                   static_cast<int>(D.s), static_cast<int>(D.H),
+                                   static_cast<int>(D.d), W.status, st));
+  // B6  QKV: db_qkv, dWqkv = dqkv^T ln1, dln1 = sum_p dqkv_p Wqkv_p
+  MC_TRY(launch_colsum(W.dqkv, true, D.T, 3 * D.a, G.b_qkv, acc, nullptr, W.partials, W.status, st));
+  MC_TRY(launch_gemm(3 * D.a, D.h, D.T, W.dqkv, 3 * D.a, 1, S.ln1, D.h, 1, G.w_qkv, D.h,
+                     MC_EPI_STORE_F32, nullptr, nullptr, 0, acc, 1, W.status, st));
+  MC_TRY(launch_gemm(D.T, D.h, 3 * D.a, W.dqkv, 3 * D.a, 0, w->w_qkv, D.h, 1, W.dln, D.h,
+                     MC_EPI_STORE_F32, nullptr, nullptr, 0, 0, t, W.status, st));
+  // B7  LN1 backward: dx = dx1 + LN1^T(dln1); dgamma1, dbeta1
+  MC_TRY(launch_layernorm_backward(W.dln, x, S.mu1, S.rs1, w->ln1_g, W.dx1, dx, nullptr, G.ln1_g,
+                                   G.ln1_b, nullptr, acc, W.partials, D.T, h, W.status, st));
+  return MC_OK;
+}
+
+int mc_layer_device_status(const void* ws, void* stream) {
+  if (!ws) return MC_ERR_NULLPTR;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int host[2] = {0, 0};
+  if (cudaMemcpyAsync(host, ws, sizeof(host), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return MC_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MC_ERR_CUDA;
+  return host[0];
+}
+
+const char* mc_strerror(int code) {
+  switch (code) {
+    case MC_OK: return "ok";
+    case MC_ERR_SHAPE: return "illegal shape (non-positive field or divisibility rule broken)";
+    case MC_ERR_UNSUPPORTED: return "shape not supported by this build";
+    case MC_ERR_NULLPTR: return "required pointer is NULL";
+    case MC_ERR_ALIGN: return "pointer or leading dimension not aligned as required";
+    case MC_ERR_WORKSPACE: return "workspace smaller than mc_layer_workspace_bytes()";
+    case MC_ERR_CUDA: return "CUDA runtime error";
+    case MC_ERR_DEVICE_TIMEOUT: return "device: bounded wait gave up";
+    case MC_ERR_DEVICE_BOUNDS: return "device: index check failed";
+    case MC_ERR_ARGUMENT: return "invalid argument";
+    default: return "unknown status code";
+  }
+}
+
+// ---- stage entry points -------------------------------------------------
+int mc_layernorm_forward(const float* x, const uint16_t* gamma, const uint16_t* beta,
+                         uint16_t* out, float* mean, float* rstd, int64_t rows, int32_t h,
+                         int* status, void* stream) {
+  return launch_layernorm_forward(x, gamma, beta, out, mean, rstd, rows, h, status,
+                                  static_cast<cudaStream_t>(stream));
+}
+
+int mc_layernorm_backward(const float* dout, const float* x, const float* mean, const float* rstd,
+                          const uint16_t* gamma, const float* resid, float* dx, uint16_t* dx_bf16,
+                          float* dgamma, float* dbeta, float* colsum_dx, int accumulate,
+                          float* partials, int64_t rows, int32_t h, int* status, void* stream) {
+  return launch_layernorm_backward(dout, x, mean, rstd, gamma, resid, dx, dx_bf16, dgamma, dbeta,
+                                   colsum_dx, accumulate, partials, rows, h, status,
+                                   static_cast<cudaStream_t>(stream));
+}
+
+size_t mc_layernorm_backward_scratch_floats(int64_t rows, int32_t h) {
+  return layernorm_backward_scratch_floats(rows, h);
+}
+
+int mc_gemm(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda, int a_layout,
+            const uint16_t* B, int64_t ldb, int b_layout, void* out, int64_t ldc, int epilogue,
+            const uint16_t* bias, const void* aux, int64_t ldaux, int accumulate, int k_parts,
+            int* status, void* stream) {
+  return launch_gemm(M, N, K, A, lda, a_layout, B, ldb, b_layout, out, ldc, epilogue, bias, aux,
+                     ldaux, accumulate, k_parts, status, static_cast<cudaStream_t>(stream));
+}
+
+int mc_attention_forward(const uint16_t* qkv, uint16_t* o, float* lse, int32_t micro_batch,
+                         int32_t seq_len, int32_t heads, int32_t head_dim, int* status,
+                         void* stream) {
+  return launch_attention_forward(qkv, o, lse, micro_batch, seq_len, heads, head_dim, status,
+                                  static_cast<cudaStream_t>(stream));
+}
+
+int mc_attention_backward(const uint16_t* qkv, const uint16_t* o, const float* lse,
+                          const uint16_t* dout, uint16_t* dqkv, float* delta, int32_t micro_batch,
+                          int32_t seq_len, int32_t heads, int32_t head_dim, int* status,
+                          void* stream) {
+  return launch_attention_backward(qkv, o, lse, dout, dqkv, delta, micro_batch, seq_len, heads,
+                                   head_dim, status, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

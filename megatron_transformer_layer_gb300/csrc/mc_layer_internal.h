@@ -1,0 +1,71 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/mc_layer.h"
+
+#ifdef __CUDACC__
+#include <cuda_runtime.h>
+#endif
+
+namespace mc {
+
+// Status block at the start of a workspace: int[64] (256 bytes).
+// status[0] = first error code recorded on the device, status[1] = where.
+constexpr size_t kStatusBytes = 256;
+
+// Where a device error was recorded (status[1]).
+enum ErrorSite : int {
+  kSiteGemmProducer = 1,
+  kSiteGemmMma = 2,
+  kSiteGemmEpilogue = 3,
+  kSiteGemmDrain = 4,
+  kSiteLayerNorm = 10,
+  kSiteAttention = 20,
+};
+
+// Row-major bf16 leading dimension bound used by the shape checks.
+constexpr int kMaxLayerNormHidden = 16384;
+
+// Grid cap of the LayerNorm-backward kernel; its column partial sums take
+// 3 * min(rows, kLnBwdMaxBlocks) * h floats of scratch.
+constexpr int kLnBwdMaxBlocks = 304;
+
+// Row splits of the column-sum (bias gradient) kernel.
+constexpr int kColsumRowSplits = 64;
+
+int num_sms();  // SM count of the current device (cached per device)
+
+#ifdef __CUDACC__
+// Launchers (enqueue on `stream`; return MC_OK or MC_ERR_*).
+int launch_layernorm_forward(const float* x, const uint16_t* gamma, const uint16_t* beta,
+                             uint16_t* out, float* mean, float* rstd, int64_t rows, int h,
+                             int* status, cudaStream_t stream);
+int launch_layernorm_backward(const float* dout, const float* x, const float* mean,
+                              const float* rstd, const uint16_t* gamma, const float* resid,
+                              float* dx, uint16_t* dx_bf16, float* dgamma, float* dbeta,
+                              float* colsum_dx, int accumulate, float* partials, int64_t rows,
+                              int h, int* status, cudaStream_t stream);
+size_t layernorm_backward_scratch_floats(int64_t rows, int h);
+
+// Column sums over rows of a [rows, n] matrix (bf16 if in_bf16 else fp32);
+// optionally writes a bf16 copy of an fp32 input.  out[n] = (accumulate ?
+// out : 0) + sum.  `partials` holds kColsumRowSplits * n floats.
+int launch_colsum(const void* in, bool in_bf16, int64_t rows, int64_t n, float* out,
+                  int accumulate, uint16_t* bf16_copy, float* partials, int* status,
+                  cudaStream_t stream);
+
+int launch_gemm(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda, int a_layout,
+                const uint16_t* B, int64_t ldb, int b_layout, void* out, int64_t ldc, int epi,
+                const uint16_t* bias, const void* aux, int64_t ldaux, int accumulate, int k_parts,
+                int* status, cudaStream_t stream);
+
+int launch_attention_forward(const uint16_t* qkv, uint16_t* o, float* lse, int b, int s, int H,
+                             int d, int* status, cudaStream_t stream);
+int launch_attention_backward(const uint16_t* qkv, const uint16_t* o, const float* lse,
+                              const uint16_t* dout, uint16_t* dqkv, float* delta, int b, int s,
+                              int H, int d, int* status, cudaStream_t stream);
+#endif
+
+}  // namespace mc

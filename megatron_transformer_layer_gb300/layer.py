@@ -1,0 +1,80 @@
+"""Device-buffer owner for one layer: torch allocates, libmclayer computes."""
+from __future__ import annotations
+
+import torch
+
+from . import _lib as L
+
+
+def _check(rc: int, where: str) -> None:
+    if rc != L.MC_OK:
+        raise L.McError(rc, where)
+
+
+def bf16_tensor(bits, device) -> torch.Tensor:
+    """uint16 bf16 bit patterns (numpy) -> bf16 device tensor (bit-exact)."""
+    t = torch.from_numpy(bits.astype("int16", copy=False).view("int16").copy())
+    return t.view(torch.bfloat16).to(device)
+
+
+class TransformerLayer:
+    """One GPT pre-LN layer on one GPU.
+
+    ``params`` maps parameter names to bf16 device tensors.  Gradients are fp32
+    device tensors owned here.  ``forward``/``backward`` enqueue on the current
+    torch stream (or ``stream``) and return without synchronising.
+    """
+
+    def __init__(self, micro_batch, seq_len, hidden, heads, ffn_hidden, tp_parts=1, head_dim=0,
+                 params=None, device="cuda", accumulate_grads=False):
+        self.shape = L.make_shape(micro_batch, seq_len, hidden, heads, ffn_hidden, tp_parts,
+                                  head_dim, L.MC_ACCUMULATE_GRADS if accumulate_grads else 0)
+        _check(L.mc_layer_check_shape(self.shape), "mc_layer_check_shape")
+        self.device = torch.device(device)
+        self.tokens = micro_batch * seq_len
+        self.hidden = hidden
+        self.saved_bytes = L.mc_layer_saved_bytes(self.shape)
+        self.ws_bytes = L.mc_layer_workspace_bytes(self.shape)
+        # uint8 buffers: the caching allocator returns >= 512-byte aligned blocks
+        self.saved = torch.empty(self.saved_bytes, dtype=torch.uint8, device=self.device)
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=self.device)
+        self.params = params
+        self.weights = L.make_weights(params) if params is not None else None
+        d = head_dim if head_dim else hidden // heads
+        a = heads * d
+        shapes = {"ln1_g": (hidden,), "ln1_b": (hidden,), "w_qkv": (3 * a, hidden),
+                  "b_qkv": (3 * a,), "w_o": (hidden, a), "b_o": (hidden,), "ln2_g": (hidden,),
+                  "ln2_b": (hidden,), "w_fc1": (ffn_hidden, hidden), "b_fc1": (ffn_hidden,),
+                  "w_fc2": (hidden, ffn_hidden), "b_fc2": (hidden,)}
+        self.grads = {k: torch.zeros(v, dtype=torch.float32, device=self.device)
+                      for k, v in shapes.items()}
+        self._grads_c = L.make_grads(self.grads)
+        self._x = None
+
+    def set_params(self, params):
+        self.params = params
+        self.weights = L.make_weights(params)
+
+    def _stream(self, stream):
+        return stream if stream is not None else torch.cuda.current_stream(self.device)
+
+    def forward(self, x: torch.Tensor, y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        if y is None:
+            y = torch.empty_like(x)
+        _check(L.mc_layer_forward(self.shape, self.weights, x, y, self.saved, self.ws,
+                                  self.ws_bytes, self._stream(stream)), "mc_layer_forward")
+        self._x = x
+        return y
+
+    def backward(self, dy: torch.Tensor, dx: torch.Tensor | None = None, x: torch.Tensor | None = None,
+                 stream=None) -> torch.Tensor:
+        x = self._x if x is None else x
+        if dx is None:
+            dx = torch.empty_like(dy)
+        _check(L.mc_layer_backward(self.shape, self.weights, x, dy, self.saved, dx, self._grads_c,
+                                   self.ws, self.ws_bytes, self._stream(stream)),
+               "mc_layer_backward")
+        return dx
+
+    def device_status(self, stream=None) -> int:
+        return L.mc_layer_device_status(self.ws, self._stream(stream))

@@ -1,0 +1,134 @@
+"""Layer parity: the whole forward + backward through the C ABI against the
+fp64 oracle, on the same seeded inputs; y, dx and all twelve parameter
+gradients are checked per tensor."""
+import numpy as np
+import pytest
+import torch
+
+import oracle.layer as O
+from layer_inputs import LayerShape, make_layer_inputs
+from layer_inputs.generator import NONTRIVIAL_INIT
+from parity import assert_close, metrics
+
+from gpu_util import DEV, dev_f32_from_bits, run_layer, to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+def _oracle(inp, t):
+    sh = inp.shape.with_tp(t)
+    return O.layer_forward_backward(sh, inp.params_f64(), inp.f64("x"), inp.f64("dy"))
+
+
+def _check_layer(inp, t, label):
+    _, y, dx, G = run_layer(inp, t)
+    y_o, dx_o, G_o = _oracle(inp, t)
+    report = {"y": assert_close(f"{label} y", y, y_o), "dx": assert_close(f"{label} dx", dx, dx_o)}
+    for k in G_o:
+        report[k] = assert_close(f"{label} {k}", G[k], G_o[k])
+    worst = max(report.items(), key=lambda kv: kv[1]["mean_rel"])
+    print(f"\n{label}: worst mean_rel {worst[0]} {worst[1]}")
+    return y, dx, G
+
+
+@pytest.mark.parametrize("t", [1, 2])
+def test_config1(t):
+    """b1 s128 h768 H12 f3072, default init (biases 0, gamma 1, beta 0)."""
+    _check_layer(make_layer_inputs(LayerShape(1, 128, 768, 12, 3072, t)), t, f"c1 t={t}")
+
+
+def test_config1_nontrivial_biases_and_affine():
+    inp = make_layer_inputs(LayerShape(1, 128, 768, 12, 3072, 2), seed=3, init=NONTRIVIAL_INIT)
+    _check_layer(inp, 2, "c1 nontrivial")
+
+
+@pytest.mark.parametrize("shape", [
+    LayerShape(1, 1, 768, 12, 3072, 1),          # single token
+    LayerShape(2, 7, 768, 12, 3072, 4),          # ragged, 4 partitions
+    LayerShape(2, 129, 1024, 8, 4096, 2),        # head_dim 128, ragged tile tail
+    LayerShape(1, 200, 2048, 2, 1024, 1, 128),   # a = heads * head_dim != hidden
+])
+def test_ragged_and_special_shapes(shape):
+    inp = make_layer_inputs(shape, seed=1, init=NONTRIVIAL_INIT)
+    _check_layer(inp, shape.tp_parts, str(shape))
+
+
+def test_gpu_outputs_do_not_depend_on_tp_parts():
+    inp = make_layer_inputs(LayerShape(2, 96, 1024, 8, 4096, 1), seed=2, init=NONTRIVIAL_INIT)
+    _, y1, dx1, G1 = run_layer(inp, 1)
+    for t in (2, 4, 8):
+        _, y, dx, G = run_layer(inp, t)
+        assert metrics(y, y1)["max_rel"] < 1e-6 and metrics(dx, dx1)["max_rel"] < 1e-6
+        for k in G1:
+            assert metrics(G[k], G1[k])["max_rel"] < 1e-6, k
+
+
+def test_gpu_causality():
+    shape = LayerShape(1, 150, 768, 12, 3072, 2)
+    inp = make_layer_inputs(shape, seed=4)
+    layer, y, _, _ = run_layer(inp)
+    i = 70
+    x2 = inp.x.copy()
+    x2[:, i + 1:, :] = inp.x[:, i + 1:, :][:, ::-1, :]          # change every later token
+    x = dev_f32_from_bits(x2.reshape(-1, shape.hidden))
+    y2 = to_f64(layer.forward(x)).reshape(inp.x.shape)
+    torch.cuda.synchronize()
+    assert np.array_equal(y2[:, :i + 1], y[:, :i + 1])
+    assert not np.array_equal(y2[:, i + 1:], y[:, i + 1:])
+
+
+def test_accumulate_grads_flag():
+    inp = make_layer_inputs(LayerShape(1, 64, 768, 12, 3072, 2), seed=5, init=NONTRIVIAL_INIT)
+    layer, _, _, G = run_layer(inp, accumulate=True)
+    x = dev_f32_from_bits(inp.x.reshape(-1, 768))
+    dy = dev_f32_from_bits(inp.dy.reshape(-1, 768))
+    layer.forward(x)
+    layer.backward(dy)
+    torch.cuda.synchronize()
+    for k, v in layer.grads.items():
+        assert metrics(to_f64(v), 2 * G[k])["max_rel"] < 1e-6, k
+
+
+def test_config2_stack_of_12_layers():
+    """b4 s512 h768 H12 f3072, tp 2: twelve layers, distinct weights per
+    layer, fp32 residual stream between layers, backward in reverse."""
+    shape = LayerShape(4, 512, 768, 12, 3072, 2)
+    n_layers = 12
+    inps = [make_layer_inputs(shape, seed=0, layer=l) for l in range(n_layers)]
+    x0, dyN = inps[0].f64("x"), inps[0].f64("dy")
+    # oracle
+    caches, acts = [], [x0]
+    for l in range(n_layers):
+        y, c = O.layer_forward(shape, inps[l].params_f64(), acts[-1])
+        caches.append(c)
+        acts.append(y)
+    g = dyN
+    grads_o = [None] * n_layers
+    for l in reversed(range(n_layers)):
+        g, grads_o[l] = O.layer_backward(shape, inps[l].params_f64(), caches[l], g)
+    dx_o = g
+    # GPU
+    from megatron_transformer_layer_gb300.layer import TransformerLayer
+    from gpu_util import dev_bf16
+    layers = [TransformerLayer(4, 512, 768, 12, 3072, 2,
+                               params={k: dev_bf16(v) for k, v in inps[l].params.items()})
+              for l in range(n_layers)]
+    x = dev_f32_from_bits(inps[0].x.reshape(-1, 768))
+    outs = [x]
+    for l in range(n_layers):
+        outs.append(layers[l].forward(outs[-1]))
+    gd = dev_f32_from_bits(inps[0].dy.reshape(-1, 768))
+    for l in reversed(range(n_layers)):
+        gd = layers[l].backward(gd, x=outs[l])
+    torch.cuda.synchronize()
+    assert_close("stack y", to_f64(outs[-1]).reshape(x0.shape), acts[-1])
+    assert_close("stack dx", to_f64(gd).reshape(x0.shape), dx_o)
+    for l in (0, n_layers - 1):
+        for k, v in layers[l].grads.items():
+            assert_close(f"stack layer{l} {k}", to_f64(v), grads_o[l][k])
+
+
+@pytest.mark.parametrize("t", [1, 2, 4])
+def test_config3(t):
+    """b8 s1024 h2048 H16 (d128) f8192."""
+    _check_layer(make_layer_inputs(LayerShape(8, 1024, 2048, 16, 8192, t)), t, f"c3 t={t}")
