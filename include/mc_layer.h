@@ -77,6 +77,8 @@ extern "C" {
 #define MC_ERR_DEVICE_TIMEOUT (-7) /* device: a bounded wait gave up               */
 #define MC_ERR_DEVICE_BOUNDS (-8)  /* device: an index check failed                */
 #define MC_ERR_ARGUMENT (-9)       /* another invalid argument (e.g. an enum)      */
+#define MC_ERR_SCRATCH_LIMIT (-10) /* problem larger than the fixed scratch of an
+                                      allocation-free entry point                 */
 
 /* shape flags */
 #define MC_ACCUMULATE_GRADS 1u /* backward adds into the gradient buffers (+=)    */
@@ -210,6 +212,27 @@ int mc_attention_backward(const uint16_t* qkv, const uint16_t* o, const float* l
                           const uint16_t* dout, uint16_t* dqkv, float* delta, int32_t micro_batch,
                           int32_t seq_len, int32_t heads, int32_t head_dim, int* status,
                           void* stream);
+
+/* Allocation-free variant of mc_attention_backward.  The pages have no
+ * counterpart to this entry point; it exists for callers that cannot allocate
+ * device memory themselves -- for example a plugin whose host framework
+ * forbids cudaMalloc while it runs, or a process whose device memory is
+ * already fully reserved by another allocator -- and so cannot supply the
+ * `delta` scratch buffer.  Same arguments and results as
+ * mc_attention_backward without `delta`: the rowsum(dO * O) scratch is a fixed
+ * 4 MiB array inside the library (micro_batch * heads * seq_len <= 1,048,576;
+ * larger problems return MC_ERR_SCRATCH_LIMIT before anything is enqueued).
+ * That array is held on every GPU that loads the library until the process
+ * exits.  The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  This entry point calls no cudaMalloc, cudaFree
+ * or allocating library routine.  All calls share the array and it keeps the
+ * last call's contents (each call overwrites every element it reads); calls
+ * whose kernels overlap on the GPU, e.g. on different streams, race on it. */
+int mc_attention_backward_noalloc(const uint16_t* qkv, const uint16_t* o, const float* lse,
+                                  const uint16_t* dout, uint16_t* dqkv, int32_t micro_batch,
+                                  int32_t seq_len, int32_t heads, int32_t head_dim, int* status,
+                                  void* stream);
 
 #ifdef __cplusplus
 }

@@ -23,6 +23,7 @@ MC_ERR_CUDA = -6
 MC_ERR_DEVICE_TIMEOUT = -7
 MC_ERR_DEVICE_BOUNDS = -8
 MC_ERR_ARGUMENT = -9
+MC_ERR_SCRATCH_LIMIT = -10
 
 MC_ACCUMULATE_GRADS = 1
 
@@ -85,6 +86,7 @@ _SIGNATURES = {
                        _I64, _INT, _INT, _P, _P]),
     "mc_attention_forward": (_INT, [_P, _P, _P, _I32, _I32, _I32, _I32, _P, _P]),
     "mc_attention_backward": (_INT, [_P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _P, _P]),
+    "mc_attention_backward_noalloc": (_INT, [_P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _P, _P]),
 }
 
 
@@ -203,3 +205,11 @@ def mc_attention_backward(qkv, o, lse, dout, dqkv, delta, micro_batch, seq_len, 
     return lib().mc_attention_backward(_ptr(qkv), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dqkv),
                                        _ptr(delta), micro_batch, seq_len, heads, head_dim,
                                        _ptr(status), _stream(stream))
+
+
+def mc_attention_backward_noalloc(qkv, o, lse, dout, dqkv, micro_batch, seq_len, heads, head_dim,
+                                  status=None, stream=None) -> int:
+    """Allocation-free attention backward (fixed in-library scratch)."""
+    return lib().mc_attention_backward_noalloc(_ptr(qkv), _ptr(o), _ptr(lse), _ptr(dout),
+                                               _ptr(dqkv), micro_batch, seq_len, heads, head_dim,
+                                               _ptr(status), _stream(stream))

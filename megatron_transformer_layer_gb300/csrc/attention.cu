@@ -22,6 +22,9 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <mutex>
+#include <vector>
+
 #include "mc_layer_internal.h"
 #include "ptx.cuh"
 
@@ -674,4 +677,51 @@ int launch_attention_backward(const uint16_t* qkv, const uint16_t* o, const floa
                  : bwd_launch<128>(qkv, o, lse, dout, dqkv, delta, b, s, H, st);
 }
 
+// ---------------------------------------------------------------- no-alloc
+// Fixed device scratch of the allocation-free attention backward: the
+// delta = rowsum(dO * O) vector, kNoAllocDeltaFloats floats (4 MiB), enough
+// for micro_batch * heads * seq_len <= 1,048,576.  It lives in this module's
+// global memory on every device that loads the library, until the process
+// exits.  All calls share it (it keeps the last call's values); the backward
+// overwrites every element it reads, so nothing has to be cleared.  Calls
+// whose kernels overlap on the GPU (different streams) race on it.
+namespace {
+constexpr int64_t kNoAllocDeltaFloats = int64_t(1) << 20;
+__device__ __align__(256) float g_noalloc_delta[kNoAllocDeltaFloats];
+
+std::mutex g_noalloc_mu;
+std::vector<float*> g_noalloc_ptr;  // per device ordinal
+
+// Device address of g_noalloc_delta on the current device; looked up once per
+// device (the symbol's host-side name is only a stand-in, not an address).
+int noalloc_scratch(float** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MC_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (static_cast<int>(g_noalloc_ptr.size()) <= dev) g_noalloc_ptr.resize(dev + 1, nullptr);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_delta) != cudaSuccess || !p) return MC_ERR_CUDA;
+    g_noalloc_ptr[dev] = static_cast<float*>(p);
+  }
+  *out = g_noalloc_ptr[dev];
+  return MC_OK;
+}
+}  // namespace
+
 }  // namespace mc
+
+extern "C" int mc_attention_backward_noalloc(const uint16_t* qkv, const uint16_t* o,
+                                             const float* lse, const uint16_t* dout,
+                                             uint16_t* dqkv, int32_t micro_batch,
+                                             int32_t seq_len, int32_t heads, int32_t head_dim,
+                                             int* status, void* stream) {
+  if (micro_batch < 1 || seq_len < 1 || heads < 1) return MC_ERR_SHAPE;
+  if (static_cast<int64_t>(micro_batch) * heads * seq_len > mc::kNoAllocDeltaFloats)
+    return MC_ERR_SCRATCH_LIMIT;
+  float* delta = nullptr;
+  const int rc = mc::noalloc_scratch(&delta);
+  if (rc != MC_OK) return rc;
+  return mc::launch_attention_backward(qkv, o, lse, dout, dqkv, delta, micro_batch, seq_len, heads,
+                                       head_dim, status, static_cast<cudaStream_t>(stream));
+}

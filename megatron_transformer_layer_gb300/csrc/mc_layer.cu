@@ -306,6 +306,8 @@ const char* mc_strerror(int code) {
     case MC_ERR_DEVICE_TIMEOUT: return "device: bounded wait gave up";
     case MC_ERR_DEVICE_BOUNDS: return "device: index check failed";
     case MC_ERR_ARGUMENT: return "invalid argument";
+    case MC_ERR_SCRATCH_LIMIT:
+      return "problem exceeds the fixed device scratch of the allocation-free entry point";
     default: return "unknown status code";
   }
 }
