@@ -94,7 +94,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -228,40 +228,102 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
-def run_stage(args, w, device):
-    """Times one GEMM of the step alone (the fc1 forward product by default)."""
+def stage_launcher(name, w, device, params=None):
+    """One kernel of the step with the workload's shapes, inputs resident in
+    HBM.  Returns (launch function, algorithmic flops or bytes per launch,
+    unit, description)."""
     import torch
 
     from megatron_transformer_layer_gb300 import _lib as L
     D = dims(w)
-    T, h, f = D["T"], D["h"], D["f"]
-    g = torch.Generator(device=device).manual_seed(0)
-    A = torch.randn(T, h, device=device, generator=g).to(torch.bfloat16)
-    B = (torch.randn(f, h, device=device, generator=g) * 0.02).to(torch.bfloat16)
-    bias = torch.zeros(f, device=device, dtype=torch.bfloat16)
-    out = torch.empty(T, f, device=device, dtype=torch.bfloat16)
-    hp = torch.empty(T, f, device=device, dtype=torch.bfloat16)
+    T, h, f, a, H, d, b, s = D["T"], D["h"], D["f"], D["a"], D["H"], D["d"], D["b"], D["s"]
+    gen = torch.Generator(device=device).manual_seed(0)
     st = torch.cuda.current_stream(device)
 
-    def launch():
-        rc = L.mc_gemm(T, f, h, A, h, 0, B, h, 0, out, f, L.MC_EPI_BIAS_GELU, bias=bias, aux=hp,
-                       ldaux=f, stream=st)
-        assert rc == 0, L.mc_strerror(rc)
+    def rnd(*shape, scale=1.0, dtype=torch.bfloat16):
+        return (torch.randn(*shape, device=device, generator=gen) * scale).to(dtype)
 
-    for _ in range(args.warmup):
+    if name == "gemm_fc1":
+        A, B = rnd(T, h), (params["w_fc1"] if params else rnd(f, h, scale=0.02))
+        bias = params["b_fc1"] if params else torch.zeros(f, device=device, dtype=torch.bfloat16)
+        out, hp = rnd(T, f), rnd(T, f)
+
+        def launch():
+            rc = L.mc_gemm(T, f, h, A, h, 0, B, h, 0, out, f, L.MC_EPI_BIAS_GELU, bias=bias,
+                           aux=hp, ldaux=f, stream=st)
+            assert rc == 0, L.mc_strerror(rc)
+        return launch, 2.0 * T * h * f, "flop", "gemm_tcgen05 fc1 forward (bias+GeLU epilogue)"
+    if name == "gemm_wgrad":
+        A, B = rnd(T, f), rnd(T, h)           # dhp [T, f], ln2 [T, h]
+        out = torch.empty(f, h, device=device, dtype=torch.float32)
+
+        def launch():
+            rc = L.mc_gemm(f, h, T, A, f, 1, B, h, 1, out, h, L.MC_EPI_STORE_F32, stream=st)
+            assert rc == 0, L.mc_strerror(rc)
+        return launch, 2.0 * T * h * f, "flop", "gemm_tcgen05 wgrad dW1 = dhp^T ln2 (MN-major A and B)"
+    if name in ("attn_fwd", "attn_bwd"):
+        qkv, o = rnd(T, 3 * a), rnd(T, a)
+        lse = torch.empty(b * H * s, device=device, dtype=torch.float32)
+        dout, dqkv = rnd(T, a), rnd(T, 3 * a)
+        delta = torch.empty(b * H * s, device=device, dtype=torch.float32)
+        assert L.mc_attention_forward(qkv, o, lse, b, s, H, d, stream=st) == 0
+        causal = 2.0 * a * b * s * (s + 1)
+        if name == "attn_fwd":
+            def launch():
+                assert L.mc_attention_forward(qkv, o, lse, b, s, H, d, stream=st) == 0
+            return launch, causal, "flop", "causal attention forward"
+
+        def launch():
+            assert L.mc_attention_backward(qkv, o, lse, dout, dqkv, delta, b, s, H, d,
+                                           stream=st) == 0
+        return launch, 2.0 * causal, "flop", "causal attention backward (pre + dkdv + dq)"
+    if name == "ln_bwd":
+        dln, x, resid = (torch.randn(T, h, device=device, generator=gen) for _ in range(3))
+        mean = torch.zeros(T, device=device)
+        rstd = torch.ones(T, device=device)
+        gamma = torch.ones(h, device=device, dtype=torch.bfloat16)
+        dx = torch.empty(T, h, device=device)
+        dx16 = torch.empty(T, h, device=device, dtype=torch.bfloat16)
+        dg, db, dc = (torch.empty(h, device=device) for _ in range(3))
+        part = torch.empty(L.mc_layernorm_backward_scratch_floats(T, h), device=device)
+
+        def launch():
+            assert L.mc_layernorm_backward(dln, x, mean, rstd, gamma, resid, dx, dx16, dg, db, dc,
+                                           0, part, T, h, stream=st) == 0
+        # algorithmic bytes: read dln, x, resid (fp32), write dx fp32 + bf16
+        return launch, float(T * h * (4 * 3 + 4 + 2)), "byte", "LayerNorm backward (+bf16 copy, colsums)"
+    raise ValueError(name)
+
+
+def time_launches(launch, device, steps, warmup):
+    """Average ms per launch: CUDA events on the launching stream."""
+    import torch
+    st = torch.cuda.current_stream(device)
+    for _ in range(warmup):
         launch()
     torch.cuda.synchronize(device)
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
-    for i in range(args.steps):
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * steps)]
+    for i in range(steps):
         ev[2 * i].record(st)
         launch()
         ev[2 * i + 1].record(st)
     torch.cuda.synchronize(device)
-    ms = [ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(args.steps)]
-    flops = 2.0 * T * h * f
-    avg = sum(ms) / len(ms)
-    print(json.dumps({"stage": "gemm fc1 forward (bias+GeLU epilogue)", "M": T, "N": f, "K": h,
-                      "ms": avg, "tflops": flops / avg / 1e9}), flush=True)
+    ms = [ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(steps)]
+    return sum(ms) / len(ms)
+
+
+def run_stage(args, w, device):
+    """Times one kernel of the step alone (used for profiling)."""
+    launch, work, unit, desc = stage_launcher(args.stage, w, device)
+    ms = time_launches(launch, device, args.steps, max(args.warmup, 1))
+    rate = work / (ms / 1e3)
+    line = {"stage": args.stage, "kernel": desc, "workload": WORKLOAD_NAMES[args.workload],
+            "ms_per_launch": ms}
+    if unit == "flop":
+        line["tflops"] = rate / 1e12
+    else:
+        line["gbs"] = rate / 1e9
+    print(json.dumps(line), flush=True)
 
 
 def run_ours(args, world, rank, local):
@@ -357,17 +419,19 @@ def run_ours(args, world, rank, local):
     h2d = 2 * x.numel() * 4
     d2h = 2 * x.numel() * 4
 
-    # ---- dominant kernel: the tcgen05 GEMM, fc1 forward product, timed alone
-    Dg = D
-    g_args = argparse.Namespace(steps=max(5, min(args.steps, 20)), warmup=2)
-    gemm = time_gemm_fc1(Dg, device, g_args, layer, params)
-    gemm_flops = 2.0 * Dg["T"] * Dg["h"] * Dg["f"]
+    # ---- dominant kernel: the tcgen05 GEMM variant with the largest share of
+    # the step (the wgrad product, dW1 = dhp^T ln2), timed alone on this stream
+    launch, gemm_flops, _, desc = stage_launcher("gemm_wgrad", w, device)
+    gemm = time_launches(launch, device, max(5, min(args.steps, 20)), 2)
     achieved = gemm_flops / (gemm / 1e3) / 1e12
-    roofline = {"bound": "tensor", "kernel": "gemm_tcgen05 fc1 forward (bias+GeLU epilogue)",
-                "achieved": achieved, "peak": peak_burst, "unit": "TFLOP/s",
-                "frac": achieved / peak_burst, "peak_kind": "bf16 burst, of measured",
+    roofline = {"bound": "tensor", "kernel": desc, "achieved": achieved, "peak": peak_burst,
+                "unit": "TFLOP/s", "frac": achieved / peak_burst,
+                "peak_kind": "bf16 burst, of measured (kernel timed alone)",
                 "flops_per_launch": gemm_flops, "ms_per_launch": gemm,
                 "traffic": TRAFFIC.get(args.workload)}
+    launch_fc1, fc1_flops, _, _ = stage_launcher("gemm_fc1", w, device, params)
+    fc1_ms = time_launches(launch_fc1, device, max(5, min(args.steps, 20)), 2)
+    roofline["also_fc1_forward_tflops"] = fc1_flops / (fc1_ms / 1e3) / 1e12
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
@@ -401,50 +465,21 @@ def run_ours(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
-# dram bytes read + written per launch of the timed GEMM, from an ncu capture
-# (None until captured for the current kernel build).
-TRAFFIC = {}
-
-
-def time_gemm_fc1(D, device, args, layer, params) -> float:
-    """Average duration (ms) of the fc1 forward GEMM launch, CUDA events on
-    the launching stream, inputs resident (layer's saved LN2 output)."""
-    import torch
-
-    from megatron_transformer_layer_gb300 import _lib as L
-    T, h, f = D["T"], D["h"], D["f"]
-    ln2 = torch.empty(T, h, device=device, dtype=torch.bfloat16).normal_()
-    out = torch.empty(T, f, device=device, dtype=torch.bfloat16)
-    hp = torch.empty(T, f, device=device, dtype=torch.bfloat16)
-    st = torch.cuda.current_stream(device)
-
-    def launch():
-        rc = L.mc_gemm(T, f, h, ln2, h, 0, params["w_fc1"], h, 0, out, f, L.MC_EPI_BIAS_GELU,
-                       bias=params["b_fc1"], aux=hp, ldaux=f, stream=st)
-        assert rc == 0, L.mc_strerror(rc)
-
-    for _ in range(args.warmup):
-        launch()
-    torch.cuda.synchronize(device)
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
-    for i in range(args.steps):
-        ev[2 * i].record(st)
-        launch()
-        ev[2 * i + 1].record(st)
-    torch.cuda.synchronize(device)
-    ms = [ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(args.steps)]
-    del ln2, out, hp
-    return sum(ms) / len(ms)
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of the timed wgrad
+# GEMM, from one ncu capture of the current kernel build (c4 shapes); None
+# for workloads not captured.
+TRAFFIC = {"c4": 2.708e9}
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="c4")
-    ap.add_argument("--stage", choices=["gemm_fc1"], default=None)
+    ap.add_argument("--stage", choices=["gemm_fc1", "gemm_wgrad", "attn_fwd", "attn_bwd", "ln_bwd"],
+                    default=None)
     ap.add_argument("--ref-prefix", type=int, default=64,
                     help="tokens of the sequence the CPU oracle processes per sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
