@@ -15,7 +15,8 @@ namespace mc {
 namespace {
 
 constexpr float kLnEps = 1e-5f;
-constexpr int kLnThreads = 128;
+constexpr int kLnThreads = 128;     // forward: one CTA per row
+constexpr int kLnBwdThreads = 256;  // backward: grid-strided rows
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -23,12 +24,13 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// Sum over the block (kLnThreads threads); `red` has 2 * (kLnThreads/32) floats.
+// Sum over the block (THREADS threads); `red` has 2 * (THREADS/32) floats.
+template <int THREADS = kLnThreads>
 __device__ __forceinline__ float2 block_sum2(float a, float b, float* red) {
   a = warp_sum(a);
   b = warp_sum(b);
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  constexpr int W = kLnThreads / 32;
+  constexpr int W = THREADS / 32;
   __syncthreads();  // red may still be read by a previous call
   if (l == 0) {
     red[w] = a;
@@ -111,20 +113,22 @@ __global__ void __launch_bounds__(kLnThreads) ln_fwd_kernel(const float* __restr
 // Grid-strided over rows.  Per-column partial sums of (dout * xhat, dout, dx)
 // for this CTA's rows live in shared memory (3 * h floats; each thread owns
 // its columns, so no synchronisation is needed) and are written to
-// partials[blockIdx.x][3][h] at the end.
+// partials[blockIdx.x][3][h] at the end.  All three input rows (dout, x,
+// resid) are requested before the row's reductions so one DRAM round trip
+// covers the row.
 template <int VPT>
-__global__ void __launch_bounds__(kLnThreads) ln_bwd_kernel(
+__global__ void __launch_bounds__(kLnBwdThreads) ln_bwd_kernel(
     const float* __restrict__ dout, const float* __restrict__ x, const float* __restrict__ mean,
     const float* __restrict__ rstd, const uint16_t* __restrict__ gamma,
     const float* resid, float* dx, uint16_t* __restrict__ dx_bf16,
     float* __restrict__ partials, int64_t rows, int h, int want_colsum_dx) {
   extern __shared__ float colacc[];  // [3][h]
-  __shared__ float red[2 * kLnThreads / 32];
+  __shared__ float red[2 * kLnBwdThreads / 32];
   const int n4 = h >> 2;
   float4 gam[VPT];
 #pragma unroll
   for (int i = 0; i < VPT; ++i) {
-    const int c = threadIdx.x + i * kLnThreads;
+    const int c = threadIdx.x + i * kLnBwdThreads;
     gam[i] = c < n4 ? load_bf16x4(gamma + 4 * c) : make_float4(0.f, 0.f, 0.f, 0.f);
     if (c < n4) {
       reinterpret_cast<float4*>(colacc)[c] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -136,44 +140,39 @@ __global__ void __launch_bounds__(kLnThreads) ln_bwd_kernel(
     const float mu = mean[row], rs = rstd[row];
     const float4* dr = reinterpret_cast<const float4*>(dout + row * h);
     const float4* xr = reinterpret_cast<const float4*>(x + row * h);
-    float4 dy[VPT], xh[VPT];
+    const float4* rr = resid ? reinterpret_cast<const float4*>(resid + row * h) : nullptr;
+    float4 dy[VPT], xh[VPT], rv[VPT];
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const int c = threadIdx.x + i * kLnBwdThreads;
+      const bool ok = c < n4;
+      dy[i] = ok ? dr[c] : make_float4(0.f, 0.f, 0.f, 0.f);
+      xh[i] = ok ? xr[c] : make_float4(0.f, 0.f, 0.f, 0.f);
+      rv[i] = (ok && rr) ? rr[c] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     float s1 = 0.f, s2 = 0.f;
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
-      const int c = threadIdx.x + i * kLnThreads;
-      if (c < n4) {
-        dy[i] = dr[c];
-        const float4 xv = xr[c];
-        xh[i] = make_float4((xv.x - mu) * rs, (xv.y - mu) * rs, (xv.z - mu) * rs, (xv.w - mu) * rs);
-        const float4 gg = make_float4(dy[i].x * gam[i].x, dy[i].y * gam[i].y, dy[i].z * gam[i].z,
-                                      dy[i].w * gam[i].w);
-        s1 += (gg.x + gg.y) + (gg.z + gg.w);
-        s2 += (gg.x * xh[i].x + gg.y * xh[i].y) + (gg.z * xh[i].z + gg.w * xh[i].w);
-      } else {
-        dy[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-        xh[i] = dy[i];
-      }
+      xh[i] = make_float4((xh[i].x - mu) * rs, (xh[i].y - mu) * rs, (xh[i].z - mu) * rs,
+                          (xh[i].w - mu) * rs);
+      const float4 gg = make_float4(dy[i].x * gam[i].x, dy[i].y * gam[i].y, dy[i].z * gam[i].z,
+                                    dy[i].w * gam[i].w);
+      s1 += (gg.x + gg.y) + (gg.z + gg.w);
+      s2 += (gg.x * xh[i].x + gg.y * xh[i].y) + (gg.z * xh[i].z + gg.w * xh[i].w);
     }
-    const float2 r = block_sum2(s1, s2, red);
+    const float2 r = block_sum2<kLnBwdThreads>(s1, s2, red);
     const float m1 = r.x / h, m2 = r.y / h;
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
-      const int c = threadIdx.x + i * kLnThreads;
+      const int c = threadIdx.x + i * kLnBwdThreads;
       if (c < n4) {
         const float4 gg = make_float4(dy[i].x * gam[i].x, dy[i].y * gam[i].y, dy[i].z * gam[i].z,
                                       dy[i].w * gam[i].w);
         float4 o;
-        o.x = rs * (gg.x - m1 - xh[i].x * m2);
-        o.y = rs * (gg.y - m1 - xh[i].y * m2);
-        o.z = rs * (gg.z - m1 - xh[i].z * m2);
-        o.w = rs * (gg.w - m1 - xh[i].w * m2);
-        if (resid) {
-          const float4 rr = reinterpret_cast<const float4*>(resid + row * h)[c];
-          o.x += rr.x;
-          o.y += rr.y;
-          o.z += rr.z;
-          o.w += rr.w;
-        }
+        o.x = rs * (gg.x - m1 - xh[i].x * m2) + rv[i].x;
+        o.y = rs * (gg.y - m1 - xh[i].y * m2) + rv[i].y;
+        o.z = rs * (gg.z - m1 - xh[i].z * m2) + rv[i].z;
+        o.w = rs * (gg.w - m1 - xh[i].w * m2) + rv[i].w;
         reinterpret_cast<float4*>(dx + row * h)[c] = o;
         if (dx_bf16) store_bf16x4(dx_bf16 + row * h + 4 * c, o);
         float4* cg = reinterpret_cast<float4*>(colacc) + c;
@@ -204,7 +203,7 @@ __global__ void __launch_bounds__(kLnThreads) ln_bwd_kernel(
   float4* dst = reinterpret_cast<float4*>(partials + static_cast<int64_t>(blockIdx.x) * 3 * h);
 #pragma unroll
   for (int i = 0; i < VPT; ++i) {
-    const int c = threadIdx.x + i * kLnThreads;
+    const int c = threadIdx.x + i * kLnBwdThreads;
     if (c < n4) {
       dst[c] = reinterpret_cast<float4*>(colacc)[c];
       dst[n4 + c] = reinterpret_cast<float4*>(colacc + h)[c];
@@ -296,15 +295,15 @@ int ln_bwd_launch(const float* dout, const float* x, const float* mean, const fl
                              static_cast<int>(smem)) != cudaSuccess)
       return MC_ERR_CUDA;
   }
-  kern<<<grid, kLnThreads, smem, st>>>(dout, x, mean, rstd, gamma, resid, dx, dx_bf16, partials,
+  kern<<<grid, kLnBwdThreads, smem, st>>>(dout, x, mean, rstd, gamma, resid, dx, dx_bf16, partials,
                                        rows, h, want_colsum_dx);
   return cudaGetLastError() == cudaSuccess ? MC_OK : MC_ERR_CUDA;
 }
 
-int vpt_for(int h) {
+int vpt_for(int h, int threads = kLnThreads) {
   const int n4 = h / 4;
   int vpt = 1;
-  while (vpt * kLnThreads < n4) vpt *= 2;
+  while (vpt * threads < n4) vpt *= 2;
   return vpt;
 }
 
@@ -354,13 +353,12 @@ int launch_layernorm_backward(const float* dout, const float* x, const float* me
   const int grid = static_cast<int>(rows < kLnBwdMaxBlocks ? rows : kLnBwdMaxBlocks);
   const int want = colsum_dx != nullptr;
   int rc;
-  switch (vpt_for(h)) {
+  switch (vpt_for(h, kLnBwdThreads)) {
     case 1: rc = ln_bwd_launch<1>(dout, x, mean, rstd, gamma, resid, dx, dx_bf16, partials, rows, h, want, grid, st); break;
     case 2: rc = ln_bwd_launch<2>(dout, x, mean, rstd, gamma, resid, dx, dx_bf16, partials, rows, h, want, grid, st); break;
     case 4: rc = ln_bwd_launch<4>(dout, x, mean, rstd, gamma, resid, dx, dx_bf16, partials, rows, h, want, grid, st); break;
     case 8: rc = ln_bwd_launch<8>(dout, x, mean, rstd, gamma, resid, dx, dx_bf16, partials, rows, h, want, grid, st); break;
     case 16: rc = ln_bwd_launch<16>(dout, x, mean, rstd, gamma, resid, dx, dx_bf16, partials, rows, h, want, grid, st); break;
-    case 32: rc = ln_bwd_launch<32>(dout, x, mean, rstd, gamma, resid, dx, dx_bf16, partials, rows, h, want, grid, st); break;
     default: return MC_ERR_UNSUPPORTED;
   }
   if (rc != MC_OK) return rc;

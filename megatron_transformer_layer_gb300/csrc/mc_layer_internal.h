@@ -30,7 +30,7 @@ constexpr int kMaxLayerNormHidden = 16384;
 
 // Grid cap of the LayerNorm-backward kernel; its column partial sums take
 // 3 * min(rows, kLnBwdMaxBlocks) * h floats of scratch.
-constexpr int kLnBwdMaxBlocks = 304;
+constexpr int kLnBwdMaxBlocks = 456;
 
 // Row splits of the column-sum (bias gradient) kernel.
 constexpr int kColsumRowSplits = 64;

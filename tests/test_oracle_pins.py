@@ -376,3 +376,21 @@ def test_planted_partition_mistake_is_caught(monkeypatch):
 
     monkeypatch.setattr(L, "layer_forward", bias_per_partition)
     assert tp_invariance_error(shape, P, x, dy, tps=(1, 2)) > 1e-6
+
+
+# --------------------------------------------------------------------------
+# Sampled outputs (used for sequences too long for the full oracle)
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("shape,rows,tail", [
+    (LayerShape(2, 23, 16, 2, 32, 1), [0, 5, 22], 4),
+    (LayerShape(1, 40, 32, 4, 64, 2), [3, 39], 7),
+    (LayerShape(1, 9, 16, 2, 32, 1), [8], 9),        # tail = whole sequence
+])
+def test_sampled_rows_and_tail_match_full_oracle(shape, rows, tail):
+    from oracle.sampled import sampled_rows_and_tail
+    P, x, dy = _tiny_inputs(shape, wstd=0.2)
+    y, dx, _ = L.layer_forward_backward(shape, P, x, dy)
+    ys, dxs = sampled_rows_and_tail(shape, P, x, dy, rows, tail)
+    assert _rel(ys, y[:, rows]) < 1e-12
+    assert _rel(dxs, dx[:, -tail:]) < 1e-12
