@@ -1,15 +1,12 @@
-// Causal flash attention, forward and backward, for head_dim 64 and 128.
+// Causal flash attention backward for head_dim 64 and 128 (the forward is
+// the tcgen05 kernel in attention_tc.cu; this file also holds the launcher
+// entry points and the allocation-free variant).
 //
 // Layout: qkv [T, 3a] bf16 (token-major; Q | K | V blocks, head k at columns
 // k*d of its block), o / dO [T, a] bf16, lse / delta [b, H, s] fp32.
-//
-// Forward: one CTA per (128-query block, head, batch); 8 warps own 16 query
-// rows each.  K/V blocks of 64 keys are streamed through a double-buffered,
-// XOR-swizzled shared-memory ring with cp.async; S = Q K^T and O += P V run on
-// the tensor cores (mma.sync m16n8k16 bf16 -> fp32); the softmax is online
-// (running max and sum in registers, exp2 with the log2(e)/sqrt(d) scale
-// folded in).  Key blocks entirely above the diagonal are skipped and the
-// diagonal block is masked.
+// Key/query blocks of 64 are streamed through double-buffered, XOR-swizzled
+// shared memory with cp.async; products run on mma.sync m16n8k16
+// (bf16 -> fp32) with exp2 and the log2(e)/sqrt(d) scale folded in.
 //
 // Backward (recompute P from the saved log-sum-exp):
 //   pre:   delta_i = sum_c dO_ic O_ic
@@ -130,167 +127,6 @@ __device__ __forceinline__ void c_to_a(const float (&c0)[4], const float (&c1)[4
   a[1] = pack_bf16x2(c0[2], c0[3]);
   a[2] = pack_bf16x2(c1[0], c1[1]);
   a[3] = pack_bf16x2(c1[2], c1[3]);
-}
-
-// ---------------------------------------------------------------- forward
-constexpr int kFwdBM = 128, kFwdBN = 64, kFwdThreads = 256;
-
-template <int D>
-__global__ void __launch_bounds__(kFwdThreads, 1)
-    attn_fwd_kernel(const uint16_t* __restrict__ qkv, uint16_t* __restrict__ out,
-                    float* __restrict__ lse, int s, int H) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  const uint32_t sQ = smem_u32(smem);
-  const uint32_t sK0 = sQ + kFwdBM * D * 2;
-  const uint32_t sV0 = sK0 + 2 * kFwdBN * D * 2;
-  constexpr uint32_t kKV = kFwdBN * D * 2;
-
-  const int a = H * D;
-  const int64_t ld = 3 * static_cast<int64_t>(a);
-  const int q_blk = gridDim.x - 1 - blockIdx.x;  // heaviest blocks first
-  const int hh = blockIdx.y, bi = blockIdx.z;
-  const int q0 = q_blk * kFwdBM;
-  const uint16_t* base = qkv + static_cast<int64_t>(bi) * s * ld;
-  const uint16_t* gQ = base + hh * D;
-  const uint16_t* gK = base + a + hh * D;
-  const uint16_t* gV = base + 2 * a + hh * D;
-  const int warp = threadIdx.x >> 5, l = threadIdx.x & 31;
-  const int g = l >> 2, t = l & 3;
-
-  const int kv_end = min(q0 + kFwdBM, s);
-  const int n_kb = (kv_end + kFwdBN - 1) / kFwdBN;
-
-  load_tile<D, kFwdBM, kFwdThreads>(sQ, gQ, ld, q0, s);
-  load_tile<D, kFwdBN, kFwdThreads>(sK0, gK, ld, 0, s);
-  load_tile<D, kFwdBN, kFwdThreads>(sV0, gV, ld, 0, s);
-  cp_async_commit();
-
-  const float scale = rsqrtf(static_cast<float>(D)) * kLog2e;
-  uint32_t qf[D / 16][4];
-  float o[D / 8][4];
-#pragma unroll
-  for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-  float m_r[2] = {-INFINITY, -INFINITY}, l_r[2] = {0.f, 0.f};
-  const int row_a = q0 + warp * 16 + g, row_b = row_a + 8;
-
-  for (int kb = 0; kb < n_kb; ++kb) {
-    const int buf = kb & 1;
-    if (kb + 1 < n_kb) {
-      load_tile<D, kFwdBN, kFwdThreads>(sK0 + (buf ^ 1) * kKV, gK, ld, (kb + 1) * kFwdBN, s);
-      load_tile<D, kFwdBN, kFwdThreads>(sV0 + (buf ^ 1) * kKV, gV, ld, (kb + 1) * kFwdBN, s);
-    }
-    cp_async_commit();
-    cp_async_wait<1>();
-    __syncthreads();
-    if (kb == 0) load_a_frags<D>(sQ, warp * 16, qf);
-    const uint32_t sK = sK0 + buf * kKV, sV = sV0 + buf * kKV;
-
-    float sc[kFwdBN / 8][4];
-#pragma unroll
-    for (int i = 0; i < kFwdBN / 8; ++i) sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.f;
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-#pragma unroll
-      for (int nb = 0; nb < kFwdBN / 16; ++nb) {
-        uint32_t b[4];
-        load_b_nk<D>(sK, nb * 16, kk, b);
-        mma16816(sc[2 * nb], qf[kk], b[0], b[1]);
-        mma16816(sc[2 * nb + 1], qf[kk], b[2], b[3]);
-      }
-    }
-    const int key0 = kb * kFwdBN;
-    const bool need_mask = (key0 + kFwdBN - 1 > q0 + warp * 16) || (key0 + kFwdBN > s);
-    float mx[2] = {m_r[0], m_r[1]};
-#pragma unroll
-    for (int i = 0; i < kFwdBN / 8; ++i) {
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        float v = sc[i][j] * scale;
-        if (need_mask) {
-          const int key = key0 + i * 8 + 2 * t + (j & 1);
-          const int row = j < 2 ? row_a : row_b;
-          if (key > row || key >= s) v = -INFINITY;
-        }
-        sc[i][j] = v;
-        mx[j >> 1] = fmaxf(mx[j >> 1], v);
-      }
-    }
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
-      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-    }
-    float alpha[2];
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      // mx is finite: key 0 of block 0 is visible to every row.
-      alpha[r] = exp2f(m_r[r] - mx[r]);
-      m_r[r] = mx[r];
-      l_r[r] *= alpha[r];
-    }
-#pragma unroll
-    for (int i = 0; i < D / 8; ++i) {
-      o[i][0] *= alpha[0];
-      o[i][1] *= alpha[0];
-      o[i][2] *= alpha[1];
-      o[i][3] *= alpha[1];
-    }
-#pragma unroll
-    for (int i = 0; i < kFwdBN / 8; ++i) {
-      sc[i][0] = exp2f(sc[i][0] - m_r[0]);
-      sc[i][1] = exp2f(sc[i][1] - m_r[0]);
-      sc[i][2] = exp2f(sc[i][2] - m_r[1]);
-      sc[i][3] = exp2f(sc[i][3] - m_r[1]);
-      l_r[0] += sc[i][0] + sc[i][1];
-      l_r[1] += sc[i][2] + sc[i][3];
-    }
-#pragma unroll
-    for (int kk = 0; kk < kFwdBN / 16; ++kk) {
-      uint32_t pa[4];
-      c_to_a(sc[2 * kk], sc[2 * kk + 1], pa);
-#pragma unroll
-      for (int nb = 0; nb < D / 16; ++nb) {
-        uint32_t b[4];
-        load_b_kn<D>(sV, kk * 16, nb * 16, b);
-        mma16816(o[2 * nb], pa, b[0], b[1]);
-        mma16816(o[2 * nb + 1], pa, b[2], b[3]);
-      }
-    }
-    __syncthreads();
-  }
-  cp_async_wait<0>();
-
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    l_r[r] += __shfl_xor_sync(0xffffffffu, l_r[r], 1);
-    l_r[r] += __shfl_xor_sync(0xffffffffu, l_r[r], 2);
-  }
-  const float inv0 = 1.f / l_r[0], inv1 = 1.f / l_r[1];
-  // Stage the warp's 16 output rows in its own slice of sQ, then copy out.
-  uint8_t* sq = smem;
-#pragma unroll
-  for (int i = 0; i < D / 8; ++i) {
-    const int col = i * 8 + 2 * t;
-    *reinterpret_cast<uint32_t*>(sq + swz<D>(warp * 16 + g, col)) =
-        pack_bf16x2(o[i][0] * inv0, o[i][1] * inv0);
-    *reinterpret_cast<uint32_t*>(sq + swz<D>(warp * 16 + g + 8, col)) =
-        pack_bf16x2(o[i][2] * inv1, o[i][3] * inv1);
-  }
-  __syncwarp();
-  uint16_t* gO = out + static_cast<int64_t>(bi) * s * a + hh * D;
-  constexpr int CH = D / 8;
-  for (int i = l; i < 16 * CH; i += 32) {
-    const int r = i / CH, c = i % CH;
-    const int row = q0 + warp * 16 + r;
-    if (row < s)
-      *reinterpret_cast<uint4*>(gO + static_cast<int64_t>(row) * a + c * 8) =
-          *reinterpret_cast<const uint4*>(sq + swz<D>(warp * 16 + r, c * 8));
-  }
-  if (t == 0) {
-    float* L = lse + (static_cast<int64_t>(bi) * H + hh) * s;
-    if (row_a < s) L[row_a] = (m_r[0] + log2f(l_r[0])) * kLn2;
-    if (row_b < s) L[row_b] = (m_r[1] + log2f(l_r[1])) * kLn2;
-  }
 }
 
 // ---------------------------------------------------------------- backward
@@ -620,16 +456,6 @@ bool set_smem(K kern, int bytes) {
 }
 
 template <int D>
-int fwd_launch(const uint16_t* qkv, uint16_t* o, float* lse, int b, int s, int H,
-               cudaStream_t st) {
-  const int smem = (kFwdBM + 4 * kFwdBN) * D * 2;
-  if (!set_smem(attn_fwd_kernel<D>, smem)) return MC_ERR_CUDA;
-  dim3 grid((s + kFwdBM - 1) / kFwdBM, H, b);
-  attn_fwd_kernel<D><<<grid, kFwdThreads, smem, st>>>(qkv, o, lse, s, H);
-  return cudaGetLastError() == cudaSuccess ? MC_OK : MC_ERR_CUDA;
-}
-
-template <int D>
 int bwd_launch(const uint16_t* qkv, const uint16_t* o, const float* lse, const uint16_t* dout,
                uint16_t* dqkv, float* delta, int b, int s, int H, cudaStream_t st) {
   const int64_t T = static_cast<int64_t>(b) * s;
@@ -661,7 +487,7 @@ int launch_attention_forward(const uint16_t* qkv, uint16_t* o, float* lse, int b
   if (H > 65535 || b > 65535) return MC_ERR_UNSUPPORTED;
   if (!qkv || !o || !lse) return MC_ERR_NULLPTR;
   if (!al16(qkv) || !al16(o)) return MC_ERR_ALIGN;
-  return d == 64 ? fwd_launch<64>(qkv, o, lse, b, s, H, st) : fwd_launch<128>(qkv, o, lse, b, s, H, st);
+  return launch_attention_forward_tc(qkv, o, lse, b, s, H, d, status, st);
 }
 
 int launch_attention_backward(const uint16_t* qkv, const uint16_t* o, const float* lse,

@@ -8,6 +8,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "mc_layer_internal.h"
 #include "ptx.cuh"
 
@@ -290,11 +292,16 @@ int ln_bwd_launch(const float* dout, const float* x, const float* mean, const fl
                   cudaStream_t st) {
   const size_t smem = 3 * static_cast<size_t>(h) * sizeof(float);
   auto kern = ln_bwd_kernel<VPT>;
-  if (smem > 48 * 1024) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
-      return MC_ERR_CUDA;
-  }
+  // Opt in once to the largest column-partial buffer (h = kMaxLayerNormHidden);
+  // 48 KB of dynamic memory plus the kernel's static reduction buffer already
+  // exceeds the default limit at h = 4096.
+  static std::once_flag once;
+  static cudaError_t attr = cudaSuccess;
+  std::call_once(once, [&] {
+    attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                3 * kMaxLayerNormHidden * static_cast<int>(sizeof(float)));
+  });
+  if (attr != cudaSuccess) return MC_ERR_CUDA;
   kern<<<grid, kLnBwdThreads, smem, st>>>(dout, x, mean, rstd, gamma, resid, dx, dx_bf16, partials,
                                        rows, h, want_colsum_dx);
   return cudaGetLastError() == cudaSuccess ? MC_OK : MC_ERR_CUDA;

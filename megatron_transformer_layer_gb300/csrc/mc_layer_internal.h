@@ -6,6 +6,7 @@
 #include "../../include/mc_layer.h"
 
 #ifdef __CUDACC__
+#include <cuda.h>
 #include <cuda_runtime.h>
 #endif
 
@@ -38,6 +39,11 @@ constexpr int kColsumRowSplits = 64;
 int num_sms();  // SM count of the current device (cached per device)
 
 #ifdef __CUDACC__
+// bf16 tensor map with 128-byte swizzle and zero fill; strides_bytes has
+// rank - 1 entries (dimension 0 is contiguous).
+bool make_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                    const uint64_t* strides_bytes, const uint32_t* box);
+
 // Launchers (enqueue on `stream`; return MC_OK or MC_ERR_*).
 int launch_layernorm_forward(const float* x, const uint16_t* gamma, const uint16_t* beta,
                              uint16_t* out, float* mean, float* rstd, int64_t rows, int h,
@@ -63,6 +69,8 @@ int launch_gemm(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda,
 
 int launch_attention_forward(const uint16_t* qkv, uint16_t* o, float* lse, int b, int s, int H,
                              int d, int* status, cudaStream_t stream);
+int launch_attention_forward_tc(const uint16_t* qkv, uint16_t* o, float* lse, int b, int s, int H,
+                                int d, int* status, cudaStream_t stream);
 int launch_attention_backward(const uint16_t* qkv, const uint16_t* o, const float* lse,
                               const uint16_t* dout, uint16_t* dqkv, float* delta, int b, int s,
                               int H, int d, int* status, cudaStream_t stream);
