@@ -176,35 +176,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int j = 0; j < n_kb; ++j) {
       const int st = j & 1;
-      if (!mbar_wait(&s_full[st], (j >> 1) & 1, status, kSiteAttention)) {
+      if (!mbar_wait_warp(&s_full[st], (j >> 1) & 1, status, kSiteAttention)) {
         ok = false;
         break;
       }
       tc_fence_after();
       float x[BKV];
-#pragma unroll
-      for (int c = 0; c < BKV / 32; ++c) {
-        float v[32];
-        tmem_ld_32x32b_x32(tS[st] + lane_off + c * 32, v);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) x[c * 32 + i] = v[i];
-      }
+      // Issue all four TMEM loads before the single wait.
+      tmem_ld_32x32b_x32_nowait(tS[st] + lane_off + 0, x + 0);
+      tmem_ld_32x32b_x32_nowait(tS[st] + lane_off + 32, x + 32);
+      tmem_ld_32x32b_x32_nowait(tS[st] + lane_off + 64, x + 64);
+      tmem_ld_32x32b_x32_nowait(tS[st] + lane_off + 96, x + 96);
+      tmem_ld_wait();
       const int key0 = j * BKV;
-      const bool need_mask = key0 + BKV - 1 > q0 || key0 + BKV > s;
       float mx = -INFINITY;
+      if (key0 + BKV - 1 > q0 || key0 + BKV > s) {  // diagonal or ragged block
+        const int lim = min(q + 1, s) - key0;       // keys [0, lim) are visible
 #pragma unroll
-      for (int i = 0; i < BKV; ++i) {
-        float v = x[i] * scale;
-        if (need_mask && (key0 + i > q || key0 + i >= s)) v = -INFINITY;
-        x[i] = v;
-        mx = fmaxf(mx, v);
+        for (int i = 0; i < BKV; ++i) {
+          x[i] = i < lim ? x[i] : -INFINITY;
+          mx = fmaxf(mx, x[i]);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < BKV; ++i) mx = fmaxf(mx, x[i]);
       }
+      mx *= scale;  // raw scores; scale > 0 commutes with max
       const float m_new = fmaxf(m, mx);
       const bool need = j > 0 && m_new > m + kRescaleThreshold;
       if (j == 0) m = m_new;  // key 0 is visible to every row: m is finite
       if (__any_sync(0xffffffffu, need)) {
-        const float alpha = need ? exp2f(m - m_new) : 1.f;
-        if (!mbar_wait(o_ready, (j - 1) & 1, status, kSiteAttention)) {
+        const float alpha = need ? fast_exp2(m - m_new) : 1.f;
+        if (!mbar_wait_warp(o_ready, (j - 1) & 1, status, kSiteAttention)) {
           ok = false;
           break;
         }
@@ -225,14 +228,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       uint32_t pk[BKV / 2];
-      float sum = 0.f;
+      float sum0 = 0.f, sum1 = 0.f;
+      const float neg_m = -m;
 #pragma unroll
       for (int i = 0; i < BKV / 2; ++i) {
-        const float p0 = exp2f(x[2 * i] - m);
-        const float p1 = exp2f(x[2 * i + 1] - m);
-        sum += p0 + p1;
+        const float p0 = fast_exp2(fmaf(x[2 * i], scale, neg_m));
+        const float p1 = fast_exp2(fmaf(x[2 * i + 1], scale, neg_m));
+        sum0 += p0;
+        sum1 += p1;
         pk[i] = pack_bf16x2(p0, p1);
       }
+      const float sum = sum0 + sum1;
       l += sum;
 #pragma unroll
       for (int c = 0; c < BKV / 64; ++c) {
@@ -245,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(&p_full[st]);
     }
-    if (ok && mbar_wait(o_ready, (n_kb - 1) & 1, status, kSiteAttention)) {
+    if (ok && mbar_wait_warp(o_ready, (n_kb - 1) & 1, status, kSiteAttention)) {
       tc_fence_after();
       const float inv = 1.f / l;
       uint16_t* orow = out + (static_cast<int64_t>(bi) * s + q) * a + hh * D;
@@ -278,6 +284,328 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------- backward
+// Both backward kernels keep one 128-row operand block resident and stream
+// the other side through a 2-deep TMA ring; warps 2..5 own one row each.
+//   dkdv: rows = keys.  S^T = K Q_i^T and dP^T = V dO_i^T into TMEM; the
+//         compute warps form P^T = exp2(S^T c - lse2_q) and
+//         dS^T = P^T (dP^T - delta_q), write both back as bf16 into the
+//         first 64 columns of their buffers; then dV += P^T dO_i and
+//         dK += dS^T Q_i with A read from TMEM and B the same smem tiles
+//         viewed MN-major.
+//   dq:   rows = queries.  S = Q K_j^T, dP = dO V_j^T, dS as above, then
+//         dQ += dS K_j.
+template <int D>
+struct BwdCfg {
+  static constexpr int kChunks = D / 64;
+  static constexpr int kTile = 128 * D * 2;
+  static constexpr int kUsed = 6 * kTile + 4 * 128 * 4 + 16 * 8 + 1024;
+  static constexpr int kSmem = kUsed > 116 * 1024 ? kUsed : 116 * 1024;
+  static constexpr uint32_t kTmemCols = 512;
+};
+
+// Loads 32 columns of two TMEM rows (this thread's lane) with one wait.
+__device__ __forceinline__ void tmem_ld2(uint32_t a, uint32_t b, float* va, float* vb) {
+  tmem_ld_32x32b_x32_nowait(a, va);
+  tmem_ld_32x32b_x32_nowait(b, vb);
+  tmem_ld_wait();
+}
+
+template <int D, bool KV_MAJOR>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv,
+                       const __grid_constant__ CUtensorMap tm_do, const float* __restrict__ lse,
+                       const float* __restrict__ delta, uint16_t* __restrict__ dqkv, int s, int H,
+                       int* status) {
+  using C = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  // Resident pair (KV_MAJOR: K, V; else Q, dO) and the streamed ring
+  // (KV_MAJOR: Q_i, dO_i; else K_j, V_j).
+  uint8_t* sR0 = smem;
+  uint8_t* sR1 = smem + C::kTile;
+  uint8_t* sA[2] = {smem + 2 * C::kTile, smem + 3 * C::kTile};
+  uint8_t* sB[2] = {smem + 4 * C::kTile, smem + 5 * C::kTile};
+  float* sL = reinterpret_cast<float*>(smem + 6 * C::kTile);  // [2][128]
+  float* sD = sL + 256;                                       // [2][128]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sD + 256);
+  uint64_t* r_full = bars + 0;
+  uint64_t* st_full = bars + 1;   // [2]
+  uint64_t* st_empty = bars + 3;  // [2]
+  uint64_t* s_full = bars + 5;
+  uint64_t* p_full = bars + 6;
+  uint64_t* mma_done = bars + 7;
+  uint64_t* drain = bars + 8;
+  uint64_t* lse_ready = bars + 9;  // [2]: the 128 compute threads staged lse/delta
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 11);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int a = H * D;
+  const int hh = blockIdx.y, bi = blockIdx.z;
+  const int nblk = (s + 127) / 128;
+  // KV_MAJOR: this CTA's key block; streamed query blocks from the diagonal
+  // to the end.  Else: this CTA's query block (heaviest first); streamed key
+  // blocks from 0 to the diagonal.
+  const int rb = KV_MAJOR ? static_cast<int>(blockIdx.x) : nblk - 1 - static_cast<int>(blockIdx.x);
+  const int r0 = rb * 128;
+  const int first = KV_MAJOR ? rb : 0;
+  const int count = KV_MAJOR ? nblk - rb : rb + 1;
+
+  if (threadIdx.x == 0) {
+    mbar_init(r_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&st_full[i], 1);
+      mbar_init(&st_empty[i], 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(p_full, 128);
+    mbar_init(mma_done, 1);
+    mbar_init(drain, 1);
+    mbar_init(&lse_ready[0], 128);
+    mbar_init(&lse_ready[1], 128);
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_qkv);
+    tma_prefetch_desc(&tm_do);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tS = tmem, tdP = tmem + 128, tAcc0 = tmem + 256, tAcc1 = tmem + 384;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // -------------------------------------------------------- producer
+      // column offsets inside qkv of Q, K, V for this head
+      const int cq = hh * D, ck = a + hh * D, cv = 2 * a + hh * D;
+      mbar_arrive_expect_tx(r_full, 2 * C::kTile);
+      for (int c = 0; c < C::kChunks; ++c) {
+        if (KV_MAJOR) {
+          tma_load_3d(sR0 + c * 16384, &tm_qkv, r_full, ck + c * 64, r0, bi);
+          tma_load_3d(sR1 + c * 16384, &tm_qkv, r_full, cv + c * 64, r0, bi);
+        } else {
+          tma_load_3d(sR0 + c * 16384, &tm_qkv, r_full, cq + c * 64, r0, bi);
+          tma_load_3d(sR1 + c * 16384, &tm_do, r_full, hh * D + c * 64, r0, bi);
+        }
+      }
+      int issued = 0;
+      for (int i = 0; i < count; ++i) {
+        const int st = i & 1;
+        const int row = (first + i) * 128;
+        if (!mbar_wait(&st_empty[st], ((i >> 1) & 1) ^ 1u, status, kSiteAttention)) break;
+        mbar_arrive_expect_tx(&st_full[st], 2 * C::kTile);
+        for (int c = 0; c < C::kChunks; ++c) {
+          if (KV_MAJOR) {
+            tma_load_3d(sA[st] + c * 16384, &tm_qkv, &st_full[st], cq + c * 64, row, bi);
+            tma_load_3d(sB[st] + c * 16384, &tm_do, &st_full[st], hh * D + c * 64, row, bi);
+          } else {
+            tma_load_3d(sA[st] + c * 16384, &tm_qkv, &st_full[st], ck + c * 64, row, bi);
+            tma_load_3d(sB[st] + c * 16384, &tm_qkv, &st_full[st], cv + c * 64, row, bi);
+          }
+        }
+        ++issued;
+      }
+      mbar_wait(r_full, 0, status, kSiteAttention, 200000000ull, false);
+      for (int i = issued - 1; i >= 0 && i >= issued - 2; --i)
+        mbar_wait(&st_full[i & 1], (i >> 1) & 1, status, kSiteAttention, 200000000ull, false);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // -------------------------------------------------------- MMA issuer
+      constexpr uint32_t kIdescSq = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t kIdescAcc = idesc_bf16_f32(128, D, false, true);
+      bool ok = mbar_wait(r_full, 0, status, kSiteAttention);
+      const uint32_t r0b = smem_u32(sR0), r1b = smem_u32(sR1);
+      for (int i = 0; ok && i < count; ++i) {
+        const int st = i & 1;
+        if (!mbar_wait(&st_full[st], (i >> 1) & 1, status, kSiteAttention)) break;
+        // tS / tdP were last read by the previous block's accumulating MMAs.
+        if (i > 0 && !mbar_wait(mma_done, (i - 1) & 1, status, kSiteAttention)) break;
+        tc_fence_after();
+        const uint32_t ab = smem_u32(sA[st]), bb = smem_u32(sB[st]);
+        // KV_MAJOR: S^T = K Q^T (A = K resident, B = Q streamed),
+        //           dP^T = V dO^T (A = V resident, B = dO streamed).
+        // else:     S = Q K^T (A = Q resident, B = K streamed),
+        //           dP = dO V^T (A = dO resident, B = V streamed).
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          umma_bf16(tS, smem_desc_sw128(r0b + off, 16, 1024), smem_desc_sw128(ab + off, 16, 1024),
+                    kIdescSq, kk > 0 ? 1u : 0u);
+          umma_bf16(tdP, smem_desc_sw128(r1b + off, 16, 1024), smem_desc_sw128(bb + off, 16, 1024),
+                    kIdescSq, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(s_full);
+        if (!mbar_wait(p_full, i & 1, status, kSiteAttention)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 128 / 16; ++kk) {
+          const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+          if (KV_MAJOR) {
+            // dV += P^T dO_i ; dK += dS^T Q_i  (B = streamed tiles viewed MN-major)
+            umma_bf16_ts(tAcc0, tS + kk * 8, smem_desc_sw128(bb + kk * 2048, 16384, 1024),
+                         kIdescAcc, acc);
+            umma_bf16_ts(tAcc1, tdP + kk * 8, smem_desc_sw128(ab + kk * 2048, 16384, 1024),
+                         kIdescAcc, acc);
+          } else {
+            // dQ += dS K_j
+            umma_bf16_ts(tAcc0, tS + kk * 8, smem_desc_sw128(ab + kk * 2048, 16384, 1024),
+                         kIdescAcc, acc);
+          }
+        }
+        umma_commit(&st_empty[st]);
+        umma_commit(mma_done);
+      }
+      umma_commit(drain);
+      mbar_wait(drain, 0, status, kSiteAttention, 200000000ull, false);
+    }
+  } else {
+    // ---------------------------------------------------------- compute
+    const int quarter = warp & 3;
+    const int t = quarter * 32 + lane;  // thread index among the 128 compute threads
+    const int r = r0 + t;               // this thread's key (KV_MAJOR) or query
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const float scale2 = rsqrtf(static_cast<float>(D)) * kLog2e;
+    const float* L = lse + (static_cast<int64_t>(bi) * H + hh) * s;
+    const float* Dl = delta + (static_cast<int64_t>(bi) * H + hh) * s;
+    float my_l2 = 0.f, my_d = 0.f;
+    if (!KV_MAJOR && r < s) {
+      my_l2 = L[r] * kLog2e;
+      my_d = Dl[r];
+    }
+    bool ok = true;
+    for (int i = 0; i < count; ++i) {
+      const int c0 = (first + i) * 128;  // first column (query or key) of this block
+      float* l2 = sL + (i & 1) * 128;
+      float* dl = sD + (i & 1) * 128;
+      if (KV_MAJOR) {
+        const int qq = c0 + t;
+        l2[t] = qq < s ? L[qq] * kLog2e : 0.f;
+        dl[t] = qq < s ? Dl[qq] : 0.f;
+        mbar_arrive(&lse_ready[i & 1]);
+        if (!mbar_wait_warp(&lse_ready[i & 1], (i >> 1) & 1, status, kSiteAttention)) {
+          ok = false;
+          break;
+        }
+      }
+      if (!mbar_wait_warp(s_full, i & 1, status, kSiteAttention)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      // Visible (row, column) pairs: KV_MAJOR: query >= key; else key <= query;
+      // both within the sequence.
+      const bool edge = KV_MAJOR ? (c0 < r0 + 127 || c0 + 128 > s) : (c0 + 127 > r0 || c0 + 128 > s);
+#pragma unroll 1
+      for (int ch = 0; ch < 4; ++ch) {
+        float sv[32], dv[32];
+        tmem_ld2(tS + lane_off + ch * 32, tdP + lane_off + ch * 32, sv, dv);
+        uint32_t pw[16], dw[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float p[2], ds[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int col = c0 + ch * 32 + e + u;
+            const float lse2 = KV_MAJOR ? l2[ch * 32 + e + u] : my_l2;
+            const float dlt = KV_MAJOR ? dl[ch * 32 + e + u] : my_d;
+            float pv = fast_exp2(fmaf(sv[e + u], scale2, -lse2));
+            if (edge) {
+              const bool vis = KV_MAJOR ? (col >= r && col < s) : (col <= r && col < s);
+              pv = vis ? pv : 0.f;
+            }
+            p[u] = pv;
+            ds[u] = pv * (dv[e + u] - dlt);
+          }
+          pw[e / 2] = pack_bf16x2(p[0], p[1]);
+          dw[e / 2] = pack_bf16x2(ds[0], ds[1]);
+        }
+        // Columns [16 ch, 16 ch + 16) of each buffer were read in chunks <= ch.
+        if (KV_MAJOR) tmem_st_32x32b_x16(tS + lane_off + ch * 16, pw);
+        tmem_st_32x32b_x16((KV_MAJOR ? tdP : tS) + lane_off + ch * 16, dw);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(p_full);
+    }
+    if (ok && mbar_wait_warp(mma_done, (count - 1) & 1, status, kSiteAttention)) {
+      tc_fence_after();
+      const float scale = rsqrtf(static_cast<float>(D));
+      const int64_t base = (static_cast<int64_t>(bi) * s + r) * 3 * static_cast<int64_t>(a);
+#pragma unroll 1
+      for (int w = 0; w < (KV_MAJOR ? 2 : 1); ++w) {
+        // KV_MAJOR: w = 0 -> dV (tAcc0, V block), w = 1 -> dK (tAcc1, K block).
+        const uint32_t tacc = w == 0 ? tAcc0 : tAcc1;
+        const float mul = (KV_MAJOR && w == 0) ? 1.f : scale;
+        const int col = KV_MAJOR ? (w == 0 ? 2 * a : a) + hh * D : hh * D;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          float v[32];
+          tmem_ld_32x32b_x32(tacc + lane_off + c * 32, v);
+          if (r < s) {
+            uint4* dst = reinterpret_cast<uint4*>(dqkv + base + col + c * 32);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              uint4 wv;
+              wv.x = pack_bf16x2(v[8 * k + 0] * mul, v[8 * k + 1] * mul);
+              wv.y = pack_bf16x2(v[8 * k + 2] * mul, v[8 * k + 3] * mul);
+              wv.z = pack_bf16x2(v[8 * k + 4] * mul, v[8 * k + 5] * mul);
+              wv.w = pack_bf16x2(v[8 * k + 6] * mul, v[8 * k + 7] * mul);
+              dst[k] = wv;
+            }
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <int D, bool KV_MAJOR>
+int launch_bwd_tc_one(const CUtensorMap& tq, const CUtensorMap& td, const float* lse,
+                      const float* delta, uint16_t* dqkv, int b, int s, int H, int* status,
+                      cudaStream_t st) {
+  using C = BwdCfg<D>;
+  auto kern = attn_bwd_tc_kernel<D, KV_MAJOR>;
+  static std::once_flag once;
+  static cudaError_t attr = cudaSuccess;
+  std::call_once(once, [&] {
+    attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  });
+  if (attr != cudaSuccess) return MC_ERR_CUDA;
+  dim3 grid((s + 127) / 128, H, b);
+  kern<<<grid, kThreads, C::kSmem, st>>>(tq, td, lse, delta, dqkv, s, H, status);
+  return cudaGetLastError() == cudaSuccess ? MC_OK : MC_ERR_CUDA;
+}
+
+template <int D>
+int launch_bwd_tc(const uint16_t* qkv, const float* lse, const uint16_t* dout, uint16_t* dqkv,
+                  const float* delta, int b, int s, int H, int* status, cudaStream_t st) {
+  const uint64_t a = static_cast<uint64_t>(H) * D;
+  CUtensorMap tq, td;
+  const uint32_t box[3] = {64, 128, 1};
+  const uint64_t dq[3] = {3 * a, static_cast<uint64_t>(s), static_cast<uint64_t>(b)};
+  const uint64_t sq[2] = {3 * a * 2, 3 * a * 2 * static_cast<uint64_t>(s)};
+  const uint64_t dd[3] = {a, static_cast<uint64_t>(s), static_cast<uint64_t>(b)};
+  const uint64_t sd[2] = {a * 2, a * 2 * static_cast<uint64_t>(s)};
+  if (!make_tmap_bf16(&tq, qkv, 3, dq, sq, box) || !make_tmap_bf16(&td, dout, 3, dd, sd, box))
+    return MC_ERR_CUDA;
+  int rc = launch_bwd_tc_one<D, true>(tq, td, lse, delta, dqkv, b, s, H, status, st);
+  if (rc != MC_OK) return rc;
+  return launch_bwd_tc_one<D, false>(tq, td, lse, delta, dqkv, b, s, H, status, st);
+}
+
 template <int D>
 int launch_fwd_tc(const uint16_t* qkv, uint16_t* o, float* lse, int b, int s, int H, int* status,
                   cudaStream_t st) {
@@ -301,6 +629,13 @@ int launch_fwd_tc(const uint16_t* qkv, uint16_t* o, float* lse, int b, int s, in
 }
 
 }  // namespace
+
+int launch_attention_backward_tc(const uint16_t* qkv, const float* lse, const uint16_t* dout,
+                                 uint16_t* dqkv, const float* delta, int b, int s, int H, int d,
+                                 int* status, cudaStream_t st) {
+  return d == 64 ? launch_bwd_tc<64>(qkv, lse, dout, dqkv, delta, b, s, H, status, st)
+                 : launch_bwd_tc<128>(qkv, lse, dout, dqkv, delta, b, s, H, status, st);
+}
 
 int launch_attention_forward_tc(const uint16_t* qkv, uint16_t* o, float* lse, int b, int s, int H,
                                 int d, int* status, cudaStream_t st) {

@@ -320,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int tile = blockIdx.x; tile < g.num_tiles; tile += gridDim.x) {
       int mb, nb;
       tile_coords(tile, g.m_tiles, g.n_tiles, mb, nb);
-      if (!mbar_wait(&acc_full[acc], acc_phase, g.status, kSiteGemmEpilogue)) break;
+      if (!mbar_wait_warp(&acc_full[acc], acc_phase, g.status, kSiteGemmEpilogue)) break;
       tc_fence_after();
       const int row = mb * BM + quarter * 32 + lane;
       const uint32_t t_row = tmem_base + static_cast<uint32_t>(acc * BN) +

@@ -71,6 +71,9 @@ int launch_attention_forward(const uint16_t* qkv, uint16_t* o, float* lse, int b
                              int d, int* status, cudaStream_t stream);
 int launch_attention_forward_tc(const uint16_t* qkv, uint16_t* o, float* lse, int b, int s, int H,
                                 int d, int* status, cudaStream_t stream);
+int launch_attention_backward_tc(const uint16_t* qkv, const float* lse, const uint16_t* dout,
+                                 uint16_t* dqkv, const float* delta, int b, int s, int H, int d,
+                                 int* status, cudaStream_t stream);
 int launch_attention_backward(const uint16_t* qkv, const uint16_t* o, const float* lse,
                               const uint16_t* dout, uint16_t* dqkv, float* delta, int b, int s,
                               int H, int d, int* status, cudaStream_t stream);
