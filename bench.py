@@ -162,6 +162,12 @@ def max_over_ranks(value: float, world: int, device=None) -> float:
     return float(t.item())
 
 
+def replica_throughput(world: int, tokens_per_replica: int, steps: int, max_ms: float) -> float:
+    """Whole-job tokens/s of `world` independent replicas, timed by the
+    slowest rank."""
+    return world * tokens_per_replica * steps / (max_ms / 1e3)
+
+
 def barrier(world: int):
     if world > 1:
         import torch.distributed as dist
@@ -342,23 +348,37 @@ def run_ours(args, world, rank, local):
         run_stage(args, w, device)
         return
     D = dims(w)
-    inp = make_inputs(w)
-    params = {k: bf16_tensor(v, device) for k, v in inp.params.items()}
-    layer = TransformerLayer(**w, params=params, device=device)
+    from layer_inputs import LayerShape, make_layer_inputs
+    n_layers = args.layers
+    layers, params = [], None
+    for li in range(n_layers):
+        inp_l = make_layer_inputs(LayerShape(**w), seed=0, layer=li)
+        p_l = {k: bf16_tensor(v, device) for k, v in inp_l.params.items()}
+        layers.append(TransformerLayer(**w, params=p_l, device=device))
+        if li == 0:
+            inp, params = inp_l, p_l
+    layer = layers[0]
     x = torch.from_numpy(inp.f64("x").reshape(-1, D["h"]).astype(np.float32)).to(device)
     dy = torch.from_numpy(inp.f64("dy").reshape(-1, D["h"]).astype(np.float32)).to(device)
-    y = torch.empty_like(x)
-    dx = torch.empty_like(x)
+    acts = [x] + [torch.empty_like(x) for _ in range(n_layers)]
+    grads = [torch.empty_like(x) for _ in range(n_layers)]
+    y, dx = acts[-1], grads[0]
     st = torch.cuda.current_stream(device)
 
     def step():
-        layer.forward(x, y)
-        layer.backward(dy, dx)
+        # forward through the stack, then backward in reverse (fp32 residual
+        # stream between layers)
+        for li in range(n_layers):
+            layers[li].forward(acts[li], acts[li + 1])
+        g = dy
+        for li in reversed(range(n_layers)):
+            layers[li].backward(g, grads[li], x=acts[li])
+            g = grads[li]
 
     for _ in range(max(args.warmup, 1)):
         step()
     torch.cuda.synchronize(device)
-    status = layer.device_status()
+    status = max(abs(l.device_status()) for l in layers)
     if status != 0:
         raise SystemExit(f"device status {status}: {L.mc_strerror(status)}")
 
@@ -381,8 +401,8 @@ def run_ours(args, world, rank, local):
     ms_total = max_over_ranks(ms_total, world, device)
     ms_step = ms_total / args.steps
     tokens = D["T"]
-    value = world * tokens * args.steps / (ms_total / 1e3)
-    flops = layer_flops(w)
+    value = replica_throughput(world, tokens, args.steps, ms_total)
+    flops = layer_flops(w) * n_layers
     tflops = flops / (ms_step / 1e3) / 1e12
     peaks = measured_peaks()
     peak = peaks.get("bf16_tflops_sustained") or 1710.0
@@ -399,10 +419,15 @@ def run_ours(args, world, rank, local):
     def e2e_step():
         x_d.copy_(x_h, non_blocking=True)
         dy_d.copy_(dy_h, non_blocking=True)
-        layer.forward(x_d, y)
-        layer.backward(dy_d, dx, x=x_d)
-        y_h.copy_(y, non_blocking=True)
-        dx_h.copy_(dx, non_blocking=True)
+        acts[0] = x_d
+        for li in range(n_layers):
+            layers[li].forward(acts[li], acts[li + 1])
+        g = dy_d
+        for li in reversed(range(n_layers)):
+            layers[li].backward(g, grads[li], x=acts[li])
+            g = grads[li]
+        y_h.copy_(acts[-1], non_blocking=True)
+        dx_h.copy_(grads[0], non_blocking=True)
 
     for _ in range(2):
         e2e_step()
@@ -415,7 +440,7 @@ def run_ours(args, world, rank, local):
     a1.record(st)
     torch.cuda.synchronize(device)
     e2e_ms = max_over_ranks(a0.elapsed_time(a1), world, device)
-    e2e_value = world * tokens * args.steps / (e2e_ms / 1e3)
+    e2e_value = replica_throughput(world, tokens, args.steps, e2e_ms)
     h2d = 2 * x.numel() * 4
     d2h = 2 * x.numel() * 4
 
@@ -440,7 +465,9 @@ def run_ours(args, world, rank, local):
         "ms_per_step_p95": sorted(per_step)[max(0, int(round(0.95 * len(per_step))) - 1)],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD_NAMES[args.workload], **w,
+        "config": {"workload": WORKLOAD_NAMES[args.workload]
+                   + (f", stack of {n_layers} layers" if n_layers > 1 else ""), **w,
+                   "layers": n_layers,
                    "l2": "inputs larger than L2 (1.6 GB of bf16 weights plus activations read per step)"
                    if args.workload == "c4" else "working set vs L2 not checked",
                    "parallelism": f"tp{w['tp_parts']} virtual partitions on one GPU; "
@@ -450,10 +477,10 @@ def run_ours(args, world, rank, local):
         "clocks": clk.summary(),
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+        "gpu_launches": LAUNCHES_PER_STEP * n_layers * args.steps,
         "roofline": roofline,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and n_layers == 1:
         prepared = prepare_oracle(w, args.ref_prefix)
         toks = prepared[0].seq_len
         sec = oracle_step(prepared)
@@ -483,9 +510,18 @@ def main():
     ap.add_argument("--ref-prefix", type=int, default=64,
                     help="tokens of the sequence the CPU oracle processes per sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tp-parts", type=int, default=0,
+                    help="override the workload's tensor-parallel partition count")
+    ap.add_argument("--layers", type=int, default=1,
+                    help="time a stack of this many layers (distinct weights) per step")
     args = ap.parse_args()
     if args.warmup < 3 and not args.stage and args.impl == "ours":
         ap.error("--warmup must be >= 3")
+    if args.tp_parts:
+        WORKLOADS[args.workload] = dict(WORKLOADS[args.workload], tp_parts=args.tp_parts)
+        WORKLOAD_NAMES[args.workload] = WORKLOAD_NAMES[args.workload].rsplit(" tp", 1)[0] \
+            + f" tp{args.tp_parts}" if " tp" in WORKLOAD_NAMES[args.workload] else \
+            WORKLOAD_NAMES[args.workload]
     world, rank, local = dist_setup(args)
     if args.impl == "reference":
         run_reference(args, world, rank)
