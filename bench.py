@@ -350,11 +350,14 @@ def run_ours(args, world, rank, local):
     D = dims(w)
     from layer_inputs import LayerShape, make_layer_inputs
     n_layers = args.layers
-    layers, params = [], None
+    layers, params, shared_ws = [], None, None
     for li in range(n_layers):
         inp_l = make_layer_inputs(LayerShape(**w), seed=0, layer=li)
         p_l = {k: bf16_tensor(v, device) for k, v in inp_l.params.items()}
-        layers.append(TransformerLayer(**w, params=p_l, device=device))
+        layers.append(TransformerLayer(**w, params=p_l, device=device, recompute=args.recompute,
+                                       workspace=shared_ws))
+        if args.recompute:
+            shared_ws = layers[-1].ws  # recomputation: one workspace for the whole stack
         if li == 0:
             inp, params = inp_l, p_l
     layer = layers[0]
@@ -402,7 +405,7 @@ def run_ours(args, world, rank, local):
     ms_step = ms_total / args.steps
     tokens = D["T"]
     value = replica_throughput(world, tokens, args.steps, ms_total)
-    flops = layer_flops(w) * n_layers
+    flops = layer_flops(w) * n_layers  # algorithmic: the recomputed forward is not counted
     tflops = flops / (ms_step / 1e3) / 1e12
     peaks = measured_peaks()
     peak = peaks.get("bf16_tflops_sustained") or 1710.0
@@ -468,6 +471,7 @@ def run_ours(args, world, rank, local):
         "config": {"workload": WORKLOAD_NAMES[args.workload]
                    + (f", stack of {n_layers} layers" if n_layers > 1 else ""), **w,
                    "layers": n_layers,
+                   "activation_recompute": bool(args.recompute),
                    "l2": "inputs larger than L2 (1.6 GB of bf16 weights plus activations read per step)"
                    if args.workload == "c4" else "working set vs L2 not checked",
                    "parallelism": f"tp{w['tp_parts']} virtual partitions on one GPU; "
@@ -477,7 +481,10 @@ def run_ours(args, world, rank, local):
         "clocks": clk.summary(),
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": LAUNCHES_PER_STEP * n_layers * args.steps,
+        "gpu_launches": (LAUNCHES_PER_STEP + (7 if args.recompute else 0)) * n_layers * args.steps,
+        "memory": {"saved_bytes_per_layer": layer.saved_bytes,
+                   "workspace_bytes_per_layer": layer.ws_bytes,
+                   "workspace_shared_by_stack": bool(args.recompute)},
         "roofline": roofline,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline and n_layers == 1:
@@ -512,6 +519,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tp-parts", type=int, default=0,
                     help="override the workload's tensor-parallel partition count")
+    ap.add_argument("--recompute", action="store_true",
+                    help="activation recomputation: keep nothing between forward and backward")
     ap.add_argument("--layers", type=int, default=1,
                     help="time a stack of this many layers (distinct weights) per step")
     args = ap.parse_args()

@@ -82,6 +82,14 @@ extern "C" {
 
 /* shape flags */
 #define MC_ACCUMULATE_GRADS 1u /* backward adds into the gradient buffers (+=)    */
+/* Activation recomputation (the Megatron tutorial cf-1.com/news/5344657,
+ * section 6.2, and its --recompute-method block): nothing is kept between
+ * forward and backward -- mc_layer_saved_bytes() is 0 and `saved` may be
+ * NULL; the forward's intermediates live in `ws` (which grows by the size of
+ * the activations) and mc_layer_backward first re-runs the forward kernels
+ * from x.  Results are identical to the default mode.  One `ws` can then be
+ * shared by every layer of a stack run in sequence. */
+#define MC_RECOMPUTE_ACTIVATIONS 2u
 
 typedef struct mc_layer_shape {
   int32_t micro_batch; /* b  (--micro-batch-size)               */
@@ -92,7 +100,7 @@ typedef struct mc_layer_shape {
   int32_t tp_parts;    /* t  (--tensor-model-parallel-size)      */
   int32_t head_dim;    /* 0 => hidden / heads; > 0 decouples a = heads * head_dim
                           from hidden (one tensor-parallel rank's shard run alone) */
-  uint32_t flags;      /* MC_ACCUMULATE_GRADS or 0               */
+  uint32_t flags;      /* MC_ACCUMULATE_GRADS | MC_RECOMPUTE_ACTIVATIONS, or 0 */
 } mc_layer_shape;
 
 /* bf16 parameters (uint16_t bit patterns), device pointers. */
@@ -116,7 +124,8 @@ int mc_layer_check_shape(const mc_layer_shape* shape);
 
 /* Bytes of the `saved` buffer (activations kept from forward to backward):
  * LN1/LN2 outputs and statistics, Q|K|V, attention output and log-sum-exp,
- * x1, fc1 pre-activation and GeLU output.  0 for an illegal shape. */
+ * x1, fc1 pre-activation and GeLU output.  0 for an illegal shape and with
+ * MC_RECOMPUTE_ACTIVATIONS. */
 size_t mc_layer_saved_bytes(const mc_layer_shape* shape);
 
 /* Bytes of the `ws` scratch buffer, including the 256-byte device status

@@ -26,6 +26,7 @@ MC_ERR_ARGUMENT = -9
 MC_ERR_SCRATCH_LIMIT = -10
 
 MC_ACCUMULATE_GRADS = 1
+MC_RECOMPUTE_ACTIVATIONS = 2
 
 MC_EPI_STORE_F32 = 0
 MC_EPI_STORE_BF16 = 1

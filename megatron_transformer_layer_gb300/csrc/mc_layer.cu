@@ -52,7 +52,7 @@ int check_shape(const mc_layer_shape* sh) {
   if (sh->micro_batch <= 0 || sh->seq_len <= 0 || sh->hidden <= 0 || sh->heads <= 0 ||
       sh->ffn_hidden <= 0 || sh->tp_parts <= 0 || sh->head_dim < 0)
     return MC_ERR_SHAPE;
-  if ((sh->flags & ~MC_ACCUMULATE_GRADS) != 0) return MC_ERR_ARGUMENT;
+  if ((sh->flags & ~(MC_ACCUMULATE_GRADS | MC_RECOMPUTE_ACTIVATIONS)) != 0) return MC_ERR_ARGUMENT;
   const int t = sh->tp_parts;
   // Divisibility: hidden size and heads (and the ffn slice of the column
   // split) must divide by the tensor-parallel degree.
@@ -86,7 +86,7 @@ struct Saved {
   float *mu1, *rs1, *lse, *x1, *mu2, *rs2;
 };
 
-Saved plan_saved(const Dims& D, void* p, size_t* bytes) {
+Saved plan_saved(const Dims& D, void* p, size_t* bytes) {  // NOLINT
   Carver c(p);
   Saved S;
   S.ln1 = c.take<uint16_t>(D.T * D.h);
@@ -109,9 +109,14 @@ struct Work {
   int* status;
   uint16_t *dy16, *dhp, *dx1_16, *dO, *dqkv;
   float *dln, *dx1, *delta, *partials;
+  void* recompute_saved;  // activations region when they are recomputed
 };
 
-Work plan_ws(const Dims& D, void* p, size_t* bytes) {
+Saved plan_saved(const Dims& D, void* p, size_t* bytes);
+
+bool recompute(const mc_layer_shape& sh) { return (sh.flags & MC_RECOMPUTE_ACTIVATIONS) != 0; }
+
+Work plan_ws(const Dims& D, bool with_saved, void* p, size_t* bytes) {
   Carver c(p);
   Work W;
   W.status = c.take<int>(kStatusBytes / sizeof(int));
@@ -128,6 +133,12 @@ Work plan_ws(const Dims& D, void* p, size_t* bytes) {
   if (D.h > widest) widest = D.h;
   const size_t col_part = static_cast<size_t>(kColsumRowSplits) * widest;
   W.partials = c.take<float>(ln_part > col_part ? ln_part : col_part);
+  W.recompute_saved = nullptr;
+  if (with_saved) {
+    size_t sb = 0;
+    plan_saved(D, nullptr, &sb);
+    W.recompute_saved = c.take<uint8_t>(sb);
+  }
   if (bytes) *bytes = (c.off + 255) & ~static_cast<size_t>(255);
   return W;
 }
@@ -173,6 +184,7 @@ int mc_layer_check_shape(const mc_layer_shape* shape) { return check_shape(shape
 
 size_t mc_layer_saved_bytes(const mc_layer_shape* shape) {
   if (check_shape(shape) != MC_OK) return 0;
+  if (recompute(*shape)) return 0;  // nothing is kept between the passes
   size_t n = 0;
   plan_saved(dims_of(*shape), nullptr, &n);
   return n;
@@ -181,27 +193,17 @@ size_t mc_layer_saved_bytes(const mc_layer_shape* shape) {
 size_t mc_layer_workspace_bytes(const mc_layer_shape* shape) {
   if (check_shape(shape) != MC_OK) return 0;
   size_t n = 0;
-  plan_ws(dims_of(*shape), nullptr, &n);
+  plan_ws(dims_of(*shape), recompute(*shape), nullptr, &n);
   return n;
 }
 
-int mc_layer_forward(const mc_layer_shape* shape, const mc_layer_weights* w, const float* x,
-                     float* y, void* saved, void* ws, size_t ws_bytes, void* stream) {
-  MC_TRY(check_shape(shape));
-  MC_TRY(check_weights(w));
-  if (!x || !y || !saved || !ws) return MC_ERR_NULLPTR;
-  if (!al(x, 16) || !al(y, 16) || !al(saved, 256) || !al(ws, 256)) return MC_ERR_ALIGN;
-  const Dims D = dims_of(*shape);
-  size_t need = 0;
-  plan_ws(D, nullptr, &need);
-  if (ws_bytes < need) return MC_ERR_WORKSPACE;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const Saved S = plan_saved(D, saved, nullptr);
-  const Work W = plan_ws(D, ws, nullptr);
+namespace mc {
+namespace {
+// F1..F7: the forward launch sequence into the activations `S`.
+int enqueue_forward(const Dims& D, const mc_layer_weights* w, const float* x, float* y,
+                    const Saved& S, const Work& W, cudaStream_t st) {
   const int t = static_cast<int>(D.t);
   const int h = static_cast<int>(D.h);
-
-  if (cudaMemsetAsync(W.status, 0, kStatusBytes, st) != cudaSuccess) return MC_ERR_CUDA;
   // F1  LN1
   MC_TRY(launch_layernorm_forward(x, w->ln1_g, w->ln1_b, S.ln1, S.mu1, S.rs1, D.T, h, W.status, st));
   // F2  QKV (column-parallel: every partition's heads are output columns)
@@ -224,6 +226,26 @@ int mc_layer_forward(const mc_layer_shape* shape, const mc_layer_weights* w, con
                      w->b_fc2, S.x1, D.h, 0, t, W.status, st));
   return MC_OK;
 }
+}  // namespace
+}  // namespace mc
+
+int mc_layer_forward(const mc_layer_shape* shape, const mc_layer_weights* w, const float* x,
+                     float* y, void* saved, void* ws, size_t ws_bytes, void* stream) {
+  MC_TRY(check_shape(shape));
+  MC_TRY(check_weights(w));
+  const bool rc_mode = recompute(*shape);
+  if (!x || !y || (!saved && !rc_mode) || !ws) return MC_ERR_NULLPTR;
+  if (!al(x, 16) || !al(y, 16) || (saved && !al(saved, 256)) || !al(ws, 256)) return MC_ERR_ALIGN;
+  const Dims D = dims_of(*shape);
+  size_t need = 0;
+  plan_ws(D, rc_mode, nullptr, &need);
+  if (ws_bytes < need) return MC_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const Work W = plan_ws(D, rc_mode, ws, nullptr);
+  const Saved S = plan_saved(D, rc_mode ? W.recompute_saved : saved, nullptr);
+  if (cudaMemsetAsync(W.status, 0, kStatusBytes, st) != cudaSuccess) return MC_ERR_CUDA;
+  return enqueue_forward(D, w, x, y, S, W, st);
+}
 
 int mc_layer_backward(const mc_layer_shape* shape, const mc_layer_weights* w, const float* x,
                       const float* dy, const void* saved, float* dx, const mc_layer_grads* grads,
@@ -231,16 +253,22 @@ int mc_layer_backward(const mc_layer_shape* shape, const mc_layer_weights* w, co
   MC_TRY(check_shape(shape));
   MC_TRY(check_weights(w));
   MC_TRY(check_grads(grads));
-  if (!x || !dy || !saved || !dx || !ws) return MC_ERR_NULLPTR;
-  if (!al(x, 16) || !al(dy, 16) || !al(dx, 16) || !al(saved, 256) || !al(ws, 256))
+  const bool rc_mode = recompute(*shape);
+  if (!x || !dy || (!saved && !rc_mode) || !dx || !ws) return MC_ERR_NULLPTR;
+  if (!al(x, 16) || !al(dy, 16) || !al(dx, 16) || (saved && !al(saved, 256)) || !al(ws, 256))
     return MC_ERR_ALIGN;
   const Dims D = dims_of(*shape);
   size_t need = 0;
-  plan_ws(D, nullptr, &need);
+  plan_ws(D, rc_mode, nullptr, &need);
   if (ws_bytes < need) return MC_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const Saved S = plan_saved(D, const_cast<void*>(saved), nullptr);
-  const Work W = plan_ws(D, ws, nullptr);
+  const Work W = plan_ws(D, rc_mode, ws, nullptr);
+  const Saved S = plan_saved(D, rc_mode ? W.recompute_saved : const_cast<void*>(saved), nullptr);
+  if (rc_mode) {
+    // Activation recomputation: rebuild F1..F7's activations from x.  The
+    // recomputed y lands in dx1's buffer, which B3 overwrites later.
+    MC_TRY(enqueue_forward(D, w, x, W.dx1, S, W, st));
+  }
   const int acc = (shape->flags & MC_ACCUMULATE_GRADS) ? 1 : 0;
   const int t = static_cast<int>(D.t);
   const int h = static_cast<int>(D.h);

@@ -26,18 +26,28 @@ class TransformerLayer:
     """
 
     def __init__(self, micro_batch, seq_len, hidden, heads, ffn_hidden, tp_parts=1, head_dim=0,
-                 params=None, device="cuda", accumulate_grads=False):
+                 params=None, device="cuda", accumulate_grads=False, recompute=False,
+                 workspace=None):
+        flags = (L.MC_ACCUMULATE_GRADS if accumulate_grads else 0) | \
+            (L.MC_RECOMPUTE_ACTIVATIONS if recompute else 0)
         self.shape = L.make_shape(micro_batch, seq_len, hidden, heads, ffn_hidden, tp_parts,
-                                  head_dim, L.MC_ACCUMULATE_GRADS if accumulate_grads else 0)
+                                  head_dim, flags)
         _check(L.mc_layer_check_shape(self.shape), "mc_layer_check_shape")
         self.device = torch.device(device)
         self.tokens = micro_batch * seq_len
         self.hidden = hidden
         self.saved_bytes = L.mc_layer_saved_bytes(self.shape)
         self.ws_bytes = L.mc_layer_workspace_bytes(self.shape)
-        # uint8 buffers: the caching allocator returns >= 512-byte aligned blocks
-        self.saved = torch.empty(self.saved_bytes, dtype=torch.uint8, device=self.device)
-        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=self.device)
+        # uint8 buffers: the caching allocator returns >= 512-byte aligned blocks.
+        # With recomputation nothing is saved and a workspace may be shared by
+        # the layers of a stack (pass the same `workspace` tensor to each).
+        self.saved = (torch.empty(self.saved_bytes, dtype=torch.uint8, device=self.device)
+                      if self.saved_bytes else None)
+        if workspace is not None:
+            assert workspace.numel() >= self.ws_bytes
+            self.ws = workspace
+        else:
+            self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=self.device)
         self.params = params
         self.weights = L.make_weights(params) if params is not None else None
         d = head_dim if head_dim else hidden // heads

@@ -133,3 +133,22 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(L, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not found"):
         L.lib()
+
+
+def test_recompute_flag_plans_no_saved_buffer():
+    base = L.make_shape(2, 100, 768, 12, 3072, 2)
+    rc = L.make_shape(2, 100, 768, 12, 3072, 2, 0, L.MC_RECOMPUTE_ACTIVATIONS)
+    both = L.make_shape(2, 100, 768, 12, 3072, 2, 0,
+                        L.MC_RECOMPUTE_ACTIVATIONS | L.MC_ACCUMULATE_GRADS)
+    assert L.mc_layer_check_shape(rc) == L.MC_OK and L.mc_layer_check_shape(both) == L.MC_OK
+    assert L.mc_layer_saved_bytes(rc) == 0
+    assert L.mc_layer_workspace_bytes(rc) >= L.mc_layer_workspace_bytes(base) + \
+        L.mc_layer_saved_bytes(base)
+    # NULL `saved` is accepted in recompute mode (the checks get past it to the
+    # workspace-size rule, still before any launch) and rejected otherwise
+    w = _weights()
+    wsb = L.mc_layer_workspace_bytes(rc)
+    assert L.mc_layer_forward(rc, w, 0x20000000, 0x30000000, None, 0x50000000,
+                              wsb - 256) == L.MC_ERR_WORKSPACE
+    assert L.mc_layer_forward(base, w, 0x20000000, 0x30000000, None, 0x50000000,
+                              wsb) == L.MC_ERR_NULLPTR

@@ -132,3 +132,41 @@ def test_config2_stack_of_12_layers():
 def test_config3(t):
     """b8 s1024 h2048 H16 (d128) f8192."""
     _check_layer(make_layer_inputs(LayerShape(8, 1024, 2048, 16, 8192, t)), t, f"c3 t={t}")
+
+
+def test_activation_recomputation_matches_default_mode():
+    """MC_RECOMPUTE_ACTIVATIONS: nothing saved between the passes, the
+    backward re-runs the forward; results identical to the default mode, and
+    one workspace shared by a 3-layer stack."""
+    from megatron_transformer_layer_gb300.layer import TransformerLayer
+    from gpu_util import dev_bf16
+    shape = LayerShape(2, 129, 1024, 8, 4096, 2)
+    inps = [make_layer_inputs(shape, seed=6, layer=l, init=NONTRIVIAL_INIT) for l in range(3)]
+    x = dev_f32_from_bits(inps[0].x.reshape(-1, 1024))
+    dy = dev_f32_from_bits(inps[0].dy.reshape(-1, 1024))
+
+    def run(recompute, workspace=None):
+        layers = [TransformerLayer(2, 129, 1024, 8, 4096, 2, recompute=recompute,
+                                   workspace=workspace,
+                                   params={k: dev_bf16(v) for k, v in inp.params.items()})
+                  for inp in inps]
+        acts = [x]
+        for ly in layers:
+            acts.append(ly.forward(acts[-1]))
+        g = dy
+        for i in reversed(range(3)):
+            g = layers[i].backward(g, x=acts[i])
+        torch.cuda.synchronize()
+        assert all(ly.device_status() == 0 for ly in layers)
+        return to_f64(acts[-1]), to_f64(g), [{k: to_f64(v) for k, v in ly.grads.items()} for ly in layers]
+
+    y0, dx0, G0 = run(False)
+    probe = TransformerLayer(2, 129, 1024, 8, 4096, 2, recompute=True,
+                             params={k: dev_bf16(v) for k, v in inps[0].params.items()})
+    assert probe.saved is None
+    shared = torch.empty(probe.ws_bytes, dtype=torch.uint8, device=DEV)
+    y1, dx1, G1 = run(True, shared)
+    assert np.array_equal(y0, y1) and np.array_equal(dx0, dx1)
+    for a, b in zip(G0, G1):
+        for k in a:
+            assert np.array_equal(a[k], b[k]), k
