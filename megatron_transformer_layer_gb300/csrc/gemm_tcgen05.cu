@@ -6,9 +6,10 @@
 //   warp 0      TMA producer: 128B-swizzled A/B boxes -> STAGES-deep smem ring
 //   warp 1      allocates TMEM (2 accumulators of BN fp32 columns) and, from
 //               one thread, issues tcgen05.mma (M = 128, N = BN, K = 16)
-//   warps 2..5  epilogue: tcgen05.ld the accumulator, apply the fused
-//               epilogue, store to global memory; the second accumulator lets
-//               the next tile's main loop run underneath.
+//   warps 2..9  epilogue: tcgen05.ld the accumulator, apply the fused
+//               epilogue, store to global memory; two warps per TMEM lane
+//               quarter, each taking half of the tile's columns; the second
+//               accumulator lets the next tile's main loop run underneath.
 //
 // Operands may be K-major ([rows, K] in memory) or MN-major ([K, rows] in
 // memory); the latter is how the dgrad (W used as [K, N]) and wgrad
@@ -33,8 +34,9 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 64;  // one 128-byte swizzle atom of bf16 along K
-constexpr int kThreads = 192;
-constexpr int kEpilogueThreads = 128;
+constexpr int kEpilogueWarps = 8;  // two per TMEM lane quarter, splitting the columns
+constexpr int kThreads = 64 + 32 * kEpilogueWarps;
+constexpr int kEpilogueThreads = 32 * kEpilogueWarps;
 
 struct GemmArgs {
   int M, N, K;
@@ -314,7 +316,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int quarter = warp & 3;  // TMEM lanes [32 q, 32 q + 32)
+    const int quarter = warp & 3;      // TMEM lanes [32 q, 32 q + 32)
+    const int half = (warp - 2) >> 2;  // which half of the tile's columns
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < g.num_tiles; tile += gridDim.x) {
@@ -326,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t t_row = tmem_base + static_cast<uint32_t>(acc * BN) +
                              (static_cast<uint32_t>(quarter * 32) << 16);
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
+      for (int c = half * (BN / 64); c < (half + 1) * (BN / 64); ++c) {
         float v[32];
         tmem_ld_32x32b_x32(t_row + c * 32, v);
         const int col0 = nb * BN + c * 32;
