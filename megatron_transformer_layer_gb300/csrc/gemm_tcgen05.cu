@@ -42,6 +42,7 @@ struct GemmArgs {
   int M, N, K;
   int num_kb;
   int m_tiles, n_tiles, num_tiles;
+  int m_pairs, num_units;  // paired variant: units = (pair of M-tiles, N-tile)
   void* out;
   int64_t ldc;
   const __nv_bfloat16* bias;
@@ -173,7 +174,12 @@ __device__ __forceinline__ void epilogue32(float (&v)[32], int row, int col0, co
   }
 }
 
-template <bool A_MN, bool B_MN, int BN, int EPI>
+// PAIR: CTAs run in clusters of two along M.  Both CTAs of a cluster work on
+// the same N-tile (M-tiles 2p and 2p + 1), so each loads one half of the
+// BN x BK B tile and multicasts it to both; a stage is refilled only when
+// both CTAs' MMAs have finished with it (each MMA commit arrives on the
+// stage's empty barrier in both CTAs).  L2 reads of B halve.
+template <bool A_MN, bool B_MN, int BN, int EPI, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB, const GemmArgs g) {
@@ -195,11 +201,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t crank = PAIR ? cluster_ctarank() : 0u;
+  // Work units: output tiles, or (PAIR) pairs of M-tiles sharing an N-tile.
+  const int unit0 = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int ustride = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  const int n_units = PAIR ? g.num_units : g.num_tiles;
+  auto unit_coords = [&](int u, int& mb, int& nb) {
+    if constexpr (PAIR) {
+      int mp;
+      tile_coords(u, g.m_pairs, g.n_tiles, mp, nb);
+      mb = 2 * mp + static_cast<int>(crank);
+    } else {
+      tile_coords(u, g.m_tiles, g.n_tiles, mb, nb);
+    }
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], PAIR ? 2 : 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&acc_full[i], 1);
@@ -218,6 +238,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // The peer's multicasts and commits target this CTA's barriers: both CTAs
+  // must have initialised theirs first.
+  if constexpr (PAIR) cluster_sync();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -226,9 +249,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       int issued = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < g.num_tiles; tile += gridDim.x) {
+      for (int u = unit0; ok && u < n_units; u += ustride) {
         int mb, nb;
-        tile_coords(tile, g.m_tiles, g.n_tiles, mb, nb);
+        unit_coords(u, mb, nb);
         for (int kb = 0; kb < g.num_kb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, g.status, kSiteGemmProducer)) {
             ok = false;
@@ -244,7 +267,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(a_dst, &tmA, &full[stage], mb * BM, k0);
             tma_load_2d(a_dst + 64 * BK * 2, &tmA, &full[stage], mb * BM + 64, k0);
           }
-          if constexpr (!B_MN) {
+          if constexpr (PAIR) {
+            // this CTA's half of B, to both CTAs
+            if constexpr (!B_MN) {
+              tma_load_2d_mc(b_dst + crank * (BN / 2) * (BK * 2), &tmB, &full[stage], k0,
+                             nb * BN + static_cast<int>(crank) * (BN / 2), 0x3);
+            } else {
+#pragma unroll
+              for (int j = 0; j < BN / 128; ++j) {
+                const int jj = static_cast<int>(crank) * (BN / 128) + j;
+                tma_load_2d_mc(b_dst + jj * 64 * BK * 2, &tmB, &full[stage], nb * BN + jj * 64, k0,
+                               0x3);
+              }
+            }
+          } else if constexpr (!B_MN) {
             tma_load_2d(b_dst, &tmB, &full[stage], k0, nb * BN);
           } else {
 #pragma unroll
@@ -275,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < g.num_tiles; tile += gridDim.x) {
+      for (int u = unit0; ok && u < n_units; u += ustride) {
         if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, g.status, kSiteGemmMma)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
@@ -299,7 +335,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      : smem_desc_sw128(b0 + k * 32, 16, 1024);
             umma_bf16(d_tmem, ad, bd, kIdesc, (kb | k) != 0 ? 1u : 0u);
           }
-          umma_commit(&empty[stage]);
+          if constexpr (PAIR)
+            umma_commit_mc(&empty[stage], 0x3);  // frees the stage in both CTAs
+          else
+            umma_commit(&empty[stage]);
           if (++stage == S) {
             stage = 0;
             phase ^= 1u;
@@ -320,9 +359,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int half = (warp - 2) >> 2;  // which half of the tile's columns
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = blockIdx.x; tile < g.num_tiles; tile += gridDim.x) {
+    for (int u = unit0; u < n_units; u += ustride) {
       int mb, nb;
-      tile_coords(tile, g.m_tiles, g.n_tiles, mb, nb);
+      unit_coords(u, mb, nb);
       if (!mbar_wait_warp(&acc_full[acc], acc_phase, g.status, kSiteGemmEpilogue)) break;
       tc_fence_after();
       const int row = mb * BM + quarter * 32 + lane;
@@ -348,6 +387,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, Cfg::kTmemCols);
   }
+  // Neither CTA may exit while its peer can still write into its shared
+  // memory or arrive on its barriers.
+  if constexpr (PAIR) cluster_sync();
 }
 
 // ------------------------------------------------------------------ host side
@@ -381,48 +423,84 @@ bool make_tmap(CUtensorMap* map, const void* base, uint64_t inner, uint64_t oute
   return r == CUDA_SUCCESS;
 }
 
-template <bool A_MN, bool B_MN, int BN, int EPI>
+template <bool A_MN, bool B_MN, int BN, int EPI, bool PAIR>
 int launch_variant(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& g,
                    cudaStream_t stream) {
   using Cfg = GemmCfg<BN>;
-  auto kern = gemm_tcgen05_kernel<A_MN, B_MN, BN, EPI>;
+  auto kern = gemm_tcgen05_kernel<A_MN, B_MN, BN, EPI, PAIR>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
+  static int max_clusters = 0;
   std::call_once(once, [&] {
     attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     Cfg::kSmemBytes);
+    if (attr_err == cudaSuccess && PAIR) {
+      // Clusters of two that fit on the device at once (pairs must share a
+      // GPC, so this can be below half the SM count).
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute at[1];
+      at[0].id = cudaLaunchAttributeClusterDimension;
+      at[0].val.clusterDim.x = 2;
+      at[0].val.clusterDim.y = 1;
+      at[0].val.clusterDim.z = 1;
+      cfg.gridDim = dim3(2 * num_sms(), 1, 1);
+      cfg.blockDim = dim3(kThreads, 1, 1);
+      cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+      cfg.attrs = at;
+      cfg.numAttrs = 1;
+      attr_err = cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg);
+      if (attr_err == cudaSuccess && max_clusters < 1) attr_err = cudaErrorInvalidConfiguration;
+    }
   });
   if (attr_err != cudaSuccess) return MC_ERR_CUDA;
-  const int grid = g.num_tiles < num_sms() ? g.num_tiles : num_sms();
-  kern<<<grid, kThreads, Cfg::kSmemBytes, stream>>>(ta, tb, g);
+  if constexpr (PAIR) {
+    const int clusters = g.num_units < max_clusters ? g.num_units : max_clusters;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * clusters, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+    cfg.stream = stream;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, ta, tb, g) != cudaSuccess) return MC_ERR_CUDA;
+  } else {
+    const int grid = g.num_tiles < num_sms() ? g.num_tiles : num_sms();
+    kern<<<grid, kThreads, Cfg::kSmemBytes, stream>>>(ta, tb, g);
+  }
   return cudaGetLastError() == cudaSuccess ? MC_OK : MC_ERR_CUDA;
 }
 
-template <int BN, int EPI>
+template <int BN, int EPI, bool PAIR>
 int dispatch_layouts(int a_layout, int b_layout, const CUtensorMap& ta, const CUtensorMap& tb,
                      const GemmArgs& g, cudaStream_t stream) {
-  if (!a_layout && !b_layout) return launch_variant<false, false, BN, EPI>(ta, tb, g, stream);
-  if (!a_layout && b_layout) return launch_variant<false, true, BN, EPI>(ta, tb, g, stream);
-  if (a_layout && b_layout) return launch_variant<true, true, BN, EPI>(ta, tb, g, stream);
-  return launch_variant<true, false, BN, EPI>(ta, tb, g, stream);
+  if (!a_layout && !b_layout) return launch_variant<false, false, BN, EPI, PAIR>(ta, tb, g, stream);
+  if (!a_layout && b_layout) return launch_variant<false, true, BN, EPI, PAIR>(ta, tb, g, stream);
+  if (a_layout && b_layout) return launch_variant<true, true, BN, EPI, PAIR>(ta, tb, g, stream);
+  return launch_variant<true, false, BN, EPI, PAIR>(ta, tb, g, stream);
 }
 
-template <int BN>
+template <int BN, bool PAIR>
 int dispatch_epilogue(int epi, int a_layout, int b_layout, const CUtensorMap& ta,
                       const CUtensorMap& tb, const GemmArgs& g, cudaStream_t stream) {
   switch (epi) {
     case MC_EPI_STORE_F32:
-      return dispatch_layouts<BN, MC_EPI_STORE_F32>(a_layout, b_layout, ta, tb, g, stream);
+      return dispatch_layouts<BN, MC_EPI_STORE_F32, PAIR>(a_layout, b_layout, ta, tb, g, stream);
     case MC_EPI_STORE_BF16:
-      return dispatch_layouts<BN, MC_EPI_STORE_BF16>(a_layout, b_layout, ta, tb, g, stream);
+      return dispatch_layouts<BN, MC_EPI_STORE_BF16, PAIR>(a_layout, b_layout, ta, tb, g, stream);
     case MC_EPI_BIAS_BF16:
-      return dispatch_layouts<BN, MC_EPI_BIAS_BF16>(a_layout, b_layout, ta, tb, g, stream);
+      return dispatch_layouts<BN, MC_EPI_BIAS_BF16, PAIR>(a_layout, b_layout, ta, tb, g, stream);
     case MC_EPI_BIAS_GELU:
-      return dispatch_layouts<BN, MC_EPI_BIAS_GELU>(a_layout, b_layout, ta, tb, g, stream);
+      return dispatch_layouts<BN, MC_EPI_BIAS_GELU, PAIR>(a_layout, b_layout, ta, tb, g, stream);
     case MC_EPI_BIAS_RESID_F32:
-      return dispatch_layouts<BN, MC_EPI_BIAS_RESID_F32>(a_layout, b_layout, ta, tb, g, stream);
+      return dispatch_layouts<BN, MC_EPI_BIAS_RESID_F32, PAIR>(a_layout, b_layout, ta, tb, g,
+                                                               stream);
     case MC_EPI_GELU_BWD:
-      return dispatch_layouts<BN, MC_EPI_GELU_BWD>(a_layout, b_layout, ta, tb, g, stream);
+      return dispatch_layouts<BN, MC_EPI_GELU_BWD, PAIR>(a_layout, b_layout, ta, tb, g, stream);
     default:
       return MC_ERR_ARGUMENT;
   }
@@ -475,14 +553,17 @@ int launch_gemm(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda,
       (needs_aux && ldaux < N))
     return MC_ERR_ARGUMENT;
 
-  // Wide tiles when there are enough of them to fill the machine.
+  // Wide tiles when there are enough of them to fill the machine; wide-tile
+  // problems with at least two M-tiles run as multicast pairs.
   const int64_t m_tiles = (M + BM - 1) / BM;
   const int bn = ((N % 256 == 0) && m_tiles * (N / 256) >= num_sms()) ? 256 : 128;
+  const bool pair = bn == 256 && m_tiles >= 2;
 
   CUtensorMap ta, tb;
   bool ok = a_layout == 0 ? make_tmap(&ta, A, K, M, lda, BK, BM)
                           : make_tmap(&ta, A, M, K, lda, 64, BK);
-  ok = ok && (b_layout == 0 ? make_tmap(&tb, B, K, N, ldb, BK, bn)
+  // K-major B: a paired CTA loads half of the tile's rows
+  ok = ok && (b_layout == 0 ? make_tmap(&tb, B, K, N, ldb, BK, pair ? bn / 2 : bn)
                             : make_tmap(&tb, B, N, K, ldb, 64, BK));
   if (!ok) return MC_ERR_CUDA;
 
@@ -496,6 +577,8 @@ int launch_gemm(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda,
   const int64_t tiles = m_tiles * g.n_tiles;
   if (tiles > (1 << 30)) return MC_ERR_UNSUPPORTED;
   g.num_tiles = static_cast<int>(tiles);
+  g.m_pairs = static_cast<int>((m_tiles + 1) / 2);
+  g.num_units = g.m_pairs * g.n_tiles;
   g.out = out;
   g.ldc = ldc;
   g.bias = reinterpret_cast<const __nv_bfloat16*>(bias);
@@ -503,8 +586,9 @@ int launch_gemm(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda,
   g.ldaux = ldaux;
   g.accumulate = accumulate;
   g.status = status;
-  return bn == 256 ? dispatch_epilogue<256>(epi, a_layout, b_layout, ta, tb, g, stream)
-                   : dispatch_epilogue<128>(epi, a_layout, b_layout, ta, tb, g, stream);
+  if (pair) return dispatch_epilogue<256, true>(epi, a_layout, b_layout, ta, tb, g, stream);
+  return bn == 256 ? dispatch_epilogue<256, false>(epi, a_layout, b_layout, ta, tb, g, stream)
+                   : dispatch_epilogue<128, false>(epi, a_layout, b_layout, ta, tb, g, stream);
 }
 
 }  // namespace mc
