@@ -28,7 +28,8 @@
 namespace mc {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 192;     // forward: producer, MMA, 4 softmax warps
+constexpr int kBwdThreads = 320;  // backward: producer, MMA, 8 compute warps
 constexpr int BQ = 128;   // query rows per CTA
 constexpr int BKV = 128;  // keys per block
 constexpr float kLog2e = 1.4426950408889634f;
@@ -299,7 +300,7 @@ template <int D>
 struct BwdCfg {
   static constexpr int kChunks = D / 64;
   static constexpr int kTile = 128 * D * 2;
-  static constexpr int kUsed = 6 * kTile + 4 * 128 * 4 + 16 * 8 + 1024;
+  static constexpr int kUsed = 6 * kTile + 4 * 128 * 4 + 24 * 8 + 1024;
   static constexpr int kSmem = kUsed > 116 * 1024 ? kUsed : 116 * 1024;
   static constexpr uint32_t kTmemCols = 512;
 };
@@ -312,7 +313,7 @@ __device__ __forceinline__ void tmem_ld2(uint32_t a, uint32_t b, float* va, floa
 }
 
 template <int D, bool KV_MAJOR>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv,
                        const __grid_constant__ CUtensorMap tm_do, const float* __restrict__ lse,
                        const float* __restrict__ delta, uint16_t* __restrict__ dqkv, int s, int H,
@@ -337,8 +338,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* p_full = bars + 6;
   uint64_t* mma_done = bars + 7;
   uint64_t* drain = bars + 8;
-  uint64_t* lse_ready = bars + 9;  // [2]: the 128 compute threads staged lse/delta
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 11);
+  uint64_t* lse_ready = bars + 9;  // [2]: the compute threads staged lse/delta
+  uint64_t* ld_done = bars + 11;   // [4]: both warps of a lane quarter read S, dP
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int a = H * D;
@@ -359,11 +361,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&st_empty[i], 1);
     }
     mbar_init(s_full, 1);
-    mbar_init(p_full, 128);
+    mbar_init(p_full, 256);
     mbar_init(mma_done, 1);
     mbar_init(drain, 1);
-    mbar_init(&lse_ready[0], 128);
-    mbar_init(&lse_ready[1], 128);
+    mbar_init(&lse_ready[0], 256);
+    mbar_init(&lse_ready[1], 256);
+    for (int q = 0; q < 4; ++q) mbar_init(&ld_done[q], 64);
     fence_mbar_init();
     tma_prefetch_desc(&tm_qkv);
     tma_prefetch_desc(&tm_do);
@@ -466,8 +469,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ---------------------------------------------------------- compute
+    // Two warps per TMEM lane quarter; `half` picks 64 of the 128 columns
+    // (the backward's per-element work needs no reduction along the row).
     const int quarter = warp & 3;
-    const int t = quarter * 32 + lane;  // thread index among the 128 compute threads
+    const int half = (warp - 2) >> 2;
+    const int t = quarter * 32 + lane;  // row within the block
     const int r = r0 + t;               // this thread's key (KV_MAJOR) or query
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const float scale2 = rsqrtf(static_cast<float>(D)) * kLog2e;
@@ -485,8 +491,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       float* dl = sD + (i & 1) * 128;
       if (KV_MAJOR) {
         const int qq = c0 + t;
-        l2[t] = qq < s ? L[qq] * kLog2e : 0.f;
-        dl[t] = qq < s ? Dl[qq] : 0.f;
+        if (half == 0) {
+          l2[t] = qq < s ? L[qq] * kLog2e : 0.f;
+          dl[t] = qq < s ? Dl[qq] : 0.f;
+        }
         mbar_arrive(&lse_ready[i & 1]);
         if (!mbar_wait_warp(&lse_ready[i & 1], (i >> 1) & 1, status, kSiteAttention)) {
           ok = false;
@@ -501,10 +509,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Visible (row, column) pairs: KV_MAJOR: query >= key; else key <= query;
       // both within the sequence.
       const bool edge = KV_MAJOR ? (c0 < r0 + 127 || c0 + 128 > s) : (c0 + 127 > r0 || c0 + 128 > s);
-#pragma unroll 1
-      for (int ch = 0; ch < 4; ++ch) {
-        float sv[32], dv[32];
-        tmem_ld2(tS + lane_off + ch * 32, tdP + lane_off + ch * 32, sv, dv);
+      // Read this warp's 64 columns of S and dP, then wait until the other
+      // warp of the lane quarter has read its own: P / dS are written into the
+      // first 64 columns of the same buffers, which span both warps' columns.
+      float sva[64], dva[64];
+      tmem_ld_32x32b_x32_nowait(tS + lane_off + half * 64, sva);
+      tmem_ld_32x32b_x32_nowait(tS + lane_off + half * 64 + 32, sva + 32);
+      tmem_ld_32x32b_x32_nowait(tdP + lane_off + half * 64, dva);
+      tmem_ld_32x32b_x32_nowait(tdP + lane_off + half * 64 + 32, dva + 32);
+      tmem_ld_wait();
+      mbar_arrive(&ld_done[quarter]);
+      if (!mbar_wait_warp(&ld_done[quarter], i & 1, status, kSiteAttention)) {
+        ok = false;
+        break;
+      }
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int ch = 2 * half + cc;
+        const float* sv = sva + cc * 32;
+        const float* dv = dva + cc * 32;
         uint32_t pw[16], dw[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
@@ -525,7 +548,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           pw[e / 2] = pack_bf16x2(p[0], p[1]);
           dw[e / 2] = pack_bf16x2(ds[0], ds[1]);
         }
-        // Columns [16 ch, 16 ch + 16) of each buffer were read in chunks <= ch.
         if (KV_MAJOR) tmem_st_32x32b_x16(tS + lane_off + ch * 16, pw);
         tmem_st_32x32b_x16((KV_MAJOR ? tdP : tS) + lane_off + ch * 16, dw);
       }
@@ -544,7 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float mul = (KV_MAJOR && w == 0) ? 1.f : scale;
         const int col = KV_MAJOR ? (w == 0 ? 2 * a : a) + hh * D : hh * D;
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = half * (D / 64); c < (half + 1) * (D / 64); ++c) {
           float v[32];
           tmem_ld_32x32b_x32(tacc + lane_off + c * 32, v);
           if (r < s) {
@@ -585,7 +607,7 @@ int launch_bwd_tc_one(const CUtensorMap& tq, const CUtensorMap& td, const float*
   });
   if (attr != cudaSuccess) return MC_ERR_CUDA;
   dim3 grid((s + 127) / 128, H, b);
-  kern<<<grid, kThreads, C::kSmem, st>>>(tq, td, lse, delta, dqkv, s, H, status);
+  kern<<<grid, kBwdThreads, C::kSmem, st>>>(tq, td, lse, delta, dqkv, s, H, status);
   return cudaGetLastError() == cudaSuccess ? MC_OK : MC_ERR_CUDA;
 }
 

@@ -215,17 +215,30 @@ __global__ void __launch_bounds__(kLnBwdThreads) ln_bwd_kernel(
 }
 
 // out_j[c] = (accumulate ? out_j[c] : 0) + sum_b partials[b][j][c], j < nsum.
-__global__ void reduce_partials_kernel(const float* __restrict__ partials, int nblocks, int nsum,
-                                       int64_t n, float* out0, float* out1, float* out2,
-                                       int accumulate) {
-  const int64_t c = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+// A CTA of 256 threads owns 32 columns of one sum j: thread (c, r) adds the
+// partial rows r, r + 8, ... of column c, then the 8 row-group sums are
+// combined in a fixed order through shared memory (deterministic).
+__global__ void __launch_bounds__(256) reduce_partials_kernel(const float* __restrict__ partials,
+                                                              int nblocks, int nsum, int64_t n,
+                                                              float* out0, float* out1, float* out2,
+                                                              int accumulate) {
+  __shared__ float part[8][33];
+  const int cl = threadIdx.x & 31, rg = threadIdx.x >> 5;
+  const int64_t c = blockIdx.x * 32 + cl;
   const int j = blockIdx.y;
-  if (c >= n || j >= nsum) return;
-  float* out = j == 0 ? out0 : (j == 1 ? out1 : out2);
-  if (!out) return;
   float s = 0.f;
-  for (int b = 0; b < nblocks; ++b) s += partials[(static_cast<int64_t>(b) * nsum + j) * n + c];
-  out[c] = accumulate ? out[c] + s : s;
+  if (c < n && j < nsum)
+    for (int b = rg; b < nblocks; b += 8) s += partials[(static_cast<int64_t>(b) * nsum + j) * n + c];
+  part[rg][cl] = s;
+  __syncthreads();
+  if (rg == 0 && c < n && j < nsum) {
+    float* out = j == 0 ? out0 : (j == 1 ? out1 : out2);
+    if (!out) return;
+    float t = 0.f;
+#pragma unroll
+    for (int r = 0; r < 8; ++r) t += part[r][cl];
+    out[c] = accumulate ? out[c] + t : t;
+  }
 }
 
 // Column partial sums of a [rows, n] matrix over kColsumRowSplits row ranges;
@@ -369,7 +382,7 @@ int launch_layernorm_backward(const float* dout, const float* x, const float* me
     default: return MC_ERR_UNSUPPORTED;
   }
   if (rc != MC_OK) return rc;
-  dim3 rgrid(static_cast<unsigned>((h + 255) / 256), want ? 3 : 2);
+  dim3 rgrid(static_cast<unsigned>((h + 31) / 32), want ? 3 : 2);
   reduce_partials_kernel<<<rgrid, 256, 0, st>>>(partials, grid, 3, h, dgamma, dbeta, colsum_dx,
                                                 accumulate);
   return cudaGetLastError() == cudaSuccess ? MC_OK : MC_ERR_CUDA;
@@ -390,7 +403,7 @@ int launch_colsum(const void* in, bool in_bf16, int64_t rows, int64_t n, float* 
   else
     colsum_partial_kernel<false><<<grid, 128, 0, st>>>(in, rows, n, partials, bf16_copy);
   if (cudaGetLastError() != cudaSuccess) return MC_ERR_CUDA;
-  dim3 rgrid(static_cast<unsigned>((n + 255) / 256), 1);
+  dim3 rgrid(static_cast<unsigned>((n + 31) / 32), 1);
   reduce_partials_kernel<<<rgrid, 256, 0, st>>>(partials, splits, 1, n, out, nullptr, nullptr,
                                                 accumulate);
   return cudaGetLastError() == cudaSuccess ? MC_OK : MC_ERR_CUDA;
