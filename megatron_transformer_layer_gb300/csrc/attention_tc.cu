@@ -306,6 +306,17 @@ struct BwdCfg {
 };
 
 // Loads 32 columns of two TMEM rows (this thread's lane) with one wait.
+template <int D>
+struct DqCfg {
+  static constexpr int kChunks = D / 64;
+  static constexpr int kTile = 128 * D * 2;
+  // Q, dO, three K stages, two V stages, barriers, alignment slack
+  static constexpr int kUsed = 7 * kTile + 24 * 8 + 1024;
+  static constexpr int kSmem = kUsed > 116 * 1024 ? kUsed : 116 * 1024;
+  static constexpr uint32_t kTmemCols = 512;
+  static_assert(kUsed <= 227 * 1024, "dq kernel shared memory");
+};
+
 __device__ __forceinline__ void tmem_ld2(uint32_t a, uint32_t b, float* va, float* vb) {
   tmem_ld_32x32b_x32_nowait(a, va);
   tmem_ld_32x32b_x32_nowait(b, vb);
@@ -594,6 +605,255 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 }
 
+// dQ, with the next block's products overlapping this block's dS.
+//   TMEM: S [0, 128), dP [128, 256), dQ [256, 256 + D), dS (bf16) [384, 448).
+// The compute warps read S_j and dP_j into registers and release them at once
+// (s_free), so S_{j+1} = Q K_{j+1}^T and dP_{j+1} = dO V_{j+1}^T run while
+// dS_j is formed; dQ += dS_j K_j follows when dS_j is in TMEM (ds_full), and
+// its completion (ds_free) lets dS_{j+1} be written.
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv,
+                          const __grid_constant__ CUtensorMap tm_do, const float* __restrict__ lse,
+                          const float* __restrict__ delta, uint16_t* __restrict__ dqkv, int s,
+                          int H, int* status) {
+  using C = DqCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  // K_j is needed until dQ_j, V_j only until dP_j: separate rings (K 3 deep,
+  // V 2 deep) keep the next blocks' loads ahead of the overlapped products.
+  uint8_t* sQ = smem;
+  uint8_t* sdO = smem + C::kTile;
+  uint8_t* sK[3] = {smem + 2 * C::kTile, smem + 3 * C::kTile, smem + 4 * C::kTile};
+  uint8_t* sV[2] = {smem + 5 * C::kTile, smem + 6 * C::kTile};
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 7 * C::kTile);
+  uint64_t* r_full = bars + 0;
+  uint64_t* k_full = bars + 1;    // [3]
+  uint64_t* k_empty = bars + 4;   // [3]
+  uint64_t* v_full = bars + 7;    // [2]
+  uint64_t* v_empty = bars + 9;   // [2]
+  uint64_t* s_full = bars + 11;
+  uint64_t* s_free = bars + 12;
+  uint64_t* ds_full = bars + 13;
+  uint64_t* ds_free = bars + 14;
+  uint64_t* drain = bars + 15;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int a = H * D;
+  const int hh = blockIdx.y, bi = blockIdx.z;
+  const int nblk = (s + 127) / 128;
+  const int qb = nblk - 1 - static_cast<int>(blockIdx.x);  // heaviest first
+  const int q0 = qb * 128;
+  const int count = qb + 1;  // key blocks 0 .. qb
+
+  if (threadIdx.x == 0) {
+    mbar_init(r_full, 1);
+    for (int i = 0; i < 3; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(s_free, 256);
+    mbar_init(ds_full, 256);
+    mbar_init(ds_free, 1);
+    mbar_init(drain, 1);
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_qkv);
+    tma_prefetch_desc(&tm_do);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tS = tmem, tdP = tmem + 128, tdQ = tmem + 256, tdS = tmem + 384;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // -------------------------------------------------------- producer
+      mbar_arrive_expect_tx(r_full, 2 * C::kTile);
+      for (int c = 0; c < C::kChunks; ++c) {
+        tma_load_3d(sQ + c * 16384, &tm_qkv, r_full, hh * D + c * 64, q0, bi);
+        tma_load_3d(sdO + c * 16384, &tm_do, r_full, hh * D + c * 64, q0, bi);
+      }
+      int k_issued = 0, v_issued = 0;
+      for (int j = 0; j < count; ++j) {
+        const int ks = j % 3, kph = (j / 3) & 1, vs = j & 1, vph = (j >> 1) & 1;
+        if (!mbar_wait(&k_empty[ks], kph ^ 1u, status, kSiteAttention)) break;
+        mbar_arrive_expect_tx(&k_full[ks], C::kTile);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(sK[ks] + c * 16384, &tm_qkv, &k_full[ks], a + hh * D + c * 64, j * 128, bi);
+        ++k_issued;
+        if (!mbar_wait(&v_empty[vs], vph ^ 1u, status, kSiteAttention)) break;
+        mbar_arrive_expect_tx(&v_full[vs], C::kTile);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(sV[vs] + c * 16384, &tm_qkv, &v_full[vs], 2 * a + hh * D + c * 64, j * 128,
+                      bi);
+        ++v_issued;
+      }
+      // Copies still in flight must land before the CTA exits: the last
+      // K loads (up to 3) and V loads (up to 2).
+      mbar_wait(r_full, 0, status, kSiteAttention, 200000000ull, false);
+      for (int j = k_issued - 1; j >= 0 && j >= k_issued - 3; --j)
+        mbar_wait(&k_full[j % 3], (j / 3) & 1, status, kSiteAttention, 200000000ull, false);
+      for (int j = v_issued - 1; j >= 0 && j >= v_issued - 2; --j)
+        mbar_wait(&v_full[j & 1], (j >> 1) & 1, status, kSiteAttention, 200000000ull, false);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // -------------------------------------------------------- MMA issuer
+      constexpr uint32_t kIdescSq = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t kIdescAcc = idesc_bf16_f32(128, D, false, true);
+      bool ok = mbar_wait(r_full, 0, status, kSiteAttention);
+      const uint32_t qb0 = smem_u32(sQ), dob = smem_u32(sdO);
+      for (int j = 0; ok && j <= count; ++j) {
+        if (j < count) {
+          const int ks = j % 3, vs = j & 1;
+          if (!mbar_wait(&k_full[ks], (j / 3) & 1, status, kSiteAttention)) break;
+          if (!mbar_wait(&v_full[vs], (j >> 1) & 1, status, kSiteAttention)) break;
+          // S / dP of block j - 1 are in the compute warps' registers.
+          if (j > 0 && !mbar_wait(s_free, (j - 1) & 1, status, kSiteAttention)) break;
+          tc_fence_after();
+          const uint32_t kb = smem_u32(sK[ks]), vb = smem_u32(sV[vs]);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+            umma_bf16(tS, smem_desc_sw128(qb0 + off, 16, 1024), smem_desc_sw128(kb + off, 16, 1024),
+                      kIdescSq, kk > 0 ? 1u : 0u);
+            umma_bf16(tdP, smem_desc_sw128(dob + off, 16, 1024),
+                      smem_desc_sw128(vb + off, 16, 1024), kIdescSq, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(s_full);
+          umma_commit(&v_empty[vs]);  // V_j is done once dP_j is
+        }
+        if (j > 0) {
+          const int pj = j - 1, pks = pj % 3;
+          if (!mbar_wait(ds_full, pj & 1, status, kSiteAttention)) break;
+          tc_fence_after();
+          const uint32_t kb = smem_u32(sK[pks]);
+#pragma unroll
+          for (int kk = 0; kk < 128 / 16; ++kk)
+            umma_bf16_ts(tdQ, tdS + kk * 8, smem_desc_sw128(kb + kk * 2048, 16384, 1024), kIdescAcc,
+                         (pj > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(&k_empty[pks]);
+          umma_commit(ds_free);
+        }
+      }
+      umma_commit(drain);
+      mbar_wait(drain, 0, status, kSiteAttention, 200000000ull, false);
+    }
+  } else {
+    // ---------------------------------------------------------- compute
+    const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;   // 64 of the block's 128 key columns
+    const int r = q0 + quarter * 32 + lane;  // this thread's query row
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const float scale2 = rsqrtf(static_cast<float>(D)) * kLog2e;
+    const float* L = lse + (static_cast<int64_t>(bi) * H + hh) * s;
+    const float* Dl = delta + (static_cast<int64_t>(bi) * H + hh) * s;
+    const float my_l2 = r < s ? L[r] * kLog2e : 0.f;
+    const float my_d = r < s ? Dl[r] : 0.f;
+    bool ok = true;
+    for (int j = 0; j < count; ++j) {
+      if (!mbar_wait_warp(s_full, j & 1, status, kSiteAttention)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float sv[64], dv[64];
+      tmem_ld_32x32b_x32_nowait(tS + lane_off + half * 64, sv);
+      tmem_ld_32x32b_x32_nowait(tS + lane_off + half * 64 + 32, sv + 32);
+      tmem_ld_32x32b_x32_nowait(tdP + lane_off + half * 64, dv);
+      tmem_ld_32x32b_x32_nowait(tdP + lane_off + half * 64 + 32, dv + 32);
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(s_free);
+      const int c0 = j * 128 + half * 64;
+      const bool edge = c0 + 63 > q0 || c0 + 64 > s;
+      uint32_t dw[32];
+#pragma unroll
+      for (int e = 0; e < 64; e += 2) {
+        float ds[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          float pv = fast_exp2(fmaf(sv[e + u], scale2, -my_l2));
+          if (edge) {
+            const int col = c0 + e + u;
+            pv = (col <= r && col < s) ? pv : 0.f;
+          }
+          ds[u] = pv * (dv[e + u] - my_d);
+        }
+        dw[e / 2] = pack_bf16x2(ds[0], ds[1]);
+      }
+      // dS_{j-1} must have been consumed by its dQ product.
+      if (j > 0 && !mbar_wait_warp(ds_free, (j - 1) & 1, status, kSiteAttention)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      tmem_st_32x32b_x32(tdS + lane_off + half * 32, dw);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(ds_full);
+    }
+    if (ok && mbar_wait_warp(ds_free, (count - 1) & 1, status, kSiteAttention)) {
+      tc_fence_after();
+      const float scale = rsqrtf(static_cast<float>(D));
+      const int64_t base = (static_cast<int64_t>(bi) * s + r) * 3 * static_cast<int64_t>(a);
+#pragma unroll 1
+      for (int c = half * (D / 64); c < (half + 1) * (D / 64); ++c) {
+        float v[32];
+        tmem_ld_32x32b_x32(tdQ + lane_off + c * 32, v);
+        if (r < s) {
+          uint4* dst = reinterpret_cast<uint4*>(dqkv + base + hh * D + c * 32);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            uint4 wv;
+            wv.x = pack_bf16x2(v[8 * k + 0] * scale, v[8 * k + 1] * scale);
+            wv.y = pack_bf16x2(v[8 * k + 2] * scale, v[8 * k + 3] * scale);
+            wv.z = pack_bf16x2(v[8 * k + 4] * scale, v[8 * k + 5] * scale);
+            wv.w = pack_bf16x2(v[8 * k + 6] * scale, v[8 * k + 7] * scale);
+            dst[k] = wv;
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <int D>
+int launch_bwd_dq_tc(const CUtensorMap& tq, const CUtensorMap& td, const float* lse,
+                     const float* delta, uint16_t* dqkv, int b, int s, int H, int* status,
+                     cudaStream_t st) {
+  using C = DqCfg<D>;
+  auto kern = attn_bwd_dq_tc_kernel<D>;
+  static std::once_flag once;
+  static cudaError_t attr = cudaSuccess;
+  std::call_once(once, [&] {
+    attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  });
+  if (attr != cudaSuccess) return MC_ERR_CUDA;
+  dim3 grid((s + 127) / 128, H, b);
+  kern<<<grid, kBwdThreads, C::kSmem, st>>>(tq, td, lse, delta, dqkv, s, H, status);
+  return cudaGetLastError() == cudaSuccess ? MC_OK : MC_ERR_CUDA;
+}
+
 template <int D, bool KV_MAJOR>
 int launch_bwd_tc_one(const CUtensorMap& tq, const CUtensorMap& td, const float* lse,
                       const float* delta, uint16_t* dqkv, int b, int s, int H, int* status,
@@ -625,7 +885,7 @@ int launch_bwd_tc(const uint16_t* qkv, const float* lse, const uint16_t* dout, u
     return MC_ERR_CUDA;
   int rc = launch_bwd_tc_one<D, true>(tq, td, lse, delta, dqkv, b, s, H, status, st);
   if (rc != MC_OK) return rc;
-  return launch_bwd_tc_one<D, false>(tq, td, lse, delta, dqkv, b, s, H, status, st);
+  return launch_bwd_dq_tc<D>(tq, td, lse, delta, dqkv, b, s, H, status, st);
 }
 
 template <int D>
