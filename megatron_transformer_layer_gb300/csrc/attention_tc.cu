@@ -62,13 +62,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sV[2] = {smem + 3 * C::kTile, smem + 4 * C::kTile};
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 5 * C::kTile);
   uint64_t* q_full = bars + 0;
-  uint64_t* kv_full = bars + 1;   // [2]
-  uint64_t* kv_empty = bars + 3;  // [2]
+  uint64_t* k_full = bars + 1;    // [2]  K_j is released after S_j,
+  uint64_t* k_empty = bars + 3;   // [2]
   uint64_t* s_full = bars + 5;    // [2]
   uint64_t* p_full = bars + 7;    // [2]
   uint64_t* o_ready = bars + 9;
   uint64_t* drain = bars + 10;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 11);
+  uint64_t* v_full = bars + 11;   // [2]  V_j only after PV_j
+  uint64_t* v_empty = bars + 13;  // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int a = H * D;
@@ -80,8 +82,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&kv_full[i], 1);
-      mbar_init(&kv_empty[i], 1);
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], 128);
     }
@@ -107,21 +111,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive_expect_tx(q_full, C::kTile);
       for (int c = 0; c < C::kChunks; ++c)
         tma_load_3d(sQ + c * 16384, &tm, q_full, hh * D + c * 64, q0, bi);
-      int issued = 0;
+      int k_issued = 0, v_issued = 0;
       for (int j = 0; j < n_kb; ++j) {
         const int st = j & 1;
-        if (!mbar_wait(&kv_empty[st], ((j >> 1) & 1) ^ 1u, status, kSiteAttention)) break;
-        mbar_arrive_expect_tx(&kv_full[st], 2 * C::kTile);
-        for (int c = 0; c < C::kChunks; ++c) {
-          tma_load_3d(sK[st] + c * 16384, &tm, &kv_full[st], a + hh * D + c * 64, j * BKV, bi);
-          tma_load_3d(sV[st] + c * 16384, &tm, &kv_full[st], 2 * a + hh * D + c * 64, j * BKV, bi);
-        }
-        ++issued;
+        const uint32_t ph = ((j >> 1) & 1) ^ 1u;
+        if (!mbar_wait(&k_empty[st], ph, status, kSiteAttention)) break;
+        mbar_arrive_expect_tx(&k_full[st], C::kTile);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(sK[st] + c * 16384, &tm, &k_full[st], a + hh * D + c * 64, j * BKV, bi);
+        ++k_issued;
+        if (!mbar_wait(&v_empty[st], ph, status, kSiteAttention)) break;
+        mbar_arrive_expect_tx(&v_full[st], C::kTile);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(sV[st] + c * 16384, &tm, &v_full[st], 2 * a + hh * D + c * 64, j * BKV, bi);
+        ++v_issued;
       }
       // Copies still in flight must land before the CTA exits.
       mbar_wait(q_full, 0, status, kSiteAttention, 200000000ull, false);
-      for (int j = issued - 1; j >= 0 && j >= issued - 2; --j)
-        mbar_wait(&kv_full[j & 1], (j >> 1) & 1, status, kSiteAttention, 200000000ull, false);
+      for (int j = k_issued - 1; j >= 0 && j >= k_issued - 2; --j)
+        mbar_wait(&k_full[j & 1], (j >> 1) & 1, status, kSiteAttention, 200000000ull, false);
+      for (int j = v_issued - 1; j >= 0 && j >= v_issued - 2; --j)
+        mbar_wait(&v_full[j & 1], (j >> 1) & 1, status, kSiteAttention, 200000000ull, false);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -133,7 +143,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; ok && j <= n_kb; ++j) {
         if (j < n_kb) {
           const int st = j & 1;
-          if (!mbar_wait(&kv_full[st], (j >> 1) & 1, status, kSiteAttention)) break;
+          if (!mbar_wait(&k_full[st], (j >> 1) & 1, status, kSiteAttention)) break;
           // S buffer st was last read (as P) by PV_{j-2}.
           if (j >= 2 && !mbar_wait(o_ready, (j - 2) & 1, status, kSiteAttention)) break;
           tc_fence_after();
@@ -145,10 +155,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                       smem_desc_sw128(k_base + off, 16, 1024), kIdescQK, kk > 0 ? 1u : 0u);
           }
           umma_commit(&s_full[st]);
+          umma_commit(&k_empty[st]);
         }
         if (j >= 1) {
           const int pj = j - 1, pst = pj & 1;
           if (!mbar_wait(&p_full[pst], (pj >> 1) & 1, status, kSiteAttention)) break;
+          if (!mbar_wait(&v_full[pst], (pj >> 1) & 1, status, kSiteAttention)) break;
           tc_fence_after();
           const uint32_t v_base = smem_u32(sV[pst]);
 #pragma unroll
@@ -159,7 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                          smem_desc_sw128(v_base + kk * 2048, 16384, 1024), kIdescPV,
                          (pj > 0 || kk > 0) ? 1u : 0u);
           }
-          umma_commit(&kv_empty[pst]);
+          umma_commit(&v_empty[pst]);
           umma_commit(o_ready);
         }
       }
