@@ -381,6 +381,22 @@ def run_ours(args, world, rank, local):
     for _ in range(max(args.warmup, 1)):
         step()
     torch.cuda.synchronize(device)
+    if args.graph:
+        # Capture one whole step (every launch of the stack's forward and
+        # backward) and replay it: for launch-bound small shapes.  The first
+        # calls above did the one-time set-up, and the step allocates nothing.
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        torch.cuda.synchronize(device)
+        eager_step = step
+
+        def step():  # noqa: F811
+            graph.replay()
+
+        step()
+        torch.cuda.synchronize(device)
+        del eager_step
     status = max(abs(l.device_status()) for l in layers)
     if status != 0:
         raise SystemExit(f"device status {status}: {L.mc_strerror(status)}")
@@ -472,6 +488,7 @@ def run_ours(args, world, rank, local):
                    + (f", stack of {n_layers} layers" if n_layers > 1 else ""), **w,
                    "layers": n_layers,
                    "activation_recompute": bool(args.recompute),
+                   "cuda_graph": bool(args.graph),
                    "l2": "inputs larger than L2 (1.6 GB of bf16 weights plus activations read per step)"
                    if args.workload == "c4" else "working set vs L2 not checked",
                    "parallelism": f"tp{w['tp_parts']} virtual partitions on one GPU; "
@@ -519,6 +536,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tp-parts", type=int, default=0,
                     help="override the workload's tensor-parallel partition count")
+    ap.add_argument("--graph", action="store_true",
+                    help="capture one step in a CUDA graph and time its replays")
     ap.add_argument("--recompute", action="store_true",
                     help="activation recomputation: keep nothing between forward and backward")
     ap.add_argument("--layers", type=int, default=1,

@@ -170,3 +170,35 @@ def test_activation_recomputation_matches_default_mode():
     for a, b in zip(G0, G1):
         for k in a:
             assert np.array_equal(a[k], b[k]), k
+
+
+def test_cuda_graph_capture_matches_eager():
+    """The C ABI enqueues only launches and memsets on the caller's stream, so
+    a whole forward + backward can be captured in a CUDA graph (after a first
+    uncaptured call has done the one-time set-up) and replayed on new inputs."""
+    shape = LayerShape(1, 96, 768, 12, 3072, 2)
+    inp = make_layer_inputs(shape, seed=8, init=NONTRIVIAL_INIT)
+    inp2 = make_layer_inputs(shape, seed=9, init=NONTRIVIAL_INIT)
+    inp2.params = inp.params  # same weights; new x and dy
+    layer, _, _, _ = run_layer(inp)
+    x = dev_f32_from_bits(inp.x.reshape(-1, 768))
+    dy = dev_f32_from_bits(inp.dy.reshape(-1, 768))
+    y = torch.empty_like(x)
+    dx = torch.empty_like(x)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        layer.forward(x, y)
+        layer.backward(dy, dx, x=x)
+    torch.cuda.synchronize()
+    # new inputs into the captured buffers, replay, compare with eager
+    x.copy_(dev_f32_from_bits(inp2.x.reshape(-1, 768)))
+    dy.copy_(dev_f32_from_bits(inp2.dy.reshape(-1, 768)))
+    graph.replay()
+    torch.cuda.synchronize()
+    y_g, dx_g = to_f64(y), to_f64(dx)
+    G_g = {k: to_f64(v) for k, v in layer.grads.items()}
+    _, y_e, dx_e, G_e = run_layer(inp2, layer=layer)
+    assert np.array_equal(y_g.reshape(y_e.shape), y_e)
+    assert np.array_equal(dx_g.reshape(dx_e.shape), dx_e)
+    for k in G_e:
+        assert np.array_equal(G_g[k], G_e[k]), k
