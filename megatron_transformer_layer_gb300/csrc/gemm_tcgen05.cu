@@ -52,12 +52,25 @@ struct GemmArgs {
   int* status;
 };
 
-template <int BN>
+// Execution modes of the GEMM kernel.
+//   kSolo   one CTA per 128 x BN tile
+//   kDuo    clusters of two CTAs run one 256 x BN tile (M-tiles 2p, 2p + 1 of
+//           one N-tile) with tcgen05.mma.cta_group::2: each CTA holds only its
+//           own 128 rows of A and its half of B, and the even CTA issues the
+//           MMAs for both.  Per flop each SM receives 2/3 of the operand bytes
+//           of a 128 x 256 tile, which is what keeps the tensor pipe fed from L2.
+constexpr int kSolo = 0, kDuo = 1;
+
+template <int BN, int MODE>
 struct GemmCfg {
-  static constexpr int kStages = BN == 256 ? 4 : 6;
   static constexpr int kABytes = BM * BK * 2;
-  static constexpr int kBBytes = BN * BK * 2;
+  // B bytes held per CTA and stage
+  static constexpr int kBBytes = (MODE == kDuo ? BN / 2 : BN) * BK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStages = kStageBytes > 32768 ? 4 : 6;
+  // bytes that complete one stage's full barrier (kDuo: both CTAs' copies
+  // land on the even CTA's barrier)
+  static constexpr int kTxBytes = MODE == kDuo ? 2 * kStageBytes : kStageBytes;
   static constexpr int kTmemCols = 2 * BN;
   // ring + barriers (full, empty, acc_full x2, acc_empty x2, drain) + tmem slot
   static constexpr int kBarrierBytes = (2 * kStages + 5) * 8 + 8;
@@ -174,18 +187,21 @@ __device__ __forceinline__ void epilogue32(float (&v)[32], int row, int col0, co
   }
 }
 
-// PAIR: CTAs run in clusters of two along M.  Both CTAs of a cluster work on
-// the same N-tile (M-tiles 2p and 2p + 1), so each loads one half of the
-// BN x BK B tile and multicasts it to both; a stage is refilled only when
-// both CTAs' MMAs have finished with it (each MMA commit arrives on the
-// stage's empty barrier in both CTAs).  L2 reads of B halve.
-template <bool A_MN, bool B_MN, int BN, int EPI, bool PAIR>
+// kDuo: CTAs run in clusters of two along M.  Each CTA loads its A rows and
+// its half of B into its own shared memory, both signalling the even CTA's
+// full barrier; the even CTA issues 256 x BN x 16 MMAs that read both CTAs'
+// operands and write each CTA's 128 accumulator rows into its own TMEM, and
+// its commits arrive on the barriers of both CTAs (a stage is refilled, an
+// accumulator read, only then); the odd CTA's epilogue releases the
+// accumulator on the even CTA's barrier.
+template <bool A_MN, bool B_MN, int BN, int EPI, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB, const GemmArgs g) {
-  using Cfg = GemmCfg<BN>;
+  using Cfg = GemmCfg<BN, MODE>;
   constexpr int S = Cfg::kStages;
-  constexpr uint32_t kIdesc = idesc_bf16_f32(BM, BN, A_MN, B_MN);
+  constexpr bool kDuoMode = MODE == kDuo;
+  constexpr uint32_t kIdesc = idesc_bf16_f32(kDuoMode ? 2 * BM : BM, BN, A_MN, B_MN);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -201,13 +217,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t crank = PAIR ? cluster_ctarank() : 0u;
-  // Work units: output tiles, or (PAIR) pairs of M-tiles sharing an N-tile.
-  const int unit0 = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
-  const int ustride = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
-  const int n_units = PAIR ? g.num_units : g.num_tiles;
+  const uint32_t crank = kDuoMode ? cluster_ctarank() : 0u;
+  const bool issuer_cta = crank == 0u;  // kDuo: the CTA that issues the pair's MMAs
+  // Work units: output tiles, or (pairs) pairs of M-tiles sharing an N-tile.
+  const int unit0 = kDuoMode ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int ustride = kDuoMode ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  const int n_units = kDuoMode ? g.num_units : g.num_tiles;
   auto unit_coords = [&](int u, int& mb, int& nb) {
-    if constexpr (PAIR) {
+    if constexpr (kDuoMode) {
       int mp;
       tile_coords(u, g.m_pairs, g.n_tiles, mp, nb);
       mb = 2 * mp + static_cast<int>(crank);
@@ -219,11 +236,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], PAIR ? 2 : 1);
+      mbar_init(&empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], kEpilogueThreads);
+      // kDuo: one arrival per epilogue warp of both CTAs
+      mbar_init(&acc_empty[i], kDuoMode ? 2 * kEpilogueWarps : kEpilogueThreads);
     }
     mbar_init(drain, 1);
     fence_mbar_init();
@@ -231,20 +249,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmB);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, Cfg::kTmemCols);
-    tmem_relinquish();
+    if constexpr (kDuoMode) {
+      tmem_alloc_pair(tmem_slot, Cfg::kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_slot, Cfg::kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  // The peer's multicasts and commits target this CTA's barriers: both CTAs
-  // must have initialised theirs first.
-  if constexpr (PAIR) cluster_sync();
+  // The peer's copies, commits and arrivals target this CTA's
+  // barriers: both CTAs must have initialised theirs first.
+  if constexpr (kDuoMode) cluster_sync();
 
   if (warp == 0) {
     if (lane == 0) {
       // ---------------------------------------------------------- producer
+      // kDuo: the even CTA's full barriers, which count both CTAs' bytes
+      const uint32_t full0_pair = kDuoMode ? mapa_shared(full, 0) : 0u;
       int stage = 0;
       uint32_t phase = 0;
       int issued = 0;
@@ -257,35 +282,43 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[stage], Cfg::kStageBytes);
           const int k0 = kb * BK;
           uint8_t* a_dst = sA + stage * Cfg::kABytes;
           uint8_t* b_dst = sB + stage * Cfg::kBBytes;
-          if constexpr (!A_MN) {
-            tma_load_2d(a_dst, &tmA, &full[stage], k0, mb * BM);
-          } else {
-            tma_load_2d(a_dst, &tmA, &full[stage], mb * BM, k0);
-            tma_load_2d(a_dst + 64 * BK * 2, &tmA, &full[stage], mb * BM + 64, k0);
-          }
-          if constexpr (PAIR) {
-            // this CTA's half of B, to both CTAs
+          if constexpr (kDuoMode) {
+            if (issuer_cta) mbar_arrive_expect_tx(&full[stage], Cfg::kTxBytes);
+            const uint32_t fb = full0_pair + static_cast<uint32_t>(stage) * 8u;
+            if constexpr (!A_MN) {
+              tma_load_2d_pair(a_dst, &tmA, fb, k0, mb * BM);
+            } else {
+              tma_load_2d_pair(a_dst, &tmA, fb, mb * BM, k0);
+              tma_load_2d_pair(a_dst + 64 * BK * 2, &tmA, fb, mb * BM + 64, k0);
+            }
+            // this CTA's half of the B tile: N rows [nb BN + crank BN/2, + BN/2)
             if constexpr (!B_MN) {
-              tma_load_2d_mc(b_dst + crank * (BN / 2) * (BK * 2), &tmB, &full[stage], k0,
-                             nb * BN + static_cast<int>(crank) * (BN / 2), 0x3);
+              tma_load_2d_pair(b_dst, &tmB, fb, k0, nb * BN + static_cast<int>(crank) * (BN / 2));
             } else {
 #pragma unroll
               for (int j = 0; j < BN / 128; ++j) {
                 const int jj = static_cast<int>(crank) * (BN / 128) + j;
-                tma_load_2d_mc(b_dst + jj * 64 * BK * 2, &tmB, &full[stage], nb * BN + jj * 64, k0,
-                               0x3);
+                tma_load_2d_pair(b_dst + j * 64 * BK * 2, &tmB, fb, nb * BN + jj * 64, k0);
               }
             }
-          } else if constexpr (!B_MN) {
-            tma_load_2d(b_dst, &tmB, &full[stage], k0, nb * BN);
           } else {
+            mbar_arrive_expect_tx(&full[stage], Cfg::kTxBytes);
+            if constexpr (!A_MN) {
+              tma_load_2d(a_dst, &tmA, &full[stage], k0, mb * BM);
+            } else {
+              tma_load_2d(a_dst, &tmA, &full[stage], mb * BM, k0);
+              tma_load_2d(a_dst + 64 * BK * 2, &tmA, &full[stage], mb * BM + 64, k0);
+            }
+            if constexpr (!B_MN) {
+              tma_load_2d(b_dst, &tmB, &full[stage], k0, nb * BN);
+            } else {
 #pragma unroll
-            for (int j = 0; j < BN / 64; ++j)
-              tma_load_2d(b_dst + j * 64 * BK * 2, &tmB, &full[stage], nb * BN + j * 64, k0);
+              for (int j = 0; j < BN / 64; ++j)
+                tma_load_2d(b_dst + j * 64 * BK * 2, &tmB, &full[stage], nb * BN + j * 64, k0);
+            }
           }
           ++issued;
           if (++stage == S) {
@@ -294,17 +327,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      // Wait for this thread's copies still in flight (the last use of each
-      // stage) before the CTA may exit.
-      const int pending = issued < S ? issued : S;
-      for (int i = 0; i < pending; ++i) {
-        stage = stage == 0 ? S - 1 : stage - 1;
-        if (stage == S - 1) phase ^= 1u;
-        mbar_wait(&full[stage], phase, g.status, kSiteGemmDrain, 200000000ull, false);
+      // Wait for the copies still in flight (the last use of each stage)
+      // before the CTA may exit.  kDuo: the even CTA's full barriers count
+      // both CTAs' copies, and the closing cluster barrier holds the odd CTA
+      // until the even one has seen them land.
+      if (!kDuoMode || issuer_cta) {
+        const int pending = issued < S ? issued : S;
+        for (int i = 0; i < pending; ++i) {
+          stage = stage == 0 ? S - 1 : stage - 1;
+          if (stage == S - 1) phase ^= 1u;
+          mbar_wait(&full[stage], phase, g.status, kSiteGemmDrain, 200000000ull, false);
+        }
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && (!kDuoMode || issuer_cta)) {
       // ---------------------------------------------------------- MMA issuer
       int stage = 0;
       uint32_t phase = 0;
@@ -312,7 +349,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int u = unit0; ok && u < n_units; u += ustride) {
-        if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, g.status, kSiteGemmMma)) break;
+        const bool got = kDuoMode ? mbar_wait<true>(&acc_empty[acc], acc_phase ^ 1u, g.status,
+                                                    kSiteGemmMma)
+                                  : mbar_wait(&acc_empty[acc], acc_phase ^ 1u, g.status,
+                                              kSiteGemmMma);
+        if (!got) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
         // The K loop runs over the partitions' K-slices in order; all of them
@@ -333,10 +374,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      : smem_desc_sw128(a0 + k * 32, 16, 1024);
             const uint64_t bd = B_MN ? smem_desc_sw128(b0 + k * 2048, 64 * BK * 2, 1024)
                                      : smem_desc_sw128(b0 + k * 32, 16, 1024);
-            umma_bf16(d_tmem, ad, bd, kIdesc, (kb | k) != 0 ? 1u : 0u);
+            if constexpr (kDuoMode)
+              umma_bf16_pair(d_tmem, ad, bd, kIdesc, (kb | k) != 0 ? 1u : 0u);
+            else
+              umma_bf16(d_tmem, ad, bd, kIdesc, (kb | k) != 0 ? 1u : 0u);
           }
-          if constexpr (PAIR)
-            umma_commit_mc(&empty[stage], 0x3);  // frees the stage in both CTAs
+          if constexpr (kDuoMode)
+            umma_commit_pair_mc(&empty[stage], 0x3);  // frees the stage in both CTAs
           else
             umma_commit(&empty[stage]);
           if (++stage == S) {
@@ -345,18 +389,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (!ok) break;
-        umma_commit(&acc_full[acc]);
+        if constexpr (kDuoMode)
+          umma_commit_pair_mc(&acc_full[acc], 0x3);
+        else
+          umma_commit(&acc_full[acc]);
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
       }
       // Every MMA issued by this thread must be complete before TMEM is freed.
-      umma_commit(drain);
+      if constexpr (kDuoMode)
+        umma_commit_pair_mc(drain, 0x3);
+      else
+        umma_commit(drain);
+      mbar_wait(drain, 0, g.status, kSiteGemmDrain, 200000000ull, false);
+    } else if (kDuoMode && lane == 0) {
+      // The odd CTA's TMEM is written by the even CTA's MMAs.
       mbar_wait(drain, 0, g.status, kSiteGemmDrain, 200000000ull, false);
     }
   } else {
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;      // TMEM lanes [32 q, 32 q + 32)
     const int half = (warp - 2) >> 2;  // which half of the tile's columns
+    const uint32_t acc_empty_pair = kDuoMode ? mapa_shared(acc_empty, 0) : 0u;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int u = unit0; u < n_units; u += ustride) {
@@ -375,21 +429,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (row < g.M && col0 < g.N) epilogue32<EPI>(v, row, col0, g);
       }
       tc_fence_before();
-      mbar_arrive(&acc_empty[acc]);
+      if constexpr (kDuoMode) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(acc_empty_pair + static_cast<uint32_t>(acc) * 8u);
+      } else {
+        mbar_arrive(&acc_empty[acc]);
+      }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
   }
 
   tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem_base, Cfg::kTmemCols);
+  if constexpr (kDuoMode) {
+    // Both CTAs are done with both CTAs' TMEM, barriers and shared memory
+    // before the pair frees its tensor memory together and exits.
+    cluster_sync();
+    if (warp == 1) {
+      tc_fence_after();
+      tmem_dealloc_pair(tmem_base, Cfg::kTmemCols);
+    }
+  } else {
+    __syncthreads();
+    if (warp == 1) {
+      tc_fence_after();
+      tmem_dealloc(tmem_base, Cfg::kTmemCols);
+    }
   }
-  // Neither CTA may exit while its peer can still write into its shared
-  // memory or arrive on its barriers.
-  if constexpr (PAIR) cluster_sync();
 }
 
 // ------------------------------------------------------------------ host side
@@ -423,11 +489,12 @@ bool make_tmap(CUtensorMap* map, const void* base, uint64_t inner, uint64_t oute
   return r == CUDA_SUCCESS;
 }
 
-template <bool A_MN, bool B_MN, int BN, int EPI, bool PAIR>
+template <bool A_MN, bool B_MN, int BN, int EPI, int MODE>
 int launch_variant(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& g,
                    cudaStream_t stream) {
-  using Cfg = GemmCfg<BN>;
-  auto kern = gemm_tcgen05_kernel<A_MN, B_MN, BN, EPI, PAIR>;
+  using Cfg = GemmCfg<BN, MODE>;
+  constexpr bool PAIR = MODE == kDuo;
+  auto kern = gemm_tcgen05_kernel<A_MN, B_MN, BN, EPI, MODE>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   static int max_clusters = 0;
@@ -475,32 +542,32 @@ int launch_variant(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs&
   return cudaGetLastError() == cudaSuccess ? MC_OK : MC_ERR_CUDA;
 }
 
-template <int BN, int EPI, bool PAIR>
+template <int BN, int EPI, int MODE>
 int dispatch_layouts(int a_layout, int b_layout, const CUtensorMap& ta, const CUtensorMap& tb,
                      const GemmArgs& g, cudaStream_t stream) {
-  if (!a_layout && !b_layout) return launch_variant<false, false, BN, EPI, PAIR>(ta, tb, g, stream);
-  if (!a_layout && b_layout) return launch_variant<false, true, BN, EPI, PAIR>(ta, tb, g, stream);
-  if (a_layout && b_layout) return launch_variant<true, true, BN, EPI, PAIR>(ta, tb, g, stream);
-  return launch_variant<true, false, BN, EPI, PAIR>(ta, tb, g, stream);
+  if (!a_layout && !b_layout) return launch_variant<false, false, BN, EPI, MODE>(ta, tb, g, stream);
+  if (!a_layout && b_layout) return launch_variant<false, true, BN, EPI, MODE>(ta, tb, g, stream);
+  if (a_layout && b_layout) return launch_variant<true, true, BN, EPI, MODE>(ta, tb, g, stream);
+  return launch_variant<true, false, BN, EPI, MODE>(ta, tb, g, stream);
 }
 
-template <int BN, bool PAIR>
+template <int BN, int MODE>
 int dispatch_epilogue(int epi, int a_layout, int b_layout, const CUtensorMap& ta,
                       const CUtensorMap& tb, const GemmArgs& g, cudaStream_t stream) {
   switch (epi) {
     case MC_EPI_STORE_F32:
-      return dispatch_layouts<BN, MC_EPI_STORE_F32, PAIR>(a_layout, b_layout, ta, tb, g, stream);
+      return dispatch_layouts<BN, MC_EPI_STORE_F32, MODE>(a_layout, b_layout, ta, tb, g, stream);
     case MC_EPI_STORE_BF16:
-      return dispatch_layouts<BN, MC_EPI_STORE_BF16, PAIR>(a_layout, b_layout, ta, tb, g, stream);
+      return dispatch_layouts<BN, MC_EPI_STORE_BF16, MODE>(a_layout, b_layout, ta, tb, g, stream);
     case MC_EPI_BIAS_BF16:
-      return dispatch_layouts<BN, MC_EPI_BIAS_BF16, PAIR>(a_layout, b_layout, ta, tb, g, stream);
+      return dispatch_layouts<BN, MC_EPI_BIAS_BF16, MODE>(a_layout, b_layout, ta, tb, g, stream);
     case MC_EPI_BIAS_GELU:
-      return dispatch_layouts<BN, MC_EPI_BIAS_GELU, PAIR>(a_layout, b_layout, ta, tb, g, stream);
+      return dispatch_layouts<BN, MC_EPI_BIAS_GELU, MODE>(a_layout, b_layout, ta, tb, g, stream);
     case MC_EPI_BIAS_RESID_F32:
-      return dispatch_layouts<BN, MC_EPI_BIAS_RESID_F32, PAIR>(a_layout, b_layout, ta, tb, g,
+      return dispatch_layouts<BN, MC_EPI_BIAS_RESID_F32, MODE>(a_layout, b_layout, ta, tb, g,
                                                                stream);
     case MC_EPI_GELU_BWD:
-      return dispatch_layouts<BN, MC_EPI_GELU_BWD, PAIR>(a_layout, b_layout, ta, tb, g, stream);
+      return dispatch_layouts<BN, MC_EPI_GELU_BWD, MODE>(a_layout, b_layout, ta, tb, g, stream);
     default:
       return MC_ERR_ARGUMENT;
   }
@@ -554,7 +621,7 @@ int launch_gemm(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda,
     return MC_ERR_ARGUMENT;
 
   // Wide tiles when there are enough of them to fill the machine; wide-tile
-  // problems with at least two M-tiles run as multicast pairs.
+  // problems with at least two M-tiles run on SM pairs (256 x 256 tiles).
   const int64_t m_tiles = (M + BM - 1) / BM;
   const int bn = ((N % 256 == 0) && m_tiles * (N / 256) >= num_sms()) ? 256 : 128;
   const bool pair = bn == 256 && m_tiles >= 2;
@@ -586,9 +653,9 @@ int launch_gemm(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda,
   g.ldaux = ldaux;
   g.accumulate = accumulate;
   g.status = status;
-  if (pair) return dispatch_epilogue<256, true>(epi, a_layout, b_layout, ta, tb, g, stream);
-  return bn == 256 ? dispatch_epilogue<256, false>(epi, a_layout, b_layout, ta, tb, g, stream)
-                   : dispatch_epilogue<128, false>(epi, a_layout, b_layout, ta, tb, g, stream);
+  if (pair) return dispatch_epilogue<256, kDuo>(epi, a_layout, b_layout, ta, tb, g, stream);
+  return bn == 256 ? dispatch_epilogue<256, kSolo>(epi, a_layout, b_layout, ta, tb, g, stream)
+                   : dispatch_epilogue<128, kSolo>(epi, a_layout, b_layout, ta, tb, g, stream);
 }
 
 }  // namespace mc

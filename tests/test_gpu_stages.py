@@ -133,10 +133,23 @@ def test_gemm_accumulate_and_partitions():
     _gemm_case(256, 256, 512, 0, 0, L.MC_EPI_STORE_F32, k_parts=4)
 
 
-@pytest.mark.parametrize("a_layout,b_layout", [(0, 0), (0, 1), (1, 1)])
+@pytest.mark.parametrize("a_layout,b_layout", [(0, 0), (0, 1), (1, 1), (1, 0)])
 def test_gemm_wide_tiles(a_layout, b_layout):
-    # Enough 128x256 tiles to select the wide-tile variant; ragged M.
+    # Enough 128x256 tiles to select the wide-tile variant, which runs on SM
+    # pairs (256 x 256 per pair); ragged M.
     _gemm_case(2000, 2560, 256, a_layout, b_layout, L.MC_EPI_STORE_F32, seed=3)
+
+
+@pytest.mark.parametrize("epi", [L.MC_EPI_STORE_BF16, L.MC_EPI_BIAS_BF16, L.MC_EPI_BIAS_GELU,
+                                 L.MC_EPI_BIAS_RESID_F32, L.MC_EPI_GELU_BWD])
+def test_gemm_paired_tiles_odd_m_tiles(epi):
+    # 17 M-tiles: the last pair's second half lies wholly past M.
+    _gemm_case(2100, 2304, 192, 0, 1 if epi == L.MC_EPI_GELU_BWD else 0, epi, seed=4)
+
+
+def test_gemm_paired_tiles_partitions_and_accumulate():
+    _gemm_case(1152, 4608, 512, 0, 0, L.MC_EPI_BIAS_RESID_F32, k_parts=8, seed=5)
+    _gemm_case(2048, 2560, 300, 1, 1, L.MC_EPI_STORE_F32, accumulate=1, seed=6)
 
 
 # ---------------------------------------------------------------- attention
