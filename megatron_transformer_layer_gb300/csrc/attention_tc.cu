@@ -40,7 +40,7 @@ template <int D>
 struct FwdCfg {
   static constexpr int kChunks = D / 64;              // 128-byte boxes per row
   static constexpr int kTile = 128 * D * 2;           // [128 rows][D] bf16
-  static constexpr int kBarBytes = 16 * 8;
+  static constexpr int kBarBytes = 18 * 8;
   static constexpr int kUsed = 5 * kTile + kBarBytes + 1024;
   // At least 116 KB so that two CTAs never share an SM (each holds all 512
   // TMEM columns).
@@ -70,7 +70,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* drain = bars + 10;
   uint64_t* v_full = bars + 11;   // [2]  V_j only after PV_j
   uint64_t* v_empty = bars + 13;  // [2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
+  // Completes once, after the last PV: O is final.  (o_ready cannot serve:
+  // when the last S arrives only PV_{n-3} is known to be done, so a parity
+  // wait for PV_{n-1} could be satisfied by PV_{n-3}'s phase.)
+  uint64_t* o_final = bars + 15;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int a = H * D;
@@ -90,6 +94,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&p_full[i], 128);
     }
     mbar_init(o_ready, 1);
+    mbar_init(o_final, 1);
     mbar_init(drain, 1);
     fence_mbar_init();
     tma_prefetch_desc(&tm);
@@ -175,6 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_commit(o_ready);
         }
       }
+      umma_commit(o_final);
       umma_commit(drain);
       mbar_wait(drain, 0, status, kSiteAttention, 200000000ull, false);
     }
@@ -220,6 +226,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (j == 0) m = m_new;  // key 0 is visible to every row: m is finite
       if (__any_sync(0xffffffffu, need)) {
         const float alpha = need ? fast_exp2(m - m_new) : 1.f;
+        // S_j was issued after PV_{j-2} completed, so this parity can only
+        // name PV_{j-1}.
         if (!mbar_wait_warp(o_ready, (j - 1) & 1, status, kSiteAttention)) {
           ok = false;
           break;
@@ -264,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(&p_full[st]);
     }
-    if (ok && mbar_wait_warp(o_ready, (n_kb - 1) & 1, status, kSiteAttention)) {
+    if (ok && mbar_wait_warp(o_final, 0, status, kSiteAttention)) {
       tc_fence_after();
       const float inv = 1.f / l;
       uint16_t* orow = out + (static_cast<int64_t>(bi) * s + q) * a + hh * D;

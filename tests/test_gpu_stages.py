@@ -203,3 +203,43 @@ def test_attention_forward_backward(b, s, H, d):
     got = to_f64(dqkv).reshape(b, s, 3 * a)
     for name, sl in (("dq", slice(0, a)), ("dk", slice(a, 2 * a)), ("dv", slice(2 * a, 3 * a))):
         assert_close(name, got[:, :, sl], g_ref[:, :, sl])
+
+
+def test_attention_long_sequence_many_heads():
+    """s = 4096 with 64 heads (the 96-layer GPT's shard shape): 32 key blocks
+    per heaviest tile and every SM busy, where the last products of a tile can
+    trail its softmax.  Bitwise-repeatable over three runs, and sampled heads
+    equal to the oracle."""
+    b, s, H, d = 1, 4096, 64, 128
+    a = H * d
+    qb = bits(b * s * 3 * a, 21, std=1.8)
+    q64 = bf16_bits_to_f64(qb).reshape(b, s, 3 * a)
+    dob = bits(b * s * a, 31)
+    qkv, dout = dev_bf16(qb), dev_bf16(dob)
+    runs = []
+    for _ in range(3):
+        o = torch.empty(b * s * a, dtype=torch.bfloat16, device=DEV)
+        lse = torch.empty(b * H * s, dtype=torch.float32, device=DEV)
+        dqkv = torch.empty(b * s * 3 * a, dtype=torch.bfloat16, device=DEV)
+        delta = torch.empty(b * H * s, dtype=torch.float32, device=DEV)
+        st = status()
+        assert L.mc_attention_forward(qkv, o, lse, b, s, H, d, st) == 0
+        assert L.mc_attention_backward(qkv, o, lse, dout, dqkv, delta, b, s, H, d, st) == 0
+        check_status(st)
+        runs.append((o, lse, dqkv))
+    for o, lse, dqkv in runs[1:]:
+        assert torch.equal(o, runs[0][0]) and torch.equal(lse, runs[0][1])
+        assert torch.equal(dqkv, runs[0][2])
+    o = to_f64(runs[0][0]).reshape(s, a)
+    g = to_f64(runs[0][2]).reshape(s, 3 * a)
+    do64 = bf16_bits_to_f64(dob).reshape(s, a)
+    for hh in (0, 9, 40, 63):
+        c = slice(hh * d, (hh + 1) * d)
+        ck, cv = slice(a + hh * d, a + (hh + 1) * d), slice(2 * a + hh * d, 2 * a + (hh + 1) * d)
+        q, k, v = q64[0, :, c], q64[0, :, ck], q64[0, :, cv]
+        o_ref, lse_ref = O.causal_attention_forward(q, k, v)
+        assert_close(f"attn_o head {hh}", o[:, c], o_ref)
+        dq, dk, dv = O.causal_attention_backward(q, k, v, o_ref, lse_ref, do64[:, c])
+        assert_close(f"dq head {hh}", g[:, c], dq)
+        assert_close(f"dk head {hh}", g[:, ck], dk)
+        assert_close(f"dv head {hh}", g[:, cv], dv)
