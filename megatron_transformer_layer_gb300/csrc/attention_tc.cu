@@ -306,98 +306,83 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------- backward
-// Both backward kernels keep one 128-row operand block resident and stream
-// the other side through a 2-deep TMA ring; warps 2..5 own one row each.
-//   dkdv: rows = keys.  S^T = K Q_i^T and dP^T = V dO_i^T into TMEM; the
-//         compute warps form P^T = exp2(S^T c - lse2_q) and
-//         dS^T = P^T (dP^T - delta_q), write both back as bf16 into the
-//         first 64 columns of their buffers; then dV += P^T dO_i and
-//         dK += dS^T Q_i with A read from TMEM and B the same smem tiles
-//         viewed MN-major.
-//   dq:   rows = queries.  S = Q K_j^T, dP = dO V_j^T, dS as above, then
-//         dQ += dS K_j.
+// Two kernels after the delta pre-pass, each keeping one 128-row operand
+// block resident and streaming the other side through TMA rings:
+//   dkdv: rows = keys (K, V resident; Q_i, dO_i streamed), accumulates dV, dK.
+//   dq:   rows = queries (Q, dO resident; K_j, V_j streamed), accumulates dQ.
 template <int D>
 struct BwdCfg {
   static constexpr int kChunks = D / 64;
   static constexpr int kTile = 128 * D * 2;
+  // K, V, two (Q_i, dO_i) stages, lse/delta staging [2][2][128], barriers
   static constexpr int kUsed = 6 * kTile + 4 * 128 * 4 + 24 * 8 + 1024;
   static constexpr int kSmem = kUsed > 116 * 1024 ? kUsed : 116 * 1024;
   static constexpr uint32_t kTmemCols = 512;
+  static_assert(kUsed <= 227 * 1024, "dkdv kernel shared memory");
 };
 
-// Loads 32 columns of two TMEM rows (this thread's lane) with one wait.
+// dK, dV for one 128-key block.  TMEM: S^T [0, 128), dP^T [128, 256),
+// dV [256, 256 + D), dK [384, 384 + D).  Per query block i:
+//   MMA      S^T_i = K Q_i^T (as soon as the compute warps hold S^T_{i-1} in
+//            registers), then dV += P^T_{i-1} dO_{i-1}, dK += dS^T_{i-1} Q_{i-1},
+//            then (those done) dP^T_i = V dO_i^T.
+//   compute  load S^T_i, release it; P^T = exp2(S^T c - lse2) while the MMAs
+//            above run; then load dP^T_i and form dS^T = P^T (dP^T - delta).
+// Each compute thread owns one key row and 64 query columns of dP^T, and
+// writes its P^T and dS^T (bf16 pairs) back over exactly those columns: the
+// 16 queries of group g (dP^T columns [16g, 16g + 16)) leave P at columns
+// [16g, 16g + 8) and dS at [16g + 8, 16g + 16).  No thread overwrites
+// columns another thread still has to read.
 template <int D>
-struct DqCfg {
-  static constexpr int kChunks = D / 64;
-  static constexpr int kTile = 128 * D * 2;
-  // Q, dO, three K stages, two V stages, barriers, alignment slack
-  static constexpr int kUsed = 7 * kTile + 24 * 8 + 1024;
-  static constexpr int kSmem = kUsed > 116 * 1024 ? kUsed : 116 * 1024;
-  static constexpr uint32_t kTmemCols = 512;
-  static_assert(kUsed <= 227 * 1024, "dq kernel shared memory");
-};
-
-__device__ __forceinline__ void tmem_ld2(uint32_t a, uint32_t b, float* va, float* vb) {
-  tmem_ld_32x32b_x32_nowait(a, va);
-  tmem_ld_32x32b_x32_nowait(b, vb);
-  tmem_ld_wait();
-}
-
-template <int D, bool KV_MAJOR>
 __global__ void __launch_bounds__(kBwdThreads, 1)
-    attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv,
-                       const __grid_constant__ CUtensorMap tm_do, const float* __restrict__ lse,
-                       const float* __restrict__ delta, uint16_t* __restrict__ dqkv, int s, int H,
-                       int* status) {
+    attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv,
+                            const __grid_constant__ CUtensorMap tm_do, const float* __restrict__ lse,
+                            const float* __restrict__ delta, uint16_t* __restrict__ dqkv, int s,
+                            int H, int* status) {
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  // Resident pair (KV_MAJOR: K, V; else Q, dO) and the streamed ring
-  // (KV_MAJOR: Q_i, dO_i; else K_j, V_j).
-  uint8_t* sR0 = smem;
-  uint8_t* sR1 = smem + C::kTile;
-  uint8_t* sA[2] = {smem + 2 * C::kTile, smem + 3 * C::kTile};
-  uint8_t* sB[2] = {smem + 4 * C::kTile, smem + 5 * C::kTile};
-  float* sL = reinterpret_cast<float*>(smem + 6 * C::kTile);  // [2][128]
-  float* sD = sL + 256;                                       // [2][128]
+  uint8_t* sK = smem;
+  uint8_t* sV = smem + C::kTile;
+  uint8_t* sQ[2] = {smem + 2 * C::kTile, smem + 3 * C::kTile};
+  uint8_t* sdO[2] = {smem + 4 * C::kTile, smem + 5 * C::kTile};
+  float* sL = reinterpret_cast<float*>(smem + 6 * C::kTile);  // [2][128] lse * log2(e)
+  float* sD = sL + 256;                                       // [2][128] delta
   uint64_t* bars = reinterpret_cast<uint64_t*>(sD + 256);
   uint64_t* r_full = bars + 0;
-  uint64_t* st_full = bars + 1;   // [2]
-  uint64_t* st_empty = bars + 3;  // [2]
-  uint64_t* s_full = bars + 5;
-  uint64_t* p_full = bars + 6;
-  uint64_t* mma_done = bars + 7;
-  uint64_t* drain = bars + 8;
-  uint64_t* lse_ready = bars + 9;  // [2]: the compute threads staged lse/delta
-  uint64_t* ld_done = bars + 11;   // [4]: both warps of a lane quarter read S, dP
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
+  uint64_t* st_full = bars + 1;    // [2]
+  uint64_t* st_empty = bars + 3;   // [2]
+  uint64_t* s_full = bars + 5;     // S^T_i in TMEM
+  uint64_t* s_free = bars + 6;     // compute warps hold S^T_i in registers
+  uint64_t* dp_full = bars + 7;    // dP^T_i in TMEM
+  uint64_t* p_full = bars + 8;     // P^T_i, dS^T_i in TMEM
+  uint64_t* acc_done = bars + 9;   // dV, dK products of block i complete
+  uint64_t* drain = bars + 10;
+  uint64_t* lse_ready = bars + 11;  // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 13);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int a = H * D;
   const int hh = blockIdx.y, bi = blockIdx.z;
   const int nblk = (s + 127) / 128;
-  // KV_MAJOR: this CTA's key block; streamed query blocks from the diagonal
-  // to the end.  Else: this CTA's query block (heaviest first); streamed key
-  // blocks from 0 to the diagonal.
-  const int rb = KV_MAJOR ? static_cast<int>(blockIdx.x) : nblk - 1 - static_cast<int>(blockIdx.x);
-  const int r0 = rb * 128;
-  const int first = KV_MAJOR ? rb : 0;
-  const int count = KV_MAJOR ? nblk - rb : rb + 1;
+  const int kb = static_cast<int>(blockIdx.x);  // this CTA's key block
+  const int r0 = kb * 128;
+  const int count = nblk - kb;  // query blocks kb .. nblk - 1
 
   if (threadIdx.x == 0) {
     mbar_init(r_full, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&st_full[i], 1);
       mbar_init(&st_empty[i], 1);
+      mbar_init(&lse_ready[i], 256);
     }
     mbar_init(s_full, 1);
+    mbar_init(s_free, 256);
+    mbar_init(dp_full, 1);
     mbar_init(p_full, 256);
-    mbar_init(mma_done, 1);
+    mbar_init(acc_done, 1);
     mbar_init(drain, 1);
-    mbar_init(&lse_ready[0], 256);
-    mbar_init(&lse_ready[1], 256);
-    for (int q = 0; q < 4; ++q) mbar_init(&ld_done[q], 64);
     fence_mbar_init();
     tma_prefetch_desc(&tm_qkv);
     tma_prefetch_desc(&tm_do);
@@ -410,37 +395,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS = tmem, tdP = tmem + 128, tAcc0 = tmem + 256, tAcc1 = tmem + 384;
+  const uint32_t tS = tmem, tdP = tmem + 128, tdV = tmem + 256, tdK = tmem + 384;
 
   if (warp == 0) {
     if (lane == 0) {
       // -------------------------------------------------------- producer
-      // column offsets inside qkv of Q, K, V for this head
       const int cq = hh * D, ck = a + hh * D, cv = 2 * a + hh * D;
       mbar_arrive_expect_tx(r_full, 2 * C::kTile);
       for (int c = 0; c < C::kChunks; ++c) {
-        if (KV_MAJOR) {
-          tma_load_3d(sR0 + c * 16384, &tm_qkv, r_full, ck + c * 64, r0, bi);
-          tma_load_3d(sR1 + c * 16384, &tm_qkv, r_full, cv + c * 64, r0, bi);
-        } else {
-          tma_load_3d(sR0 + c * 16384, &tm_qkv, r_full, cq + c * 64, r0, bi);
-          tma_load_3d(sR1 + c * 16384, &tm_do, r_full, hh * D + c * 64, r0, bi);
-        }
+        tma_load_3d(sK + c * 16384, &tm_qkv, r_full, ck + c * 64, r0, bi);
+        tma_load_3d(sV + c * 16384, &tm_qkv, r_full, cv + c * 64, r0, bi);
       }
       int issued = 0;
       for (int i = 0; i < count; ++i) {
         const int st = i & 1;
-        const int row = (first + i) * 128;
+        const int row = (kb + i) * 128;
         if (!mbar_wait(&st_empty[st], ((i >> 1) & 1) ^ 1u, status, kSiteAttention)) break;
         mbar_arrive_expect_tx(&st_full[st], 2 * C::kTile);
         for (int c = 0; c < C::kChunks; ++c) {
-          if (KV_MAJOR) {
-            tma_load_3d(sA[st] + c * 16384, &tm_qkv, &st_full[st], cq + c * 64, row, bi);
-            tma_load_3d(sB[st] + c * 16384, &tm_do, &st_full[st], hh * D + c * 64, row, bi);
-          } else {
-            tma_load_3d(sA[st] + c * 16384, &tm_qkv, &st_full[st], ck + c * 64, row, bi);
-            tma_load_3d(sB[st] + c * 16384, &tm_qkv, &st_full[st], cv + c * 64, row, bi);
-          }
+          tma_load_3d(sQ[st] + c * 16384, &tm_qkv, &st_full[st], cq + c * 64, row, bi);
+          tma_load_3d(sdO[st] + c * 16384, &tm_do, &st_full[st], hh * D + c * 64, row, bi);
         }
         ++issued;
       }
@@ -454,148 +428,156 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       constexpr uint32_t kIdescSq = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t kIdescAcc = idesc_bf16_f32(128, D, false, true);
       bool ok = mbar_wait(r_full, 0, status, kSiteAttention);
-      const uint32_t r0b = smem_u32(sR0), r1b = smem_u32(sR1);
-      for (int i = 0; ok && i < count; ++i) {
+      const uint32_t kbase = smem_u32(sK), vbase = smem_u32(sV);
+      for (int i = 0; ok && i <= count; ++i) {
         const int st = i & 1;
-        if (!mbar_wait(&st_full[st], (i >> 1) & 1, status, kSiteAttention)) break;
-        // tS / tdP were last read by the previous block's accumulating MMAs.
-        if (i > 0 && !mbar_wait(mma_done, (i - 1) & 1, status, kSiteAttention)) break;
-        tc_fence_after();
-        const uint32_t ab = smem_u32(sA[st]), bb = smem_u32(sB[st]);
-        // KV_MAJOR: S^T = K Q^T (A = K resident, B = Q streamed),
-        //           dP^T = V dO^T (A = V resident, B = dO streamed).
-        // else:     S = Q K^T (A = Q resident, B = K streamed),
-        //           dP = dO V^T (A = dO resident, B = V streamed).
+        if (i < count) {
+          if (!mbar_wait(&st_full[st], (i >> 1) & 1, status, kSiteAttention)) break;
+          // tS was read into registers for block i - 1.
+          if (i > 0 && !mbar_wait(s_free, (i - 1) & 1, status, kSiteAttention)) break;
+          tc_fence_after();
+          const uint32_t qb = smem_u32(sQ[st]);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          umma_bf16(tS, smem_desc_sw128(r0b + off, 16, 1024), smem_desc_sw128(ab + off, 16, 1024),
-                    kIdescSq, kk > 0 ? 1u : 0u);
-          umma_bf16(tdP, smem_desc_sw128(r1b + off, 16, 1024), smem_desc_sw128(bb + off, 16, 1024),
-                    kIdescSq, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+            umma_bf16(tS, smem_desc_sw128(kbase + off, 16, 1024), smem_desc_sw128(qb + off, 16, 1024),
+                      kIdescSq, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(s_full);
         }
-        umma_commit(s_full);
-        if (!mbar_wait(p_full, i & 1, status, kSiteAttention)) break;
-        tc_fence_after();
+        if (i > 0) {
+          const int pi = i - 1, pst = pi & 1;
+          if (!mbar_wait(p_full, pi & 1, status, kSiteAttention)) break;
+          tc_fence_after();
+          const uint32_t qb = smem_u32(sQ[pst]), dob = smem_u32(sdO[pst]);
 #pragma unroll
-        for (int kk = 0; kk < 128 / 16; ++kk) {
-          const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-          if (KV_MAJOR) {
-            // dV += P^T dO_i ; dK += dS^T Q_i  (B = streamed tiles viewed MN-major)
-            umma_bf16_ts(tAcc0, tS + kk * 8, smem_desc_sw128(bb + kk * 2048, 16384, 1024),
-                         kIdescAcc, acc);
-            umma_bf16_ts(tAcc1, tdP + kk * 8, smem_desc_sw128(ab + kk * 2048, 16384, 1024),
-                         kIdescAcc, acc);
-          } else {
-            // dQ += dS K_j
-            umma_bf16_ts(tAcc0, tS + kk * 8, smem_desc_sw128(ab + kk * 2048, 16384, 1024),
+          for (int kk = 0; kk < 128 / 16; ++kk) {
+            // 16 queries = group kk: P at 16 kk, dS at 16 kk + 8; B tiles viewed MN-major
+            const uint32_t pcol = static_cast<uint32_t>(kk * 16);
+            const uint32_t acc = (pi > 0 || kk > 0) ? 1u : 0u;
+            umma_bf16_ts(tdV, tdP + pcol, smem_desc_sw128(dob + kk * 2048, 16384, 1024), kIdescAcc,
+                         acc);
+            umma_bf16_ts(tdK, tdP + pcol + 8, smem_desc_sw128(qb + kk * 2048, 16384, 1024),
                          kIdescAcc, acc);
           }
+          umma_commit(&st_empty[pst]);
+          umma_commit(acc_done);
         }
-        umma_commit(&st_empty[st]);
-        umma_commit(mma_done);
+        if (i < count) {
+          // dP^T_i overwrites the P^T / dS^T that the products above read.
+          if (i > 0 && !mbar_wait(acc_done, (i - 1) & 1, status, kSiteAttention)) break;
+          tc_fence_after();
+          const uint32_t dob = smem_u32(sdO[st]);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+            umma_bf16(tdP, smem_desc_sw128(vbase + off, 16, 1024),
+                      smem_desc_sw128(dob + off, 16, 1024), kIdescSq, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(dp_full);
+        }
       }
       umma_commit(drain);
       mbar_wait(drain, 0, status, kSiteAttention, 200000000ull, false);
     }
   } else {
     // ---------------------------------------------------------- compute
-    // Two warps per TMEM lane quarter; `half` picks 64 of the 128 columns
-    // (the backward's per-element work needs no reduction along the row).
+    // Two warps per TMEM lane quarter; `half` picks 64 of the 128 query
+    // columns (the per-element work needs no reduction along the row).
     const int quarter = warp & 3;
     const int half = (warp - 2) >> 2;
-    const int t = quarter * 32 + lane;  // row within the block
-    const int r = r0 + t;               // this thread's key (KV_MAJOR) or query
+    const int t = quarter * 32 + lane;  // key row within the block
+    const int r = r0 + t;               // this thread's key
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t my_cols = lane_off + static_cast<uint32_t>(half * 64);
     const float scale2 = rsqrtf(static_cast<float>(D)) * kLog2e;
     const float* L = lse + (static_cast<int64_t>(bi) * H + hh) * s;
     const float* Dl = delta + (static_cast<int64_t>(bi) * H + hh) * s;
-    float my_l2 = 0.f, my_d = 0.f;
-    if (!KV_MAJOR && r < s) {
-      my_l2 = L[r] * kLog2e;
-      my_d = Dl[r];
+    // lse / delta of query t of the next block, loaded one block ahead (half 0)
+    float nl2 = 0.f, nd = 0.f;
+    if (half == 0 && r0 + t < s) {
+      nl2 = L[r0 + t] * kLog2e;
+      nd = Dl[r0 + t];
     }
     bool ok = true;
     for (int i = 0; i < count; ++i) {
-      const int c0 = (first + i) * 128;  // first column (query or key) of this block
-      float* l2 = sL + (i & 1) * 128;
-      float* dl = sD + (i & 1) * 128;
-      if (KV_MAJOR) {
-        const int qq = c0 + t;
-        if (half == 0) {
-          l2[t] = qq < s ? L[qq] * kLog2e : 0.f;
-          dl[t] = qq < s ? Dl[qq] : 0.f;
-        }
-        mbar_arrive(&lse_ready[i & 1]);
-        if (!mbar_wait_warp(&lse_ready[i & 1], (i >> 1) & 1, status, kSiteAttention)) {
-          ok = false;
-          break;
-        }
+      const int c0 = (kb + i) * 128;  // first query of this block
+      const float* l2 = sL + (i & 1) * 128 + half * 64;
+      const float* dl = sD + (i & 1) * 128 + half * 64;
+      if (half == 0) {
+        sL[(i & 1) * 128 + t] = nl2;
+        sD[(i & 1) * 128 + t] = nd;
+        const int qn = c0 + 128 + t;
+        nl2 = qn < s ? L[qn] * kLog2e : 0.f;
+        nd = qn < s ? Dl[qn] : 0.f;
       }
-      if (!mbar_wait_warp(s_full, i & 1, status, kSiteAttention)) {
+      mbar_arrive(&lse_ready[i & 1]);
+      if (!mbar_wait_warp(&lse_ready[i & 1], (i >> 1) & 1, status, kSiteAttention) ||
+          !mbar_wait_warp(s_full, i & 1, status, kSiteAttention)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      // Visible (row, column) pairs: KV_MAJOR: query >= key; else key <= query;
-      // both within the sequence.
-      const bool edge = KV_MAJOR ? (c0 < r0 + 127 || c0 + 128 > s) : (c0 + 127 > r0 || c0 + 128 > s);
-      // Read this warp's 64 columns of S and dP, then wait until the other
-      // warp of the lane quarter has read its own: P / dS are written into the
-      // first 64 columns of the same buffers, which span both warps' columns.
-      float sva[64], dva[64];
-      tmem_ld_32x32b_x32_nowait(tS + lane_off + half * 64, sva);
-      tmem_ld_32x32b_x32_nowait(tS + lane_off + half * 64 + 32, sva + 32);
-      tmem_ld_32x32b_x32_nowait(tdP + lane_off + half * 64, dva);
-      tmem_ld_32x32b_x32_nowait(tdP + lane_off + half * 64 + 32, dva + 32);
+      float p[64];
+      tmem_ld_32x32b_x32_nowait(tS + my_cols, p);
+      tmem_ld_32x32b_x32_nowait(tS + my_cols + 32, p + 32);
       tmem_ld_wait();
-      mbar_arrive(&ld_done[quarter]);
-      if (!mbar_wait_warp(&ld_done[quarter], i & 1, status, kSiteAttention)) {
+      tc_fence_before();
+      mbar_arrive(s_free);
+      // Visible: query >= key, both within the sequence.
+      const int q0 = c0 + half * 64;
+      const bool edge = q0 < r0 + 127 || q0 + 64 > s;
+#pragma unroll
+      for (int e = 0; e < 64; e += 4) {
+        const float4 lv = *reinterpret_cast<const float4*>(l2 + e);
+        p[e] = fast_exp2(fmaf(p[e], scale2, -lv.x));
+        p[e + 1] = fast_exp2(fmaf(p[e + 1], scale2, -lv.y));
+        p[e + 2] = fast_exp2(fmaf(p[e + 2], scale2, -lv.z));
+        p[e + 3] = fast_exp2(fmaf(p[e + 3], scale2, -lv.w));
+      }
+      if (edge) {
+#pragma unroll
+        for (int e = 0; e < 64; ++e) {
+          const int q = q0 + e;
+          p[e] = (q >= r && q < s) ? p[e] : 0.f;
+        }
+      }
+      if (!mbar_wait_warp(dp_full, i & 1, status, kSiteAttention)) {
         ok = false;
         break;
       }
+      tc_fence_after();
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        const int ch = 2 * half + cc;
-        const float* sv = sva + cc * 32;
-        const float* dv = dva + cc * 32;
-        uint32_t pw[16], dw[16];
+      for (int g = 0; g < 4; ++g) {
+        float dv[16];
+        tmem_ld_32x32b_x16(tdP + my_cols + g * 16, dv);
+        uint32_t w[16];  // [P of the 16 queries | dS of the 16 queries]
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float p[2], ds[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int col = c0 + ch * 32 + e + u;
-            const float lse2 = KV_MAJOR ? l2[ch * 32 + e + u] : my_l2;
-            const float dlt = KV_MAJOR ? dl[ch * 32 + e + u] : my_d;
-            float pv = fast_exp2(fmaf(sv[e + u], scale2, -lse2));
-            if (edge) {
-              const bool vis = KV_MAJOR ? (col >= r && col < s) : (col <= r && col < s);
-              pv = vis ? pv : 0.f;
-            }
-            p[u] = pv;
-            ds[u] = pv * (dv[e + u] - dlt);
-          }
-          pw[e / 2] = pack_bf16x2(p[0], p[1]);
-          dw[e / 2] = pack_bf16x2(ds[0], ds[1]);
+        for (int e = 0; e < 16; e += 4) {
+          const float4 dlv = *reinterpret_cast<const float4*>(dl + g * 16 + e);
+          const float* pp = p + g * 16 + e;
+          w[e / 2] = pack_bf16x2(pp[0], pp[1]);
+          w[e / 2 + 1] = pack_bf16x2(pp[2], pp[3]);
+          w[8 + e / 2] = pack_bf16x2(pp[0] * (dv[e] - dlv.x), pp[1] * (dv[e + 1] - dlv.y));
+          w[8 + e / 2 + 1] = pack_bf16x2(pp[2] * (dv[e + 2] - dlv.z), pp[3] * (dv[e + 3] - dlv.w));
         }
-        if (KV_MAJOR) tmem_st_32x32b_x16(tS + lane_off + ch * 16, pw);
-        tmem_st_32x32b_x16((KV_MAJOR ? tdP : tS) + lane_off + ch * 16, dw);
+        // over this thread's own dP^T columns, already in registers
+        tmem_st_32x32b_x16(tdP + my_cols + g * 16, w);
       }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(p_full);
     }
-    if (ok && mbar_wait_warp(mma_done, (count - 1) & 1, status, kSiteAttention)) {
+    if (ok && mbar_wait_warp(acc_done, (count - 1) & 1, status, kSiteAttention)) {
       tc_fence_after();
       const float scale = rsqrtf(static_cast<float>(D));
       const int64_t base = (static_cast<int64_t>(bi) * s + r) * 3 * static_cast<int64_t>(a);
 #pragma unroll 1
-      for (int w = 0; w < (KV_MAJOR ? 2 : 1); ++w) {
-        // KV_MAJOR: w = 0 -> dV (tAcc0, V block), w = 1 -> dK (tAcc1, K block).
-        const uint32_t tacc = w == 0 ? tAcc0 : tAcc1;
-        const float mul = (KV_MAJOR && w == 0) ? 1.f : scale;
-        const int col = KV_MAJOR ? (w == 0 ? 2 * a : a) + hh * D : hh * D;
+      for (int w = 0; w < 2; ++w) {
+        // w = 0: dV (V's columns of dqkv), w = 1: dK scaled by 1/sqrt(d)
+        const uint32_t tacc = w == 0 ? tdV : tdK;
+        const float mul = w == 0 ? 1.f : scale;
+        const int col = (w == 0 ? 2 * a : a) + hh * D;
 #pragma unroll 1
         for (int c = half * (D / 64); c < (half + 1) * (D / 64); ++c) {
           float v[32];
@@ -624,6 +606,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tmem_dealloc(tmem, C::kTmemCols);
   }
 }
+
+template <int D>
+struct DqCfg {
+  static constexpr int kChunks = D / 64;
+  static constexpr int kTile = 128 * D * 2;
+  // Q, dO, three K stages, two V stages, barriers, alignment slack
+  static constexpr int kUsed = 7 * kTile + 24 * 8 + 1024;
+  static constexpr int kSmem = kUsed > 116 * 1024 ? kUsed : 116 * 1024;
+  static constexpr uint32_t kTmemCols = 512;
+  static_assert(kUsed <= 227 * 1024, "dq kernel shared memory");
+};
 
 // dQ, with the next block's products overlapping this block's dS.
 //   TMEM: S [0, 128), dP [128, 256), dQ [256, 256 + D), dS (bf16) [384, 448).
@@ -874,12 +867,12 @@ int launch_bwd_dq_tc(const CUtensorMap& tq, const CUtensorMap& td, const float* 
   return cudaGetLastError() == cudaSuccess ? MC_OK : MC_ERR_CUDA;
 }
 
-template <int D, bool KV_MAJOR>
-int launch_bwd_tc_one(const CUtensorMap& tq, const CUtensorMap& td, const float* lse,
-                      const float* delta, uint16_t* dqkv, int b, int s, int H, int* status,
-                      cudaStream_t st) {
+template <int D>
+int launch_bwd_dkdv_tc(const CUtensorMap& tq, const CUtensorMap& td, const float* lse,
+                       const float* delta, uint16_t* dqkv, int b, int s, int H, int* status,
+                       cudaStream_t st) {
   using C = BwdCfg<D>;
-  auto kern = attn_bwd_tc_kernel<D, KV_MAJOR>;
+  auto kern = attn_bwd_dkdv_tc_kernel<D>;
   static std::once_flag once;
   static cudaError_t attr = cudaSuccess;
   std::call_once(once, [&] {
@@ -903,7 +896,7 @@ int launch_bwd_tc(const uint16_t* qkv, const float* lse, const uint16_t* dout, u
   const uint64_t sd[2] = {a * 2, a * 2 * static_cast<uint64_t>(s)};
   if (!make_tmap_bf16(&tq, qkv, 3, dq, sq, box) || !make_tmap_bf16(&td, dout, 3, dd, sd, box))
     return MC_ERR_CUDA;
-  int rc = launch_bwd_tc_one<D, true>(tq, td, lse, delta, dqkv, b, s, H, status, st);
+  int rc = launch_bwd_dkdv_tc<D>(tq, td, lse, delta, dqkv, b, s, H, status, st);
   if (rc != MC_OK) return rc;
   return launch_bwd_dq_tc<D>(tq, td, lse, delta, dqkv, b, s, H, status, st);
 }
