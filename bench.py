@@ -234,7 +234,7 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
-def stage_launcher(name, w, device, params=None):
+def stage_launcher(name, w, device, params=None, cp_parts=4):
     """One kernel of the step with the workload's shapes, inputs resident in
     HBM.  Returns (launch function, algorithmic flops or bytes per launch,
     unit, description)."""
@@ -283,6 +283,28 @@ def stage_launcher(name, w, device, params=None):
             assert L.mc_attention_backward(qkv, o, lse, dout, dqkv, delta, b, s, H, d,
                                            stream=st) == 0
         return launch, 2.0 * causal, "flop", "causal attention backward (pre + dkdv + dq)"
+    if name in ("attn_fwd_cp", "attn_bwd_cp"):
+        cp = cp_parts
+        qkv, o = rnd(T, 3 * a), rnd(T, a)
+        lse = torch.empty(b * H * s, device=device, dtype=torch.float32)
+        dout, dqkv = rnd(T, a), rnd(T, 3 * a)
+        delta = torch.empty(b * H * s, device=device, dtype=torch.float32)
+        nbytes = L.mc_attention_cp_workspace_bytes(b, s, H, d, cp)
+        if nbytes == 0:
+            raise SystemExit(f"seq_len {s} does not split into {2 * cp} whole 128-token chunks")
+        ws = torch.empty(nbytes, device=device, dtype=torch.uint8)
+        assert L.mc_attention_forward_cp(qkv, o, lse, b, s, H, d, cp, ws, nbytes, stream=st) == 0
+        causal = 2.0 * a * b * s * (s + 1)
+        if name == "attn_fwd_cp":
+            def launch():
+                assert L.mc_attention_forward_cp(qkv, o, lse, b, s, H, d, cp, ws, nbytes,
+                                                 stream=st) == 0
+            return launch, causal, "flop", f"context-parallel causal attention forward, cp {cp}"
+
+        def launch():
+            assert L.mc_attention_backward_cp(qkv, o, lse, dout, dqkv, delta, b, s, H, d, cp, ws,
+                                              nbytes, stream=st) == 0
+        return launch, 2.0 * causal, "flop", f"context-parallel causal attention backward, cp {cp}"
     if name == "ln_bwd":
         dln, x, resid = (torch.randn(T, h, device=device, generator=gen) for _ in range(3))
         mean = torch.zeros(T, device=device)
@@ -320,7 +342,7 @@ def time_launches(launch, device, steps, warmup):
 
 def run_stage(args, w, device):
     """Times one kernel of the step alone (used for profiling)."""
-    launch, work, unit, desc = stage_launcher(args.stage, w, device)
+    launch, work, unit, desc = stage_launcher(args.stage, w, device, cp_parts=args.cp)
     ms = time_launches(launch, device, args.steps, max(args.warmup, 1))
     rate = work / (ms / 1e3)
     line = {"stage": args.stage, "kernel": desc, "workload": WORKLOAD_NAMES[args.workload],
@@ -588,7 +610,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="c4")
-    ap.add_argument("--stage", choices=["gemm_fc1", "gemm_wgrad", "attn_fwd", "attn_bwd", "ln_bwd"],
+    ap.add_argument("--stage", choices=["gemm_fc1", "gemm_wgrad", "attn_fwd", "attn_bwd",
+                                        "attn_fwd_cp", "attn_bwd_cp", "ln_bwd"],
                     default=None)
     ap.add_argument("--ref-prefix", type=int, default=64,
                     help="tokens of the sequence the CPU oracle processes per sample")
@@ -601,6 +624,8 @@ def main():
                     help="activation recomputation: keep nothing between forward and backward")
     ap.add_argument("--layers", type=int, default=1,
                     help="time a stack of this many layers (distinct weights) per step")
+    ap.add_argument("--cp", type=int, default=4,
+                    help="context-parallel partitions for the attn_*_cp stages")
     args = ap.parse_args()
     if args.warmup < 3 and not args.stage and args.impl == "ours":
         ap.error("--warmup must be >= 3")

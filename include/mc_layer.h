@@ -243,6 +243,57 @@ int mc_attention_backward_noalloc(const uint16_t* qkv, const uint16_t* o, const 
                                   int32_t seq_len, int32_t heads, int32_t head_dim, int* status,
                                   void* stream);
 
+/* ---- Context-parallel causal attention (virtual CP partitions on one GPU).
+ *
+ * The pages (the Megatron Core guide: parallelism table and the section on
+ * proving semantics unchanged; the Megatron-Core listing: dynamic context
+ * parallelism) describe context parallelism as splitting the sequence
+ * dimension of inputs and activations across ranks, attention still needing
+ * every earlier token's K and V from the other ranks, and masks checked
+ * across sequence lengths.  Here the sequence of every micro-batch is cut
+ * into 2 * cp_parts chunks of c = seq_len / (2 cp_parts) tokens; virtual rank
+ * r owns chunks r and 2 cp_parts - 1 - r (queries, keys and values), which
+ * gives every rank the same causal work.  In ring step t rank r holds the K/V
+ * chunks of rank (r - t) mod cp_parts and computes, for each of its query
+ * chunks i and each held key chunk j <= i, the partial attention of chunk i
+ * over chunk j (causal mask inside the diagonal pair); the partials of a
+ * query chunk are merged with the log-sum-exp rule.  On one GPU the K/V
+ * exchange is the read of the other chunk's rows, and all ranks' partials of
+ * a step run as kernels on `stream` in schedule order.  Results equal
+ * mc_attention_forward / _backward up to fp32 rounding of the merge.
+ *
+ * Requirements: cp_parts >= 1, seq_len a multiple of 256 * cp_parts,
+ * head_dim 64 or 128; the caller-owned workspace of
+ * mc_attention_cp_workspace_bytes bytes (16-byte aligned) holds the fp32
+ * partials (chunk pairs x micro_batch x c x 3a floats plus the partial lse).
+ * Errors as mc_attention_forward, plus MC_ERR_SHAPE for an unsupported
+ * seq_len / cp_parts pair and MC_ERR_WORKSPACE for a short workspace. */
+
+/* The pairs (query chunk, key chunk) that virtual rank `rank` computes in
+ * ring step `step`: writes up to 4 pairs as pairs[2k] = query chunk,
+ * pairs[2k + 1] = key chunk and returns their number, or MC_ERR_ARGUMENT.
+ * Host only; every pair j <= i of the 2 cp_parts chunks occurs exactly once
+ * over all ranks and steps. */
+int mc_cp_schedule(int32_t cp_parts, int32_t rank, int32_t step, int32_t* pairs);
+
+size_t mc_attention_cp_workspace_bytes(int32_t micro_batch, int32_t seq_len, int32_t heads,
+                                       int32_t head_dim, int32_t cp_parts);
+
+/* Same results and layouts as mc_attention_forward (o bf16, lse fp32). */
+int mc_attention_forward_cp(const uint16_t* qkv, uint16_t* o, float* lse, int32_t micro_batch,
+                            int32_t seq_len, int32_t heads, int32_t head_dim, int32_t cp_parts,
+                            void* workspace, size_t workspace_bytes, int* status, void* stream);
+
+/* Same results and layouts as mc_attention_backward: each pair's dQ, dK, dV
+ * use the merged lse and delta = rowsum(dO * O); a chunk's dQ is the sum of
+ * its pairs' (key chunks in order), a chunk's dK and dV the sum over the
+ * query chunks that saw it (in order), each summed in fp32. */
+int mc_attention_backward_cp(const uint16_t* qkv, const uint16_t* o, const float* lse,
+                             const uint16_t* dout, uint16_t* dqkv, float* delta,
+                             int32_t micro_batch, int32_t seq_len, int32_t heads,
+                             int32_t head_dim, int32_t cp_parts, void* workspace,
+                             size_t workspace_bytes, int* status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -88,6 +88,11 @@ _SIGNATURES = {
     "mc_attention_forward": (_INT, [_P, _P, _P, _I32, _I32, _I32, _I32, _P, _P]),
     "mc_attention_backward": (_INT, [_P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _P, _P]),
     "mc_attention_backward_noalloc": (_INT, [_P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _P, _P]),
+    "mc_cp_schedule": (_INT, [_I32, _I32, _I32, ctypes.POINTER(_I32)]),
+    "mc_attention_cp_workspace_bytes": (_SZ, [_I32, _I32, _I32, _I32, _I32]),
+    "mc_attention_forward_cp": (_INT, [_P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P, _SZ, _P, _P]),
+    "mc_attention_backward_cp": (_INT, [_P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P,
+                                        _SZ, _P, _P]),
 }
 
 
@@ -214,3 +219,33 @@ def mc_attention_backward_noalloc(qkv, o, lse, dout, dqkv, micro_batch, seq_len,
     return lib().mc_attention_backward_noalloc(_ptr(qkv), _ptr(o), _ptr(lse), _ptr(dout),
                                                _ptr(dqkv), micro_batch, seq_len, heads, head_dim,
                                                _ptr(status), _stream(stream))
+
+
+def mc_cp_schedule(cp_parts, rank, step):
+    """(query chunk, key chunk) pairs of a virtual CP rank in a ring step
+    (host only); raises on an invalid argument."""
+    buf = (_I32 * 8)()
+    n = lib().mc_cp_schedule(cp_parts, rank, step, buf)
+    if n < 0:
+        raise ValueError(mc_strerror(n))
+    return [(buf[2 * k], buf[2 * k + 1]) for k in range(n)]
+
+
+def mc_attention_cp_workspace_bytes(micro_batch, seq_len, heads, head_dim, cp_parts) -> int:
+    return lib().mc_attention_cp_workspace_bytes(micro_batch, seq_len, heads, head_dim, cp_parts)
+
+
+def mc_attention_forward_cp(qkv, o, lse, micro_batch, seq_len, heads, head_dim, cp_parts,
+                            workspace, workspace_bytes, status=None, stream=None) -> int:
+    return lib().mc_attention_forward_cp(_ptr(qkv), _ptr(o), _ptr(lse), micro_batch, seq_len,
+                                         heads, head_dim, cp_parts, _ptr(workspace),
+                                         workspace_bytes, _ptr(status), _stream(stream))
+
+
+def mc_attention_backward_cp(qkv, o, lse, dout, dqkv, delta, micro_batch, seq_len, heads,
+                             head_dim, cp_parts, workspace, workspace_bytes, status=None,
+                             stream=None) -> int:
+    return lib().mc_attention_backward_cp(_ptr(qkv), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dqkv),
+                                          _ptr(delta), micro_batch, seq_len, heads, head_dim,
+                                          cp_parts, _ptr(workspace), workspace_bytes,
+                                          _ptr(status), _stream(stream))

@@ -63,6 +63,17 @@ bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
 
+int launch_attention_delta(const uint16_t* o, const uint16_t* dout, float* delta, int b, int s,
+                           int H, int d, cudaStream_t st) {
+  const int64_t T = static_cast<int64_t>(b) * s;
+  const unsigned blocks = static_cast<unsigned>((T * H * 32 + 255) / 256);
+  if (d == 64)
+    attn_bwd_pre_kernel<64><<<blocks, 256, 0, st>>>(o, dout, delta, T, s, H);
+  else
+    attn_bwd_pre_kernel<128><<<blocks, 256, 0, st>>>(o, dout, delta, T, s, H);
+  return cudaGetLastError() == cudaSuccess ? MC_OK : MC_ERR_CUDA;
+}
+
 int launch_attention_forward(const uint16_t* qkv, uint16_t* o, float* lse, int b, int s, int H,
                              int d, int* status, cudaStream_t st) {
   (void)status;

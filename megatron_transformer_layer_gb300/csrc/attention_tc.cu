@@ -36,6 +36,20 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;
 
+// A rectangle of the causal score matrix, for the context-parallel path:
+// forward and dQ take query rows [base, base + len) against key blocks
+// [blk_lo, blk_hi); dK/dV take key rows [base, base + len) against query
+// blocks [blk_lo, blk_hi).  Results go to fp32 partials indexed by the row
+// within the rectangle: forward O [b, len, a] and lse [b, H, len]; dQ
+// [b, len, a]; dK | dV [b, len, 2a].  The fused kernels use the whole
+// matrix (base 0, len s, blocks [0, INT_MAX)) and ignore the partials.
+struct AttnPart {
+  int base, len;
+  int blk_lo, blk_hi;
+  float* out;
+  float* lse;
+};
+
 template <int D>
 struct FwdCfg {
   static constexpr int kChunks = D / 64;              // 128-byte boxes per row
@@ -49,10 +63,10 @@ struct FwdCfg {
   static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
 };
 
-template <int D>
+template <int D, bool PART>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, uint16_t* __restrict__ out,
-                       float* __restrict__ lse, int s, int H, int* status) {
+                       float* __restrict__ lse, int s, int H, int* status, const AttnPart part) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -78,10 +92,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int a = H * D;
-  const int q_blk = gridDim.x - 1 - blockIdx.x;
+  const int q_blk = part.base / BQ + static_cast<int>(gridDim.x - 1 - blockIdx.x);
   const int hh = blockIdx.y, bi = blockIdx.z;
   const int q0 = q_blk * BQ;
-  const int n_kb = (min(q0 + BQ, s) + BKV - 1) / BKV;
+  const int kb0 = part.blk_lo;  // first key block
+  const int n_kb = min((min(q0 + BQ, s) + BKV - 1) / BKV, part.blk_hi) - kb0;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -123,12 +138,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(&k_empty[st], ph, status, kSiteAttention)) break;
         mbar_arrive_expect_tx(&k_full[st], C::kTile);
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d(sK[st] + c * 16384, &tm, &k_full[st], a + hh * D + c * 64, j * BKV, bi);
+          tma_load_3d(sK[st] + c * 16384, &tm, &k_full[st], a + hh * D + c * 64, (kb0 + j) * BKV,
+                      bi);
         ++k_issued;
         if (!mbar_wait(&v_empty[st], ph, status, kSiteAttention)) break;
         mbar_arrive_expect_tx(&v_full[st], C::kTile);
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d(sV[st] + c * 16384, &tm, &v_full[st], 2 * a + hh * D + c * 64, j * BKV, bi);
+          tma_load_3d(sV[st] + c * 16384, &tm, &v_full[st], 2 * a + hh * D + c * 64,
+                      (kb0 + j) * BKV, bi);
         ++v_issued;
       }
       // Copies still in flight must land before the CTA exits.
@@ -207,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld_32x32b_x32_nowait(tS[st] + lane_off + 64, x + 64);
       tmem_ld_32x32b_x32_nowait(tS[st] + lane_off + 96, x + 96);
       tmem_ld_wait();
-      const int key0 = j * BKV;
+      const int key0 = (kb0 + j) * BKV;
       float mx = -INFINITY;
       if (key0 + BKV - 1 > q0 || key0 + BKV > s) {  // diagonal or ragged block
         const int lim = min(q + 1, s) - key0;       // keys [0, lim) are visible
@@ -272,7 +289,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(&p_full[st]);
     }
-    if (ok && mbar_wait_warp(o_final, 0, status, kSiteAttention)) {
+    if (PART && ok && mbar_wait_warp(o_final, 0, status, kSiteAttention)) {
+      // fp32 partial O (normalised over this rectangle's keys) and its lse
+      tc_fence_after();
+      const float inv = 1.f / l;
+      const int qr = q - part.base;
+      float* orow = part.out + (static_cast<int64_t>(bi) * part.len + qr) * a + hh * D;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        float v[32];
+        tmem_ld_32x32b_x32(tO + lane_off + c * 32, v);
+        if (q < s) {
+          float4* dst = reinterpret_cast<float4*>(orow + c * 32);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            dst[i] = make_float4(v[4 * i] * inv, v[4 * i + 1] * inv, v[4 * i + 2] * inv,
+                                 v[4 * i + 3] * inv);
+        }
+      }
+      if (q < s) part.lse[(static_cast<int64_t>(bi) * H + hh) * part.len + qr] = (m + log2f(l)) * kLn2;
+    } else if (!PART && ok && mbar_wait_warp(o_final, 0, status, kSiteAttention)) {
       tc_fence_after();
       const float inv = 1.f / l;
       uint16_t* orow = out + (static_cast<int64_t>(bi) * s + q) * a + hh * D;
@@ -333,12 +369,12 @@ struct BwdCfg {
 // 16 queries of group g (dP^T columns [16g, 16g + 16)) leave P at columns
 // [16g, 16g + 8) and dS at [16g + 8, 16g + 16).  No thread overwrites
 // columns another thread still has to read.
-template <int D>
+template <int D, bool PART>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv,
                             const __grid_constant__ CUtensorMap tm_do, const float* __restrict__ lse,
                             const float* __restrict__ delta, uint16_t* __restrict__ dqkv, int s,
-                            int H, int* status) {
+                            int H, int* status, const AttnPart part) {
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -366,9 +402,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int a = H * D;
   const int hh = blockIdx.y, bi = blockIdx.z;
   const int nblk = (s + 127) / 128;
-  const int kb = static_cast<int>(blockIdx.x);  // this CTA's key block
+  const int kb = part.base / 128 + static_cast<int>(blockIdx.x);  // this CTA's key block
   const int r0 = kb * 128;
-  const int count = nblk - kb;  // query blocks kb .. nblk - 1
+  // query blocks qb0 .. qb0 + count - 1 (fused: kb .. nblk - 1)
+  const int qb0 = max(kb, part.blk_lo);
+  const int count = min(nblk, part.blk_hi) - qb0;
 
   if (threadIdx.x == 0) {
     mbar_init(r_full, 1);
@@ -409,7 +447,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       int issued = 0;
       for (int i = 0; i < count; ++i) {
         const int st = i & 1;
-        const int row = (kb + i) * 128;
+        const int row = (qb0 + i) * 128;
         if (!mbar_wait(&st_empty[st], ((i >> 1) & 1) ^ 1u, status, kSiteAttention)) break;
         mbar_arrive_expect_tx(&st_full[st], 2 * C::kTile);
         for (int c = 0; c < C::kChunks; ++c) {
@@ -495,13 +533,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const float* Dl = delta + (static_cast<int64_t>(bi) * H + hh) * s;
     // lse / delta of query t of the next block, loaded one block ahead (half 0)
     float nl2 = 0.f, nd = 0.f;
-    if (half == 0 && r0 + t < s) {
-      nl2 = L[r0 + t] * kLog2e;
-      nd = Dl[r0 + t];
+    if (half == 0 && qb0 * 128 + t < s) {
+      nl2 = L[qb0 * 128 + t] * kLog2e;
+      nd = Dl[qb0 * 128 + t];
     }
     bool ok = true;
     for (int i = 0; i < count; ++i) {
-      const int c0 = (kb + i) * 128;  // first query of this block
+      const int c0 = (qb0 + i) * 128;  // first query of this block
       const float* l2 = sL + (i & 1) * 128 + half * 64;
       const float* dl = sD + (i & 1) * 128 + half * 64;
       if (half == 0) {
@@ -582,7 +620,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int c = half * (D / 64); c < (half + 1) * (D / 64); ++c) {
           float v[32];
           tmem_ld_32x32b_x32(tacc + lane_off + c * 32, v);
-          if (r < s) {
+          if (PART && r < s) {
+            // fp32 partials of this rectangle: dK at [0, a), dV at [a, 2a)
+            float4* dst = reinterpret_cast<float4*>(
+                part.out + (static_cast<int64_t>(bi) * part.len + (r - part.base)) * 2 * a +
+                (w == 0 ? a : 0) + hh * D + c * 32);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              dst[k] = make_float4(v[4 * k] * mul, v[4 * k + 1] * mul, v[4 * k + 2] * mul,
+                                   v[4 * k + 3] * mul);
+          } else if (!PART && r < s) {
             uint4* dst = reinterpret_cast<uint4*>(dqkv + base + col + c * 32);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
@@ -624,12 +671,12 @@ struct DqCfg {
 // (s_free), so S_{j+1} = Q K_{j+1}^T and dP_{j+1} = dO V_{j+1}^T run while
 // dS_j is formed; dQ += dS_j K_j follows when dS_j is in TMEM (ds_full), and
 // its completion (ds_free) lets dS_{j+1} be written.
-template <int D>
+template <int D, bool PART>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv,
                           const __grid_constant__ CUtensorMap tm_do, const float* __restrict__ lse,
                           const float* __restrict__ delta, uint16_t* __restrict__ dqkv, int s,
-                          int H, int* status) {
+                          int H, int* status, const AttnPart part) {
   using C = DqCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -656,10 +703,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int a = H * D;
   const int hh = blockIdx.y, bi = blockIdx.z;
-  const int nblk = (s + 127) / 128;
-  const int qb = nblk - 1 - static_cast<int>(blockIdx.x);  // heaviest first
+  // heaviest first; fused: query blocks 0 .. nblk - 1 against key blocks 0 .. qb
+  const int qb = part.base / 128 + static_cast<int>(gridDim.x - 1 - blockIdx.x);
   const int q0 = qb * 128;
-  const int count = qb + 1;  // key blocks 0 .. qb
+  const int kb0 = part.blk_lo;
+  const int count = min(qb + 1, part.blk_hi) - kb0;  // key blocks kb0 .. kb0 + count - 1
 
   if (threadIdx.x == 0) {
     mbar_init(r_full, 1);
@@ -704,12 +752,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (!mbar_wait(&k_empty[ks], kph ^ 1u, status, kSiteAttention)) break;
         mbar_arrive_expect_tx(&k_full[ks], C::kTile);
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d(sK[ks] + c * 16384, &tm_qkv, &k_full[ks], a + hh * D + c * 64, j * 128, bi);
+          tma_load_3d(sK[ks] + c * 16384, &tm_qkv, &k_full[ks], a + hh * D + c * 64,
+                      (kb0 + j) * 128, bi);
         ++k_issued;
         if (!mbar_wait(&v_empty[vs], vph ^ 1u, status, kSiteAttention)) break;
         mbar_arrive_expect_tx(&v_full[vs], C::kTile);
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d(sV[vs] + c * 16384, &tm_qkv, &v_full[vs], 2 * a + hh * D + c * 64, j * 128,
+          tma_load_3d(sV[vs] + c * 16384, &tm_qkv, &v_full[vs], 2 * a + hh * D + c * 64,
+                      (kb0 + j) * 128,
                       bi);
         ++v_issued;
       }
@@ -790,7 +840,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(s_free);
-      const int c0 = j * 128 + half * 64;
+      const int c0 = (kb0 + j) * 128 + half * 64;
       const bool edge = c0 + 63 > q0 || c0 + 64 > s;
       uint32_t dw[32];
 #pragma unroll
@@ -826,7 +876,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int c = half * (D / 64); c < (half + 1) * (D / 64); ++c) {
         float v[32];
         tmem_ld_32x32b_x32(tdQ + lane_off + c * 32, v);
-        if (r < s) {
+        if (PART && r < s) {
+          // fp32 partial dQ of this rectangle
+          float4* dst = reinterpret_cast<float4*>(
+              part.out + (static_cast<int64_t>(bi) * part.len + (r - part.base)) * a + hh * D +
+              c * 32);
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            dst[k] = make_float4(v[4 * k] * scale, v[4 * k + 1] * scale, v[4 * k + 2] * scale,
+                                 v[4 * k + 3] * scale);
+        } else if (!PART && r < s) {
           uint4* dst = reinterpret_cast<uint4*>(dqkv + base + hh * D + c * 32);
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
@@ -850,60 +909,67 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 }
 
-template <int D>
+template <int D, bool PART>
 int launch_bwd_dq_tc(const CUtensorMap& tq, const CUtensorMap& td, const float* lse,
                      const float* delta, uint16_t* dqkv, int b, int s, int H, int* status,
-                     cudaStream_t st) {
+                     cudaStream_t st, const AttnPart& part) {
   using C = DqCfg<D>;
-  auto kern = attn_bwd_dq_tc_kernel<D>;
+  auto kern = attn_bwd_dq_tc_kernel<D, PART>;
   static std::once_flag once;
   static cudaError_t attr = cudaSuccess;
   std::call_once(once, [&] {
     attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   });
   if (attr != cudaSuccess) return MC_ERR_CUDA;
-  dim3 grid((s + 127) / 128, H, b);
-  kern<<<grid, kBwdThreads, C::kSmem, st>>>(tq, td, lse, delta, dqkv, s, H, status);
+  dim3 grid(PART ? part.len / 128 : (s + 127) / 128, H, b);
+  kern<<<grid, kBwdThreads, C::kSmem, st>>>(tq, td, lse, delta, dqkv, s, H, status, part);
   return cudaGetLastError() == cudaSuccess ? MC_OK : MC_ERR_CUDA;
 }
 
-template <int D>
+template <int D, bool PART>
 int launch_bwd_dkdv_tc(const CUtensorMap& tq, const CUtensorMap& td, const float* lse,
                        const float* delta, uint16_t* dqkv, int b, int s, int H, int* status,
-                       cudaStream_t st) {
+                       cudaStream_t st, const AttnPart& part) {
   using C = BwdCfg<D>;
-  auto kern = attn_bwd_dkdv_tc_kernel<D>;
+  auto kern = attn_bwd_dkdv_tc_kernel<D, PART>;
   static std::once_flag once;
   static cudaError_t attr = cudaSuccess;
   std::call_once(once, [&] {
     attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   });
   if (attr != cudaSuccess) return MC_ERR_CUDA;
-  dim3 grid((s + 127) / 128, H, b);
-  kern<<<grid, kBwdThreads, C::kSmem, st>>>(tq, td, lse, delta, dqkv, s, H, status);
+  dim3 grid(PART ? part.len / 128 : (s + 127) / 128, H, b);
+  kern<<<grid, kBwdThreads, C::kSmem, st>>>(tq, td, lse, delta, dqkv, s, H, status, part);
   return cudaGetLastError() == cudaSuccess ? MC_OK : MC_ERR_CUDA;
 }
 
-template <int D>
-int launch_bwd_tc(const uint16_t* qkv, const float* lse, const uint16_t* dout, uint16_t* dqkv,
-                  const float* delta, int b, int s, int H, int* status, cudaStream_t st) {
-  const uint64_t a = static_cast<uint64_t>(H) * D;
-  CUtensorMap tq, td;
+// Tensor maps over Q|K|V [b, s, 3a] and dO [b, s, a] with 64 x 128 boxes.
+bool make_bwd_maps(CUtensorMap* tq, CUtensorMap* td, const uint16_t* qkv, const uint16_t* dout,
+                   int b, int s, int a_) {
+  const uint64_t a = static_cast<uint64_t>(a_);
   const uint32_t box[3] = {64, 128, 1};
   const uint64_t dq[3] = {3 * a, static_cast<uint64_t>(s), static_cast<uint64_t>(b)};
   const uint64_t sq[2] = {3 * a * 2, 3 * a * 2 * static_cast<uint64_t>(s)};
   const uint64_t dd[3] = {a, static_cast<uint64_t>(s), static_cast<uint64_t>(b)};
   const uint64_t sd[2] = {a * 2, a * 2 * static_cast<uint64_t>(s)};
-  if (!make_tmap_bf16(&tq, qkv, 3, dq, sq, box) || !make_tmap_bf16(&td, dout, 3, dd, sd, box))
-    return MC_ERR_CUDA;
-  int rc = launch_bwd_dkdv_tc<D>(tq, td, lse, delta, dqkv, b, s, H, status, st);
-  if (rc != MC_OK) return rc;
-  return launch_bwd_dq_tc<D>(tq, td, lse, delta, dqkv, b, s, H, status, st);
+  return make_tmap_bf16(tq, qkv, 3, dq, sq, box) && make_tmap_bf16(td, dout, 3, dd, sd, box);
 }
 
+constexpr AttnPart kWhole = {0, 0, 0, 0x7fffffff, nullptr, nullptr};
+
 template <int D>
+int launch_bwd_tc(const uint16_t* qkv, const float* lse, const uint16_t* dout, uint16_t* dqkv,
+                  const float* delta, int b, int s, int H, int* status, cudaStream_t st) {
+  CUtensorMap tq, td;
+  if (!make_bwd_maps(&tq, &td, qkv, dout, b, s, H * D)) return MC_ERR_CUDA;
+  int rc = launch_bwd_dkdv_tc<D, false>(tq, td, lse, delta, dqkv, b, s, H, status, st, kWhole);
+  if (rc != MC_OK) return rc;
+  return launch_bwd_dq_tc<D, false>(tq, td, lse, delta, dqkv, b, s, H, status, st, kWhole);
+}
+
+template <int D, bool PART>
 int launch_fwd_tc(const uint16_t* qkv, uint16_t* o, float* lse, int b, int s, int H, int* status,
-                  cudaStream_t st) {
+                  cudaStream_t st, const AttnPart& part) {
   using C = FwdCfg<D>;
   const uint64_t a3 = 3ull * H * D;
   CUtensorMap tm;
@@ -911,15 +977,15 @@ int launch_fwd_tc(const uint16_t* qkv, uint16_t* o, float* lse, int b, int s, in
   const uint64_t strides[2] = {a3 * 2, a3 * 2 * static_cast<uint64_t>(s)};
   const uint32_t box[3] = {64, 128, 1};
   if (!make_tmap_bf16(&tm, qkv, 3, dims, strides, box)) return MC_ERR_CUDA;
-  auto kern = attn_fwd_tc_kernel<D>;
+  auto kern = attn_fwd_tc_kernel<D, PART>;
   static std::once_flag once;
   static cudaError_t attr = cudaSuccess;
   std::call_once(once, [&] {
     attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   });
   if (attr != cudaSuccess) return MC_ERR_CUDA;
-  dim3 grid((s + BQ - 1) / BQ, H, b);
-  kern<<<grid, kThreads, C::kSmem, st>>>(tm, o, lse, s, H, status);
+  dim3 grid(PART ? part.len / BQ : (s + BQ - 1) / BQ, H, b);
+  kern<<<grid, kThreads, C::kSmem, st>>>(tm, o, lse, s, H, status, part);
   return cudaGetLastError() == cudaSuccess ? MC_OK : MC_ERR_CUDA;
 }
 
@@ -934,8 +1000,38 @@ int launch_attention_backward_tc(const uint16_t* qkv, const float* lse, const ui
 
 int launch_attention_forward_tc(const uint16_t* qkv, uint16_t* o, float* lse, int b, int s, int H,
                                 int d, int* status, cudaStream_t st) {
-  return d == 64 ? launch_fwd_tc<64>(qkv, o, lse, b, s, H, status, st)
-                 : launch_fwd_tc<128>(qkv, o, lse, b, s, H, status, st);
+  return d == 64 ? launch_fwd_tc<64, false>(qkv, o, lse, b, s, H, status, st, kWhole)
+                 : launch_fwd_tc<128, false>(qkv, o, lse, b, s, H, status, st, kWhole);
+}
+
+int launch_attention_forward_part(const uint16_t* qkv, int b, int s, int H, int d, int q_base,
+                                  int q_len, int kb_lo, int kb_hi, float* part_o, float* part_lse,
+                                  int* status, cudaStream_t st) {
+  const AttnPart part = {q_base, q_len, kb_lo, kb_hi, part_o, part_lse};
+  return d == 64 ? launch_fwd_tc<64, true>(qkv, nullptr, nullptr, b, s, H, status, st, part)
+                 : launch_fwd_tc<128, true>(qkv, nullptr, nullptr, b, s, H, status, st, part);
+}
+
+int launch_attention_dq_part(const uint16_t* qkv, const float* lse, const uint16_t* dout,
+                             const float* delta, int b, int s, int H, int d, int q_base, int q_len,
+                             int kb_lo, int kb_hi, float* part_dq, int* status, cudaStream_t st) {
+  CUtensorMap tq, td;
+  if (!make_bwd_maps(&tq, &td, qkv, dout, b, s, H * d)) return MC_ERR_CUDA;
+  const AttnPart part = {q_base, q_len, kb_lo, kb_hi, part_dq, nullptr};
+  return d == 64 ? launch_bwd_dq_tc<64, true>(tq, td, lse, delta, nullptr, b, s, H, status, st, part)
+                 : launch_bwd_dq_tc<128, true>(tq, td, lse, delta, nullptr, b, s, H, status, st, part);
+}
+
+int launch_attention_dkdv_part(const uint16_t* qkv, const float* lse, const uint16_t* dout,
+                               const float* delta, int b, int s, int H, int d, int k_base,
+                               int k_len, int qb_lo, int qb_hi, float* part_dkv, int* status,
+                               cudaStream_t st) {
+  CUtensorMap tq, td;
+  if (!make_bwd_maps(&tq, &td, qkv, dout, b, s, H * d)) return MC_ERR_CUDA;
+  const AttnPart part = {k_base, k_len, qb_lo, qb_hi, part_dkv, nullptr};
+  return d == 64
+             ? launch_bwd_dkdv_tc<64, true>(tq, td, lse, delta, nullptr, b, s, H, status, st, part)
+             : launch_bwd_dkdv_tc<128, true>(tq, td, lse, delta, nullptr, b, s, H, status, st, part);
 }
 
 }  // namespace mc

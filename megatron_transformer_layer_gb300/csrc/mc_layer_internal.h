@@ -77,6 +77,27 @@ int launch_attention_backward_tc(const uint16_t* qkv, const float* lse, const ui
 int launch_attention_backward(const uint16_t* qkv, const uint16_t* o, const float* lse,
                               const uint16_t* dout, uint16_t* dqkv, float* delta, int b, int s,
                               int H, int d, int* status, cudaStream_t stream);
+
+// delta[b, h, i] = rowsum(dO * O) for head h of token i (the backward's pre-pass).
+int launch_attention_delta(const uint16_t* o, const uint16_t* dout, float* delta, int b, int s,
+                           int H, int d, cudaStream_t stream);
+
+// Rectangles of the causal score matrix with fp32 partial results, for the
+// context-parallel path (query or key rows [base, base + len), blocks of 128
+// on the other side in [blk_lo, blk_hi)):
+//   forward: O [b, len, a] normalised over the rectangle's keys, lse [b, H, len];
+//   dq:      dQ [b, len, a] (scaled by 1/sqrt(d)), using the full lse and delta;
+//   dkdv:    dK | dV [b, len, 2a] (dK scaled by 1/sqrt(d)).
+int launch_attention_forward_part(const uint16_t* qkv, int b, int s, int H, int d, int q_base,
+                                  int q_len, int kb_lo, int kb_hi, float* part_o, float* part_lse,
+                                  int* status, cudaStream_t stream);
+int launch_attention_dq_part(const uint16_t* qkv, const float* lse, const uint16_t* dout,
+                             const float* delta, int b, int s, int H, int d, int q_base, int q_len,
+                             int kb_lo, int kb_hi, float* part_dq, int* status, cudaStream_t stream);
+int launch_attention_dkdv_part(const uint16_t* qkv, const float* lse, const uint16_t* dout,
+                               const float* delta, int b, int s, int H, int d, int k_base,
+                               int k_len, int qb_lo, int qb_hi, float* part_dkv, int* status,
+                               cudaStream_t stream);
 #endif
 
 }  // namespace mc

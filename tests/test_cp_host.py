@@ -1,0 +1,119 @@
+"""Context-parallel attention: the schedule, the argument checks (no launch),
+and the chunk-pair decomposition of causal attention checked against the
+oracle on the CPU.
+
+The pages say only that context parallelism splits the sequence across
+ranks and that attention still needs the earlier tokens' K and V from the
+other ranks (Megatron Core guide, parallelism table and the section on
+proving semantics unchanged).  The reading taken: 2 cp chunks, rank r owns
+chunks r and 2 cp - 1 - r, ring steps pass K/V chunks, partials merged by
+log-sum-exp.
+"""
+import numpy as np
+import pytest
+
+import oracle.layer as O
+from megatron_transformer_layer_gb300 import _lib as L
+
+
+@pytest.mark.parametrize("cp", [1, 2, 3, 4, 8])
+def test_schedule_covers_every_causal_chunk_pair_once(cp):
+    C = 2 * cp
+    seen = {}
+    for r in range(cp):
+        for t in range(cp):
+            for i, j in L.mc_cp_schedule(cp, r, t):
+                assert (i, j) not in seen, (i, j)
+                seen[(i, j)] = (r, t)
+                # rank r owns query chunk i; the K/V chunk j belongs to the
+                # rank whose K/V r holds in step t
+                assert i in (r, C - 1 - r)
+                src = (r - t) % cp
+                assert j in (src, C - 1 - src)
+                assert j <= i
+    assert set(seen) == {(i, j) for i in range(C) for j in range(i + 1)}
+
+
+@pytest.mark.parametrize("cp", [1, 2, 4, 8])
+def test_schedule_balances_causal_work(cp):
+    """Every rank computes 2 cp - 1 full chunk pairs and 2 diagonal (half)
+    ones: the same causal work."""
+    for r in range(cp):
+        pairs = [p for t in range(cp) for p in L.mc_cp_schedule(cp, r, t)]
+        diag = sum(1 for i, j in pairs if i == j)
+        assert diag == 2 and len(pairs) == 2 * cp + 1
+
+
+def test_schedule_rejects_bad_arguments():
+    for args in [(0, 0, 0), (2, 2, 0), (2, 0, 2), (2, -1, 0)]:
+        with pytest.raises(ValueError):
+            L.mc_cp_schedule(*args)
+
+
+def test_workspace_bytes():
+    b, s, H, d, cp = 2, 2048, 4, 128, 4
+    C, c, a = 2 * cp, s // (2 * cp), H * d
+    pairs = C * (C + 1) // 2
+    assert L.mc_attention_cp_workspace_bytes(b, s, H, d, cp) == pairs * b * c * 3 * a * 4
+    assert L.mc_attention_cp_workspace_bytes(b, 2048 + 128, H, d, cp) == 0  # chunk not whole tiles
+    assert L.mc_attention_cp_workspace_bytes(b, s, H, 96, cp) == 0
+    assert L.mc_attention_cp_workspace_bytes(b, s, H, d, 0) == 0
+
+
+def test_cp_entry_points_reject_bad_arguments_before_launch():
+    fake = 1 << 20  # 16-byte aligned, never dereferenced: every case fails on the host
+    ws = L.mc_attention_cp_workspace_bytes(1, 1024, 2, 128, 2)
+    f = L.lib().mc_attention_forward_cp
+    assert f(fake, fake, fake, 1, 1000, 2, 128, 2, fake, ws, None, None) == L.MC_ERR_SHAPE
+    assert f(fake, fake, fake, 1, 1024, 2, 128, 0, fake, ws, None, None) == L.MC_ERR_SHAPE
+    assert f(fake, fake, fake, 1, 1024, 2, 80, 2, fake, ws, None, None) == L.MC_ERR_UNSUPPORTED
+    assert f(None, fake, fake, 1, 1024, 2, 128, 2, fake, ws, None, None) == L.MC_ERR_NULLPTR
+    assert f(fake + 4, fake, fake, 1, 1024, 2, 128, 2, fake, ws, None, None) == L.MC_ERR_ALIGN
+    assert f(fake, fake, fake, 1, 1024, 2, 128, 2, fake, ws - 1, None, None) == L.MC_ERR_WORKSPACE
+    g = L.lib().mc_attention_backward_cp
+    assert g(fake, fake, fake, fake, fake, fake, 1, 1024, 2, 128, 2, fake, ws - 1, None,
+             None) == L.MC_ERR_WORKSPACE
+    assert g(fake, fake, fake, None, fake, fake, 1, 1024, 2, 128, 2, fake, ws, None,
+             None) == L.MC_ERR_NULLPTR
+
+
+def _partial(q, k, v, q0, k0, causal):
+    """Softmax attention of rows q (absolute positions q0..) over keys k
+    (absolute positions k0..), causal mask inside; returns (O, lse)."""
+    sc = (q @ k.T) / np.sqrt(q.shape[1])
+    if causal:
+        rows = np.arange(q.shape[0])[:, None] + q0
+        cols = np.arange(k.shape[0])[None, :] + k0
+        sc = np.where(cols <= rows, sc, -np.inf)
+    m = sc.max(axis=1, keepdims=True)
+    e = np.exp(sc - m)
+    l = e.sum(axis=1, keepdims=True)
+    return (e / l) @ v, (m + np.log(l))[:, 0]
+
+
+@pytest.mark.parametrize("cp", [1, 2, 3])
+def test_chunk_pair_partials_merge_to_causal_attention(cp):
+    """The decomposition the CP path computes: merging the chunk-pair
+    partials of each query chunk with the log-sum-exp rule gives the oracle's
+    causal attention (and its LSE)."""
+    rng = np.random.default_rng(3)
+    C, c, d = 2 * cp, 8, 16
+    s = C * c
+    q, k, v = (rng.standard_normal((s, d)) * 1.5 for _ in range(3))
+    o_ref, lse_ref = O.causal_attention_forward(q, k, v)
+    o = np.empty_like(o_ref)
+    lse = np.empty_like(lse_ref)
+    parts = {}
+    for r in range(cp):
+        for t in range(cp):
+            for i, j in L.mc_cp_schedule(cp, r, t):
+                qs, ks = slice(i * c, (i + 1) * c), slice(j * c, (j + 1) * c)
+                parts[(i, j)] = _partial(q[qs], k[ks], v[ks], i * c, j * c, i == j)
+    for i in range(C):
+        ls = np.stack([parts[(i, j)][1] for j in range(i + 1)])      # [pairs, c]
+        l = np.log(np.exp(ls - ls.max(axis=0)).sum(axis=0)) + ls.max(axis=0)
+        w = np.exp(ls - l)                                            # weights sum to 1
+        o[i * c:(i + 1) * c] = sum(w[j][:, None] * parts[(i, j)][0] for j in range(i + 1))
+        lse[i * c:(i + 1) * c] = l
+    np.testing.assert_allclose(o, o_ref, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(lse, lse_ref, rtol=1e-12, atol=1e-12)
