@@ -90,6 +90,18 @@ extern "C" {
  * from x.  Results are identical to the default mode.  One `ws` can then be
  * shared by every layer of a stack run in sequence. */
 #define MC_RECOMPUTE_ACTIVATIONS 2u
+/* Sequence-parallel tensor parallelism (named with TP and EP in the Megatron
+ * Core guide's record card and parallelism table): LayerNorm, residual and
+ * bias-add run on sequence shards, the partial sums after out-proj and fc2
+ * become a reduce-scatter over the shards and QKV / fc1 read the
+ * all-gathered LayerNorm output.  Its contract is that the token count
+ * micro_batch * seq_len divides by tp_parts (MC_ERR_SHAPE otherwise).  With
+ * all partitions on one GPU the reduce-scatter is the in-accumulator
+ * partition sum written tile by tile (each output row belongs to exactly one
+ * shard), the shards of LayerNorm and residual lie side by side in one
+ * buffer, and the all-gather reads them in place, so results equal the
+ * default mode bit for bit and no kernel changes. */
+#define MC_SEQUENCE_PARALLEL 4u
 
 typedef struct mc_layer_shape {
   int32_t micro_batch; /* b  (--micro-batch-size)               */
@@ -100,7 +112,8 @@ typedef struct mc_layer_shape {
   int32_t tp_parts;    /* t  (--tensor-model-parallel-size)      */
   int32_t head_dim;    /* 0 => hidden / heads; > 0 decouples a = heads * head_dim
                           from hidden (one tensor-parallel rank's shard run alone) */
-  uint32_t flags;      /* MC_ACCUMULATE_GRADS | MC_RECOMPUTE_ACTIVATIONS, or 0 */
+  uint32_t flags;      /* MC_ACCUMULATE_GRADS | MC_RECOMPUTE_ACTIVATIONS |
+                          MC_SEQUENCE_PARALLEL, or 0 */
 } mc_layer_shape;
 
 /* bf16 parameters (uint16_t bit patterns), device pointers. */

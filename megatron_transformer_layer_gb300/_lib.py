@@ -27,6 +27,7 @@ MC_ERR_SCRATCH_LIMIT = -10
 
 MC_ACCUMULATE_GRADS = 1
 MC_RECOMPUTE_ACTIVATIONS = 2
+MC_SEQUENCE_PARALLEL = 4
 
 MC_EPI_STORE_F32 = 0
 MC_EPI_STORE_BF16 = 1

@@ -52,8 +52,13 @@ int check_shape(const mc_layer_shape* sh) {
   if (sh->micro_batch <= 0 || sh->seq_len <= 0 || sh->hidden <= 0 || sh->heads <= 0 ||
       sh->ffn_hidden <= 0 || sh->tp_parts <= 0 || sh->head_dim < 0)
     return MC_ERR_SHAPE;
-  if ((sh->flags & ~(MC_ACCUMULATE_GRADS | MC_RECOMPUTE_ACTIVATIONS)) != 0) return MC_ERR_ARGUMENT;
+  if ((sh->flags & ~(MC_ACCUMULATE_GRADS | MC_RECOMPUTE_ACTIVATIONS | MC_SEQUENCE_PARALLEL)) != 0)
+    return MC_ERR_ARGUMENT;
   const int t = sh->tp_parts;
+  // Sequence-parallel contract: the tokens split evenly into t shards.
+  if ((sh->flags & MC_SEQUENCE_PARALLEL) &&
+      (static_cast<int64_t>(sh->micro_batch) * sh->seq_len) % t != 0)
+    return MC_ERR_SHAPE;
   // Divisibility: hidden size and heads (and the ffn slice of the column
   // split) must divide by the tensor-parallel degree.
   if (sh->hidden % t || sh->heads % t || sh->ffn_hidden % t) return MC_ERR_SHAPE;

@@ -64,7 +64,7 @@ def test_saved_bytes_cover_the_activations():
 
 
 def test_unknown_flag_rejected():
-    assert L.mc_layer_check_shape(L.make_shape(1, 8, 768, 12, 3072, 1, 0, 4)) == L.MC_ERR_ARGUMENT
+    assert L.mc_layer_check_shape(L.make_shape(1, 8, 768, 12, 3072, 1, 0, 8)) == L.MC_ERR_ARGUMENT
 
 
 def test_strerror_covers_all_codes():
@@ -152,3 +152,16 @@ def test_recompute_flag_plans_no_saved_buffer():
                               wsb - 256) == L.MC_ERR_WORKSPACE
     assert L.mc_layer_forward(base, w, 0x20000000, 0x30000000, None, 0x50000000,
                               wsb) == L.MC_ERR_NULLPTR
+
+
+def test_sequence_parallel_contract():
+    """MC_SEQUENCE_PARALLEL: the tokens must split evenly into tp_parts shards."""
+    ok = L.make_shape(2, 6, 768, 12, 3072, 4, 0, L.MC_SEQUENCE_PARALLEL)   # 12 tokens / 4
+    bad = L.make_shape(1, 7, 768, 12, 3072, 2, 0, L.MC_SEQUENCE_PARALLEL)  # 7 tokens / 2
+    plain = L.make_shape(1, 7, 768, 12, 3072, 2, 0, 0)
+    assert L.mc_layer_check_shape(ok) == L.MC_OK
+    assert L.mc_layer_check_shape(bad) == L.MC_ERR_SHAPE
+    assert L.mc_layer_check_shape(plain) == L.MC_OK
+    both = L.make_shape(2, 6, 768, 12, 3072, 4, 0,
+                        L.MC_SEQUENCE_PARALLEL | L.MC_RECOMPUTE_ACTIVATIONS)
+    assert L.mc_layer_check_shape(both) == L.MC_OK

@@ -202,3 +202,27 @@ def test_cuda_graph_capture_matches_eager():
     assert np.array_equal(dx_g.reshape(dx_e.shape), dx_e)
     for k in G_e:
         assert np.array_equal(G_g[k], G_e[k]), k
+
+
+def test_sequence_parallel_flag_changes_nothing():
+    """MC_SEQUENCE_PARALLEL on one GPU: the reduce-scatter is the partition
+    sum written per row tile and the all-gather reads the shards in place, so
+    y, dx and every gradient equal the default mode bit for bit."""
+    from megatron_transformer_layer_gb300.layer import TransformerLayer
+    from gpu_util import dev_bf16
+    shape = LayerShape(2, 130, 1024, 8, 4096, 4)
+    inp = make_layer_inputs(shape, seed=9, init=NONTRIVIAL_INIT)
+    x = dev_f32_from_bits(inp.x.reshape(-1, 1024))
+    dy = dev_f32_from_bits(inp.dy.reshape(-1, 1024))
+    out = []
+    for sp in (False, True):
+        ly = TransformerLayer(2, 130, 1024, 8, 4096, 4, sequence_parallel=sp,
+                              params={k: dev_bf16(v) for k, v in inp.params.items()})
+        y = ly.forward(x)
+        dx = ly.backward(dy)
+        torch.cuda.synchronize()
+        assert ly.device_status() == 0
+        out.append((y.clone(), dx.clone(), {k: v.clone() for k, v in ly.grads.items()}))
+    assert torch.equal(out[0][0], out[1][0]) and torch.equal(out[0][1], out[1][1])
+    for k in out[0][2]:
+        assert torch.equal(out[0][2][k], out[1][2][k]), k
