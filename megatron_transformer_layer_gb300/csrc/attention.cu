@@ -16,7 +16,6 @@
 namespace mc {
 namespace {
 
-
 // ---------------------------------------------------------------- backward
 // delta[b, h, i] = sum_c dO[i, h*D + c] * O[i, h*D + c]; one warp per (token, head).
 template <int D>
