@@ -226,3 +226,35 @@ def test_sequence_parallel_flag_changes_nothing():
     assert torch.equal(out[0][0], out[1][0]) and torch.equal(out[0][1], out[1][1])
     for k in out[0][2]:
         assert torch.equal(out[0][2][k], out[1][2][k]), k
+
+
+def test_c4_layer_is_bitwise_repeatable():
+    """The whole layer at the benchmark shape (one layer of the 96-layer GPT,
+    8 partitions) twice on the same inputs: y, dx and all twelve gradients
+    identical to the bit (no atomics, fixed-order reductions), which would
+    expose a race in any kernel of the step."""
+    from megatron_transformer_layer_gb300.layer import TransformerLayer
+    b, s, h, H, f, t = 1, 4096, 8192, 64, 32768, 8
+    g = torch.Generator(device=DEV).manual_seed(11)
+    shapes = {"ln1_g": (h,), "ln1_b": (h,), "w_qkv": (3 * h, h), "b_qkv": (3 * h,),
+              "w_o": (h, h), "b_o": (h,), "ln2_g": (h,), "ln2_b": (h,), "w_fc1": (f, h),
+              "b_fc1": (f,), "w_fc2": (h, f), "b_fc2": (h,)}
+    params = {}
+    for k, shp in shapes.items():
+        std = 0.02 if k.startswith("w_") else 0.1
+        mean = 1.0 if k.endswith("_g") else 0.0
+        params[k] = (torch.randn(*shp, device=DEV, generator=g) * std + mean).bfloat16()
+    x = torch.randn(b * s, h, device=DEV, generator=g).bfloat16().float()
+    dy = torch.randn(b * s, h, device=DEV, generator=g).bfloat16().float()
+    ly = TransformerLayer(b, s, h, H, f, t, params=params)
+    runs = []
+    for _ in range(2):
+        y = ly.forward(x).clone()
+        dx = ly.backward(dy).clone()
+        torch.cuda.synchronize()
+        assert ly.device_status() == 0
+        runs.append((y, dx, {k: v.clone() for k, v in ly.grads.items()}))
+    assert torch.equal(runs[0][0], runs[1][0]) and torch.equal(runs[0][1], runs[1][1])
+    for k in runs[0][2]:
+        assert torch.equal(runs[0][2][k], runs[1][2][k]), k
+    assert torch.isfinite(runs[0][0]).all() and torch.isfinite(runs[0][1]).all()
