@@ -259,6 +259,23 @@ def stage_launcher(name, w, device, params=None, cp_parts=4):
                            aux=hp, ldaux=f, stream=st)
             assert rc == 0, L.mc_strerror(rc)
         return launch, 2.0 * T * h * f, "flop", "gemm_tcgen05 fc1 forward (bias+GeLU epilogue)"
+    if name == "gemm_fc1_fp8":
+        # fc1 with E4M3 operands (per-tensor scales), quantised once outside the timing
+        A32, B32 = rnd(T, h, dtype=torch.float32), rnd(f, h, scale=0.02, dtype=torch.float32)
+        qa = torch.empty(T * h, dtype=torch.uint8, device=device)
+        qb = torch.empty(f * h, dtype=torch.uint8, device=device)
+        sa, sb = (torch.empty(1, device=device) for _ in range(2))
+        scratch = torch.empty(L.mc_fp8_scratch_floats(), device=device)
+        assert L.mc_fp8_quantize(A32, qa, sa, scratch, L.FP8_E4M3, stream=st) == 0
+        assert L.mc_fp8_quantize(B32, qb, sb, scratch, L.FP8_E4M3, stream=st) == 0
+        bias = torch.zeros(f, device=device, dtype=torch.bfloat16)
+        out, hp = rnd(T, f), rnd(T, f)
+
+        def launch():
+            rc = L.mc_gemm_fp8(T, f, h, qa, h, L.FP8_E4M3, qb, h, L.FP8_E4M3, sa, sb, out, f,
+                               L.MC_EPI_BIAS_GELU, bias=bias, aux=hp, ldaux=f, stream=st)
+            assert rc == 0, L.mc_strerror(rc)
+        return launch, 2.0 * T * h * f, "flop", "gemm_tcgen05 fc1 forward, E4M3 operands (kind::f8f6f4)"
     if name == "gemm_wgrad":
         A, B = rnd(T, f), rnd(T, h)           # dhp [T, f], ln2 [T, h]
         out = torch.empty(f, h, device=device, dtype=torch.float32)
@@ -610,7 +627,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="c4")
-    ap.add_argument("--stage", choices=["gemm_fc1", "gemm_wgrad", "attn_fwd", "attn_bwd",
+    ap.add_argument("--stage", choices=["gemm_fc1", "gemm_fc1_fp8", "gemm_wgrad", "attn_fwd",
+                                        "attn_bwd",
                                         "attn_fwd_cp", "attn_bwd_cp", "ln_bwd"],
                     default=None)
     ap.add_argument("--ref-prefix", type=int, default=64,

@@ -256,6 +256,34 @@ int mc_attention_backward_noalloc(const uint16_t* qkv, const uint16_t* o, const 
                                   int32_t seq_len, int32_t heads, int32_t head_dim, int* status,
                                   void* stream);
 
+/* ---- 8-bit floating-point GEMMs (the Megatron-Core listing, 混合精度:
+ * FP8 / FP4 training on Blackwell Ultra, --fp8-format hybrid = E4M3 forward,
+ * E5M2 gradients).  Formats: 0 = E4M3 (largest finite 448), 1 = E5M2
+ * (57344), OCP 8-bit floating point.  The pages give no scaling recipe; the
+ * one implemented is per-tensor current scaling (below). */
+
+/* Floats of device scratch that mc_fp8_quantize needs. */
+size_t mc_fp8_scratch_floats(void);
+
+/* Quantises n values of `in` (fp32, or bf16 when in_bf16 != 0; 16-byte
+ * aligned) to `out` (n bytes, 8-byte aligned): amax = max |x|, scale =
+ * fmax / amax (fp32 division; 1 when amax is 0), out = round-to-nearest-even
+ * of x * scale (fp32 product) saturated to +-fmax; writes the device scalar
+ * *scale_inv = 1 / scale.  Enqueued on `stream`; deterministic. */
+int mc_fp8_quantize(const void* in, int32_t in_bf16, int64_t n, int32_t format, uint8_t* out,
+                    float* scale_inv, float* scratch, int* status, void* stream);
+
+/* out = epilogue((A B^T) * *a_scale_inv * *b_scale_inv) with A [M, K] and
+ * B [N, K] row-major 8-bit floats (K contiguous; lda, ldb multiples of 16),
+ * fp32 accumulation on the tensor cores (tcgen05 kind::f8f6f4, SM pairs for
+ * large problems).  Epilogues, bias / aux / accumulate / k_parts and errors as
+ * mc_gemm; K a multiple of 16 (a ragged last 128-wide block reads zeros). */
+int mc_gemm_fp8(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_t lda, int32_t a_format,
+                const uint8_t* B, int64_t ldb, int32_t b_format, const float* a_scale_inv,
+                const float* b_scale_inv, void* out, int64_t ldc, int32_t epilogue,
+                const uint16_t* bias, const void* aux, int64_t ldaux, int32_t accumulate,
+                int32_t k_parts, int* status, void* stream);
+
 /* ---- Context-parallel causal attention (virtual CP partitions on one GPU).
  *
  * The pages (the Megatron Core guide: parallelism table and the section on

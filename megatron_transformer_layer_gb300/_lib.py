@@ -89,6 +89,10 @@ _SIGNATURES = {
     "mc_attention_forward": (_INT, [_P, _P, _P, _I32, _I32, _I32, _I32, _P, _P]),
     "mc_attention_backward": (_INT, [_P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _P, _P]),
     "mc_attention_backward_noalloc": (_INT, [_P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _P, _P]),
+    "mc_fp8_scratch_floats": (_SZ, []),
+    "mc_fp8_quantize": (_INT, [_P, _I32, _I64, _I32, _P, _P, _P, _P, _P]),
+    "mc_gemm_fp8": (_INT, [_I64, _I64, _I64, _P, _I64, _I32, _P, _I64, _I32, _P, _P, _P, _I64,
+                           _I32, _P, _P, _I64, _I32, _I32, _P, _P]),
     "mc_cp_schedule": (_INT, [_I32, _I32, _I32, ctypes.POINTER(_I32)]),
     "mc_attention_cp_workspace_bytes": (_SZ, [_I32, _I32, _I32, _I32, _I32]),
     "mc_attention_forward_cp": (_INT, [_P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P, _SZ, _P, _P]),
@@ -250,3 +254,28 @@ def mc_attention_backward_cp(qkv, o, lse, dout, dqkv, delta, micro_batch, seq_le
                                           _ptr(delta), micro_batch, seq_len, heads, head_dim,
                                           cp_parts, _ptr(workspace), workspace_bytes,
                                           _ptr(status), _stream(stream))
+
+
+FP8_E4M3 = 0
+FP8_E5M2 = 1
+
+
+def mc_fp8_scratch_floats() -> int:
+    return lib().mc_fp8_scratch_floats()
+
+
+def mc_fp8_quantize(x, out, scale_inv, scratch, fmt, status=None, stream=None) -> int:
+    """Per-tensor current scaling of x (fp32 or bf16 tensor) to 8-bit bytes."""
+    import torch
+    in_bf16 = 1 if x.dtype == torch.bfloat16 else 0
+    return lib().mc_fp8_quantize(_ptr(x), in_bf16, x.numel(), fmt, _ptr(out), _ptr(scale_inv),
+                                 _ptr(scratch), _ptr(status), _stream(stream))
+
+
+def mc_gemm_fp8(M, N, K, A, lda, a_format, B, ldb, b_format, a_scale_inv, b_scale_inv, out, ldc,
+                epilogue, bias=None, aux=None, ldaux=0, accumulate=0, k_parts=1, status=None,
+                stream=None) -> int:
+    return lib().mc_gemm_fp8(M, N, K, _ptr(A), lda, a_format, _ptr(B), ldb, b_format,
+                             _ptr(a_scale_inv), _ptr(b_scale_inv), _ptr(out), ldc, epilogue,
+                             _ptr(bias), _ptr(aux), ldaux, accumulate, k_parts, _ptr(status),
+                             _stream(stream))

@@ -50,6 +50,11 @@ struct GemmArgs {
   int64_t ldaux;
   int accumulate;
   int* status;
+  // 8-bit operands: the instruction descriptor (formats) and the device
+  // scalars whose product dequantises the fp32 accumulator
+  uint32_t idesc_f8;
+  const float* a_scale_inv;
+  const float* b_scale_inv;
 };
 
 // Execution modes of the GEMM kernel.
@@ -194,13 +199,19 @@ __device__ __forceinline__ void epilogue32(float (&v)[32], int row, int col0, co
 // its commits arrive on the barriers of both CTAs (a stage is refilled, an
 // accumulator read, only then); the odd CTA's epilogue releases the
 // accumulator on the even CTA's barrier.
-template <bool A_MN, bool B_MN, int BN, int EPI, int MODE>
+// F8: operands are 8-bit floats (E4M3 / E5M2, K-major only): a 128-byte
+// swizzled row then holds 128 elements of K instead of 64, each MMA takes
+// K = 32 (kind::f8f6f4) and the epilogue multiplies by the two operands'
+// dequantisation scales before the fused epilogue.
+template <bool A_MN, bool B_MN, int BN, int EPI, int MODE, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB, const GemmArgs g) {
   using Cfg = GemmCfg<BN, MODE>;
   constexpr int S = Cfg::kStages;
   constexpr bool kDuoMode = MODE == kDuo;
+  static_assert(!F8 || (!A_MN && !B_MN), "8-bit operands are K-major");
+  constexpr int kBKE = F8 ? 2 * BK : BK;  // K elements per 128-byte row
   constexpr uint32_t kIdesc = idesc_bf16_f32(kDuoMode ? 2 * BM : BM, BN, A_MN, B_MN);
 
   extern __shared__ uint8_t smem_raw[];
@@ -282,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          const int k0 = kb * BK;
+          const int k0 = kb * kBKE;
           uint8_t* a_dst = sA + stage * Cfg::kABytes;
           uint8_t* b_dst = sB + stage * Cfg::kBBytes;
           if constexpr (kDuoMode) {
@@ -368,13 +379,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t b0 = smem_u32(sB + stage * Cfg::kBBytes);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
-            // K-major: a K step of 16 bf16 is 32 bytes inside the swizzled row.
+            // K-major: a K step of 16 bf16 (32 fp8) is 32 bytes inside the swizzled row.
             // MN-major: a K step is 16 rows of 128 bytes; LBO = 64-wide MN chunk.
             const uint64_t ad = A_MN ? smem_desc_sw128(a0 + k * 2048, 64 * BK * 2, 1024)
                                      : smem_desc_sw128(a0 + k * 32, 16, 1024);
             const uint64_t bd = B_MN ? smem_desc_sw128(b0 + k * 2048, 64 * BK * 2, 1024)
                                      : smem_desc_sw128(b0 + k * 32, 16, 1024);
-            if constexpr (kDuoMode)
+            if constexpr (F8 && kDuoMode)
+              umma_f8_pair(d_tmem, ad, bd, g.idesc_f8, (kb | k) != 0 ? 1u : 0u);
+            else if constexpr (F8)
+              umma_f8(d_tmem, ad, bd, g.idesc_f8, (kb | k) != 0 ? 1u : 0u);
+            else if constexpr (kDuoMode)
               umma_bf16_pair(d_tmem, ad, bd, kIdesc, (kb | k) != 0 ? 1u : 0u);
             else
               umma_bf16(d_tmem, ad, bd, kIdesc, (kb | k) != 0 ? 1u : 0u);
@@ -411,6 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;      // TMEM lanes [32 q, 32 q + 32)
     const int half = (warp - 2) >> 2;  // which half of the tile's columns
     const uint32_t acc_empty_pair = kDuoMode ? mapa_shared(acc_empty, 0) : 0u;
+    const float dq = F8 ? *g.a_scale_inv * *g.b_scale_inv : 1.f;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int u = unit0; u < n_units; u += ustride) {
@@ -426,6 +442,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         float v[32];
         tmem_ld_32x32b_x32(t_row + c * 32, v);
         const int col0 = nb * BN + c * 32;
+        if constexpr (F8) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] *= dq;
+        }
         if (row < g.M && col0 < g.N) epilogue32<EPI>(v, row, col0, g);
       }
       tc_fence_before();
@@ -475,26 +495,28 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
 
 // 2D bf16 tensor map over a row-major matrix [outer, inner] with row stride
 // `ld` elements, box [box_outer, box_inner], 128-byte swizzle, zero fill.
+// u8: 8-bit elements (ld in elements = bytes) instead of bf16.
 bool make_tmap(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t ld,
-               uint32_t box_inner, uint32_t box_outer) {
+               uint32_t box_inner, uint32_t box_outer, bool u8 = false) {
   auto enc = get_encode_fn();
   if (!enc) return false;
   cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {ld * 2};
+  cuuint64_t strides[1] = {ld * (u8 ? 1 : 2)};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+  CUresult r = enc(map, u8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                   const_cast<void*>(base), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
-template <bool A_MN, bool B_MN, int BN, int EPI, int MODE>
+template <bool A_MN, bool B_MN, int BN, int EPI, int MODE, bool F8 = false>
 int launch_variant(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& g,
                    cudaStream_t stream) {
   using Cfg = GemmCfg<BN, MODE>;
   constexpr bool PAIR = MODE == kDuo;
-  auto kern = gemm_tcgen05_kernel<A_MN, B_MN, BN, EPI, MODE>;
+  auto kern = gemm_tcgen05_kernel<A_MN, B_MN, BN, EPI, MODE, F8>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   static int max_clusters = 0;
@@ -568,6 +590,28 @@ int dispatch_epilogue(int epi, int a_layout, int b_layout, const CUtensorMap& ta
                                                                stream);
     case MC_EPI_GELU_BWD:
       return dispatch_layouts<BN, MC_EPI_GELU_BWD, MODE>(a_layout, b_layout, ta, tb, g, stream);
+    default:
+      return MC_ERR_ARGUMENT;
+  }
+}
+
+template <int BN, int MODE>
+int dispatch_epilogue_f8(int epi, const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& g,
+                         cudaStream_t stream) {
+  switch (epi) {
+    case MC_EPI_STORE_F32:
+      return launch_variant<false, false, BN, MC_EPI_STORE_F32, MODE, true>(ta, tb, g, stream);
+    case MC_EPI_STORE_BF16:
+      return launch_variant<false, false, BN, MC_EPI_STORE_BF16, MODE, true>(ta, tb, g, stream);
+    case MC_EPI_BIAS_BF16:
+      return launch_variant<false, false, BN, MC_EPI_BIAS_BF16, MODE, true>(ta, tb, g, stream);
+    case MC_EPI_BIAS_GELU:
+      return launch_variant<false, false, BN, MC_EPI_BIAS_GELU, MODE, true>(ta, tb, g, stream);
+    case MC_EPI_BIAS_RESID_F32:
+      return launch_variant<false, false, BN, MC_EPI_BIAS_RESID_F32, MODE, true>(ta, tb, g,
+                                                                                  stream);
+    case MC_EPI_GELU_BWD:
+      return launch_variant<false, false, BN, MC_EPI_GELU_BWD, MODE, true>(ta, tb, g, stream);
     default:
       return MC_ERR_ARGUMENT;
   }
@@ -653,9 +697,70 @@ int launch_gemm(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda,
   g.ldaux = ldaux;
   g.accumulate = accumulate;
   g.status = status;
+  g.idesc_f8 = 0;
+  g.a_scale_inv = g.b_scale_inv = nullptr;
   if (pair) return dispatch_epilogue<256, kDuo>(epi, a_layout, b_layout, ta, tb, g, stream);
   return bn == 256 ? dispatch_epilogue<256, kSolo>(epi, a_layout, b_layout, ta, tb, g, stream)
                    : dispatch_epilogue<128, kSolo>(epi, a_layout, b_layout, ta, tb, g, stream);
+}
+
+int launch_gemm_fp8(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_t lda, int a_format,
+                    const uint8_t* B, int64_t ldb, int b_format, const float* a_scale_inv,
+                    const float* b_scale_inv, void* out, int64_t ldc, int epi,
+                    const uint16_t* bias, const void* aux, int64_t ldaux, int accumulate,
+                    int k_parts, int* status, cudaStream_t stream) {
+  if (M < 1 || N < 64 || K < 1 || N % 64 != 0 || K % 16 != 0) return MC_ERR_UNSUPPORTED;
+  if (M > (1 << 30) || N > (1 << 30) || K > (1 << 30)) return MC_ERR_UNSUPPORTED;
+  if (k_parts < 1 || K % k_parts != 0) return MC_ERR_ARGUMENT;
+  if (a_format < 0 || a_format > 1 || b_format < 0 || b_format > 1) return MC_ERR_ARGUMENT;
+  if (epi < MC_EPI_STORE_F32 || epi > MC_EPI_GELU_BWD) return MC_ERR_ARGUMENT;
+  if (!A || !B || !out || !a_scale_inv || !b_scale_inv) return MC_ERR_NULLPTR;
+  const bool needs_bias =
+      epi == MC_EPI_BIAS_BF16 || epi == MC_EPI_BIAS_GELU || epi == MC_EPI_BIAS_RESID_F32;
+  const bool needs_aux =
+      epi == MC_EPI_BIAS_GELU || epi == MC_EPI_BIAS_RESID_F32 || epi == MC_EPI_GELU_BWD;
+  if ((needs_bias && !bias) || (needs_aux && !aux)) return MC_ERR_NULLPTR;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(out) || (bias && !aligned16(bias)) ||
+      (aux && !aligned16(aux)) || (reinterpret_cast<uintptr_t>(a_scale_inv) & 3u) ||
+      (reinterpret_cast<uintptr_t>(b_scale_inv) & 3u))
+    return MC_ERR_ALIGN;
+  if (lda % 16 || ldb % 16 || ldc % 8 || (needs_aux && ldaux % 8)) return MC_ERR_ALIGN;
+  if (lda < K || ldb < K || ldc < N || (needs_aux && ldaux < N)) return MC_ERR_ARGUMENT;
+
+  const int64_t m_tiles = (M + BM - 1) / BM;
+  const int bn = ((N % 256 == 0) && m_tiles * (N / 256) >= num_sms()) ? 256 : 128;
+  const bool pair = bn == 256 && m_tiles >= 2;
+  constexpr int kBKE = 2 * BK;  // 128 one-byte elements per swizzled row
+  CUtensorMap ta, tb;
+  if (!make_tmap(&ta, A, K, M, lda, kBKE, BM, true) ||
+      !make_tmap(&tb, B, K, N, ldb, kBKE, pair ? bn / 2 : bn, true))
+    return MC_ERR_CUDA;
+
+  GemmArgs g;
+  g.M = static_cast<int>(M);
+  g.N = static_cast<int>(N);
+  g.K = static_cast<int>(K);
+  g.num_kb = static_cast<int>((K + kBKE - 1) / kBKE);
+  g.m_tiles = static_cast<int>(m_tiles);
+  g.n_tiles = static_cast<int>((N + bn - 1) / bn);
+  const int64_t tiles = m_tiles * g.n_tiles;
+  if (tiles > (1 << 30)) return MC_ERR_UNSUPPORTED;
+  g.num_tiles = static_cast<int>(tiles);
+  g.m_pairs = static_cast<int>((m_tiles + 1) / 2);
+  g.num_units = g.m_pairs * g.n_tiles;
+  g.out = out;
+  g.ldc = ldc;
+  g.bias = reinterpret_cast<const __nv_bfloat16*>(bias);
+  g.aux = aux;
+  g.ldaux = ldaux;
+  g.accumulate = accumulate;
+  g.status = status;
+  g.idesc_f8 = idesc_f8_f32(pair ? 2 * BM : BM, bn, a_format, b_format);
+  g.a_scale_inv = a_scale_inv;
+  g.b_scale_inv = b_scale_inv;
+  if (pair) return dispatch_epilogue_f8<256, kDuo>(epi, ta, tb, g, stream);
+  return bn == 256 ? dispatch_epilogue_f8<256, kSolo>(epi, ta, tb, g, stream)
+                   : dispatch_epilogue_f8<128, kSolo>(epi, ta, tb, g, stream);
 }
 
 }  // namespace mc

@@ -67,6 +67,22 @@ int launch_gemm(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda,
                 const uint16_t* bias, const void* aux, int64_t ldaux, int accumulate, int k_parts,
                 int* status, cudaStream_t stream);
 
+// 8-bit floating-point GEMM: A [M, K], B [N, K] K-major bytes (format 0 =
+// E4M3, 1 = E5M2), fp32 accumulation scaled by *a_scale_inv * *b_scale_inv,
+// then the same fused epilogues as launch_gemm.
+int launch_gemm_fp8(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_t lda, int a_format,
+                    const uint8_t* B, int64_t ldb, int b_format, const float* a_scale_inv,
+                    const float* b_scale_inv, void* out, int64_t ldc, int epi,
+                    const uint16_t* bias, const void* aux, int64_t ldaux, int accumulate,
+                    int k_parts, int* status, cudaStream_t stream);
+
+// Per-tensor current scaling to 8-bit floats: amax of n fp32 (in_bf16 =
+// false) or bf16 values, scale = fmax / amax, out = RNE_satfinite(x * scale);
+// writes scale_inv[0] = 1 / scale.  `scratch` holds fp8_scratch_floats().
+size_t fp8_scratch_floats();
+int launch_fp8_quantize(const void* in, bool in_bf16, int64_t n, int format, uint8_t* out,
+                        float* scale_inv, float* scratch, cudaStream_t stream);
+
 int launch_attention_forward(const uint16_t* qkv, uint16_t* o, float* lse, int b, int s, int H,
                              int d, int* status, cudaStream_t stream);
 int launch_attention_forward_tc(const uint16_t* qkv, uint16_t* o, float* lse, int b, int s, int H,

@@ -265,6 +265,27 @@ __device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, 
       : "memory");
 }
 
+// 8-bit floating-point MMA (kind::f8f6f4, K = 32 per instruction): the
+// operand formats (E4M3 = 0, E5M2 = 1) are in the instruction descriptor.
+__device__ __forceinline__ void umma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                        uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_f8_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Commit of the pair's MMAs, arriving on the mbarrier at the same offset in
 // each CTA of the cluster in `mask`.
 __device__ __forceinline__ void umma_commit_pair_mc(uint64_t* bar, uint16_t mask) {
@@ -380,6 +401,16 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n, bool a_mn_ma
          | (static_cast<uint32_t>(b_mn_major) << 16)  // B major-ness
          | (static_cast<uint32_t>(n >> 3) << 17)    // N / 8
          | (static_cast<uint32_t>(m >> 4) << 24);   // M / 16
+}
+
+// Instruction descriptor of a kind::f8f6f4 MMA with fp32 accumulation:
+// a_fmt / b_fmt 0 = E4M3, 1 = E5M2; K-major operands.
+__host__ __device__ constexpr uint32_t idesc_f8_f32(int m, int n, int a_fmt, int b_fmt) {
+  return (1u << 4)                                   // D format: f32
+         | (static_cast<uint32_t>(a_fmt) << 7)       // A format
+         | (static_cast<uint32_t>(b_fmt) << 10)      // B format
+         | (static_cast<uint32_t>(n >> 3) << 17)     // N / 8
+         | (static_cast<uint32_t>(m >> 4) << 24);    // M / 16
 }
 
 // ---------------------------------------------------------------- misc

@@ -1,0 +1,131 @@
+"""FP8 path on the GPU against the oracle (oracle/fp8.py): the quantiser
+bit for bit (bytes and scale), the GEMM on oracle-quantised operands against
+the exact product of the decoded operands, and the whole quantise + GEMM
+pipeline."""
+import numpy as np
+import pytest
+import torch
+
+import oracle.layer as O
+from oracle import fp8 as F
+from megatron_transformer_layer_gb300 import _lib as L
+from parity import assert_close
+
+from gpu_util import DEV, check_status, status, to_f64
+
+pytestmark = pytest.mark.gpu
+
+FMT = {"e4m3": L.FP8_E4M3, "e5m2": L.FP8_E5M2}
+
+
+def _quantize_gpu(x, fmt):
+    out = torch.empty(x.numel(), dtype=torch.uint8, device=DEV)
+    sinv = torch.empty(1, dtype=torch.float32, device=DEV)
+    scratch = torch.empty(L.mc_fp8_scratch_floats(), dtype=torch.float32, device=DEV)
+    assert L.mc_fp8_quantize(x, out, sinv, scratch, FMT[fmt]) == 0
+    torch.cuda.synchronize()
+    return out, sinv
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+@pytest.mark.parametrize("n,bf16", [(100003, False), (65536, True), (7, False)])
+def test_quantize_bit_exact(fmt, n, bf16):
+    rng = np.random.default_rng(n)
+    x = (rng.standard_normal(n) * 3.0 * 2.0 ** rng.integers(-8, 8, n)).astype(np.float32)
+    xt = torch.from_numpy(x).to(DEV)
+    if bf16:
+        xt = xt.bfloat16()
+        x = xt.float().cpu().numpy()
+    q, sinv = _quantize_gpu(xt, fmt)
+    q_ref, sinv_ref = F.quantize(x, fmt)
+    assert np.float32(sinv.item()) == sinv_ref
+    got = q.cpu().numpy()
+    bad = np.nonzero(got != q_ref)[0]
+    assert bad.size == 0, f"{bad.size} bytes differ, first at {bad[:5]}: {got[bad[:5]]} vs {q_ref[bad[:5]]}"
+
+
+def _gemm_case(M, N, K, afmt, bfmt, epi, seed=0):
+    rng = np.random.default_rng(seed)
+    a32 = rng.standard_normal((M, K)).astype(np.float32)
+    b32 = (rng.standard_normal((N, K)) * 0.05).astype(np.float32)
+    qa, sa = F.quantize(a32, afmt)
+    qb, sb = F.quantize(b32, bfmt)
+    acc = F.gemm_fp8(qa, afmt, sa, qb, bfmt, sb)
+    bias = rng.standard_normal(N).astype(np.float32)
+    bias_bf16 = torch.from_numpy(bias).bfloat16()
+    bias64 = bias_bf16.double().numpy()
+    aux64 = rng.standard_normal((M, N))
+    A = torch.from_numpy(qa).to(DEV)
+    B = torch.from_numpy(qb).to(DEV)
+    SA = torch.tensor([sa], dtype=torch.float32, device=DEV)
+    SB = torch.tensor([sb], dtype=torch.float32, device=DEV)
+    f32_out = epi in (L.MC_EPI_STORE_F32, L.MC_EPI_BIAS_RESID_F32)
+    out = torch.zeros(M * N, dtype=torch.float32 if f32_out else torch.bfloat16, device=DEV)
+    aux = None
+    if epi == L.MC_EPI_BIAS_GELU:
+        aux = torch.empty(M * N, dtype=torch.bfloat16, device=DEV)
+    elif epi == L.MC_EPI_BIAS_RESID_F32:
+        aux = torch.from_numpy(aux64.astype(np.float32)).to(DEV)
+        aux64 = aux64.astype(np.float32).astype(np.float64)
+    elif epi == L.MC_EPI_GELU_BWD:
+        aux_b = torch.from_numpy(aux64.astype(np.float32)).bfloat16()
+        aux64 = aux_b.double().numpy()
+        aux = aux_b.to(DEV)
+    st = status()
+    rc = L.mc_gemm_fp8(M, N, K, A, K, FMT[afmt], B, K, FMT[bfmt], SA, SB, out, N, epi,
+                       bias=bias_bf16.to(DEV), aux=aux, ldaux=N, status=st)
+    assert rc == 0, L.mc_strerror(rc)
+    check_status(st)
+    got = to_f64(out).reshape(M, N)
+    if epi == L.MC_EPI_STORE_F32:
+        # fp32 accumulation of exactly representable products
+        assert_close("fp8 gemm f32", got, acc, 1e-4, 1e-5)
+        return
+    if epi == L.MC_EPI_STORE_BF16:
+        ref = acc
+    elif epi == L.MC_EPI_BIAS_BF16:
+        ref = acc + bias64
+    elif epi == L.MC_EPI_BIAS_GELU:
+        assert_close("fp8 gemm hp", to_f64(aux).reshape(M, N), acc + bias64)
+        ref = O.gelu_tanh(acc + bias64)
+    elif epi == L.MC_EPI_BIAS_RESID_F32:
+        ref = acc + bias64 + aux64
+    else:
+        ref = acc * O.gelu_tanh_grad(aux64)
+    assert_close(f"fp8 gemm epi={epi}", got, ref)
+
+
+@pytest.mark.parametrize("M,N,K", [(200, 320, 192), (130, 256, 512), (2000, 2560, 256),
+                                   (2100, 2304, 384)])
+@pytest.mark.parametrize("afmt,bfmt", [("e4m3", "e4m3"), ("e5m2", "e4m3")])
+def test_gemm_fp8_is_the_product_of_the_decoded_operands(M, N, K, afmt, bfmt):
+    _gemm_case(M, N, K, afmt, bfmt, L.MC_EPI_STORE_F32, seed=M + K)
+
+
+@pytest.mark.parametrize("epi", [L.MC_EPI_STORE_BF16, L.MC_EPI_BIAS_BF16, L.MC_EPI_BIAS_GELU,
+                                 L.MC_EPI_BIAS_RESID_F32, L.MC_EPI_GELU_BWD])
+def test_gemm_fp8_epilogues(epi):
+    _gemm_case(2100, 2304, 256, "e4m3", "e4m3", epi, seed=7)
+
+
+def test_quantize_then_gemm_pipeline():
+    """GPU quantisation of both operands, then the FP8 GEMM: equals the
+    oracle's pipeline (bit-exact quantisation makes the inputs identical)."""
+    M, N, K = 1024, 2048, 1024
+    rng = np.random.default_rng(5)
+    a32 = rng.standard_normal((M, K)).astype(np.float32)
+    b32 = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+    qa, sa = _quantize_gpu(torch.from_numpy(a32).to(DEV), "e4m3")
+    qb, sb = _quantize_gpu(torch.from_numpy(b32).to(DEV), "e4m3")
+    out = torch.empty(M * N, dtype=torch.float32, device=DEV)
+    st = status()
+    assert L.mc_gemm_fp8(M, N, K, qa, K, 0, qb, K, 0, sa, sb, out, N, L.MC_EPI_STORE_F32,
+                         status=st) == 0
+    check_status(st)
+    ra, rsa = F.quantize(a32, "e4m3")
+    rb, rsb = F.quantize(b32, "e4m3")
+    ref = F.gemm_fp8(ra, "e4m3", rsa, rb, "e4m3", rsb)
+    assert_close("fp8 pipeline", to_f64(out).reshape(M, N), ref, 1e-4, 1e-5)
+    # and against the unquantised product: FP8 operand rounding only
+    m = np.abs(to_f64(out).reshape(M, N) - a32.astype(np.float64) @ b32.T.astype(np.float64))
+    assert m.mean() / np.abs(a32.astype(np.float64) @ b32.T.astype(np.float64)).mean() < 0.05
