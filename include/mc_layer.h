@@ -256,6 +256,14 @@ int mc_attention_backward_noalloc(const uint16_t* qkv, const uint16_t* o, const 
                                   int32_t seq_len, int32_t heads, int32_t head_dim, int* status,
                                   void* stream);
 
+/* Failure-detection self-test: one kernel waits on an mbarrier that nothing
+ * arrives on, bounded by timeout_ns (1 us to 100 ms, else MC_ERR_ARGUMENT),
+ * exactly as every wait of the library is bounded.  When the limit passes it
+ * records MC_ERR_DEVICE_TIMEOUT in status[0] and the site code 30 in
+ * status[1] (status: int[64] device memory, zeroed by the caller) and
+ * returns; the context stays usable.  No fault, trap or hang is involved. */
+int mc_selftest_wait_timeout(int64_t timeout_ns, int* status, void* stream);
+
 /* ---- 8-bit floating-point GEMMs (the Megatron-Core listing, 混合精度:
  * FP8 / FP4 training on Blackwell Ultra, --fp8-format hybrid = E4M3 forward,
  * E5M2 gradients).  Formats: 0 = E4M3 (largest finite 448), 1 = E5M2

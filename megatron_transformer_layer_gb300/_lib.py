@@ -89,6 +89,7 @@ _SIGNATURES = {
     "mc_attention_forward": (_INT, [_P, _P, _P, _I32, _I32, _I32, _I32, _P, _P]),
     "mc_attention_backward": (_INT, [_P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _P, _P]),
     "mc_attention_backward_noalloc": (_INT, [_P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _P, _P]),
+    "mc_selftest_wait_timeout": (_INT, [_I64, _P, _P]),
     "mc_fp8_scratch_floats": (_SZ, []),
     "mc_fp8_quantize": (_INT, [_P, _I32, _I64, _I32, _P, _P, _P, _P, _P]),
     "mc_gemm_fp8": (_INT, [_I64, _I64, _I64, _P, _I64, _I32, _P, _I64, _I32, _P, _P, _P, _I64,
@@ -279,3 +280,8 @@ def mc_gemm_fp8(M, N, K, A, lda, a_format, B, ldb, b_format, a_scale_inv, b_scal
                              _ptr(a_scale_inv), _ptr(b_scale_inv), _ptr(out), ldc, epilogue,
                              _ptr(bias), _ptr(aux), ldaux, accumulate, k_parts, _ptr(status),
                              _stream(stream))
+
+
+def mc_selftest_wait_timeout(timeout_ns, status, stream=None) -> int:
+    """Runs a kernel whose bounded wait is made to run out (failure-path test)."""
+    return lib().mc_selftest_wait_timeout(timeout_ns, _ptr(status), _stream(stream))

@@ -24,6 +24,7 @@ enum ErrorSite : int {
   kSiteGemmDrain = 4,
   kSiteLayerNorm = 10,
   kSiteAttention = 20,
+  kSiteSelfTest = 30,
 };
 
 // Row-major bf16 leading dimension bound used by the shape checks.

@@ -115,6 +115,14 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, i
   return __all_sync(0xffffffffu, ok);
 }
 
+// mbar_wait_warp with an explicit time limit (the library's own waits use the
+// default limit).
+__device__ __forceinline__ bool mbar_wait_warp_limit(uint64_t* bar, uint32_t parity, int* status,
+                                                     int where, uint64_t timeout_ns) {
+  const bool ok = mbar_wait(bar, parity, status, where, timeout_ns);
+  return __all_sync(0xffffffffu, ok);
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

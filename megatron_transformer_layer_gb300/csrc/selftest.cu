@@ -1,0 +1,34 @@
+// Self-test of the failure path every kernel of the library relies on: a
+// bounded mbarrier wait that runs out records MC_ERR_DEVICE_TIMEOUT and where
+// in the status word, and the kernel returns, leaving the context usable.
+#include <cuda_runtime.h>
+
+#include "mc_layer_internal.h"
+#include "ptx.cuh"
+
+namespace mc {
+namespace {
+
+// One warp waits (bounded) on an mbarrier that nothing arrives on.
+__global__ void wait_timeout_kernel(uint64_t timeout_ns, int* status) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  mbar_wait_warp_limit(&bar, 0, status, kSiteSelfTest, timeout_ns);
+}
+
+}  // namespace
+}  // namespace mc
+
+using namespace mc;
+
+extern "C" int mc_selftest_wait_timeout(int64_t timeout_ns, int* status, void* stream) {
+  if (timeout_ns < 1000 || timeout_ns > 100000000) return MC_ERR_ARGUMENT;  // 1 us .. 100 ms
+  if (!status) return MC_ERR_NULLPTR;
+  wait_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<uint64_t>(timeout_ns), status);
+  return cudaGetLastError() == cudaSuccess ? MC_OK : MC_ERR_CUDA;
+}

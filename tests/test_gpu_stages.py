@@ -243,3 +243,15 @@ def test_attention_long_sequence_many_heads():
         assert_close(f"dq head {hh}", g[:, c], dq)
         assert_close(f"dk head {hh}", g[:, ck], dk)
         assert_close(f"dv head {hh}", g[:, cv], dv)
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    """Failure detection on the GPU without a fault: a wait on a barrier that
+    nothing arrives on gives up after its limit, the status word says
+    MC_ERR_DEVICE_TIMEOUT at the self-test site, and the next launches run."""
+    st = status()
+    assert L.mc_selftest_wait_timeout(2_000_000, st) == 0  # 2 ms
+    torch.cuda.synchronize()
+    assert int(st[0].item()) == L.MC_ERR_DEVICE_TIMEOUT and int(st[1].item()) == 30
+    assert L.mc_selftest_wait_timeout(10**9, st) == L.MC_ERR_ARGUMENT  # limits capped
+    _gemm_case(130, 192, 128, 0, 0, L.MC_EPI_STORE_BF16)  # the context still works
