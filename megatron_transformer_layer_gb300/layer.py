@@ -62,6 +62,23 @@ class TransformerLayer:
         self._grads_c = L.make_grads(self.grads)
         self._x = None
 
+    @staticmethod
+    def random_params(hidden, heads, ffn_hidden, head_dim=0, device="cuda", seed=0, std=0.02):
+        """bf16 parameters in the library's layout: weights N(0, std^2), biases
+        0, LayerNorm gains 1 and shifts 0 (the usual GPT initialisation)."""
+        d = head_dim if head_dim else hidden // heads
+        a = heads * d
+        g = torch.Generator(device=device).manual_seed(seed)
+        w = {"w_qkv": (3 * a, hidden), "w_o": (hidden, a), "w_fc1": (ffn_hidden, hidden),
+             "w_fc2": (hidden, ffn_hidden)}
+        p = {k: (torch.randn(*v, device=device, generator=g) * std).bfloat16() for k, v in w.items()}
+        for k, n in (("b_qkv", 3 * a), ("b_o", hidden), ("b_fc1", ffn_hidden), ("b_fc2", hidden),
+                     ("ln1_b", hidden), ("ln2_b", hidden)):
+            p[k] = torch.zeros(n, device=device, dtype=torch.bfloat16)
+        for k in ("ln1_g", "ln2_g"):
+            p[k] = torch.ones(hidden, device=device, dtype=torch.bfloat16)
+        return p
+
     def set_params(self, params):
         self.params = params
         self.weights = L.make_weights(params)

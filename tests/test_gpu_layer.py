@@ -258,3 +258,20 @@ def test_c4_layer_is_bitwise_repeatable():
     for k in runs[0][2]:
         assert torch.equal(runs[0][2][k], runs[1][2][k]), k
     assert torch.isfinite(runs[0][0]).all() and torch.isfinite(runs[0][1]).all()
+
+
+def test_random_params_layer_runs():
+    """The convenience initialisation (used in the README) gives a runnable
+    layer whose output is finite and whose fc2 bias gradient is the column sum
+    of dy."""
+    from megatron_transformer_layer_gb300.layer import TransformerLayer
+    params = TransformerLayer.random_params(1024, 8, 4096)
+    layer = TransformerLayer(1, 256, 1024, 8, 4096, tp_parts=2, params=params)
+    x = torch.randn(256, 1024, device=DEV)
+    dy = torch.randn(256, 1024, device=DEV).bfloat16().float()
+    y = layer.forward(x)
+    layer.backward(dy)
+    torch.cuda.synchronize()
+    assert layer.device_status() == 0 and torch.isfinite(y).all()
+    ref = dy.double().sum(0)
+    assert torch.allclose(layer.grads["b_fc2"].double(), ref, rtol=1e-5, atol=1e-3)
