@@ -619,6 +619,33 @@ int dispatch_epilogue_f8(int epi, const CUtensorMap& ta, const CUtensorMap& tb, 
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Tile shape of an M x N product: the one whose estimated time, waves x time
+// per tile, is smallest.  Clocks per 16-deep K step (bf16; 32-deep fp8)
+// measured on this GPU with one MMA stream per SM and operands resident:
+// SM-pair 256 x 256 tile 128 (each SM reads 8 KB of operands per step), one
+// CTA 128 x 256 161, one CTA 128 x 128 97 (shared-memory operand reads bound
+// the single-CTA shapes).  Pairs need N % 256 == 0 and two M-tiles.
+struct TileChoice {
+  int bn;
+  bool pair;
+};
+TileChoice choose_tiles(int64_t m_tiles, int64_t N) {
+  const int64_t sms = num_sms();
+  const int64_t clusters = sms / 2;
+  auto waves = [](int64_t units, int64_t slots) { return (units + slots - 1) / slots; };
+  TileChoice best = {128, false};
+  int64_t best_cost = waves(m_tiles * ((N + 127) / 128), sms) * 97;
+  if (N % 256 == 0) {
+    const int64_t solo = waves(m_tiles * (N / 256), sms) * 161;
+    if (solo < best_cost) best = {256, false}, best_cost = solo;
+    if (m_tiles >= 2) {
+      const int64_t duo = waves(((m_tiles + 1) / 2) * (N / 256), clusters) * 128;
+      if (duo <= best_cost) best = {256, true}, best_cost = duo;
+    }
+  }
+  return best;
+}
+
 }  // namespace
 
 bool make_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
@@ -664,11 +691,10 @@ int launch_gemm(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda,
       (needs_aux && ldaux < N))
     return MC_ERR_ARGUMENT;
 
-  // Wide tiles when there are enough of them to fill the machine; wide-tile
-  // problems with at least two M-tiles run on SM pairs (256 x 256 tiles).
   const int64_t m_tiles = (M + BM - 1) / BM;
-  const int bn = ((N % 256 == 0) && m_tiles * (N / 256) >= num_sms()) ? 256 : 128;
-  const bool pair = bn == 256 && m_tiles >= 2;
+  const TileChoice tc = choose_tiles(m_tiles, N);
+  const int bn = tc.bn;
+  const bool pair = tc.pair;
 
   CUtensorMap ta, tb;
   bool ok = a_layout == 0 ? make_tmap(&ta, A, K, M, lda, BK, BM)
@@ -728,8 +754,9 @@ int launch_gemm_fp8(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_t l
   if (lda < K || ldb < K || ldc < N || (needs_aux && ldaux < N)) return MC_ERR_ARGUMENT;
 
   const int64_t m_tiles = (M + BM - 1) / BM;
-  const int bn = ((N % 256 == 0) && m_tiles * (N / 256) >= num_sms()) ? 256 : 128;
-  const bool pair = bn == 256 && m_tiles >= 2;
+  const TileChoice tc = choose_tiles(m_tiles, N);
+  const int bn = tc.bn;
+  const bool pair = tc.pair;
   constexpr int kBKE = 2 * BK;  // 128 one-byte elements per swizzled row
   CUtensorMap ta, tb;
   if (!make_tmap(&ta, A, K, M, lda, kBKE, BM, true) ||
