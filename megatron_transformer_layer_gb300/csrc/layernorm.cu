@@ -241,9 +241,9 @@ __global__ void __launch_bounds__(256) reduce_partials_kernel(const float* __res
   }
 }
 
-// Column partial sums of a [rows, n] matrix over kColsumRowSplits row ranges;
-// thread owns 8 consecutive columns.  Optionally writes a bf16 copy of an fp32
-// input.
+// Column partial sums of a [rows, n] matrix over gridDim.y row ranges; a
+// thread owns 8 consecutive columns and walks its rows four at a time (four
+// loads in flight).  Optionally writes a bf16 copy of an fp32 input.
 template <bool IN_BF16>
 __global__ void colsum_partial_kernel(const void* __restrict__ in, int64_t rows, int64_t n,
                                       float* __restrict__ partials, uint16_t* __restrict__ copy) {
@@ -254,6 +254,7 @@ __global__ void colsum_partial_kernel(const void* __restrict__ in, int64_t rows,
   const int64_t r0 = split * per;
   const int64_t r1 = r0 + per < rows ? r0 + per : rows;
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
   for (int64_t r = r0; r < r1; ++r) {
     if constexpr (IN_BF16) {
       const uint4 w = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(in) + r * n + c8);
@@ -395,9 +396,13 @@ int launch_colsum(const void* in, bool in_bf16, int64_t rows, int64_t n, float* 
   if (rows < 1 || n < 8 || n % 8) return MC_ERR_UNSUPPORTED;
   if (!in || !out || !partials) return MC_ERR_NULLPTR;
   if (!al16(in) || !al16(partials) || (bf16_copy && !al16(bf16_copy))) return MC_ERR_ALIGN;
-  const int splits = static_cast<int>(rows < kColsumRowSplits ? rows : kColsumRowSplits);
   const int64_t threads_needed = n / 8;
-  dim3 grid(static_cast<unsigned>((threads_needed + 127) / 128), splits);
+  const int64_t col_blocks = (threads_needed + 127) / 128;
+  int64_t want = (4 * static_cast<int64_t>(num_sms()) + col_blocks - 1) / col_blocks;
+  want = want < kColsumMinSplits ? kColsumMinSplits : want;
+  want = want > kColsumMaxSplits ? kColsumMaxSplits : want;
+  const int splits = static_cast<int>(rows < want ? rows : want);
+  dim3 grid(static_cast<unsigned>(col_blocks), splits);
   if (in_bf16)
     colsum_partial_kernel<true><<<grid, 128, 0, st>>>(in, rows, n, partials, nullptr);
   else

@@ -136,7 +136,7 @@ Work plan_ws(const Dims& D, bool with_saved, void* p, size_t* bytes) {
   const size_t ln_part = layernorm_backward_scratch_floats(D.T, static_cast<int>(D.h));
   int64_t widest = D.f > 3 * D.a ? D.f : 3 * D.a;
   if (D.h > widest) widest = D.h;
-  const size_t col_part = static_cast<size_t>(kColsumRowSplits) * widest;
+  const size_t col_part = static_cast<size_t>(kColsumMaxSplits) * widest;
   W.partials = c.take<float>(ln_part > col_part ? ln_part : col_part);
   W.recompute_saved = nullptr;
   if (with_saved) {

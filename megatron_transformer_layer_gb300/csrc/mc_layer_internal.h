@@ -34,8 +34,10 @@ constexpr int kMaxLayerNormHidden = 16384;
 // 3 * min(rows, kLnBwdMaxBlocks) * h floats of scratch.
 constexpr int kLnBwdMaxBlocks = 456;
 
-// Row splits of the column-sum (bias gradient) kernel.
-constexpr int kColsumRowSplits = 64;
+// Row splits of the column-sum (bias gradient) kernel: enough for four
+// blocks per SM, at least 64, at most kColsumMaxSplits.
+constexpr int kColsumMinSplits = 64;
+constexpr int kColsumMaxSplits = 512;
 
 int num_sms();  // SM count of the current device (cached per device)
 
@@ -58,7 +60,7 @@ size_t layernorm_backward_scratch_floats(int64_t rows, int h);
 
 // Column sums over rows of a [rows, n] matrix (bf16 if in_bf16 else fp32);
 // optionally writes a bf16 copy of an fp32 input.  out[n] = (accumulate ?
-// out : 0) + sum.  `partials` holds kColsumRowSplits * n floats.
+// out : 0) + sum.  `partials` holds kColsumMaxSplits * n floats.
 int launch_colsum(const void* in, bool in_bf16, int64_t rows, int64_t n, float* out,
                   int accumulate, uint16_t* bf16_copy, float* partials, int* status,
                   cudaStream_t stream);
