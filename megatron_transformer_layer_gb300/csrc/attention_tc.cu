@@ -225,18 +225,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld_32x32b_x32_nowait(tS[st] + lane_off + 96, x + 96);
       tmem_ld_wait();
       const int key0 = (kb0 + j) * BKV;
-      float mx = -INFINITY;
       if (key0 + BKV - 1 > q0 || key0 + BKV > s) {  // diagonal or ragged block
         const int lim = min(q + 1, s) - key0;       // keys [0, lim) are visible
 #pragma unroll
-        for (int i = 0; i < BKV; ++i) {
-          x[i] = i < lim ? x[i] : -INFINITY;
-          mx = fmaxf(mx, x[i]);
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < BKV; ++i) mx = fmaxf(mx, x[i]);
+        for (int i = 0; i < BKV; ++i) x[i] = i < lim ? x[i] : -INFINITY;
       }
+      // Row maximum as eight independent chains, then a tree: one warp per
+      // scheduler has no other work to hide a 128-long dependent chain.
+      float mx8[8];
+#pragma unroll
+      for (int r = 0; r < 8; ++r) mx8[r] = x[r];
+#pragma unroll
+      for (int i = 8; i < BKV; i += 8) {
+#pragma unroll
+        for (int r = 0; r < 8; ++r) mx8[r] = fmaxf(mx8[r], x[i + r]);
+      }
+      float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       mx *= scale;  // raw scores; scale > 0 commutes with max
       const float m_new = fmaxf(m, mx);
       const bool need = j > 0 && m_new > m + kRescaleThreshold;
@@ -266,17 +271,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       uint32_t pk[BKV / 2];
-      float sum0 = 0.f, sum1 = 0.f;
+      float sm8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       const float neg_m = -m;
 #pragma unroll
       for (int i = 0; i < BKV / 2; ++i) {
         const float p0 = fast_exp2(fmaf(x[2 * i], scale, neg_m));
         const float p1 = fast_exp2(fmaf(x[2 * i + 1], scale, neg_m));
-        sum0 += p0;
-        sum1 += p1;
+        sm8[(2 * i) & 7] += p0;
+        sm8[(2 * i + 1) & 7] += p1;
         pk[i] = pack_bf16x2(p0, p1);
       }
-      const float sum = sum0 + sum1;
+      const float sum = ((sm8[0] + sm8[1]) + (sm8[2] + sm8[3])) +
+                        ((sm8[4] + sm8[5]) + (sm8[6] + sm8[7]));
       l += sum;
 #pragma unroll
       for (int c = 0; c < BKV / 64; ++c) {
