@@ -21,6 +21,8 @@ namespace {
 template <int D>
 __global__ void attn_bwd_pre_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
                                     float* __restrict__ delta, int64_t T, int s, int H) {
+  pdl_wait();  // the previous kernel on the stream has completed
+  pdl_launch();
   const int64_t wid = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
   const int l = threadIdx.x & 31;
   if (wid >= T * H) return;
@@ -52,7 +54,7 @@ int bwd_launch(const uint16_t* qkv, const uint16_t* o, const float* lse, const u
                uint16_t* dqkv, float* delta, int b, int s, int H, int* status, cudaStream_t st) {
   const int64_t T = static_cast<int64_t>(b) * s;
   const int64_t warps = T * H;
-  attn_bwd_pre_kernel<D><<<static_cast<unsigned>((warps * 32 + 255) / 256), 256, 0, st>>>(
+  launch_kernel(attn_bwd_pre_kernel<D>, dim3(static_cast<unsigned>((warps * 32 + 255) / 256)), dim3(256), 0, st, 1, 
       o, dout, delta, T, s, H);
   if (cudaGetLastError() != cudaSuccess) return MC_ERR_CUDA;
   return launch_attention_backward_tc(qkv, lse, dout, dqkv, delta, b, s, H, D, status, st);
@@ -67,9 +69,9 @@ int launch_attention_delta(const uint16_t* o, const uint16_t* dout, float* delta
   const int64_t T = static_cast<int64_t>(b) * s;
   const unsigned blocks = static_cast<unsigned>((T * H * 32 + 255) / 256);
   if (d == 64)
-    attn_bwd_pre_kernel<64><<<blocks, 256, 0, st>>>(o, dout, delta, T, s, H);
+    launch_kernel(attn_bwd_pre_kernel<64>, dim3(blocks), dim3(256), 0, st, 1, o, dout, delta, T, s, H);
   else
-    attn_bwd_pre_kernel<128><<<blocks, 256, 0, st>>>(o, dout, delta, T, s, H);
+    launch_kernel(attn_bwd_pre_kernel<128>, dim3(blocks), dim3(256), 0, st, 1, o, dout, delta, T, s, H);
   return cudaGetLastError() == cudaSuccess ? MC_OK : MC_ERR_CUDA;
 }
 

@@ -45,6 +45,8 @@ template <int D>
 __global__ void cp_merge_kernel(const float* __restrict__ part_o, const float* __restrict__ part_lse,
                                 uint16_t* __restrict__ o, float* __restrict__ lse, int b, int s,
                                 int H, int c) {
+  pdl_wait();  // the previous kernel on the stream has completed
+  pdl_launch();
   const int64_t wid = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (wid >= static_cast<int64_t>(b) * s * H) return;
@@ -78,6 +80,8 @@ __global__ void cp_merge_kernel(const float* __restrict__ part_o, const float* _
 // One thread per 4 consecutive columns of a token's dQ | dK | dV row.
 __global__ void cp_reduce_kernel(const float* __restrict__ part_dq, const float* __restrict__ part_dkv,
                                  uint16_t* __restrict__ dqkv, int b, int s, int a, int c, int C) {
+  pdl_wait();  // the previous kernel on the stream has completed
+  pdl_launch();
   const int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
   const int64_t per_tok = 3 * static_cast<int64_t>(a) / 4;
   if (idx >= static_cast<int64_t>(b) * s * per_tok) return;
@@ -182,9 +186,9 @@ int mc_attention_forward_cp(const uint16_t* qkv, uint16_t* o, float* lse, int32_
   const int64_t warps = static_cast<int64_t>(b) * s * H;
   const unsigned blocks = static_cast<unsigned>((warps * 32 + 255) / 256);
   if (d == 64)
-    cp_merge_kernel<64><<<blocks, 256, 0, st>>>(part_o, part_lse, o, lse, b, s, H, c);
+    launch_kernel(cp_merge_kernel<64>, dim3(blocks), dim3(256), 0, st, 1, part_o, part_lse, o, lse, b, s, H, c);
   else
-    cp_merge_kernel<128><<<blocks, 256, 0, st>>>(part_o, part_lse, o, lse, b, s, H, c);
+    launch_kernel(cp_merge_kernel<128>, dim3(blocks), dim3(256), 0, st, 1, part_o, part_lse, o, lse, b, s, H, c);
   return cudaGetLastError() == cudaSuccess ? MC_OK : MC_ERR_CUDA;
 }
 
@@ -223,7 +227,7 @@ int mc_attention_backward_cp(const uint16_t* qkv, const uint16_t* o, const float
       }
     }
   const int64_t threads = static_cast<int64_t>(b) * s * (3 * a / 4);
-  cp_reduce_kernel<<<static_cast<unsigned>((threads + 255) / 256), 256, 0, st>>>(
+  launch_kernel(cp_reduce_kernel, dim3(static_cast<unsigned>((threads + 255) / 256)), dim3(256), 0, st, 1, 
       part_dq, part_dkv, dqkv, b, s, static_cast<int>(a), c, C);
   return cudaGetLastError() == cudaSuccess ? MC_OK : MC_ERR_CUDA;
 }

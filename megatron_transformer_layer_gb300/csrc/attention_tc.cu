@@ -122,6 +122,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();  // the previous kernel on the stream has completed
   const uint32_t tS[2] = {tmem + C::kColS0, tmem + C::kColS1};
   const uint32_t tO = tmem + C::kColO;
 
@@ -148,6 +149,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       (kb0 + j) * BKV, bi);
         ++v_issued;
       }
+      pdl_launch();  // every load of this CTA is issued
       // Copies still in flight must land before the CTA exits.
       mbar_wait(q_full, 0, status, kSiteAttention, 200000000ull, false);
       for (int j = k_issued - 1; j >= 0 && j >= k_issued - 2; --j)
@@ -439,6 +441,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();  // the previous kernel on the stream has completed
   const uint32_t tS = tmem, tdP = tmem + 128, tdV = tmem + 256, tdK = tmem + 384;
 
   if (warp == 0) {
@@ -462,6 +465,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         ++issued;
       }
+      pdl_launch();  // every load of this CTA is issued
       mbar_wait(r_full, 0, status, kSiteAttention, 200000000ull, false);
       for (int i = issued - 1; i >= 0 && i >= issued - 2; --i)
         mbar_wait(&st_full[i & 1], (i >> 1) & 1, status, kSiteAttention, 200000000ull, false);
@@ -742,6 +746,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();  // the previous kernel on the stream has completed
   const uint32_t tS = tmem, tdP = tmem + 128, tdQ = tmem + 256, tdS = tmem + 384;
 
   if (warp == 0) {
@@ -769,6 +774,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                       bi);
         ++v_issued;
       }
+      pdl_launch();  // every load of this CTA is issued
       // Copies still in flight must land before the CTA exits: the last
       // K loads (up to 3) and V loads (up to 2).
       mbar_wait(r_full, 0, status, kSiteAttention, 200000000ull, false);
@@ -928,7 +934,7 @@ int launch_bwd_dq_tc(const CUtensorMap& tq, const CUtensorMap& td, const float* 
   });
   if (attr != cudaSuccess) return MC_ERR_CUDA;
   dim3 grid(PART ? part.len / 128 : (s + 127) / 128, H, b);
-  kern<<<grid, kBwdThreads, C::kSmem, st>>>(tq, td, lse, delta, dqkv, s, H, status, part);
+  launch_kernel(kern, dim3(grid), dim3(kBwdThreads), C::kSmem, st, 1, tq, td, lse, delta, dqkv, s, H, status, part);
   return cudaGetLastError() == cudaSuccess ? MC_OK : MC_ERR_CUDA;
 }
 
@@ -945,7 +951,7 @@ int launch_bwd_dkdv_tc(const CUtensorMap& tq, const CUtensorMap& td, const float
   });
   if (attr != cudaSuccess) return MC_ERR_CUDA;
   dim3 grid(PART ? part.len / 128 : (s + 127) / 128, H, b);
-  kern<<<grid, kBwdThreads, C::kSmem, st>>>(tq, td, lse, delta, dqkv, s, H, status, part);
+  launch_kernel(kern, dim3(grid), dim3(kBwdThreads), C::kSmem, st, 1, tq, td, lse, delta, dqkv, s, H, status, part);
   return cudaGetLastError() == cudaSuccess ? MC_OK : MC_ERR_CUDA;
 }
 
@@ -991,7 +997,7 @@ int launch_fwd_tc(const uint16_t* qkv, uint16_t* o, float* lse, int b, int s, in
   });
   if (attr != cudaSuccess) return MC_ERR_CUDA;
   dim3 grid(PART ? part.len / BQ : (s + BQ - 1) / BQ, H, b);
-  kern<<<grid, kThreads, C::kSmem, st>>>(tm, o, lse, s, H, status, part);
+  launch_kernel(kern, dim3(grid), dim3(kThreads), C::kSmem, st, 1, tm, o, lse, s, H, status, part);
   return cudaGetLastError() == cudaSuccess ? MC_OK : MC_ERR_CUDA;
 }
 

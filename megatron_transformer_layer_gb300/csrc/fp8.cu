@@ -31,6 +31,8 @@ __device__ __forceinline__ float load_elem(const void* in, bool bf16, int64_t i)
 template <bool BF16>
 __global__ void amax_partial_kernel(const void* __restrict__ in, int64_t n,
                                     float* __restrict__ partials) {
+  pdl_wait();  // the previous kernel on the stream has completed
+  pdl_launch();
   float m = 0.f;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n; i += stride)
@@ -50,6 +52,8 @@ __global__ void amax_partial_kernel(const void* __restrict__ in, int64_t n,
 // One block of kAmaxBlocks threads.  state[0] = scale; scale_inv[0] = 1 / scale.
 __global__ void fp8_scale_kernel(const float* __restrict__ partials, float fmax,
                                  float* __restrict__ state, float* __restrict__ scale_inv) {
+  pdl_wait();  // the previous kernel on the stream has completed
+  pdl_launch();
   float m = partials[threadIdx.x];
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
@@ -68,6 +72,8 @@ __global__ void fp8_scale_kernel(const float* __restrict__ partials, float fmax,
 template <bool BF16, int FMT>
 __global__ void fp8_cast_kernel(const void* __restrict__ in, int64_t n,
                                 const float* __restrict__ state, uint8_t* __restrict__ out) {
+  pdl_wait();  // the previous kernel on the stream has completed
+  pdl_launch();
   const float sc = state[0];
   constexpr __nv_fp8_interpretation_t kInterp = FMT == 0 ? __NV_E4M3 : __NV_E5M2;
   const int64_t n8 = n / 8;
@@ -119,20 +125,20 @@ int launch_fp8_quantize(const void* in, bool in_bf16, int64_t n, int format, uin
   const int64_t want = (n + kThreadsPerBlock - 1) / kThreadsPerBlock;
   // every partial is written: the grid is exactly kAmaxBlocks blocks
   if (in_bf16)
-    amax_partial_kernel<true><<<kAmaxBlocks, kThreadsPerBlock, 0, st>>>(in, n, partials);
+    launch_kernel(amax_partial_kernel<true>, dim3(kAmaxBlocks), dim3(kThreadsPerBlock), 0, st, 1, in, n, partials);
   else
-    amax_partial_kernel<false><<<kAmaxBlocks, kThreadsPerBlock, 0, st>>>(in, n, partials);
-  fp8_scale_kernel<<<1, kAmaxBlocks, 0, st>>>(partials, fmax, state, scale_inv);
+    launch_kernel(amax_partial_kernel<false>, dim3(kAmaxBlocks), dim3(kThreadsPerBlock), 0, st, 1, in, n, partials);
+  launch_kernel(fp8_scale_kernel, dim3(1), dim3(kAmaxBlocks), 0, st, 1, partials, fmax, state, scale_inv);
   const unsigned grid = static_cast<unsigned>(
       want / 8 + 1 < 4 * static_cast<int64_t>(num_sms()) ? want / 8 + 1 : 4 * num_sms());
   if (in_bf16 && format == 0)
-    fp8_cast_kernel<true, 0><<<grid, kThreadsPerBlock, 0, st>>>(in, n, state, out);
+    launch_kernel(fp8_cast_kernel<true, 0>, dim3(grid), dim3(kThreadsPerBlock), 0, st, 1, in, n, state, out);
   else if (in_bf16)
-    fp8_cast_kernel<true, 1><<<grid, kThreadsPerBlock, 0, st>>>(in, n, state, out);
+    launch_kernel(fp8_cast_kernel<true, 1>, dim3(grid), dim3(kThreadsPerBlock), 0, st, 1, in, n, state, out);
   else if (format == 0)
-    fp8_cast_kernel<false, 0><<<grid, kThreadsPerBlock, 0, st>>>(in, n, state, out);
+    launch_kernel(fp8_cast_kernel<false, 0>, dim3(grid), dim3(kThreadsPerBlock), 0, st, 1, in, n, state, out);
   else
-    fp8_cast_kernel<false, 1><<<grid, kThreadsPerBlock, 0, st>>>(in, n, state, out);
+    launch_kernel(fp8_cast_kernel<false, 1>, dim3(grid), dim3(kThreadsPerBlock), 0, st, 1, in, n, state, out);
   return cudaGetLastError() == cudaSuccess ? MC_OK : MC_ERR_CUDA;
 }
 

@@ -275,6 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // The peer's copies, commits and arrivals target this CTA's
   // barriers: both CTAs must have initialised theirs first.
   if constexpr (kDuoMode) cluster_sync();
+  pdl_wait();  // the previous kernel on the stream has completed
 
   if (warp == 0) {
     if (lane == 0) {
@@ -338,6 +339,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      // Every load of this CTA is issued: the next kernel on the stream may
+      // start its prologue on SMs this grid releases.
+      pdl_launch();
       // Wait for the copies still in flight (the last use of each stage)
       // before the CTA may exit.  kDuo: the even CTA's full barriers count
       // both CTAs' copies, and the closing cluster barrier holds the odd CTA
@@ -544,22 +548,14 @@ int launch_variant(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs&
   if (attr_err != cudaSuccess) return MC_ERR_CUDA;
   if constexpr (PAIR) {
     const int clusters = g.num_units < max_clusters ? g.num_units : max_clusters;
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute at[1];
-    at[0].id = cudaLaunchAttributeClusterDimension;
-    at[0].val.clusterDim.x = 2;
-    at[0].val.clusterDim.y = 1;
-    at[0].val.clusterDim.z = 1;
-    cfg.gridDim = dim3(2 * clusters, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = Cfg::kSmemBytes;
-    cfg.stream = stream;
-    cfg.attrs = at;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, kern, ta, tb, g) != cudaSuccess) return MC_ERR_CUDA;
+    if (launch_kernel(kern, dim3(2 * clusters), dim3(kThreads), Cfg::kSmemBytes, stream, 2u, ta,
+                      tb, g) != cudaSuccess)
+      return MC_ERR_CUDA;
   } else {
     const int grid = g.num_tiles < num_sms() ? g.num_tiles : num_sms();
-    kern<<<grid, kThreads, Cfg::kSmemBytes, stream>>>(ta, tb, g);
+    if (launch_kernel(kern, dim3(grid), dim3(kThreads), Cfg::kSmemBytes, stream, 1u, ta, tb, g) !=
+        cudaSuccess)
+      return MC_ERR_CUDA;
   }
   return cudaGetLastError() == cudaSuccess ? MC_OK : MC_ERR_CUDA;
 }

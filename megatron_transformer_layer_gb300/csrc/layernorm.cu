@@ -68,6 +68,8 @@ __global__ void __launch_bounds__(kLnThreads) ln_fwd_kernel(const float* __restr
                                                             uint16_t* __restrict__ out,
                                                             float* __restrict__ mean_out,
                                                             float* __restrict__ rstd_out, int h) {
+  pdl_wait();  // the previous kernel on the stream has completed
+  pdl_launch();
   __shared__ float red[2 * kLnThreads / 32];
   const int64_t row = blockIdx.x;
   const int n4 = h >> 2;
@@ -124,6 +126,8 @@ __global__ void __launch_bounds__(kLnBwdThreads) ln_bwd_kernel(
     const float* __restrict__ rstd, const uint16_t* __restrict__ gamma,
     const float* resid, float* dx, uint16_t* __restrict__ dx_bf16,
     float* __restrict__ partials, int64_t rows, int h, int want_colsum_dx) {
+  pdl_wait();  // the previous kernel on the stream has completed
+  pdl_launch();
   extern __shared__ float colacc[];  // [3][h]
   __shared__ float red[2 * kLnBwdThreads / 32];
   const int n4 = h >> 2;
@@ -222,6 +226,8 @@ __global__ void __launch_bounds__(256) reduce_partials_kernel(const float* __res
                                                               int nblocks, int nsum, int64_t n,
                                                               float* out0, float* out1, float* out2,
                                                               int accumulate) {
+  pdl_wait();  // the previous kernel on the stream has completed
+  pdl_launch();
   __shared__ float part[8][33];
   const int cl = threadIdx.x & 31, rg = threadIdx.x >> 5;
   const int64_t c = blockIdx.x * 32 + cl;
@@ -247,6 +253,8 @@ __global__ void __launch_bounds__(256) reduce_partials_kernel(const float* __res
 template <bool IN_BF16>
 __global__ void colsum_partial_kernel(const void* __restrict__ in, int64_t rows, int64_t n,
                                       float* __restrict__ partials, uint16_t* __restrict__ copy) {
+  pdl_wait();  // the previous kernel on the stream has completed
+  pdl_launch();
   const int64_t c8 = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) * 8;
   if (c8 >= n) return;
   const int split = blockIdx.y;
@@ -295,7 +303,7 @@ __global__ void colsum_partial_kernel(const void* __restrict__ in, int64_t rows,
 template <int VPT>
 int ln_fwd_launch(const float* x, const uint16_t* g, const uint16_t* b, uint16_t* out,
                   float* mean, float* rstd, int64_t rows, int h, cudaStream_t st) {
-  ln_fwd_kernel<VPT><<<static_cast<unsigned>(rows), kLnThreads, 0, st>>>(x, g, b, out, mean, rstd, h);
+  launch_kernel(ln_fwd_kernel<VPT>, dim3(static_cast<unsigned>(rows)), dim3(kLnThreads), 0, st, 1, x, g, b, out, mean, rstd, h);
   return cudaGetLastError() == cudaSuccess ? MC_OK : MC_ERR_CUDA;
 }
 
@@ -316,7 +324,7 @@ int ln_bwd_launch(const float* dout, const float* x, const float* mean, const fl
                                 3 * kMaxLayerNormHidden * static_cast<int>(sizeof(float)));
   });
   if (attr != cudaSuccess) return MC_ERR_CUDA;
-  kern<<<grid, kLnBwdThreads, smem, st>>>(dout, x, mean, rstd, gamma, resid, dx, dx_bf16, partials,
+  launch_kernel(kern, dim3(grid), dim3(kLnBwdThreads), smem, st, 1, dout, x, mean, rstd, gamma, resid, dx, dx_bf16, partials,
                                        rows, h, want_colsum_dx);
   return cudaGetLastError() == cudaSuccess ? MC_OK : MC_ERR_CUDA;
 }
@@ -384,7 +392,7 @@ int launch_layernorm_backward(const float* dout, const float* x, const float* me
   }
   if (rc != MC_OK) return rc;
   dim3 rgrid(static_cast<unsigned>((h + 31) / 32), want ? 3 : 2);
-  reduce_partials_kernel<<<rgrid, 256, 0, st>>>(partials, grid, 3, h, dgamma, dbeta, colsum_dx,
+  launch_kernel(reduce_partials_kernel, dim3(rgrid), dim3(256), 0, st, 1, partials, grid, 3, h, dgamma, dbeta, colsum_dx,
                                                 accumulate);
   return cudaGetLastError() == cudaSuccess ? MC_OK : MC_ERR_CUDA;
 }
@@ -404,12 +412,12 @@ int launch_colsum(const void* in, bool in_bf16, int64_t rows, int64_t n, float* 
   const int splits = static_cast<int>(rows < want ? rows : want);
   dim3 grid(static_cast<unsigned>(col_blocks), splits);
   if (in_bf16)
-    colsum_partial_kernel<true><<<grid, 128, 0, st>>>(in, rows, n, partials, nullptr);
+    launch_kernel(colsum_partial_kernel<true>, dim3(grid), dim3(128), 0, st, 1, in, rows, n, partials, nullptr);
   else
-    colsum_partial_kernel<false><<<grid, 128, 0, st>>>(in, rows, n, partials, bf16_copy);
+    launch_kernel(colsum_partial_kernel<false>, dim3(grid), dim3(128), 0, st, 1, in, rows, n, partials, bf16_copy);
   if (cudaGetLastError() != cudaSuccess) return MC_ERR_CUDA;
   dim3 rgrid(static_cast<unsigned>((n + 31) / 32), 1);
-  reduce_partials_kernel<<<rgrid, 256, 0, st>>>(partials, splits, 1, n, out, nullptr, nullptr,
+  launch_kernel(reduce_partials_kernel, dim3(rgrid), dim3(256), 0, st, 1, partials, splits, 1, n, out, nullptr, nullptr,
                                                 accumulate);
   return cudaGetLastError() == cudaSuccess ? MC_OK : MC_ERR_CUDA;
 }

@@ -12,6 +12,37 @@
 
 namespace mc {
 
+#ifdef __CUDACC__
+// Launches `kern` on `st` with programmatic stream serialisation, and in
+// clusters of cluster_x CTAs along x when cluster_x > 1.  The kernel may then
+// start (run its prologue) while the previous kernel on the stream finishes;
+// every kernel of this library calls pdl_wait() before touching global memory.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                 cudaStream_t st, unsigned cluster_x, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute at[2];
+  unsigned n = 0;
+  at[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster_x > 1) {
+    at[n].id = cudaLaunchAttributeClusterDimension;
+    at[n].val.clusterDim.x = cluster_x;
+    at[n].val.clusterDim.y = 1;
+    at[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = at;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+#endif
+
 // Status block at the start of a workspace: int[64] (256 bytes).
 // status[0] = first error code recorded on the device, status[1] = where.
 constexpr size_t kStatusBytes = 256;

@@ -18,6 +18,20 @@
 
 namespace mc {
 
+// ---------------------------------------------------------------- PDL
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialisation (launch_kernel) may start while the kernel before it on the
+// stream is still running: pdl_wait() blocks until that kernel has completed
+// and its memory operations are visible, so every kernel calls it before its
+// first global-memory access (its prologue — barrier init, TMEM allocation,
+// descriptor prefetch — runs before).  pdl_launch() lets the next kernel be
+// scheduled once every CTA of this grid has issued it or exited.  Both are
+// no-ops in a kernel launched without the attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
