@@ -307,10 +307,14 @@ int ln_fwd_launch(const float* x, const uint16_t* g, const uint16_t* b, uint16_t
   return cudaGetLastError() == cudaSuccess ? MC_OK : MC_ERR_CUDA;
 }
 
+// Launches the backward over min(rows, kLnBwdMaxBlocks, CTAs resident at once)
+// CTAs -- one wave: at large h the [3][h] column partials limit an SM to two
+// CTAs, and a second, half-occupied wave would cost more than longer row
+// loops -- and returns that count in *grid_out.
 template <int VPT>
 int ln_bwd_launch(const float* dout, const float* x, const float* mean, const float* rstd,
                   const uint16_t* gamma, const float* resid, float* dx, uint16_t* dx_bf16,
-                  float* partials, int64_t rows, int h, int want_colsum_dx, int grid,
+                  float* partials, int64_t rows, int h, int want_colsum_dx, int* grid_out,
                   cudaStream_t st) {
   const size_t smem = 3 * static_cast<size_t>(h) * sizeof(float);
   auto kern = ln_bwd_kernel<VPT>;
@@ -324,8 +328,17 @@ int ln_bwd_launch(const float* dout, const float* x, const float* mean, const fl
                                 3 * kMaxLayerNormHidden * static_cast<int>(sizeof(float)));
   });
   if (attr != cudaSuccess) return MC_ERR_CUDA;
-  launch_kernel(kern, dim3(grid), dim3(kLnBwdThreads), smem, st, 1, dout, x, mean, rstd, gamma, resid, dx, dx_bf16, partials,
-                                       rows, h, want_colsum_dx);
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kLnBwdThreads, smem) !=
+          cudaSuccess ||
+      per_sm < 1)
+    return MC_ERR_CUDA;
+  int64_t grid = rows < kLnBwdMaxBlocks ? rows : kLnBwdMaxBlocks;
+  const int64_t resident = static_cast<int64_t>(per_sm) * num_sms();
+  if (resident > 0 && grid > resident) grid = resident;
+  *grid_out = static_cast<int>(grid);
+  launch_kernel(kern, dim3(static_cast<unsigned>(grid)), dim3(kLnBwdThreads), smem, st, 1, dout,
+                x, mean, rstd, gamma, resid, dx, dx_bf16, partials, rows, h, want_colsum_dx);
   return cudaGetLastError() == cudaSuccess ? MC_OK : MC_ERR_CUDA;
 }
 
@@ -379,15 +392,15 @@ int launch_layernorm_backward(const float* dout, const float* x, const float* me
       (dx_bf16 && (reinterpret_cast<uintptr_t>(dx_bf16) & 7u)) ||
       (reinterpret_cast<uintptr_t>(gamma) & 7u))
     return MC_ERR_ALIGN;
-  const int grid = static_cast<int>(rows < kLnBwdMaxBlocks ? rows : kLnBwdMaxBlocks);
+  int grid = 0;  // set by the launch: the CTAs (and partial rows) used
   const int want = colsum_dx != nullptr;
   int rc;
   switch (vpt_for(h, kLnBwdThreads)) {
-    case 1: rc = ln_bwd_launch<1>(dout, x, mean, rstd, gamma, resid, dx, dx_bf16, partials, rows, h, want, grid, st); break;
-    case 2: rc = ln_bwd_launch<2>(dout, x, mean, rstd, gamma, resid, dx, dx_bf16, partials, rows, h, want, grid, st); break;
-    case 4: rc = ln_bwd_launch<4>(dout, x, mean, rstd, gamma, resid, dx, dx_bf16, partials, rows, h, want, grid, st); break;
-    case 8: rc = ln_bwd_launch<8>(dout, x, mean, rstd, gamma, resid, dx, dx_bf16, partials, rows, h, want, grid, st); break;
-    case 16: rc = ln_bwd_launch<16>(dout, x, mean, rstd, gamma, resid, dx, dx_bf16, partials, rows, h, want, grid, st); break;
+    case 1: rc = ln_bwd_launch<1>(dout, x, mean, rstd, gamma, resid, dx, dx_bf16, partials, rows, h, want, &grid, st); break;
+    case 2: rc = ln_bwd_launch<2>(dout, x, mean, rstd, gamma, resid, dx, dx_bf16, partials, rows, h, want, &grid, st); break;
+    case 4: rc = ln_bwd_launch<4>(dout, x, mean, rstd, gamma, resid, dx, dx_bf16, partials, rows, h, want, &grid, st); break;
+    case 8: rc = ln_bwd_launch<8>(dout, x, mean, rstd, gamma, resid, dx, dx_bf16, partials, rows, h, want, &grid, st); break;
+    case 16: rc = ln_bwd_launch<16>(dout, x, mean, rstd, gamma, resid, dx, dx_bf16, partials, rows, h, want, &grid, st); break;
     default: return MC_ERR_UNSUPPORTED;
   }
   if (rc != MC_OK) return rc;
