@@ -17,35 +17,57 @@ namespace mc {
 namespace {
 
 // ---------------------------------------------------------------- backward
-// delta[b, h, i] = sum_c dO[i, h*D + c] * O[i, h*D + c]; one warp per (token, head).
+// delta[b, h, i] = sum_c dO[i, h*D + c] * O[i, h*D + c].  D/8 threads share a
+// (token, head) row, each loading 16 bytes of O and of dO; rows are taken
+// head-major (token fastest), so a block's delta stores are contiguous, and
+// each thread handles kDeltaPasses rows with all their loads issued first.
+constexpr int kDeltaThreads = 256;
+constexpr int kDeltaPasses = 4;
+
 template <int D>
-__global__ void attn_bwd_pre_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
-                                    float* __restrict__ delta, int64_t T, int s, int H) {
+__host__ __device__ constexpr int64_t delta_rows_per_block() {
+  return static_cast<int64_t>(kDeltaThreads / (D / 8)) * kDeltaPasses;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kDeltaThreads)
+    attn_bwd_pre_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
+                        float* __restrict__ delta, int64_t T, int s, int H) {
   pdl_wait();  // the previous kernel on the stream has completed
   pdl_launch();
-  const int64_t wid = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
-  const int l = threadIdx.x & 31;
-  if (wid >= T * H) return;
-  const int64_t tok = wid / H;
-  const int hh = static_cast<int>(wid % H);
-  const int a = H * D;
-  constexpr int PER = D / 32;  // 2 or 4 elements per lane
-  const uint16_t* po = o + tok * a + hh * D + l * PER;
-  const uint16_t* pd = dout + tok * a + hh * D + l * PER;
-  float acc = 0.f;
-  if constexpr (PER == 4) {
-    const uint2 x = *reinterpret_cast<const uint2*>(po), y = *reinterpret_cast<const uint2*>(pd);
-    acc = bf16_lo(x.x) * bf16_lo(y.x) + bf16_hi(x.x) * bf16_hi(y.x) + bf16_lo(x.y) * bf16_lo(y.y) +
-          bf16_hi(x.y) * bf16_hi(y.y);
-  } else {
-    const uint32_t x = *reinterpret_cast<const uint32_t*>(po), y = *reinterpret_cast<const uint32_t*>(pd);
-    acc = bf16_lo(x) * bf16_lo(y) + bf16_hi(x) * bf16_hi(y);
+  constexpr int TPR = D / 8;                  // threads per row: 16 (D = 128) or 8 (D = 64)
+  constexpr int RPP = kDeltaThreads / TPR;    // rows per pass of the block
+  const int sub = static_cast<int>(threadIdx.x) % TPR;
+  const int64_t rows = T * H;
+  const int64_t a = static_cast<int64_t>(H) * D;
+  const int64_t r0 = blockIdx.x * delta_rows_per_block<D>() + threadIdx.x / TPR;
+  uint4 xo[kDeltaPasses], xd[kDeltaPasses];
+#pragma unroll
+  for (int p = 0; p < kDeltaPasses; ++p) {
+    const int64_t r = r0 + p * RPP;  // r = head * T + token
+    xo[p] = make_uint4(0u, 0u, 0u, 0u);
+    xd[p] = make_uint4(0u, 0u, 0u, 0u);
+    if (r < rows) {
+      const int64_t off = (r % T) * a + (r / T) * D + sub * 8;
+      xo[p] = __ldg(reinterpret_cast<const uint4*>(o + off));
+      xd[p] = __ldg(reinterpret_cast<const uint4*>(dout + off));
+    }
   }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (l == 0) {
-    const int64_t bi = tok / s, i = tok % s;
-    delta[(bi * H + hh) * s + i] = acc;
+  for (int p = 0; p < kDeltaPasses; ++p) {
+    float acc = bf16_lo(xo[p].x) * bf16_lo(xd[p].x) + bf16_hi(xo[p].x) * bf16_hi(xd[p].x) +
+                bf16_lo(xo[p].y) * bf16_lo(xd[p].y) + bf16_hi(xo[p].y) * bf16_hi(xd[p].y) +
+                bf16_lo(xo[p].z) * bf16_lo(xd[p].z) + bf16_hi(xo[p].z) * bf16_hi(xd[p].z) +
+                bf16_lo(xo[p].w) * bf16_lo(xd[p].w) + bf16_hi(xo[p].w) * bf16_hi(xd[p].w);
+    // the TPR lanes of a row are consecutive and aligned within the warp
+#pragma unroll
+    for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    const int64_t r = r0 + p * RPP;
+    if (sub == 0 && r < rows) {
+      const int64_t hh = r / T, tok = r % T;
+      const int64_t bi = tok / s, i = tok % s;
+      delta[(bi * H + hh) * s + i] = acc;
+    }
   }
 }
 
@@ -53,9 +75,9 @@ template <int D>
 int bwd_launch(const uint16_t* qkv, const uint16_t* o, const float* lse, const uint16_t* dout,
                uint16_t* dqkv, float* delta, int b, int s, int H, int* status, cudaStream_t st) {
   const int64_t T = static_cast<int64_t>(b) * s;
-  const int64_t warps = T * H;
-  launch_kernel(attn_bwd_pre_kernel<D>, dim3(static_cast<unsigned>((warps * 32 + 255) / 256)), dim3(256), 0, st, 1, 
-      o, dout, delta, T, s, H);
+  const int64_t blocks = (T * H + delta_rows_per_block<D>() - 1) / delta_rows_per_block<D>();
+  launch_kernel(attn_bwd_pre_kernel<D>, dim3(static_cast<unsigned>(blocks)), dim3(kDeltaThreads),
+                0, st, 1, o, dout, delta, T, s, H);
   if (cudaGetLastError() != cudaSuccess) return MC_ERR_CUDA;
   return launch_attention_backward_tc(qkv, lse, dout, dqkv, delta, b, s, H, D, status, st);
 }
@@ -67,11 +89,16 @@ bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 int launch_attention_delta(const uint16_t* o, const uint16_t* dout, float* delta, int b, int s,
                            int H, int d, cudaStream_t st) {
   const int64_t T = static_cast<int64_t>(b) * s;
-  const unsigned blocks = static_cast<unsigned>((T * H * 32 + 255) / 256);
   if (d == 64)
-    launch_kernel(attn_bwd_pre_kernel<64>, dim3(blocks), dim3(256), 0, st, 1, o, dout, delta, T, s, H);
+    launch_kernel(attn_bwd_pre_kernel<64>,
+                  dim3(static_cast<unsigned>((T * H + delta_rows_per_block<64>() - 1) /
+                                             delta_rows_per_block<64>())),
+                  dim3(kDeltaThreads), 0, st, 1, o, dout, delta, T, s, H);
   else
-    launch_kernel(attn_bwd_pre_kernel<128>, dim3(blocks), dim3(256), 0, st, 1, o, dout, delta, T, s, H);
+    launch_kernel(attn_bwd_pre_kernel<128>,
+                  dim3(static_cast<unsigned>((T * H + delta_rows_per_block<128>() - 1) /
+                                             delta_rows_per_block<128>())),
+                  dim3(kDeltaThreads), 0, st, 1, o, dout, delta, T, s, H);
   return cudaGetLastError() == cudaSuccess ? MC_OK : MC_ERR_CUDA;
 }
 
