@@ -308,9 +308,9 @@ int ln_fwd_launch(const float* x, const uint16_t* g, const uint16_t* b, uint16_t
 }
 
 // Launches the backward over min(rows, kLnBwdMaxBlocks, CTAs resident at once)
-// CTAs -- one wave: at large h the [3][h] column partials limit an SM to two
-// CTAs, and a second, half-occupied wave would cost more than longer row
-// loops -- and returns that count in *grid_out.
+// CTAs -- one wave: at large h registers and the [3][h] column partials allow
+// only one or two CTAs per SM, and further, partly occupied waves cost more
+// than longer row loops -- and returns that count in *grid_out.
 template <int VPT>
 int ln_bwd_launch(const float* dout, const float* x, const float* mean, const float* rstd,
                   const uint16_t* gamma, const float* resid, float* dx, uint16_t* dx_bf16,
