@@ -186,9 +186,11 @@ int mc_attention_forward_cp(const uint16_t* qkv, uint16_t* o, float* lse, int32_
   const int64_t warps = static_cast<int64_t>(b) * s * H;
   const unsigned blocks = static_cast<unsigned>((warps * 32 + 255) / 256);
   if (d == 64)
-    launch_kernel(cp_merge_kernel<64>, dim3(blocks), dim3(256), 0, st, 1, part_o, part_lse, o, lse, b, s, H, c);
+    launch_kernel(cp_merge_kernel<64>, dim3(blocks), dim3(256), 0, st, 1, part_o, part_lse, o, lse,
+                  b, s, H, c);
   else
-    launch_kernel(cp_merge_kernel<128>, dim3(blocks), dim3(256), 0, st, 1, part_o, part_lse, o, lse, b, s, H, c);
+    launch_kernel(cp_merge_kernel<128>, dim3(blocks), dim3(256), 0, st, 1, part_o, part_lse, o, lse,
+                  b, s, H, c);
   return cudaGetLastError() == cudaSuccess ? MC_OK : MC_ERR_CUDA;
 }
 
@@ -227,8 +229,8 @@ int mc_attention_backward_cp(const uint16_t* qkv, const uint16_t* o, const float
       }
     }
   const int64_t threads = static_cast<int64_t>(b) * s * (3 * a / 4);
-  launch_kernel(cp_reduce_kernel, dim3(static_cast<unsigned>((threads + 255) / 256)), dim3(256), 0, st, 1, 
-      part_dq, part_dkv, dqkv, b, s, static_cast<int>(a), c, C);
+  launch_kernel(cp_reduce_kernel, dim3(static_cast<unsigned>((threads + 255) / 256)), dim3(256), 0,
+                st, 1, part_dq, part_dkv, dqkv, b, s, static_cast<int>(a), c, C);
   return cudaGetLastError() == cudaSuccess ? MC_OK : MC_ERR_CUDA;
 }
 

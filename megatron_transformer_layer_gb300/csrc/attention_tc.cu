@@ -934,7 +934,8 @@ int launch_bwd_dq_tc(const CUtensorMap& tq, const CUtensorMap& td, const float* 
   });
   if (attr != cudaSuccess) return MC_ERR_CUDA;
   dim3 grid(PART ? part.len / 128 : (s + 127) / 128, H, b);
-  launch_kernel(kern, dim3(grid), dim3(kBwdThreads), C::kSmem, st, 1, tq, td, lse, delta, dqkv, s, H, status, part);
+  launch_kernel(kern, dim3(grid), dim3(kBwdThreads), C::kSmem, st, 1, tq, td, lse, delta, dqkv, s,
+                H, status, part);
   return cudaGetLastError() == cudaSuccess ? MC_OK : MC_ERR_CUDA;
 }
 
@@ -951,7 +952,8 @@ int launch_bwd_dkdv_tc(const CUtensorMap& tq, const CUtensorMap& td, const float
   });
   if (attr != cudaSuccess) return MC_ERR_CUDA;
   dim3 grid(PART ? part.len / 128 : (s + 127) / 128, H, b);
-  launch_kernel(kern, dim3(grid), dim3(kBwdThreads), C::kSmem, st, 1, tq, td, lse, delta, dqkv, s, H, status, part);
+  launch_kernel(kern, dim3(grid), dim3(kBwdThreads), C::kSmem, st, 1, tq, td, lse, delta, dqkv, s,
+                H, status, part);
   return cudaGetLastError() == cudaSuccess ? MC_OK : MC_ERR_CUDA;
 }
 

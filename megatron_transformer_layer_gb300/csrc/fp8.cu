@@ -125,20 +125,27 @@ int launch_fp8_quantize(const void* in, bool in_bf16, int64_t n, int format, uin
   const int64_t want = (n + kThreadsPerBlock - 1) / kThreadsPerBlock;
   // every partial is written: the grid is exactly kAmaxBlocks blocks
   if (in_bf16)
-    launch_kernel(amax_partial_kernel<true>, dim3(kAmaxBlocks), dim3(kThreadsPerBlock), 0, st, 1, in, n, partials);
+    launch_kernel(amax_partial_kernel<true>, dim3(kAmaxBlocks), dim3(kThreadsPerBlock), 0, st, 1,
+                  in, n, partials);
   else
-    launch_kernel(amax_partial_kernel<false>, dim3(kAmaxBlocks), dim3(kThreadsPerBlock), 0, st, 1, in, n, partials);
-  launch_kernel(fp8_scale_kernel, dim3(1), dim3(kAmaxBlocks), 0, st, 1, partials, fmax, state, scale_inv);
+    launch_kernel(amax_partial_kernel<false>, dim3(kAmaxBlocks), dim3(kThreadsPerBlock), 0, st, 1,
+                  in, n, partials);
+  launch_kernel(fp8_scale_kernel, dim3(1), dim3(kAmaxBlocks), 0, st, 1, partials, fmax, state,
+                scale_inv);
   const unsigned grid = static_cast<unsigned>(
       want / 8 + 1 < 4 * static_cast<int64_t>(num_sms()) ? want / 8 + 1 : 4 * num_sms());
   if (in_bf16 && format == 0)
-    launch_kernel(fp8_cast_kernel<true, 0>, dim3(grid), dim3(kThreadsPerBlock), 0, st, 1, in, n, state, out);
+    launch_kernel(fp8_cast_kernel<true, 0>, dim3(grid), dim3(kThreadsPerBlock), 0, st, 1, in, n,
+                  state, out);
   else if (in_bf16)
-    launch_kernel(fp8_cast_kernel<true, 1>, dim3(grid), dim3(kThreadsPerBlock), 0, st, 1, in, n, state, out);
+    launch_kernel(fp8_cast_kernel<true, 1>, dim3(grid), dim3(kThreadsPerBlock), 0, st, 1, in, n,
+                  state, out);
   else if (format == 0)
-    launch_kernel(fp8_cast_kernel<false, 0>, dim3(grid), dim3(kThreadsPerBlock), 0, st, 1, in, n, state, out);
+    launch_kernel(fp8_cast_kernel<false, 0>, dim3(grid), dim3(kThreadsPerBlock), 0, st, 1, in, n,
+                  state, out);
   else
-    launch_kernel(fp8_cast_kernel<false, 1>, dim3(grid), dim3(kThreadsPerBlock), 0, st, 1, in, n, state, out);
+    launch_kernel(fp8_cast_kernel<false, 1>, dim3(grid), dim3(kThreadsPerBlock), 0, st, 1, in, n,
+                  state, out);
   return cudaGetLastError() == cudaSuccess ? MC_OK : MC_ERR_CUDA;
 }
 

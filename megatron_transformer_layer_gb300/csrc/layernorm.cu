@@ -303,7 +303,8 @@ __global__ void colsum_partial_kernel(const void* __restrict__ in, int64_t rows,
 template <int VPT>
 int ln_fwd_launch(const float* x, const uint16_t* g, const uint16_t* b, uint16_t* out,
                   float* mean, float* rstd, int64_t rows, int h, cudaStream_t st) {
-  launch_kernel(ln_fwd_kernel<VPT>, dim3(static_cast<unsigned>(rows)), dim3(kLnThreads), 0, st, 1, x, g, b, out, mean, rstd, h);
+  launch_kernel(ln_fwd_kernel<VPT>, dim3(static_cast<unsigned>(rows)), dim3(kLnThreads), 0, st, 1,
+                x, g, b, out, mean, rstd, h);
   return cudaGetLastError() == cudaSuccess ? MC_OK : MC_ERR_CUDA;
 }
 
@@ -337,8 +338,8 @@ int ln_bwd_launch(const float* dout, const float* x, const float* mean, const fl
   const int64_t resident = static_cast<int64_t>(per_sm) * num_sms();
   if (resident > 0 && grid > resident) grid = resident;
   *grid_out = static_cast<int>(grid);
-  launch_kernel(kern, dim3(static_cast<unsigned>(grid)), dim3(kLnBwdThreads), smem, st, 1, dout,
-                x, mean, rstd, gamma, resid, dx, dx_bf16, partials, rows, h, want_colsum_dx);
+  launch_kernel(kern, dim3(static_cast<unsigned>(grid)), dim3(kLnBwdThreads), smem, st, 1, dout, x,
+                mean, rstd, gamma, resid, dx, dx_bf16, partials, rows, h, want_colsum_dx);
   return cudaGetLastError() == cudaSuccess ? MC_OK : MC_ERR_CUDA;
 }
 
@@ -405,8 +406,8 @@ int launch_layernorm_backward(const float* dout, const float* x, const float* me
   }
   if (rc != MC_OK) return rc;
   dim3 rgrid(static_cast<unsigned>((h + 31) / 32), want ? 3 : 2);
-  launch_kernel(reduce_partials_kernel, dim3(rgrid), dim3(256), 0, st, 1, partials, grid, 3, h, dgamma, dbeta, colsum_dx,
-                                                accumulate);
+  launch_kernel(reduce_partials_kernel, dim3(rgrid), dim3(256), 0, st, 1, partials, grid, 3, h,
+                dgamma, dbeta, colsum_dx, accumulate);
   return cudaGetLastError() == cudaSuccess ? MC_OK : MC_ERR_CUDA;
 }
 
@@ -425,13 +426,15 @@ int launch_colsum(const void* in, bool in_bf16, int64_t rows, int64_t n, float* 
   const int splits = static_cast<int>(rows < want ? rows : want);
   dim3 grid(static_cast<unsigned>(col_blocks), splits);
   if (in_bf16)
-    launch_kernel(colsum_partial_kernel<true>, dim3(grid), dim3(128), 0, st, 1, in, rows, n, partials, nullptr);
+    launch_kernel(colsum_partial_kernel<true>, dim3(grid), dim3(128), 0, st, 1, in, rows, n,
+                  partials, nullptr);
   else
-    launch_kernel(colsum_partial_kernel<false>, dim3(grid), dim3(128), 0, st, 1, in, rows, n, partials, bf16_copy);
+    launch_kernel(colsum_partial_kernel<false>, dim3(grid), dim3(128), 0, st, 1, in, rows, n,
+                  partials, bf16_copy);
   if (cudaGetLastError() != cudaSuccess) return MC_ERR_CUDA;
   dim3 rgrid(static_cast<unsigned>((n + 31) / 32), 1);
-  launch_kernel(reduce_partials_kernel, dim3(rgrid), dim3(256), 0, st, 1, partials, splits, 1, n, out, nullptr, nullptr,
-                                                accumulate);
+  launch_kernel(reduce_partials_kernel, dim3(rgrid), dim3(256), 0, st, 1, partials, splits, 1, n,
+                out, nullptr, nullptr, accumulate);
   return cudaGetLastError() == cudaSuccess ? MC_OK : MC_ERR_CUDA;
 }
 
