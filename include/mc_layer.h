@@ -46,6 +46,11 @@
  *   change in between.  `ws` is scratch; concurrent calls need distinct
  *   `saved`/`ws` buffers.  All pointers must be 16-byte aligned; `saved` and
  *   `ws` 256-byte aligned.
+ *   Kernels are launched with programmatic stream serialisation: a library
+ *   kernel may become resident while the kernel before it on `stream` is
+ *   still running, but it touches no global memory until that kernel has
+ *   completed and its writes are visible, so stream order holds for the
+ *   caller's own kernels, copies and events as for ordinary launches.
  *
  * Errors
  * ------
