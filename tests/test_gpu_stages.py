@@ -33,7 +33,9 @@ def test_layernorm_forward(rows, h):
 
 
 @pytest.mark.parametrize("rows,h,accumulate", [(1, 768, 0), (129, 768, 1), (700, 2048, 0),
-                                               (33, 4096, 0), (40, 8192, 0)])
+                                               (33, 4096, 0), (40, 8192, 0),
+                                               # more rows than one wave of CTAs at h = 8192
+                                               (1000, 8192, 1)])
 def test_layernorm_backward(rows, h, accumulate):
     xb, gb, bb = bits(rows * h, 4), bits(h, 5, mean=1.0, std=0.1), bits(h, 6, std=0.1)
     db, rb = bits(rows * h, 7), bits(rows * h, 8)
@@ -181,7 +183,9 @@ def _oracle_attention(q64, b, s, H, d, do64=None):
 
 
 @pytest.mark.parametrize("b,s,H,d", [(1, 1, 1, 64), (2, 7, 3, 64), (1, 129, 2, 128),
-                                     (2, 300, 2, 64), (1, 520, 2, 128)])
+                                     (2, 300, 2, 64), (1, 520, 2, 128),
+                                     # (token, head) rows of the delta pass: a ragged last block
+                                     (1, 1000, 3, 64)])
 def test_attention_forward_backward(b, s, H, d):
     a = H * d
     qb, q64 = _qkv_case(b, s, H, d)
