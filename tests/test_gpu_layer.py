@@ -1,6 +1,7 @@
 """Layer parity: the whole forward + backward through the C ABI against the
 fp64 oracle, on the same seeded inputs; y, dx and all twelve parameter
-gradients are checked per tensor."""
+gradients are checked per tensor, against the stated bounds and against the
+bf16 rounding floor of the same inputs (tests/parity.py)."""
 import numpy as np
 import pytest
 import torch
@@ -8,7 +9,8 @@ import torch
 import oracle.layer as O
 from layer_inputs import LayerShape, make_layer_inputs
 from layer_inputs.generator import NONTRIVIAL_INIT
-from parity import assert_close, metrics
+from oracle.rounding_floor import floor_norm_rel
+from parity import assert_close, assert_within_floor, floor_bound, metrics
 
 from gpu_util import DEV, dev_f32_from_bits, run_layer, to_f64
 
@@ -23,11 +25,17 @@ def _oracle(inp, t):
 def _check_layer(inp, t, label):
     _, y, dx, G = run_layer(inp, t)
     y_o, dx_o, G_o = _oracle(inp, t)
-    report = {"y": assert_close(f"{label} y", y, y_o), "dx": assert_close(f"{label} dx", dx, dx_o)}
-    for k in G_o:
-        report[k] = assert_close(f"{label} {k}", G[k], G_o[k])
-    worst = max(report.items(), key=lambda kv: kv[1]["mean_rel"])
-    print(f"\n{label}: worst mean_rel {worst[0]} {worst[1]}")
+    floor = floor_norm_rel(inp.shape.with_tp(1), inp.params_f64(), inp.f64("x"), inp.f64("dy"),
+                           exact=(y_o, dx_o, G_o))
+    got = {"y": y, "dx": dx, **G}
+    ref = {"y": y_o, "dx": dx_o, **G_o}
+    lines = []
+    for k in ref:
+        m = assert_close(f"{label} {k}", got[k], ref[k])
+        assert_within_floor(f"{label} {k}", got[k], ref[k], floor[k])
+        lines.append(f"  {k:6s} max {m['max_rel']:.2e} mean {m['mean_rel']:.2e} | norm "
+                     f"{m['norm_rel']:.2e} <= {floor_bound(floor[k]):.2e} (floor {floor[k]:.2e})")
+    print(f"\n{label}:\n" + "\n".join(lines))
     return y, dx, G
 
 

@@ -5,11 +5,13 @@ framework forbids cudaMalloc while it runs, or a process whose device memory
 another allocator has already reserved -- so they cannot pass the `delta`
 scratch buffer that mc_attention_backward takes.  This entry point uses a
 fixed scratch array inside the library instead.  Here it is called through the
-C ABI twice in a row and must give what the allocating entry point gives, and
-a problem larger than its fixed scratch must be rejected before any launch.
+C ABI twice in a row and must give what the allocating entry point gives, bit
+for bit, without changing the device's free memory; a problem larger than its
+fixed scratch must be rejected before any launch.
 This file is collected last so that a run stopping at the first failure has
 already run every other test.
 """
+import numpy as np
 import pytest
 import torch
 
@@ -39,14 +41,27 @@ def _case(b, s, H, d, seed):
 
 @pytest.mark.parametrize("b,s,H,d", [(2, 300, 4, 128), (1, 257, 3, 64)])
 def test_noalloc_backward_matches_allocating_entry_point_twice(b, s, H, d):
+    """Two calls in a row equal the allocating entry point to the bit (the
+    same kernels on the same inputs), which is also within the parity
+    tolerance; neither call changes the device's free memory or torch's
+    reserved pool, i.e. nothing is allocated."""
     qkv, o, lse, dout, ref = _case(b, s, H, d, seed=b + d)
-    for _ in range(2):
-        dqkv = torch.full((b * s * 3 * H * d,), float("nan"), dtype=torch.bfloat16, device=DEV)
-        st = status()
+    outs = [torch.full((b * s * 3 * H * d,), float("nan"), dtype=torch.bfloat16, device=DEV)
+            for _ in range(2)]
+    sts = [status() for _ in range(2)]
+    torch.cuda.synchronize()
+    free0, reserved0 = torch.cuda.mem_get_info()[0], torch.cuda.memory_reserved()
+    for dqkv, st in zip(outs, sts):
         rc = L.mc_attention_backward_noalloc(qkv, o, lse, dout, dqkv, b, s, H, d, st)
         assert rc == L.MC_OK, L.mc_strerror(rc)
+        torch.cuda.synchronize()
+        assert torch.cuda.mem_get_info()[0] == free0
+        assert torch.cuda.memory_reserved() == reserved0
+    for dqkv, st in zip(outs, sts):
         check_status(st)
-        assert_close("noalloc dqkv", to_f64(dqkv), ref)
+        got = to_f64(dqkv)
+        assert np.array_equal(got, ref)
+        assert_close("noalloc dqkv", got, ref)
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch():
