@@ -199,6 +199,80 @@ def oracle_step(prepared) -> float:
     return time.perf_counter() - t0
 
 
+def record_card(device=None) -> dict:
+    """Identity of the run, for the record: GPU, SM count, driver, CUDA and
+    torch versions, host CPU model and thread count."""
+    card = {"host_cpu": None, "host_threads": os.cpu_count()}
+    try:
+        import torch
+        card["torch"] = torch.__version__
+        card["cuda_runtime"] = torch.version.cuda
+        if device is not None and torch.cuda.is_available():
+            prop = torch.cuda.get_device_properties(device)
+            card["gpu"] = prop.name
+            card["sm_count"] = prop.multi_processor_count
+            card["gpu_memory_gib"] = round(prop.total_memory / 2 ** 30, 1)
+    except Exception:
+        pass
+    try:
+        out = subprocess.run(["nvidia-smi", "--query-gpu=driver_version", "--format=csv,noheader"],
+                             capture_output=True, text=True, timeout=20).stdout.split()
+        card["driver"] = out[0] if out else None
+    except (OSError, subprocess.TimeoutExpired):
+        card["driver"] = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=20).stdout
+        for ln in out.splitlines():
+            if ln.lower().startswith("model name"):
+                card["host_cpu"] = ln.split(":", 1)[1].strip()
+                break
+            if ln.lower().startswith("vendor id") and card["host_cpu"] is None:
+                card["host_cpu"] = ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.TimeoutExpired):
+        pass
+    return card
+
+
+def oracle_extrapolated(w, prefixes=(64, 256), head_len=2048) -> dict:
+    """Oracle tokens/s at the workload's full sequence length, extrapolated
+    (not measured).  One fp64 layer step is timed on two prefixes of the
+    sequence and modelled as c + alpha n + H beta n^2: c the per-step cost of
+    the weights and their gradients, alpha the per-token products, beta the
+    causal attention of one head, timed on its own (the oracle's attention
+    forward + backward at `head_len` tokens).  The model is evaluated at the
+    workload's micro_batch and seq_len."""
+    import numpy as np
+
+    import oracle.layer as O
+    D = dims(w)
+    n0 = min(head_len, w["seq_len"])
+    rng = np.random.default_rng(0)
+    q, k, v, do = (rng.standard_normal((n0, D["d"])) for _ in range(4))
+    t0 = time.perf_counter()
+    o, lse = O.causal_attention_forward(q, k, v)
+    O.causal_attention_backward(q, k, v, o, lse, do)
+    beta = (time.perf_counter() - t0) / (n0 * n0)
+    ns, ts = [], []
+    for n in prefixes:
+        prepared = prepare_oracle(w, n)
+        ns.append(prepared[0].seq_len)
+        ts.append(oracle_step(prepared))
+        del prepared
+    if len(set(ns)) < 2:
+        return {"value": None, "note": "sequence too short to extrapolate"}
+    lin = [t - D["H"] * beta * n * n for n, t in zip(ns, ts)]
+    alpha = max((lin[1] - lin[0]) / (ns[1] - ns[0]), 0.0)
+    c = max(lin[0] - alpha * ns[0], 0.0)
+    s_len, b = w["seq_len"], w["micro_batch"]
+    t_full = c + alpha * b * s_len + b * D["H"] * beta * s_len * s_len
+    return {"value": b * s_len / t_full, "unit": "tokens/s",
+            "kind": "extrapolated, not measured",
+            "prefix_tokens": ns, "prefix_seconds": ts,
+            "model_seconds": {"c": c, "per_token": alpha, "per_head_token_pair": beta,
+                              "attention_head_len_timed": n0},
+            "seconds_per_step_at_config": t_full}
+
+
 def oracle_threads() -> int:
     for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS"):
         if os.environ.get(var):
@@ -230,7 +304,9 @@ def run_reference(args, world, rank):
                                    f"weights, fp64 forward+backward per step"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
+        "record_card": record_card(None),
     }
+    line["cpu_baseline"]["cpu"] = line["record_card"].get("host_cpu")
     print(json.dumps(line), flush=True)
 
 
@@ -369,6 +445,49 @@ def run_stage(args, w, device):
     else:
         line["gbs"] = rate / 1e9
     print(json.dumps(line), flush=True)
+
+
+def sub_record(name, device, world, steps, warmup, peak_sustained):
+    """One more workload timed in the same run, device-resident: its step
+    (forward + backward through the C ABI, CUDA events on the launching
+    stream) and its attention kernels alone."""
+    import numpy as np
+    import torch
+
+    from layer_inputs import LayerShape, make_layer_inputs
+    from megatron_transformer_layer_gb300.layer import TransformerLayer, bf16_tensor
+    w = WORKLOADS[name]
+    D = dims(w)
+    inp = make_layer_inputs(LayerShape(**w), seed=0)
+    params = {k: bf16_tensor(v, device) for k, v in inp.params.items()}
+    layer = TransformerLayer(**w, params=params, device=device)
+    x = torch.from_numpy(inp.f64("x").reshape(-1, D["h"]).astype(np.float32)).to(device)
+    dy = torch.from_numpy(inp.f64("dy").reshape(-1, D["h"]).astype(np.float32)).to(device)
+    del inp
+    y, dx = torch.empty_like(x), torch.empty_like(x)
+
+    def step():
+        layer.forward(x, y)
+        layer.backward(dy, dx, x=x)
+
+    ms = time_launches(step, device, steps, max(warmup, 3))
+    ms = max_over_ranks(ms, world, device)
+    if layer.device_status() != 0:
+        raise SystemExit(f"{name}: device status {layer.device_status()}")
+    flops = layer_flops(w)
+    out = {"workload": WORKLOAD_NAMES[name], "steps": steps, "ms_per_step": ms,
+           "tokens_per_s": world * D["T"] / (ms / 1e3),
+           "tflops": flops / (ms / 1e3) / 1e12,
+           "frac_of_sustained": flops / (ms / 1e3) / 1e12 / peak_sustained}
+    del layer, params, x, dy, y, dx
+    torch.cuda.empty_cache()
+    for stage in ("attn_fwd", "attn_bwd"):
+        launch, work, _, _ = stage_launcher(stage, w, device)
+        sms = time_launches(launch, device, max(3, steps), 2)
+        out[f"{stage}_ms"] = sms
+        out[f"{stage}_tflops"] = work / (sms / 1e3) / 1e12
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_ours(args, world, rank, local):
@@ -602,14 +721,25 @@ def run_ours(args, world, rank, local):
                    "workspace_shared_by_stack": bool(args.recompute)},
         "roofline": roofline,
     }
+    line["record_card"] = record_card(device)
+    if args.workload == "c4" and n_layers == 1 and not args.no_c5 and not args.recompute \
+            and not args.graph:
+        # the long-sequence configuration (attention 40% of its flops), timed in
+        # the same run; all ranks run it so that max-over-ranks still holds
+        del layers, layer, acts, grads, x_d, dy_d, y_d, dx_d
+        torch.cuda.empty_cache()
+        line["c5"] = sub_record("c5", device, world, min(args.steps, 10), args.warmup, peak)
     if rank == 0 and world == 1 and not args.no_cpu_baseline and n_layers == 1:
         prepared = prepare_oracle(w, args.ref_prefix)
         toks = prepared[0].seq_len
         sec = oracle_step(prepared)
+        del prepared
         line["cpu_baseline"] = {"value": toks / sec, "unit": "tokens/s", "cores": oracle_threads(),
                                 "kind": "oracle",
+                                "cpu": line["record_card"].get("host_cpu"),
                                 "sample": f"first {toks} tokens of the sequence (micro-batch 1), "
-                                          f"full weights, one fp64 forward+backward"}
+                                          f"full weights, one fp64 forward+backward",
+                                "extrapolated_to_config": oracle_extrapolated(w)}
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -634,6 +764,8 @@ def main():
     ap.add_argument("--ref-prefix", type=int, default=64,
                     help="tokens of the sequence the CPU oracle processes per sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-c5", action="store_true",
+                    help="skip the long-sequence sub-record timed after the c4 workload")
     ap.add_argument("--tp-parts", type=int, default=0,
                     help="override the workload's tensor-parallel partition count")
     ap.add_argument("--graph", action="store_true",

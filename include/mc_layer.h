@@ -207,8 +207,13 @@ size_t mc_layernorm_backward_scratch_floats(int64_t rows, int32_t h);
  *   MC_EPI_BIAS_GELU        aux bf16  = acc + bias[n];  out bf16 = gelu_tanh(acc + bias[n])
  *   MC_EPI_BIAS_RESID_F32   out fp32  = acc + bias[n] + resid[m, n] (resid fp32, ldaux)
  *   MC_EPI_GELU_BWD         out bf16  = acc * gelu_tanh'(aux[m, n]) (aux bf16)
- * `k_parts` > 1 marks the K range as k_parts equal partitions (a row-parallel
- * product); they are summed in the accumulator in partition order.
+ * `k_parts` states that the K range is k_parts equal partitions (a
+ * row-parallel product: partition p owns k in [p K/k_parts, (p+1) K/k_parts)).
+ * It is only checked (k_parts >= 1 and dividing K, else MC_ERR_ARGUMENT):
+ * the MMAs walk K in order into one fp32 tensor-memory accumulator, so
+ * partition p's K slice is the p-th contiguous run of that walk and the
+ * epilogue sees the partitions' sum, taken in partition order.  The sum of
+ * partials is this in-accumulator accumulation, not a separate pass.
  * Requirements: M >= 1, N and K multiples of 64 (K >= 64 unless a_layout = 1,
  * where K is the token count and may be any value >= 1), 16-byte aligned
  * pointers and leading dimensions that are multiples of 8 elements. */
@@ -251,7 +256,8 @@ int mc_attention_backward(const uint16_t* qkv, const uint16_t* o, const float* l
  * larger problems return MC_ERR_SCRATCH_LIMIT before anything is enqueued).
  * That array is held on every GPU that loads the library until the process
  * exits.  The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call
+ * (cudaGetSymbolAddress) with that device current, and looks it up again if
+ * the device's context was re-created (cudaDeviceReset); make that first call
  * before any stream capture.  This entry point calls no cudaMalloc, cudaFree
  * or allocating library routine.  All calls share the array and it keeps the
  * last call's contents (each call overwrites every element it reads); calls

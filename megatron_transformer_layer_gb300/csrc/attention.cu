@@ -138,22 +138,24 @@ namespace {
 constexpr int64_t kNoAllocDeltaFloats = int64_t(1) << 20;
 __device__ __align__(256) float g_noalloc_delta[kNoAllocDeltaFloats];
 
-std::mutex g_noalloc_mu;
-std::vector<float*> g_noalloc_ptr;  // per device ordinal
+PerDeviceInit g_noalloc_init;
 
-// Device address of g_noalloc_delta on the current device; looked up once per
-// device (the symbol's host-side name is only a stand-in, not an address).
+// Device address of g_noalloc_delta on the current device, looked up with
+// cudaGetSymbolAddress the first time for each device (again if the device's
+// context was re-created); the symbol's host-side name is only a stand-in,
+// not an address a kernel may be given.
 int noalloc_scratch(float** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return MC_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (static_cast<int>(g_noalloc_ptr.size()) <= dev) g_noalloc_ptr.resize(dev + 1, nullptr);
-  if (!g_noalloc_ptr[dev]) {
+  long long addr = 0;
+  const cudaError_t e = once_per_device(g_noalloc_init, [](long long* value) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_delta) != cudaSuccess || !p) return MC_ERR_CUDA;
-    g_noalloc_ptr[dev] = static_cast<float*>(p);
-  }
-  *out = g_noalloc_ptr[dev];
+    const cudaError_t r = cudaGetSymbolAddress(&p, g_noalloc_delta);
+    if (r != cudaSuccess) return r;
+    if (!p) return cudaErrorInvalidSymbol;
+    *value = static_cast<long long>(reinterpret_cast<uintptr_t>(p));
+    return cudaSuccess;
+  }, &addr);
+  if (e != cudaSuccess || addr == 0) return MC_ERR_CUDA;
+  *out = reinterpret_cast<float*>(static_cast<uintptr_t>(addr));
   return MC_OK;
 }
 }  // namespace

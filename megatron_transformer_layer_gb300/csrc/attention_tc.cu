@@ -927,10 +927,9 @@ int launch_bwd_dq_tc(const CUtensorMap& tq, const CUtensorMap& td, const float* 
                      cudaStream_t st, const AttnPart& part) {
   using C = DqCfg<D>;
   auto kern = attn_bwd_dq_tc_kernel<D, PART>;
-  static std::once_flag once;
-  static cudaError_t attr = cudaSuccess;
-  std::call_once(once, [&] {
-    attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  static PerDeviceInit init;
+  const cudaError_t attr = once_per_device(init, [&](long long*) {
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   });
   if (attr != cudaSuccess) return MC_ERR_CUDA;
   dim3 grid(PART ? part.len / 128 : (s + 127) / 128, H, b);
@@ -945,10 +944,9 @@ int launch_bwd_dkdv_tc(const CUtensorMap& tq, const CUtensorMap& td, const float
                        cudaStream_t st, const AttnPart& part) {
   using C = BwdCfg<D>;
   auto kern = attn_bwd_dkdv_tc_kernel<D, PART>;
-  static std::once_flag once;
-  static cudaError_t attr = cudaSuccess;
-  std::call_once(once, [&] {
-    attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  static PerDeviceInit init;
+  const cudaError_t attr = once_per_device(init, [&](long long*) {
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   });
   if (attr != cudaSuccess) return MC_ERR_CUDA;
   dim3 grid(PART ? part.len / 128 : (s + 127) / 128, H, b);
@@ -992,10 +990,9 @@ int launch_fwd_tc(const uint16_t* qkv, uint16_t* o, float* lse, int b, int s, in
   const uint32_t box[3] = {64, 128, 1};
   if (!make_tmap_bf16(&tm, qkv, 3, dims, strides, box)) return MC_ERR_CUDA;
   auto kern = attn_fwd_tc_kernel<D, PART>;
-  static std::once_flag once;
-  static cudaError_t attr = cudaSuccess;
-  std::call_once(once, [&] {
-    attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  static PerDeviceInit init;
+  const cudaError_t attr = once_per_device(init, [&](long long*) {
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   });
   if (attr != cudaSuccess) return MC_ERR_CUDA;
   dim3 grid(PART ? part.len / BQ : (s + BQ - 1) / BQ, H, b);

@@ -521,13 +521,12 @@ int launch_variant(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs&
   using Cfg = GemmCfg<BN, MODE>;
   constexpr bool PAIR = MODE == kDuo;
   auto kern = gemm_tcgen05_kernel<A_MN, B_MN, BN, EPI, MODE, F8>;
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  static int max_clusters = 0;
-  std::call_once(once, [&] {
-    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    Cfg::kSmemBytes);
-    if (attr_err == cudaSuccess && PAIR) {
+  static PerDeviceInit init;
+  long long max_clusters = 0;
+  const cudaError_t attr_err = once_per_device(init, [&](long long* value) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Cfg::kSmemBytes);
+    if (e == cudaSuccess && PAIR) {
       // Clusters of two that fit on the device at once (pairs must share a
       // GPC, so this can be below half the SM count).
       cudaLaunchConfig_t cfg = {};
@@ -541,13 +540,17 @@ int launch_variant(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs&
       cfg.dynamicSmemBytes = Cfg::kSmemBytes;
       cfg.attrs = at;
       cfg.numAttrs = 1;
-      attr_err = cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg);
-      if (attr_err == cudaSuccess && max_clusters < 1) attr_err = cudaErrorInvalidConfiguration;
+      int n = 0;
+      e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+      if (e == cudaSuccess && n < 1) e = cudaErrorInvalidConfiguration;
+      *value = n;
     }
-  });
+    return e;
+  }, &max_clusters);
   if (attr_err != cudaSuccess) return MC_ERR_CUDA;
   if constexpr (PAIR) {
-    const int clusters = g.num_units < max_clusters ? g.num_units : max_clusters;
+    const int clusters =
+        g.num_units < max_clusters ? g.num_units : static_cast<int>(max_clusters);
     if (launch_kernel(kern, dim3(2 * clusters), dim3(kThreads), Cfg::kSmemBytes, stream, 2u, ta,
                       tb, g) != cudaSuccess)
       return MC_ERR_CUDA;

@@ -319,13 +319,12 @@ int ln_bwd_launch(const float* dout, const float* x, const float* mean, const fl
                   cudaStream_t st) {
   const size_t smem = 3 * static_cast<size_t>(h) * sizeof(float);
   auto kern = ln_bwd_kernel<VPT>;
-  // Opt in once to the largest column-partial buffer (h = kMaxLayerNormHidden);
+  // Opt in once per device to the largest column-partial buffer (h = kMaxLayerNormHidden);
   // 48 KB of dynamic memory plus the kernel's static reduction buffer already
   // exceeds the default limit at h = 4096.
-  static std::once_flag once;
-  static cudaError_t attr = cudaSuccess;
-  std::call_once(once, [&] {
-    attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  static PerDeviceInit init;
+  const cudaError_t attr = once_per_device(init, [&](long long*) {
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 3 * kMaxLayerNormHidden * static_cast<int>(sizeof(float)));
   });
   if (attr != cudaSuccess) return MC_ERR_CUDA;

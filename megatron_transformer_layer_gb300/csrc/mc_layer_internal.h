@@ -10,6 +10,8 @@
 #include <cuda_runtime.h>
 #endif
 
+#include <mutex>
+
 namespace mc {
 
 #ifdef __CUDACC__
@@ -71,6 +73,43 @@ constexpr int kColsumMinSplits = 64;
 constexpr int kColsumMaxSplits = 512;
 
 int num_sms();  // SM count of the current device (cached per device)
+
+#ifdef __CUDACC__
+// Identity of the current device's context: (device ordinal, context id).
+// The context id changes when the context is destroyed and re-created (e.g.
+// by cudaDeviceReset), so set-up that belongs to a context is redone then.
+cudaError_t current_context(int* dev, unsigned long long* ctx_id);
+
+// One-time set-up that belongs to a device's context -- a kernel attribute,
+// an occupancy figure, a symbol's device address: run with that device
+// current, once per device and context, its status and value cached.
+constexpr int kMaxDevices = 64;
+struct PerDeviceInit {
+  std::mutex mu;
+  unsigned long long ctx[kMaxDevices] = {};  // 0: not set up yet
+  cudaError_t err[kMaxDevices] = {};
+  long long value[kMaxDevices] = {};
+};
+
+// Runs init(&value) the first time it is called for the current device's
+// context; returns its status (and value) then and on every later call.
+template <class F>
+inline cudaError_t once_per_device(PerDeviceInit& s, F&& init, long long* value = nullptr) {
+  int dev = 0;
+  unsigned long long id = 0;
+  cudaError_t e = current_context(&dev, &id);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(s.mu);
+  if (s.ctx[dev] != id) {
+    s.value[dev] = 0;
+    s.err[dev] = init(&s.value[dev]);
+    s.ctx[dev] = id;
+  }
+  if (value) *value = s.value[dev];
+  return s.err[dev];
+}
+#endif
 
 #ifdef __CUDACC__
 // bf16 tensor map with 128-byte swizzle and zero fill; strides_bytes has
