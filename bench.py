@@ -55,6 +55,14 @@ WORKLOAD_NAMES = {
 LAUNCHES_PER_STEP = 7 + 21
 
 
+def launches_per_step(t_shards: int, recompute: bool) -> int:
+    """Kernel launches of one layer step; in sequence-parallel mode the
+    per-token kernels and the reduce-scattered GEMMs run once per shard
+    (forward 4t + 3, backward 8t + 13; t = 1 gives the 7 + 21 above)."""
+    fwd = 4 * t_shards + 3
+    return fwd + 8 * t_shards + 13 + (fwd if recompute else 0)
+
+
 def dims(w):
     d = w["head_dim"] or w["hidden"] // w["heads"]
     return dict(b=w["micro_batch"], s=w["seq_len"], T=w["micro_batch"] * w["seq_len"],
@@ -513,7 +521,7 @@ def run_ours(args, world, rank, local):
         inp_l = make_layer_inputs(LayerShape(**w), seed=0, layer=li)
         p_l = {k: bf16_tensor(v, device) for k, v in inp_l.params.items()}
         layers.append(TransformerLayer(**w, params=p_l, device=device, recompute=args.recompute,
-                                       workspace=shared_ws))
+                                       workspace=shared_ws, sequence_parallel=args.sp))
         if args.recompute:
             shared_ws = layers[-1].ws  # recomputation: one workspace for the whole stack
         if li == 0:
@@ -702,6 +710,7 @@ def run_ours(args, world, rank, local):
                    + (f", stack of {n_layers} layers" if n_layers > 1 else ""), **w,
                    "layers": n_layers,
                    "activation_recompute": bool(args.recompute),
+                   "sequence_parallel": bool(args.sp),
                    "cuda_graph": bool(args.graph),
                    "l2": "inputs larger than L2 (1.6 GB of bf16 weights plus activations read per step)"
                    if args.workload == "c4" else "working set vs L2 not checked",
@@ -715,7 +724,8 @@ def run_ours(args, world, rank, local):
                 "pipeline": "step i+1's inputs uploaded and step i's results read back on two "
                             "copy streams while step i computes (double-buffered)",
                 "serial_value": e2e_serial_value},
-        "gpu_launches": (LAUNCHES_PER_STEP + (7 if args.recompute else 0)) * n_layers * args.steps,
+        "gpu_launches": launches_per_step(w["tp_parts"] if args.sp else 1, args.recompute)
+        * n_layers * args.steps,
         "memory": {"saved_bytes_per_layer": layer.saved_bytes,
                    "workspace_bytes_per_layer": layer.ws_bytes,
                    "workspace_shared_by_stack": bool(args.recompute)},
@@ -723,7 +733,7 @@ def run_ours(args, world, rank, local):
     }
     line["record_card"] = record_card(device)
     if args.workload == "c4" and n_layers == 1 and not args.no_c5 and not args.recompute \
-            and not args.graph:
+            and not args.graph and not args.sp:
         # the long-sequence configuration (attention 40% of its flops), timed in
         # the same run; all ranks run it so that max-over-ranks still holds
         del layers, layer, acts, grads, x_d, dy_d, y_d, dx_d
@@ -772,6 +782,8 @@ def main():
                     help="capture one step in a CUDA graph and time its replays")
     ap.add_argument("--recompute", action="store_true",
                     help="activation recomputation: keep nothing between forward and backward")
+    ap.add_argument("--sp", action="store_true",
+                    help="sequence-parallel mode: per-token work launched per sequence shard")
     ap.add_argument("--layers", type=int, default=1,
                     help="time a stack of this many layers (distinct weights) per step")
     ap.add_argument("--cp", type=int, default=4,

@@ -96,16 +96,21 @@ extern "C" {
  * shared by every layer of a stack run in sequence. */
 #define MC_RECOMPUTE_ACTIVATIONS 2u
 /* Sequence-parallel tensor parallelism (named with TP and EP in the Megatron
- * Core guide's record card and parallelism table): LayerNorm, residual and
- * bias-add run on sequence shards, the partial sums after out-proj and fc2
- * become a reduce-scatter over the shards and QKV / fc1 read the
- * all-gathered LayerNorm output.  Its contract is that the token count
- * micro_batch * seq_len divides by tp_parts (MC_ERR_SHAPE otherwise).  With
- * all partitions on one GPU the reduce-scatter is the in-accumulator
- * partition sum written tile by tile (each output row belongs to exactly one
- * shard), the shards of LayerNorm and residual lie side by side in one
- * buffer, and the all-gather reads them in place, so results equal the
- * default mode bit for bit and no kernel changes. */
+ * Core guide's record card and parallelism table): the tokens are cut into
+ * tp_parts sequence shards of T / tp_parts consecutive tokens, and the
+ * per-token work each tensor-parallel rank does on its own shard is launched
+ * once per shard: LayerNorm forward and backward, the residual epilogues of
+ * the out-projection and fc2, the column sum of dy.  The sum of the
+ * row-parallel partials becomes a reduce-scatter: one out-projection / fc2
+ * launch per shard writes that shard's rows, its accumulator summing every
+ * partition's K slice; in the backward pass the QKV and fc1 input gradients
+ * are reduce-scattered the same way.  QKV and fc1 (and every weight
+ * gradient) read all shards' rows, which lie side by side in one buffer: the
+ * all-gather.  Gradients of the sequence-sharded parameters (LayerNorm gamma
+ * and beta, b_o, b_fc2) are the shards' partial sums added in shard order.
+ * Contract: micro_batch * seq_len divides by tp_parts (MC_ERR_SHAPE
+ * otherwise).  Results equal the default mode up to the order of those
+ * fp32 sums. */
 #define MC_SEQUENCE_PARALLEL 4u
 
 typedef struct mc_layer_shape {

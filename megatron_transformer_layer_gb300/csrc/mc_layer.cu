@@ -238,13 +238,35 @@ size_t mc_layer_workspace_bytes(const mc_layer_shape* shape) {
 
 namespace mc {
 namespace {
+bool seq_parallel(const mc_layer_shape& sh) { return (sh.flags & MC_SEQUENCE_PARALLEL) != 0; }
+
+// Sequence shards of the sequence-parallel mode: `shards` (t, else 1) runs
+// of Ts = T / shards consecutive tokens.  A per-token kernel (LayerNorm, the
+// residual epilogue of a row-parallel GEMM) is launched once per shard on
+// its rows -- the work one tensor-parallel rank does on its sequence shard.
+struct Shards {
+  int64_t n, rows;
+};
+
+Shards shards_of(const Dims& D, bool sp) { return sp ? Shards{D.t, D.T / D.t} : Shards{1, D.T}; }
+
 // F1..F7: the forward launch sequence into the activations `S`.
+// Sequence-parallel mode: LN1, LN2 and the two row-parallel GEMMs run per
+// sequence shard.  Each row-parallel launch covers one shard's rows and sums
+// every partition's K slice in its accumulator: the reduce-scatter of the
+// partial sums.  QKV and fc1 read all shards' LayerNorm output, which lie
+// side by side in one buffer: the all-gather.
 int enqueue_forward(const Dims& D, const mc_layer_weights* w, const float* x, float* y,
-                    const Saved& S, const Work& W, cudaStream_t st) {
+                    const Saved& S, const Work& W, bool sp, cudaStream_t st) {
   const int t = static_cast<int>(D.t);
   const int h = static_cast<int>(D.h);
-  // F1  LN1
-  MC_TRY(launch_layernorm_forward(x, w->ln1_g, w->ln1_b, S.ln1, S.mu1, S.rs1, D.T, h, W.status, st));
+  const Shards sh = shards_of(D, sp);
+  // F1  LN1 (per shard)
+  for (int64_t p = 0; p < sh.n; ++p) {
+    const int64_t r0 = p * sh.rows;
+    MC_TRY(launch_layernorm_forward(x + r0 * D.h, w->ln1_g, w->ln1_b, S.ln1 + r0 * D.h, S.mu1 + r0,
+                                    S.rs1 + r0, sh.rows, h, W.status, st));
+  }
   // F2  QKV (column-parallel: every partition's heads are output columns)
   MC_TRY(launch_gemm(D.T, 3 * D.a, D.h, S.ln1, D.h, 0, w->w_qkv, D.h, 0, S.qkv, 3 * D.a,
                      MC_EPI_BIAS_BF16, w->b_qkv, nullptr, 0, 0, 1, W.status, st));
@@ -252,17 +274,28 @@ int enqueue_forward(const Dims& D, const mc_layer_weights* w, const float* x, fl
   MC_TRY(launch_attention_forward(S.qkv, S.o, S.lse, static_cast<int>(D.b), static_cast<int>(D.s),
                                   static_cast<int>(D.H), static_cast<int>(D.d), W.status, st));
   // F4  out-projection, row-parallel: partition partials summed in the
-  //     accumulator, then + b_o + x
-  MC_TRY(launch_gemm(D.T, D.h, D.a, S.o, D.a, 0, w->w_o, D.a, 0, S.x1, D.h, MC_EPI_BIAS_RESID_F32,
-                     w->b_o, x, D.h, 0, t, W.status, st));
-  // F5  LN2
-  MC_TRY(launch_layernorm_forward(S.x1, w->ln2_g, w->ln2_b, S.ln2, S.mu2, S.rs2, D.T, h, W.status, st));
+  //     accumulator, then + b_o + x (per shard)
+  for (int64_t p = 0; p < sh.n; ++p) {
+    const int64_t r0 = p * sh.rows;
+    MC_TRY(launch_gemm(sh.rows, D.h, D.a, S.o + r0 * D.a, D.a, 0, w->w_o, D.a, 0, S.x1 + r0 * D.h,
+                       D.h, MC_EPI_BIAS_RESID_F32, w->b_o, x + r0 * D.h, D.h, 0, t, W.status, st));
+  }
+  // F5  LN2 (per shard)
+  for (int64_t p = 0; p < sh.n; ++p) {
+    const int64_t r0 = p * sh.rows;
+    MC_TRY(launch_layernorm_forward(S.x1 + r0 * D.h, w->ln2_g, w->ln2_b, S.ln2 + r0 * D.h,
+                                    S.mu2 + r0, S.rs2 + r0, sh.rows, h, W.status, st));
+  }
   // F6  fc1 + bias + GeLU (column-parallel)
   MC_TRY(launch_gemm(D.T, D.f, D.h, S.ln2, D.h, 0, w->w_fc1, D.h, 0, S.g, D.f, MC_EPI_BIAS_GELU,
                      w->b_fc1, S.hp, D.f, 0, 1, W.status, st));
-  // F7  fc2, row-parallel: partials summed, + b_fc2 + x1
-  MC_TRY(launch_gemm(D.T, D.h, D.f, S.g, D.f, 0, w->w_fc2, D.f, 0, y, D.h, MC_EPI_BIAS_RESID_F32,
-                     w->b_fc2, S.x1, D.h, 0, t, W.status, st));
+  // F7  fc2, row-parallel: partials summed, + b_fc2 + x1 (per shard)
+  for (int64_t p = 0; p < sh.n; ++p) {
+    const int64_t r0 = p * sh.rows;
+    MC_TRY(launch_gemm(sh.rows, D.h, D.f, S.g + r0 * D.f, D.f, 0, w->w_fc2, D.f, 0, y + r0 * D.h,
+                       D.h, MC_EPI_BIAS_RESID_F32, w->b_fc2, S.x1 + r0 * D.h, D.h, 0, t, W.status,
+                       st));
+  }
   return MC_OK;
 }
 }  // namespace
@@ -283,7 +316,7 @@ int mc_layer_forward(const mc_layer_shape* shape, const mc_layer_weights* w, con
   const Work W = plan_ws(D, rc_mode, ws, nullptr);
   const Saved S = plan_saved(D, rc_mode ? W.recompute_saved : saved, nullptr);
   if (cudaMemsetAsync(W.status, 0, kStatusBytes, st) != cudaSuccess) return MC_ERR_CUDA;
-  return enqueue_forward(D, w, x, y, S, W, st);
+  return enqueue_forward(D, w, x, y, S, W, seq_parallel(*shape), st);
 }
 
 int mc_layer_backward(const mc_layer_shape* shape, const mc_layer_weights* w, const float* x,
@@ -306,30 +339,53 @@ int mc_layer_backward(const mc_layer_shape* shape, const mc_layer_weights* w, co
   if (rc_mode) {
     // Activation recomputation: rebuild F1..F7's activations from x.  The
     // recomputed y lands in dx1's buffer, which B3 overwrites later.
-    MC_TRY(enqueue_forward(D, w, x, W.dx1, S, W, st));
+    MC_TRY(enqueue_forward(D, w, x, W.dx1, S, W, seq_parallel(*shape), st));
   }
   const int acc = (shape->flags & MC_ACCUMULATE_GRADS) ? 1 : 0;
   const int t = static_cast<int>(D.t);
   const int h = static_cast<int>(D.h);
   const mc_layer_grads& G = *grads;
+  // Sequence-parallel mode: the per-token steps (the column sum of dy, both
+  // LayerNorm backwards) and the two column-parallel input gradients (dln2,
+  // dln1: a reduce-scatter of the partitions' partial sums) run per sequence
+  // shard; the gradients of the sequence-sharded parameters (LayerNorm
+  // gamma / beta, the row-parallel biases) are the shards' partial sums,
+  // added in shard order (the first shard honours MC_ACCUMULATE_GRADS, the
+  // rest add).  Weight gradients and the column-parallel products read all
+  // shards' rows, which lie side by side: the all-gather.
+  const Shards sh = shards_of(D, seq_parallel(*shape));
+  auto shard_acc = [&](int64_t p) { return p == 0 ? acc : 1; };
 
   // B1  fc2: db2 = colsum(dy) (+ bf16 copy of dy as a GEMM operand),
   //     dW2 = dy^T g, dhp = (dy W2) * gelu'(hp)
-  MC_TRY(launch_colsum(dy, false, D.T, D.h, G.b_fc2, acc, W.dy16, W.partials, W.status, st));
+  for (int64_t p = 0; p < sh.n; ++p) {
+    const int64_t r0 = p * sh.rows;
+    MC_TRY(launch_colsum(dy + r0 * D.h, false, sh.rows, D.h, G.b_fc2, shard_acc(p),
+                         W.dy16 + r0 * D.h, W.partials, W.status, st));
+  }
   MC_TRY(launch_gemm(D.h, D.f, D.T, W.dy16, D.h, 1, S.g, D.f, 1, G.w_fc2, D.f, MC_EPI_STORE_F32,
                      nullptr, nullptr, 0, acc, 1, W.status, st));
   MC_TRY(launch_gemm(D.T, D.f, D.h, W.dy16, D.h, 0, w->w_fc2, D.f, 1, W.dhp, D.f, MC_EPI_GELU_BWD,
                      nullptr, S.hp, D.f, 0, 1, W.status, st));
   // B2  fc1: db1, dW1 = dhp^T ln2, dln2 = sum_p dhp_p W1_p (partition sum in
-  //     the accumulator)
+  //     the accumulator; per shard in sequence-parallel mode)
   MC_TRY(launch_colsum(W.dhp, true, D.T, D.f, G.b_fc1, acc, nullptr, W.partials, W.status, st));
   MC_TRY(launch_gemm(D.f, D.h, D.T, W.dhp, D.f, 1, S.ln2, D.h, 1, G.w_fc1, D.h, MC_EPI_STORE_F32,
                      nullptr, nullptr, 0, acc, 1, W.status, st));
-  MC_TRY(launch_gemm(D.T, D.h, D.f, W.dhp, D.f, 0, w->w_fc1, D.h, 1, W.dln, D.h, MC_EPI_STORE_F32,
-                     nullptr, nullptr, 0, 0, t, W.status, st));
+  for (int64_t p = 0; p < sh.n; ++p) {
+    const int64_t r0 = p * sh.rows;
+    MC_TRY(launch_gemm(sh.rows, D.h, D.f, W.dhp + r0 * D.f, D.f, 0, w->w_fc1, D.h, 1,
+                       W.dln + r0 * D.h, D.h, MC_EPI_STORE_F32, nullptr, nullptr, 0, 0, t, W.status,
+                       st));
+  }
   // B3  LN2 backward: dx1 = dy + LN2^T(dln2); dgamma2, dbeta2; db_o = colsum(dx1)
-  MC_TRY(launch_layernorm_backward(W.dln, S.x1, S.mu2, S.rs2, w->ln2_g, dy, W.dx1, W.dx1_16,
-                                   G.ln2_g, G.ln2_b, G.b_o, acc, W.partials, D.T, h, W.status, st));
+  for (int64_t p = 0; p < sh.n; ++p) {
+    const int64_t r0 = p * sh.rows;
+    MC_TRY(launch_layernorm_backward(W.dln + r0 * D.h, S.x1 + r0 * D.h, S.mu2 + r0, S.rs2 + r0,
+                                     w->ln2_g, dy + r0 * D.h, W.dx1 + r0 * D.h,
+                                     W.dx1_16 + r0 * D.h, G.ln2_g, G.ln2_b, G.b_o, shard_acc(p),
+                                     W.partials, sh.rows, h, W.status, st));
+  }
   // B4  out-projection: dWo = dx1^T O, dO = dx1 Wo
   MC_TRY(launch_gemm(D.h, D.a, D.T, W.dx1_16, D.h, 1, S.o, D.a, 1, G.w_o, D.a, MC_EPI_STORE_F32,
                      nullptr, nullptr, 0, acc, 1, W.status, st));
@@ -339,15 +395,25 @@ int mc_layer_backward(const mc_layer_shape* shape, const mc_layer_weights* w, co
   MC_TRY(launch_attention_backward(S.qkv, S.o, S.lse, W.dO, W.dqkv, W.delta, static_cast<int>(D.b),
                                    static_cast<int>(D.s), static_cast<int>(D.H),
                                    static_cast<int>(D.d), W.status, st));
-  // B6  QKV: db_qkv, dWqkv = dqkv^T ln1, dln1 = sum_p dqkv_p Wqkv_p
+  // B6  QKV: db_qkv, dWqkv = dqkv^T ln1, dln1 = sum_p dqkv_p Wqkv_p (per
+  //     shard in sequence-parallel mode)
   MC_TRY(launch_colsum(W.dqkv, true, D.T, 3 * D.a, G.b_qkv, acc, nullptr, W.partials, W.status, st));
   MC_TRY(launch_gemm(3 * D.a, D.h, D.T, W.dqkv, 3 * D.a, 1, S.ln1, D.h, 1, G.w_qkv, D.h,
                      MC_EPI_STORE_F32, nullptr, nullptr, 0, acc, 1, W.status, st));
-  MC_TRY(launch_gemm(D.T, D.h, 3 * D.a, W.dqkv, 3 * D.a, 0, w->w_qkv, D.h, 1, W.dln, D.h,
-                     MC_EPI_STORE_F32, nullptr, nullptr, 0, 0, t, W.status, st));
+  for (int64_t p = 0; p < sh.n; ++p) {
+    const int64_t r0 = p * sh.rows;
+    MC_TRY(launch_gemm(sh.rows, D.h, 3 * D.a, W.dqkv + r0 * 3 * D.a, 3 * D.a, 0, w->w_qkv, D.h, 1,
+                       W.dln + r0 * D.h, D.h, MC_EPI_STORE_F32, nullptr, nullptr, 0, 0, t,
+                       W.status, st));
+  }
   // B7  LN1 backward: dx = dx1 + LN1^T(dln1); dgamma1, dbeta1
-  MC_TRY(launch_layernorm_backward(W.dln, x, S.mu1, S.rs1, w->ln1_g, W.dx1, dx, nullptr, G.ln1_g,
-                                   G.ln1_b, nullptr, acc, W.partials, D.T, h, W.status, st));
+  for (int64_t p = 0; p < sh.n; ++p) {
+    const int64_t r0 = p * sh.rows;
+    MC_TRY(launch_layernorm_backward(W.dln + r0 * D.h, x + r0 * D.h, S.mu1 + r0, S.rs1 + r0,
+                                     w->ln1_g, W.dx1 + r0 * D.h, dx + r0 * D.h, nullptr, G.ln1_g,
+                                     G.ln1_b, nullptr, shard_acc(p), W.partials, sh.rows, h,
+                                     W.status, st));
+  }
   return MC_OK;
 }
 
