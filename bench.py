@@ -455,10 +455,11 @@ def run_stage(args, w, device):
     print(json.dumps(line), flush=True)
 
 
-def sub_record(name, device, world, steps, warmup, peak_sustained):
+def sub_record(name, device, world, steps, warmup, peak_sustained, fp8=False, attention=True):
     """One more workload timed in the same run, device-resident: its step
     (forward + backward through the C ABI, CUDA events on the launching
-    stream) and its attention kernels alone."""
+    stream) and, with `attention`, its attention kernels alone.  `fp8`: the
+    layer's GEMMs on 8-bit operands (MC_FP8_HYBRID)."""
     import numpy as np
     import torch
 
@@ -468,7 +469,7 @@ def sub_record(name, device, world, steps, warmup, peak_sustained):
     D = dims(w)
     inp = make_layer_inputs(LayerShape(**w), seed=0)
     params = {k: bf16_tensor(v, device) for k, v in inp.params.items()}
-    layer = TransformerLayer(**w, params=params, device=device)
+    layer = TransformerLayer(**w, params=params, device=device, fp8=fp8)
     x = torch.from_numpy(inp.f64("x").reshape(-1, D["h"]).astype(np.float32)).to(device)
     dy = torch.from_numpy(inp.f64("dy").reshape(-1, D["h"]).astype(np.float32)).to(device)
     del inp
@@ -486,10 +487,12 @@ def sub_record(name, device, world, steps, warmup, peak_sustained):
     out = {"workload": WORKLOAD_NAMES[name], "steps": steps, "ms_per_step": ms,
            "tokens_per_s": world * D["T"] / (ms / 1e3),
            "tflops": flops / (ms / 1e3) / 1e12,
-           "frac_of_sustained": flops / (ms / 1e3) / 1e12 / peak_sustained}
+           "gemm_operands": "fp8 (E4M3 forward, E5M2 gradients)" if fp8 else "bf16"}
+    if not fp8:
+        out["frac_of_sustained"] = flops / (ms / 1e3) / 1e12 / peak_sustained
     del layer, params, x, dy, y, dx
     torch.cuda.empty_cache()
-    for stage in ("attn_fwd", "attn_bwd"):
+    for stage in (("attn_fwd", "attn_bwd") if attention else ()):
         launch, work, _, _ = stage_launcher(stage, w, device)
         sms = time_launches(launch, device, max(3, steps), 2)
         out[f"{stage}_ms"] = sms
@@ -521,7 +524,8 @@ def run_ours(args, world, rank, local):
         inp_l = make_layer_inputs(LayerShape(**w), seed=0, layer=li)
         p_l = {k: bf16_tensor(v, device) for k, v in inp_l.params.items()}
         layers.append(TransformerLayer(**w, params=p_l, device=device, recompute=args.recompute,
-                                       workspace=shared_ws, sequence_parallel=args.sp))
+                                       workspace=shared_ws, sequence_parallel=args.sp,
+                                       fp8=args.fp8))
         if args.recompute:
             shared_ws = layers[-1].ws  # recomputation: one workspace for the whole stack
         if li == 0:
@@ -704,13 +708,14 @@ def run_ours(args, world, rank, local):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "ms_per_step_p50": statistics.median(per_step),
         "ms_per_step_p95": sorted(per_step)[max(0, int(round(0.95 * len(per_step))) - 1)],
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp8-hybrid" if args.fp8 else "bf16",
         "data": "synthetic",
         "config": {"workload": WORKLOAD_NAMES[args.workload]
                    + (f", stack of {n_layers} layers" if n_layers > 1 else ""), **w,
                    "layers": n_layers,
                    "activation_recompute": bool(args.recompute),
                    "sequence_parallel": bool(args.sp),
+                   "gemm_operands": "fp8 (E4M3 forward, E5M2 gradients)" if args.fp8 else "bf16",
                    "cuda_graph": bool(args.graph),
                    "l2": "inputs larger than L2 (1.6 GB of bf16 weights plus activations read per step)"
                    if args.workload == "c4" else "working set vs L2 not checked",
@@ -733,12 +738,16 @@ def run_ours(args, world, rank, local):
     }
     line["record_card"] = record_card(device)
     if args.workload == "c4" and n_layers == 1 and not args.no_c5 and not args.recompute \
-            and not args.graph and not args.sp:
+            and not args.graph and not args.sp and not args.fp8:
         # the long-sequence configuration (attention 40% of its flops), timed in
         # the same run; all ranks run it so that max-over-ranks still holds
         del layers, layer, acts, grads, x_d, dy_d, y_d, dx_d
         torch.cuda.empty_cache()
         line["c5"] = sub_record("c5", device, world, min(args.steps, 10), args.warmup, peak)
+        # the same layer with its GEMMs on 8-bit operands, for comparison
+        # (not the headline: the headline is the bf16 path)
+        line["c4_fp8"] = sub_record("c4", device, world, min(args.steps, 20), args.warmup, peak,
+                                    fp8=True, attention=False)
     if rank == 0 and world == 1 and not args.no_cpu_baseline and n_layers == 1:
         prepared = prepare_oracle(w, args.ref_prefix)
         toks = prepared[0].seq_len
@@ -782,6 +791,8 @@ def main():
                     help="capture one step in a CUDA graph and time its replays")
     ap.add_argument("--recompute", action="store_true",
                     help="activation recomputation: keep nothing between forward and backward")
+    ap.add_argument("--fp8", action="store_true",
+                    help="GEMMs on 8-bit operands (E4M3 forward, E5M2 gradients)")
     ap.add_argument("--sp", action="store_true",
                     help="sequence-parallel mode: per-token work launched per sequence shard")
     ap.add_argument("--layers", type=int, default=1,

@@ -112,6 +112,22 @@ extern "C" {
  * otherwise).  Results equal the default mode up to the order of those
  * fp32 sums. */
 #define MC_SEQUENCE_PARALLEL 4u
+/* FP8 "hybrid" GEMMs (the Megatron-Core listing, 混合精度: FP8 training on
+ * Blackwell Ultra with E4M3 in the forward pass and E5M2 for gradients):
+ * all twelve GEMMs of the layer run on 8-bit operands with fp32
+ * accumulation (tcgen05 kind::f8f6f4).  Forward operands -- ln1, O, ln2, g
+ * and the four weight matrices -- are E4M3; the gradient operands dy, dhp,
+ * dx1 and dQ|dK|dV are E5M2.  Each operand tensor is quantised with
+ * per-tensor current scaling (amax of the tensor as it stands, scale =
+ * fmax / amax, as mc_fp8_quantize), once, into a row-major copy and, where a
+ * product contracts over its rows, a transposed copy with the same scale;
+ * the GEMM epilogue multiplies by the two inverse scales.  Everything else
+ * (LayerNorm, attention, GeLU, bias and residual, the stored activations and
+ * all gradients) is as in the default mode.  Requires micro_batch * seq_len
+ * to be a multiple of 16 (MC_ERR_UNSUPPORTED otherwise) and is not combined
+ * with MC_SEQUENCE_PARALLEL (MC_ERR_ARGUMENT).  mc_layer_saved_bytes and
+ * mc_layer_workspace_bytes include the 8-bit copies. */
+#define MC_FP8_HYBRID 8u
 
 typedef struct mc_layer_shape {
   int32_t micro_batch; /* b  (--micro-batch-size)               */
@@ -123,7 +139,7 @@ typedef struct mc_layer_shape {
   int32_t head_dim;    /* 0 => hidden / heads; > 0 decouples a = heads * head_dim
                           from hidden (one tensor-parallel rank's shard run alone) */
   uint32_t flags;      /* MC_ACCUMULATE_GRADS | MC_RECOMPUTE_ACTIVATIONS |
-                          MC_SEQUENCE_PARALLEL, or 0 */
+                          MC_SEQUENCE_PARALLEL | MC_FP8_HYBRID, or 0 */
 } mc_layer_shape;
 
 /* bf16 parameters (uint16_t bit patterns), device pointers. */
@@ -296,6 +312,19 @@ size_t mc_fp8_scratch_floats(void);
  * *scale_inv = 1 / scale.  Enqueued on `stream`; deterministic. */
 int mc_fp8_quantize(const void* in, int32_t in_bf16, int64_t n, int32_t format, uint8_t* out,
                     float* scale_inv, float* scratch, int* status, void* stream);
+
+/* The same quantisation of a row-major [rows, cols] matrix (in: fp32, or
+ * bf16 when in_bf16 != 0; rows and cols multiples of 16, pointers 16-byte
+ * aligned), writing the bytes as is to `out` ([rows, cols]) and/or
+ * transposed to `out_t` ([cols, rows]); either output may be NULL.  One
+ * scale for both.  The transposed copy is the K-major operand of a product
+ * that contracts over the matrix's rows (a weight gradient contracts over
+ * tokens; an input gradient reads the weight transposed).  `scratch` as for
+ * mc_fp8_quantize; MC_ERR_SHAPE for dimensions that are not multiples of
+ * 16. */
+int mc_fp8_quantize_2d(const void* in, int32_t in_bf16, int64_t rows, int64_t cols,
+                       int32_t format, uint8_t* out, uint8_t* out_t, float* scale_inv,
+                       float* scratch, void* stream);
 
 /* out = epilogue((A B^T) * *a_scale_inv * *b_scale_inv) with A [M, K] and
  * B [N, K] row-major 8-bit floats (K contiguous; lda, ldb multiples of 16),

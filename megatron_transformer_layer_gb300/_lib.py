@@ -28,6 +28,7 @@ MC_ERR_SCRATCH_LIMIT = -10
 MC_ACCUMULATE_GRADS = 1
 MC_RECOMPUTE_ACTIVATIONS = 2
 MC_SEQUENCE_PARALLEL = 4
+MC_FP8_HYBRID = 8
 
 MC_EPI_STORE_F32 = 0
 MC_EPI_STORE_BF16 = 1
@@ -92,6 +93,7 @@ _SIGNATURES = {
     "mc_selftest_wait_timeout": (_INT, [_I64, _P, _P]),
     "mc_fp8_scratch_floats": (_SZ, []),
     "mc_fp8_quantize": (_INT, [_P, _I32, _I64, _I32, _P, _P, _P, _P, _P]),
+    "mc_fp8_quantize_2d": (_INT, [_P, _I32, _I64, _I64, _I32, _P, _P, _P, _P, _P]),
     "mc_gemm_fp8": (_INT, [_I64, _I64, _I64, _P, _I64, _I32, _P, _I64, _I32, _P, _P, _P, _I64,
                            _I32, _P, _P, _I64, _I32, _I32, _P, _P]),
     "mc_cp_schedule": (_INT, [_I32, _I32, _I32, ctypes.POINTER(_I32)]),
@@ -271,6 +273,16 @@ def mc_fp8_quantize(x, out, scale_inv, scratch, fmt, status=None, stream=None) -
     in_bf16 = 1 if x.dtype == torch.bfloat16 else 0
     return lib().mc_fp8_quantize(_ptr(x), in_bf16, x.numel(), fmt, _ptr(out), _ptr(scale_inv),
                                  _ptr(scratch), _ptr(status), _stream(stream))
+
+
+def mc_fp8_quantize_2d(x, out, out_t, scale_inv, scratch, fmt, stream=None) -> int:
+    """Per-tensor current scaling of a 2-D x (fp32 or bf16) to 8-bit bytes,
+    written as is (out) and/or transposed (out_t); either may be None."""
+    import torch
+    in_bf16 = 1 if x.dtype == torch.bfloat16 else 0
+    rows, cols = x.shape
+    return lib().mc_fp8_quantize_2d(_ptr(x), in_bf16, rows, cols, fmt, _ptr(out), _ptr(out_t),
+                                    _ptr(scale_inv), _ptr(scratch), _stream(stream))
 
 
 def mc_gemm_fp8(M, N, K, A, lda, a_format, B, ldb, b_format, a_scale_inv, b_scale_inv, out, ldc,

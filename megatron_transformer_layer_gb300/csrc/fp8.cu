@@ -107,9 +107,110 @@ __global__ void fp8_cast_kernel(const void* __restrict__ in, int64_t n,
     out[i] = __nv_cvt_float_to_fp8(__fmul_rn(load_elem(in, BF16, i), sc), __NV_SATFINITE, kInterp);
 }
 
+// The same cast over a row-major [rows, cols] matrix, writing it as is
+// (`out`, [rows, cols]) and/or transposed (`out_t`, [cols, rows]): the
+// transposed copy is the K-major form of the matrix for products that
+// contract over its rows (weight gradients, and the weight in an input
+// gradient).  One 64 x 64 tile per block, staged through shared memory;
+// cols and rows are multiples of 16.
+constexpr int kTT = 64;  // tile edge
+template <bool BF16, int FMT>
+__global__ void __launch_bounds__(256)
+    fp8_cast_2d_kernel(const void* __restrict__ in, int64_t rows, int64_t cols,
+                       const float* __restrict__ state, uint8_t* __restrict__ out,
+                       uint8_t* __restrict__ out_t) {
+  pdl_wait();  // the previous kernel on the stream has completed
+  pdl_launch();
+  __shared__ uint8_t tile[kTT][kTT + 4];
+  const float sc = state[0];
+  constexpr __nv_fp8_interpretation_t kInterp = FMT == 0 ? __NV_E4M3 : __NV_E5M2;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kTT;
+  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * kTT;
+  // load + cast: thread -> (row tid / 4, 16 columns at 16 (tid % 4))
+  {
+    const int lr = threadIdx.x >> 2, lc = (threadIdx.x & 3) * 16;
+    const int64_t r = r0 + lr, c = c0 + lc;
+    if (r < rows && c < cols) {
+      float x[16];
+      if constexpr (BF16) {
+        const uint4* src = reinterpret_cast<const uint4*>(
+            static_cast<const __nv_bfloat16*>(in) + r * cols + c);
+#pragma unroll
+        for (int v = 0; v < 2; ++v) {
+          const uint4 w = src[v];
+          x[8 * v + 0] = bf16_lo(w.x); x[8 * v + 1] = bf16_hi(w.x);
+          x[8 * v + 2] = bf16_lo(w.y); x[8 * v + 3] = bf16_hi(w.y);
+          x[8 * v + 4] = bf16_lo(w.z); x[8 * v + 5] = bf16_hi(w.z);
+          x[8 * v + 6] = bf16_lo(w.w); x[8 * v + 7] = bf16_hi(w.w);
+        }
+      } else {
+        const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(in) +
+                                                            r * cols + c);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const float4 a = src[v];
+          x[4 * v] = a.x; x[4 * v + 1] = a.y; x[4 * v + 2] = a.z; x[4 * v + 3] = a.w;
+        }
+      }
+      uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const uint8_t b = __nv_cvt_float_to_fp8(__fmul_rn(x[e], sc), __NV_SATFINITE, kInterp);
+        w[e >> 2] |= static_cast<uint32_t>(b) << (8 * (e & 3));
+        tile[lr][lc + e] = b;
+      }
+      if (out) *reinterpret_cast<uint4*>(out + r * cols + c) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+  if (!out_t) return;
+  __syncthreads();
+  // transposed store: thread -> (output row = column tid / 4, 16 source rows)
+  {
+    const int lc = threadIdx.x >> 2, lr = (threadIdx.x & 3) * 16;
+    const int64_t c = c0 + lc, r = r0 + lr;
+    if (c < cols && r < rows) {
+      uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+      for (int e = 0; e < 16; ++e) w[e >> 2] |= static_cast<uint32_t>(tile[lr + e][lc]) << (8 * (e & 3));
+      *reinterpret_cast<uint4*>(out_t + c * rows + r) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+}
+
 }  // namespace
 
 size_t fp8_scratch_floats() { return kAmaxBlocks + 1; }
+
+int launch_fp8_quantize_2d(const void* in, bool in_bf16, int64_t rows, int64_t cols, int format,
+                           uint8_t* out, uint8_t* out_t, float* scale_inv, float* scratch,
+                           cudaStream_t st) {
+  if (rows < 1 || cols < 1 || rows % 16 || cols % 16) return MC_ERR_SHAPE;
+  if ((rows + kTT - 1) / kTT > 65535 || cols > (int64_t(1) << 31)) return MC_ERR_UNSUPPORTED;
+  if (format < 0 || format > 1) return MC_ERR_ARGUMENT;
+  if (!in || (!out && !out_t) || !scale_inv || !scratch) return MC_ERR_NULLPTR;
+  if ((reinterpret_cast<uintptr_t>(in) & 15u) || (reinterpret_cast<uintptr_t>(out) & 15u) ||
+      (reinterpret_cast<uintptr_t>(out_t) & 15u) || (reinterpret_cast<uintptr_t>(scratch) & 3u) ||
+      (reinterpret_cast<uintptr_t>(scale_inv) & 3u))
+    return MC_ERR_ALIGN;
+  const int64_t n = rows * cols;
+  const float fmax = format == 0 ? 448.f : 57344.f;
+  float* partials = scratch;
+  float* state = scratch + kAmaxBlocks;
+  if (in_bf16)
+    launch_kernel(amax_partial_kernel<true>, dim3(kAmaxBlocks), dim3(kThreadsPerBlock), 0, st, 1,
+                  in, n, partials);
+  else
+    launch_kernel(amax_partial_kernel<false>, dim3(kAmaxBlocks), dim3(kThreadsPerBlock), 0, st, 1,
+                  in, n, partials);
+  launch_kernel(fp8_scale_kernel, dim3(1), dim3(kAmaxBlocks), 0, st, 1, partials, fmax, state,
+                scale_inv);
+  const dim3 grid(static_cast<unsigned>((cols + kTT - 1) / kTT),
+                  static_cast<unsigned>((rows + kTT - 1) / kTT));
+  auto kern = in_bf16 ? (format == 0 ? fp8_cast_2d_kernel<true, 0> : fp8_cast_2d_kernel<true, 1>)
+                      : (format == 0 ? fp8_cast_2d_kernel<false, 0> : fp8_cast_2d_kernel<false, 1>);
+  launch_kernel(kern, grid, dim3(256), 0, st, 1, in, rows, cols, state, out, out_t);
+  return cudaGetLastError() == cudaSuccess ? MC_OK : MC_ERR_CUDA;
+}
 
 int launch_fp8_quantize(const void* in, bool in_bf16, int64_t n, int format, uint8_t* out,
                         float* scale_inv, float* scratch, cudaStream_t st) {
@@ -162,6 +263,13 @@ int mc_fp8_quantize(const void* in, int32_t in_bf16, int64_t n, int32_t format, 
   (void)status;
   return launch_fp8_quantize(in, in_bf16 != 0, n, format, out, scale_inv, scratch,
                              static_cast<cudaStream_t>(stream));
+}
+
+int mc_fp8_quantize_2d(const void* in, int32_t in_bf16, int64_t rows, int64_t cols,
+                       int32_t format, uint8_t* out, uint8_t* out_t, float* scale_inv,
+                       float* scratch, void* stream) {
+  return launch_fp8_quantize_2d(in, in_bf16 != 0, rows, cols, format, out, out_t, scale_inv,
+                                scratch, static_cast<cudaStream_t>(stream));
 }
 
 int mc_gemm_fp8(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_t lda, int32_t a_format,

@@ -65,6 +65,7 @@ namespace {
 
 struct Dims {
   int64_t b, s, T, h, H, d, a, f, t;
+  bool fp8;  // MC_FP8_HYBRID
 };
 
 Dims dims_of(const mc_layer_shape& sh) {
@@ -78,6 +79,7 @@ Dims dims_of(const mc_layer_shape& sh) {
   D.a = D.H * D.d;
   D.f = sh.ffn_hidden;
   D.t = sh.tp_parts;
+  D.fp8 = (sh.flags & MC_FP8_HYBRID) != 0;
   return D;
 }
 
@@ -86,8 +88,10 @@ int check_shape(const mc_layer_shape* sh) {
   if (sh->micro_batch <= 0 || sh->seq_len <= 0 || sh->hidden <= 0 || sh->heads <= 0 ||
       sh->ffn_hidden <= 0 || sh->tp_parts <= 0 || sh->head_dim < 0)
     return MC_ERR_SHAPE;
-  if ((sh->flags & ~(MC_ACCUMULATE_GRADS | MC_RECOMPUTE_ACTIVATIONS | MC_SEQUENCE_PARALLEL)) != 0)
+  if ((sh->flags & ~(MC_ACCUMULATE_GRADS | MC_RECOMPUTE_ACTIVATIONS | MC_SEQUENCE_PARALLEL |
+                     MC_FP8_HYBRID)) != 0)
     return MC_ERR_ARGUMENT;
+  if ((sh->flags & MC_FP8_HYBRID) && (sh->flags & MC_SEQUENCE_PARALLEL)) return MC_ERR_ARGUMENT;
   const int t = sh->tp_parts;
   // Sequence-parallel contract: the tokens split evenly into t shards.
   if ((sh->flags & MC_SEQUENCE_PARALLEL) &&
@@ -103,6 +107,9 @@ int check_shape(const mc_layer_shape* sh) {
   if (D.h > kMaxLayerNormHidden) return MC_ERR_UNSUPPORTED;
   if (D.T > (1 << 24) || D.f > (1 << 20) || 3 * D.a > (1 << 20) || D.H > 65535 || D.b > 65535)
     return MC_ERR_UNSUPPORTED;
+  // FP8 products contract over tokens in the weight gradients (K = T).
+  // (and the 8-bit casts tile the token dimension in at most 65535 x 64 rows)
+  if (D.fp8 && (D.T % 16 || D.T > 65535 * 64)) return MC_ERR_UNSUPPORTED;
   return MC_OK;
 }
 
@@ -123,6 +130,12 @@ struct Carver {
 struct Saved {
   uint16_t *ln1, *qkv, *o, *ln2, *hp, *g;
   float *mu1, *rs1, *lse, *x1, *mu2, *rs2;
+  // MC_FP8_HYBRID: what the backward reads of the forward's 8-bit operands --
+  // the transposed (K-major over tokens) activations for the weight
+  // gradients, the transposed weights for the input gradients -- and the
+  // inverse scales [ln1, o, ln2, g, w_qkv, w_o, w_fc1, w_fc2].
+  uint8_t *ln1_t, *o_t, *ln2_t, *g_t, *wqkv_t, *wo_t, *w1_t, *w2_t;
+  float* scale_inv;
 };
 
 Saved plan_saved(const Dims& D, void* p, size_t* bytes) {  // NOLINT
@@ -140,6 +153,19 @@ Saved plan_saved(const Dims& D, void* p, size_t* bytes) {  // NOLINT
   S.rs2 = c.take<float>(D.T);
   S.hp = c.take<uint16_t>(D.T * D.f);
   S.g = c.take<uint16_t>(D.T * D.f);
+  S.ln1_t = S.o_t = S.ln2_t = S.g_t = S.wqkv_t = S.wo_t = S.w1_t = S.w2_t = nullptr;
+  S.scale_inv = nullptr;
+  if (D.fp8) {
+    S.ln1_t = c.take<uint8_t>(D.h * D.T);
+    S.o_t = c.take<uint8_t>(D.a * D.T);
+    S.ln2_t = c.take<uint8_t>(D.h * D.T);
+    S.g_t = c.take<uint8_t>(D.f * D.T);
+    S.wqkv_t = c.take<uint8_t>(D.h * 3 * D.a);
+    S.wo_t = c.take<uint8_t>(D.a * D.h);
+    S.w1_t = c.take<uint8_t>(D.h * D.f);
+    S.w2_t = c.take<uint8_t>(D.f * D.h);
+    S.scale_inv = c.take<float>(8);
+  }
   if (bytes) *bytes = (c.off + 255) & ~static_cast<size_t>(255);
   return S;
 }
@@ -149,6 +175,12 @@ struct Work {
   uint16_t *dy16, *dhp, *dx1_16, *dO, *dqkv;
   float *dln, *dx1, *delta, *partials;
   void* recompute_saved;  // activations region when they are recomputed
+  // MC_FP8_HYBRID: the row-major 8-bit operands (forward: ln1, o, ln2, g and
+  // the weights; backward: dy, dhp, dx1, dqkv), the backward operands'
+  // transposed copies and their inverse scales [dy, dhp, dx1, dqkv].
+  uint8_t *ln1_q, *o_q, *ln2_q, *g_q, *wqkv_q, *wo_q, *w1_q, *w2_q;
+  uint8_t *dy_q, *dy_t, *dhp_q, *dhp_t, *dx1_q, *dx1_t, *dqkv_q, *dqkv_t;
+  float* scale_inv;
 };
 
 Saved plan_saved(const Dims& D, void* p, size_t* bytes);
@@ -171,7 +203,31 @@ Work plan_ws(const Dims& D, bool with_saved, void* p, size_t* bytes) {
   int64_t widest = D.f > 3 * D.a ? D.f : 3 * D.a;
   if (D.h > widest) widest = D.h;
   const size_t col_part = static_cast<size_t>(kColsumMaxSplits) * widest;
-  W.partials = c.take<float>(ln_part > col_part ? ln_part : col_part);
+  size_t part = ln_part > col_part ? ln_part : col_part;
+  if (part < fp8_scratch_floats()) part = fp8_scratch_floats();
+  W.partials = c.take<float>(part);
+  W.ln1_q = W.o_q = W.ln2_q = W.g_q = W.wqkv_q = W.wo_q = W.w1_q = W.w2_q = nullptr;
+  W.dy_q = W.dy_t = W.dhp_q = W.dhp_t = W.dx1_q = W.dx1_t = W.dqkv_q = W.dqkv_t = nullptr;
+  W.scale_inv = nullptr;
+  if (D.fp8) {
+    W.ln1_q = c.take<uint8_t>(D.T * D.h);
+    W.o_q = c.take<uint8_t>(D.T * D.a);
+    W.ln2_q = c.take<uint8_t>(D.T * D.h);
+    W.g_q = c.take<uint8_t>(D.T * D.f);
+    W.wqkv_q = c.take<uint8_t>(3 * D.a * D.h);
+    W.wo_q = c.take<uint8_t>(D.h * D.a);
+    W.w1_q = c.take<uint8_t>(D.f * D.h);
+    W.w2_q = c.take<uint8_t>(D.h * D.f);
+    W.dy_q = c.take<uint8_t>(D.T * D.h);
+    W.dy_t = c.take<uint8_t>(D.h * D.T);
+    W.dhp_q = c.take<uint8_t>(D.T * D.f);
+    W.dhp_t = c.take<uint8_t>(D.f * D.T);
+    W.dx1_q = c.take<uint8_t>(D.T * D.h);
+    W.dx1_t = c.take<uint8_t>(D.h * D.T);
+    W.dqkv_q = c.take<uint8_t>(D.T * 3 * D.a);
+    W.dqkv_t = c.take<uint8_t>(3 * D.a * D.T);
+    W.scale_inv = c.take<float>(4);
+  }
   W.recompute_saved = nullptr;
   if (with_saved) {
     size_t sb = 0;
@@ -256,8 +312,57 @@ Shards shards_of(const Dims& D, bool sp) { return sp ? Shards{D.t, D.T / D.t} : 
 // every partition's K slice in its accumulator: the reduce-scatter of the
 // partial sums.  QKV and fc1 read all shards' LayerNorm output, which lie
 // side by side in one buffer: the all-gather.
+constexpr int kE4M3 = 0, kE5M2 = 1;
+
+// F1..F7 with FP8 GEMMs (MC_FP8_HYBRID): every GEMM operand is quantised to
+// E4M3 first (per-tensor current scaling) -- into a row-major copy for this
+// product and, with the same scale, a transposed copy kept for the backward
+// pass -- and the GEMM's epilogue multiplies by the two inverse scales.
+int enqueue_forward_fp8(const Dims& D, const mc_layer_weights* w, const float* x, float* y,
+                        const Saved& S, const Work& W, cudaStream_t st) {
+  const int t = static_cast<int>(D.t);
+  const int h = static_cast<int>(D.h);
+  float* si = S.scale_inv;  // [ln1, o, ln2, g, w_qkv, w_o, w_fc1, w_fc2]
+  auto quant = [&](const void* in, bool bf16, int64_t rows, int64_t cols, uint8_t* out,
+                   uint8_t* out_t, float* sinv) {
+    return launch_fp8_quantize_2d(in, bf16, rows, cols, kE4M3, out, out_t, sinv, W.partials, st);
+  };
+  // the weights, [out, in] as stored and transposed for the input gradients
+  MC_TRY(quant(w->w_qkv, true, 3 * D.a, D.h, W.wqkv_q, S.wqkv_t, si + 4));
+  MC_TRY(quant(w->w_o, true, D.h, D.a, W.wo_q, S.wo_t, si + 5));
+  MC_TRY(quant(w->w_fc1, true, D.f, D.h, W.w1_q, S.w1_t, si + 6));
+  MC_TRY(quant(w->w_fc2, true, D.h, D.f, W.w2_q, S.w2_t, si + 7));
+  // F1  LN1, quantised
+  MC_TRY(launch_layernorm_forward(x, w->ln1_g, w->ln1_b, S.ln1, S.mu1, S.rs1, D.T, h, W.status, st));
+  MC_TRY(quant(S.ln1, true, D.T, D.h, W.ln1_q, S.ln1_t, si + 0));
+  // F2  QKV
+  MC_TRY(launch_gemm_fp8(D.T, 3 * D.a, D.h, W.ln1_q, D.h, kE4M3, W.wqkv_q, D.h, kE4M3, si + 0,
+                         si + 4, S.qkv, 3 * D.a, MC_EPI_BIAS_BF16, w->b_qkv, nullptr, 0, 0, 1,
+                         W.status, st));
+  // F3  causal attention (bf16), O quantised
+  MC_TRY(launch_attention_forward(S.qkv, S.o, S.lse, static_cast<int>(D.b), static_cast<int>(D.s),
+                                  static_cast<int>(D.H), static_cast<int>(D.d), W.status, st));
+  MC_TRY(quant(S.o, true, D.T, D.a, W.o_q, S.o_t, si + 1));
+  // F4  out-projection: partition partials summed in the accumulator, + b_o + x
+  MC_TRY(launch_gemm_fp8(D.T, D.h, D.a, W.o_q, D.a, kE4M3, W.wo_q, D.a, kE4M3, si + 1, si + 5,
+                         S.x1, D.h, MC_EPI_BIAS_RESID_F32, w->b_o, x, D.h, 0, t, W.status, st));
+  // F5  LN2, quantised
+  MC_TRY(launch_layernorm_forward(S.x1, w->ln2_g, w->ln2_b, S.ln2, S.mu2, S.rs2, D.T, h, W.status,
+                                  st));
+  MC_TRY(quant(S.ln2, true, D.T, D.h, W.ln2_q, S.ln2_t, si + 2));
+  // F6  fc1 + bias + GeLU; g quantised
+  MC_TRY(launch_gemm_fp8(D.T, D.f, D.h, W.ln2_q, D.h, kE4M3, W.w1_q, D.h, kE4M3, si + 2, si + 6,
+                         S.g, D.f, MC_EPI_BIAS_GELU, w->b_fc1, S.hp, D.f, 0, 1, W.status, st));
+  MC_TRY(quant(S.g, true, D.T, D.f, W.g_q, S.g_t, si + 3));
+  // F7  fc2: partials summed, + b_fc2 + x1
+  MC_TRY(launch_gemm_fp8(D.T, D.h, D.f, W.g_q, D.f, kE4M3, W.w2_q, D.f, kE4M3, si + 3, si + 7, y,
+                         D.h, MC_EPI_BIAS_RESID_F32, w->b_fc2, S.x1, D.h, 0, t, W.status, st));
+  return MC_OK;
+}
+
 int enqueue_forward(const Dims& D, const mc_layer_weights* w, const float* x, float* y,
                     const Saved& S, const Work& W, bool sp, cudaStream_t st) {
+  if (D.fp8) return enqueue_forward_fp8(D, w, x, y, S, W, st);
   const int t = static_cast<int>(D.t);
   const int h = static_cast<int>(D.h);
   const Shards sh = shards_of(D, sp);
@@ -298,6 +403,65 @@ int enqueue_forward(const Dims& D, const mc_layer_weights* w, const float* x, fl
   }
   return MC_OK;
 }
+// B1..B7 with FP8 GEMMs (MC_FP8_HYBRID): the gradient operands dy, dhp, dx1
+// and dQ|dK|dV are quantised to E5M2 (row-major and transposed, one scale);
+// weight gradients contract over tokens with the transposed copies of both
+// operands, input gradients read the forward's transposed E4M3 weights.
+int enqueue_backward_fp8(const Dims& D, const mc_layer_weights* w, const float* x,
+                         const float* dy, float* dx, const mc_layer_grads& G, const Saved& S,
+                         const Work& W, int acc, cudaStream_t st) {
+  const int t = static_cast<int>(D.t);
+  const int h = static_cast<int>(D.h);
+  const float* sf = S.scale_inv;  // [ln1, o, ln2, g, w_qkv, w_o, w_fc1, w_fc2]
+  float* sb = W.scale_inv;        // [dy, dhp, dx1, dqkv]
+  auto quant = [&](const void* in, bool bf16, int64_t rows, int64_t cols, uint8_t* out,
+                   uint8_t* out_t, float* sinv) {
+    return launch_fp8_quantize_2d(in, bf16, rows, cols, kE5M2, out, out_t, sinv, W.partials, st);
+  };
+  // B1  fc2: db2 = colsum(dy); dW2 = dy^T g; dhp = (dy W2) * gelu'(hp)
+  MC_TRY(launch_colsum(dy, false, D.T, D.h, G.b_fc2, acc, nullptr, W.partials, W.status, st));
+  MC_TRY(quant(dy, false, D.T, D.h, W.dy_q, W.dy_t, sb + 0));
+  MC_TRY(launch_gemm_fp8(D.h, D.f, D.T, W.dy_t, D.T, kE5M2, S.g_t, D.T, kE4M3, sb + 0, sf + 3,
+                         G.w_fc2, D.f, MC_EPI_STORE_F32, nullptr, nullptr, 0, acc, 1, W.status,
+                         st));
+  MC_TRY(launch_gemm_fp8(D.T, D.f, D.h, W.dy_q, D.h, kE5M2, S.w2_t, D.h, kE4M3, sb + 0, sf + 7,
+                         W.dhp, D.f, MC_EPI_GELU_BWD, nullptr, S.hp, D.f, 0, 1, W.status, st));
+  // B2  fc1: db1; dW1 = dhp^T ln2; dln2 = sum_p dhp_p W1_p
+  MC_TRY(launch_colsum(W.dhp, true, D.T, D.f, G.b_fc1, acc, nullptr, W.partials, W.status, st));
+  MC_TRY(quant(W.dhp, true, D.T, D.f, W.dhp_q, W.dhp_t, sb + 1));
+  MC_TRY(launch_gemm_fp8(D.f, D.h, D.T, W.dhp_t, D.T, kE5M2, S.ln2_t, D.T, kE4M3, sb + 1, sf + 2,
+                         G.w_fc1, D.h, MC_EPI_STORE_F32, nullptr, nullptr, 0, acc, 1, W.status,
+                         st));
+  MC_TRY(launch_gemm_fp8(D.T, D.h, D.f, W.dhp_q, D.f, kE5M2, S.w1_t, D.f, kE4M3, sb + 1, sf + 6,
+                         W.dln, D.h, MC_EPI_STORE_F32, nullptr, nullptr, 0, 0, t, W.status, st));
+  // B3  LN2 backward: dx1 = dy + LN2^T(dln2); dgamma2, dbeta2; db_o
+  MC_TRY(launch_layernorm_backward(W.dln, S.x1, S.mu2, S.rs2, w->ln2_g, dy, W.dx1, nullptr,
+                                   G.ln2_g, G.ln2_b, G.b_o, acc, W.partials, D.T, h, W.status, st));
+  MC_TRY(quant(W.dx1, false, D.T, D.h, W.dx1_q, W.dx1_t, sb + 2));
+  // B4  out-projection: dWo = dx1^T O; dO = dx1 Wo
+  MC_TRY(launch_gemm_fp8(D.h, D.a, D.T, W.dx1_t, D.T, kE5M2, S.o_t, D.T, kE4M3, sb + 2, sf + 1,
+                         G.w_o, D.a, MC_EPI_STORE_F32, nullptr, nullptr, 0, acc, 1, W.status, st));
+  MC_TRY(launch_gemm_fp8(D.T, D.a, D.h, W.dx1_q, D.h, kE5M2, S.wo_t, D.h, kE4M3, sb + 2, sf + 5,
+                         W.dO, D.a, MC_EPI_STORE_BF16, nullptr, nullptr, 0, 0, 1, W.status, st));
+  // B5  attention backward (bf16) -> dQ | dK | dV
+  MC_TRY(launch_attention_backward(S.qkv, S.o, S.lse, W.dO, W.dqkv, W.delta, static_cast<int>(D.b),
+                                   static_cast<int>(D.s), static_cast<int>(D.H),
+                                   static_cast<int>(D.d), W.status, st));
+  // B6  QKV: db_qkv; dWqkv = dqkv^T ln1; dln1 = sum_p dqkv_p Wqkv_p
+  MC_TRY(launch_colsum(W.dqkv, true, D.T, 3 * D.a, G.b_qkv, acc, nullptr, W.partials, W.status, st));
+  MC_TRY(quant(W.dqkv, true, D.T, 3 * D.a, W.dqkv_q, W.dqkv_t, sb + 3));
+  MC_TRY(launch_gemm_fp8(3 * D.a, D.h, D.T, W.dqkv_t, D.T, kE5M2, S.ln1_t, D.T, kE4M3, sb + 3,
+                         sf + 0, G.w_qkv, D.h, MC_EPI_STORE_F32, nullptr, nullptr, 0, acc, 1,
+                         W.status, st));
+  MC_TRY(launch_gemm_fp8(D.T, D.h, 3 * D.a, W.dqkv_q, 3 * D.a, kE5M2, S.wqkv_t, 3 * D.a, kE4M3,
+                         sb + 3, sf + 4, W.dln, D.h, MC_EPI_STORE_F32, nullptr, nullptr, 0, 0, t,
+                         W.status, st));
+  // B7  LN1 backward: dx = dx1 + LN1^T(dln1); dgamma1, dbeta1
+  MC_TRY(launch_layernorm_backward(W.dln, x, S.mu1, S.rs1, w->ln1_g, W.dx1, dx, nullptr, G.ln1_g,
+                                   G.ln1_b, nullptr, acc, W.partials, D.T, h, W.status, st));
+  return MC_OK;
+}
+
 }  // namespace
 }  // namespace mc
 
@@ -353,6 +517,7 @@ int mc_layer_backward(const mc_layer_shape* shape, const mc_layer_weights* w, co
   // added in shard order (the first shard honours MC_ACCUMULATE_GRADS, the
   // rest add).  Weight gradients and the column-parallel products read all
   // shards' rows, which lie side by side: the all-gather.
+  if (D.fp8) return enqueue_backward_fp8(D, w, x, dy, dx, G, S, W, acc, st);
   const Shards sh = shards_of(D, seq_parallel(*shape));
   auto shard_acc = [&](int64_t p) { return p == 0 ? acc : 1; };
 

@@ -155,6 +155,12 @@ int launch_gemm_fp8(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_t l
 size_t fp8_scratch_floats();
 int launch_fp8_quantize(const void* in, bool in_bf16, int64_t n, int format, uint8_t* out,
                         float* scale_inv, float* scratch, cudaStream_t stream);
+// The same over a row-major [rows, cols] matrix (both multiples of 16),
+// writing it as is (`out`) and/or transposed (`out_t`, [cols, rows]); either
+// output may be NULL.
+int launch_fp8_quantize_2d(const void* in, bool in_bf16, int64_t rows, int64_t cols, int format,
+                           uint8_t* out, uint8_t* out_t, float* scale_inv, float* scratch,
+                           cudaStream_t stream);
 
 int launch_attention_forward(const uint16_t* qkv, uint16_t* o, float* lse, int b, int s, int H,
                              int d, int* status, cudaStream_t stream);

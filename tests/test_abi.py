@@ -64,7 +64,7 @@ def test_saved_bytes_cover_the_activations():
 
 
 def test_unknown_flag_rejected():
-    assert L.mc_layer_check_shape(L.make_shape(1, 8, 768, 12, 3072, 1, 0, 8)) == L.MC_ERR_ARGUMENT
+    assert L.mc_layer_check_shape(L.make_shape(1, 8, 768, 12, 3072, 1, 0, 16)) == L.MC_ERR_ARGUMENT
 
 
 def test_strerror_covers_all_codes():
@@ -165,3 +165,31 @@ def test_sequence_parallel_contract():
     both = L.make_shape(2, 6, 768, 12, 3072, 4, 0,
                         L.MC_SEQUENCE_PARALLEL | L.MC_RECOMPUTE_ACTIVATIONS)
     assert L.mc_layer_check_shape(both) == L.MC_OK
+
+
+def test_fp8_hybrid_contract():
+    """MC_FP8_HYBRID: tokens a multiple of 16, not combined with the
+    sequence-parallel flag; the saved activations grow by exactly the 8-bit
+    copies the backward reads (transposed activations and weights, 8 scales)."""
+    base = (1, 128, 768, 12, 3072, 2, 0)
+    ok = L.make_shape(*base, L.MC_FP8_HYBRID)
+    assert L.mc_layer_check_shape(ok) == L.MC_OK
+    assert L.mc_layer_check_shape(L.make_shape(1, 100, 768, 12, 3072, 2, 0, L.MC_FP8_HYBRID)) \
+        == L.MC_ERR_UNSUPPORTED
+    assert L.mc_layer_check_shape(
+        L.make_shape(*base, L.MC_FP8_HYBRID | L.MC_SEQUENCE_PARALLEL)) == L.MC_ERR_ARGUMENT
+    T, h, a, f = 128, 768, 768, 3072
+    extra = sum(-(-n // 256) * 256 for n in (h * T, a * T, h * T, f * T, h * 3 * a, a * h,
+                                              h * f, f * h, 8 * 4))
+    assert L.mc_layer_saved_bytes(ok) == L.mc_layer_saved_bytes(L.make_shape(*base, 0)) + extra
+    assert L.mc_layer_workspace_bytes(ok) > L.mc_layer_workspace_bytes(L.make_shape(*base, 0))
+
+
+def test_fp8_quantize_2d_rejects_on_the_host():
+    # rows / cols not multiples of 16, or no output: rejected before any launch
+    assert L.lib().mc_fp8_quantize_2d(0x10000, 1, 10, 64, 0, 0x10000, None, 0x10000, 0x10000,
+                                      None) == L.MC_ERR_SHAPE
+    assert L.lib().mc_fp8_quantize_2d(0x10000, 1, 16, 64, 0, None, None, 0x10000, 0x10000,
+                                      None) == L.MC_ERR_NULLPTR
+    assert L.lib().mc_fp8_quantize_2d(0x10000, 1, 16, 64, 2, 0x10000, None, 0x10000, 0x10000,
+                                      None) == L.MC_ERR_ARGUMENT

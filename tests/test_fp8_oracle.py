@@ -87,3 +87,114 @@ def test_gemm_is_the_product_of_the_decoded_operands():
         for j in range(3):
             ref = sum(A[i, k] * B[j, k] for k in range(7)) * float(sa) * float(sb)
             assert abs(c[i, j] - ref) <= 1e-12 * max(1.0, abs(ref))
+
+
+# --------------------------------------------------------------------------
+# The layer with FP8 hybrid GEMMs (oracle/fp8_layer.py)
+# --------------------------------------------------------------------------
+
+def _tiny(shape, seed=1):
+    from layer_inputs import make_layer_inputs
+    from layer_inputs.generator import NONTRIVIAL_INIT
+    init = dict(NONTRIVIAL_INIT)
+    for w in ("w_qkv", "w_o", "w_fc1", "w_fc2"):
+        init[w] = (0.0, 0.3)
+    inp = make_layer_inputs(shape, seed=seed, init=init)
+    return inp.params_f64(), inp.f64("x"), inp.f64("dy")
+
+
+@pytest.mark.parametrize("dims", [(1, 5, 16, 2, 32), (2, 33, 32, 4, 64), (2, 9, 16, 1, 48, 1, 8)])
+def test_fp8_layer_without_quantisation_is_the_rounding_floor(dims):
+    """With the 8-bit rounding turned off the FP8 layer is the pinned bf16
+    rounding-floor layer (its sites, except dx1, which this mode quantises
+    from fp32)."""
+    from layer_inputs import LayerShape
+    from oracle import fp8_layer as FL
+    from oracle import rounding_floor as RF
+    shape = LayerShape(*dims)
+    P, x, dy = _tiny(shape)
+    got = FL.fp8_forward_backward(shape, P, x, dy, quantize=False)
+    ref = RF.rounded_forward_backward(shape, P, x, dy,
+                                      sites=tuple(s for s in RF.GPU_ROUNDING_SITES if s != "dx1"))
+    for a, b in [(got[0], ref[0]), (got[1], ref[1])] + [(got[2][k], ref[2][k]) for k in ref[2]]:
+        assert np.abs(a - b).max() <= 1e-12 * max(1.0, np.abs(b).max())
+
+
+@pytest.mark.parametrize("fa,fb", [("e4m3", "e4m3"), ("e5m2", "e4m3")])
+def test_fp8_layer_products_are_the_gemm_of_the_encoded_operands(fa, fb):
+    from oracle import fp8_layer as FL
+    rng = np.random.default_rng(4)
+    A = rng.standard_normal((6, 32)) * 3
+    B = rng.standard_normal((5, 32)) * 0.02
+    qa, sa = F.quantize(A, fa)
+    qb, sb = F.quantize(B, fb)
+    ref = F.gemm_fp8(qa, fa, sa, qb, fb, sb)
+    got = FL.qdq(A, fa) @ FL.qdq(B, fb).T
+    assert np.abs(got - ref).max() <= 1e-12 * np.abs(ref).max()
+
+
+def _formats_used(monkeypatch, fl_module, shape, P, x, dy):
+    calls = []
+    real = F.quantize
+
+    def recording(t, fmt):
+        calls.append((np.shape(t), fmt))
+        return real(t, fmt)
+
+    monkeypatch.setattr(F, "quantize", recording)
+    fl_module.fp8_forward_backward(shape, P, x, dy)
+    return calls
+
+
+def _expected_formats(shape):
+    T, h, a, f = shape.micro_batch * shape.seq_len, shape.hidden, shape.a, shape.ffn_hidden
+    b, s = shape.micro_batch, shape.seq_len
+    fwd = [((3 * a, h), "e4m3"), ((h, a), "e4m3"), ((f, h), "e4m3"), ((h, f), "e4m3"),
+           ((b, s, h), "e4m3"), ((b, s, a), "e4m3"), ((b, s, h), "e4m3"), ((b, s, f), "e4m3")]
+    bwd = [((b, s, h), "e5m2"), ((b, s, f), "e5m2"), ((b, s, h), "e5m2"), ((b, s, 3 * a), "e5m2")]
+    assert T == b * s
+    return fwd + bwd
+
+
+def test_fp8_layer_forward_operands_are_e4m3_and_gradients_e5m2(monkeypatch):
+    """The hybrid recipe: the weights and forward activations in E4M3, the
+    gradients dy, dhp, dx1 and dQ|dK|dV in E5M2, each quantised once."""
+    from layer_inputs import LayerShape
+    from oracle import fp8_layer as FL
+    shape = LayerShape(2, 5, 32, 2, 64, 1, 8)   # a != h so that the shapes tell the operands apart
+    P, x, dy = _tiny(shape)
+    assert _formats_used(monkeypatch, FL, shape, P, x, dy) == _expected_formats(shape)
+
+
+def test_planted_e4m3_gradient_is_caught(monkeypatch):
+    from layer_inputs import LayerShape
+    from oracle import fp8_layer as FL
+    shape = LayerShape(2, 5, 32, 2, 64, 1, 8)
+    P, x, dy = _tiny(shape)
+    monkeypatch.setattr(FL, "E5M2", "e4m3")   # gradients in the forward format
+    assert _formats_used(monkeypatch, FL, shape, P, x, dy) != _expected_formats(shape)
+
+
+def test_fp8_layer_error_is_an_8_bit_rounding_floor():
+    """On config c1 the FP8 layer departs from the exact oracle by about an
+    8-bit rounding (E4M3 3 mantissa bits, E5M2 2), far above the bf16 floor
+    and far below the tensors' scale."""
+    from layer_inputs import LayerShape, make_layer_inputs
+    import oracle.layer as OL
+    from oracle import fp8_layer as FL
+    from oracle import rounding_floor as RF
+    from parity import metrics
+    shape = LayerShape(1, 128, 768, 12, 3072, 1)
+    inp = make_layer_inputs(shape)
+    P, x, dy = inp.params_f64(), inp.f64("x"), inp.f64("dy")
+    exact = OL.layer_forward_backward(shape, P, x, dy)
+    f8 = FL.fp8_forward_backward(shape, P, x, dy)
+    bf = RF.rounded_forward_backward(shape, P, x, dy)
+    names = ["y", "dx"] + list(exact[2])
+    pick = lambda r, k: r[0] if k == "y" else r[1] if k == "dx" else r[2][k]  # noqa: E731
+    for k in names:
+        if k == "b_fc2":
+            continue  # the column sum of dy: no 8-bit operand
+        e8 = metrics(pick(f8, k), pick(exact, k))["norm_rel"]
+        e16 = metrics(pick(bf, k), pick(exact, k))["norm_rel"]
+        assert 2 * e16 < e8 < 0.25, (k, e8, e16)
