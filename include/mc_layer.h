@@ -80,7 +80,8 @@ extern "C" {
 #define MC_ERR_WORKSPACE (-5)      /* ws_bytes smaller than mc_layer_workspace_bytes */
 #define MC_ERR_CUDA (-6)           /* a CUDA runtime call or launch failed         */
 #define MC_ERR_DEVICE_TIMEOUT (-7) /* device: a bounded wait gave up               */
-#define MC_ERR_DEVICE_BOUNDS (-8)  /* device: an index check failed                */
+#define MC_ERR_DEVICE_BOUNDS (-8)  /* device: an index check of a debug build
+                                      (-DMC_DEBUG) failed; the store is skipped */
 #define MC_ERR_ARGUMENT (-9)       /* another invalid argument (e.g. an enum)      */
 #define MC_ERR_SCRATCH_LIMIT (-10) /* problem larger than the fixed scratch of an
                                       allocation-free entry point                 */
@@ -295,6 +296,16 @@ int mc_attention_backward_noalloc(const uint16_t* qkv, const uint16_t* o, const 
  * status[1] (status: int[64] device memory, zeroed by the caller) and
  * returns; the context stays usable.  No fault, trap or hang is involved. */
 int mc_selftest_wait_timeout(int64_t timeout_ns, int* status, void* stream);
+
+/* Index-check self-test: one thread checks 0 <= index < extent with the
+ * check a debug build of this library (compiled with -DMC_DEBUG) runs before
+ * every global store of its kernels, and writes buf[index] = 1 only if the
+ * check passes; otherwise it records MC_ERR_DEVICE_BOUNDS in status[0] and
+ * the site code 30 in status[1], and touches nothing.  buf: int device
+ * memory of `extent` elements (NULL -> MC_ERR_NULLPTR; extent < 1 ->
+ * MC_ERR_ARGUMENT).  No fault is involved: an out-of-range index is never
+ * dereferenced. */
+int mc_selftest_bounds_check(int64_t index, int64_t extent, int* buf, int* status, void* stream);
 
 /* ---- 8-bit floating-point GEMMs (the Megatron-Core listing, 混合精度:
  * FP8 / FP4 training on Blackwell Ultra, --fp8-format hybrid = E4M3 forward,

@@ -11,7 +11,10 @@ import ctypes
 import os
 
 PKG_DIR = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(PKG_DIR, "libmclayer.so")
+# MC_LAYER_DEBUG=1 selects the debug build (-DMC_DEBUG: every global store's
+# indices are checked on the device; see build.py).
+LIB_PATH = os.path.join(PKG_DIR, "libmclayer_debug.so" if os.environ.get("MC_LAYER_DEBUG") == "1"
+                        else "libmclayer.so")
 
 MC_OK = 0
 MC_ERR_SHAPE = -1
@@ -91,6 +94,7 @@ _SIGNATURES = {
     "mc_attention_backward": (_INT, [_P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _P, _P]),
     "mc_attention_backward_noalloc": (_INT, [_P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _P, _P]),
     "mc_selftest_wait_timeout": (_INT, [_I64, _P, _P]),
+    "mc_selftest_bounds_check": (_INT, [_I64, _I64, _P, _P, _P]),
     "mc_fp8_scratch_floats": (_SZ, []),
     "mc_fp8_quantize": (_INT, [_P, _I32, _I64, _I32, _P, _P, _P, _P, _P]),
     "mc_fp8_quantize_2d": (_INT, [_P, _I32, _I64, _I64, _I32, _P, _P, _P, _P, _P]),
@@ -105,12 +109,14 @@ _SIGNATURES = {
 
 
 def lib() -> ctypes.CDLL:
-    """Loads libmclayer.so (built in-tree); raises if it is missing."""
+    """Loads libmclayer.so (or the debug build, see LIB_PATH), built in-tree;
+    raises if it is missing."""
     global _lib
     if _lib is None:
         if not os.path.exists(LIB_PATH):
             raise RuntimeError(f"{LIB_PATH} not found: build it with "
-                               "`python -m megatron_transformer_layer_gb300.build`")
+                               "`python -m megatron_transformer_layer_gb300.build` "
+                               "(`--debug` for the debug build)")
         handle = ctypes.CDLL(LIB_PATH)
         for name, (res, args) in _SIGNATURES.items():
             fn = getattr(handle, name)
@@ -292,6 +298,11 @@ def mc_gemm_fp8(M, N, K, A, lda, a_format, B, ldb, b_format, a_scale_inv, b_scal
                              _ptr(a_scale_inv), _ptr(b_scale_inv), _ptr(out), ldc, epilogue,
                              _ptr(bias), _ptr(aux), ldaux, accumulate, k_parts, _ptr(status),
                              _stream(stream))
+
+
+def mc_selftest_bounds_check(index, extent, buf, status, stream=None) -> int:
+    """Runs the index check of a debug build on one index (failure-path test)."""
+    return lib().mc_selftest_bounds_check(index, extent, _ptr(buf), _ptr(status), _stream(stream))
 
 
 def mc_selftest_wait_timeout(timeout_ns, status, stream=None) -> int:

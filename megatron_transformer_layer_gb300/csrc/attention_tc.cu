@@ -307,7 +307,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < D / 32; ++c) {
         float v[32];
         tmem_ld_32x32b_x32(tO + lane_off + c * 32, v);
-        if (q < s) {
+        if (q < s && MC_DCHECK(qr >= 0 && qr < part.len && hh * D + c * 32 + 32 <= a, status,
+                               kSiteAttention)) {
           float4* dst = reinterpret_cast<float4*>(orow + c * 32);
 #pragma unroll
           for (int i = 0; i < 8; ++i)
@@ -324,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < D / 32; ++c) {
         float v[32];
         tmem_ld_32x32b_x32(tO + lane_off + c * 32, v);
-        if (q < s) {
+        if (q < s && MC_DCHECK(q >= 0 && hh * D + c * 32 + 32 <= a, status, kSiteAttention)) {
           uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
@@ -630,7 +631,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int c = half * (D / 64); c < (half + 1) * (D / 64); ++c) {
           float v[32];
           tmem_ld_32x32b_x32(tacc + lane_off + c * 32, v);
-          if (PART && r < s) {
+          const bool in_range = MC_DCHECK(
+              r >= 0 && col + c * 32 + 32 <= 3 * a && (!PART || r - part.base < part.len), status,
+              kSiteAttention);
+          if (PART && r < s && in_range) {
             // fp32 partials of this rectangle: dK at [0, a), dV at [a, 2a)
             float4* dst = reinterpret_cast<float4*>(
                 part.out + (static_cast<int64_t>(bi) * part.len + (r - part.base)) * 2 * a +
@@ -639,7 +643,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             for (int k = 0; k < 8; ++k)
               dst[k] = make_float4(v[4 * k] * mul, v[4 * k + 1] * mul, v[4 * k + 2] * mul,
                                    v[4 * k + 3] * mul);
-          } else if (!PART && r < s) {
+          } else if (!PART && r < s && in_range) {
             uint4* dst = reinterpret_cast<uint4*>(dqkv + base + col + c * 32);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
@@ -888,7 +892,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int c = half * (D / 64); c < (half + 1) * (D / 64); ++c) {
         float v[32];
         tmem_ld_32x32b_x32(tdQ + lane_off + c * 32, v);
-        if (PART && r < s) {
+        const bool in_range =
+            MC_DCHECK(r >= 0 && hh * D + c * 32 + 32 <= a && (!PART || r - part.base < part.len),
+                      status, kSiteAttention);
+        if (PART && r < s && in_range) {
           // fp32 partial dQ of this rectangle
           float4* dst = reinterpret_cast<float4*>(
               part.out + (static_cast<int64_t>(bi) * part.len + (r - part.base)) * a + hh * D +
@@ -897,7 +904,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           for (int k = 0; k < 8; ++k)
             dst[k] = make_float4(v[4 * k] * scale, v[4 * k + 1] * scale, v[4 * k + 2] * scale,
                                  v[4 * k + 3] * scale);
-        } else if (!PART && r < s) {
+        } else if (!PART && r < s && in_range) {
           uint4* dst = reinterpret_cast<uint4*>(dqkv + base + hh * D + c * 32);
 #pragma unroll
           for (int k = 0; k < 4; ++k) {

@@ -450,7 +450,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] *= dq;
         }
-        if (row < g.M && col0 < g.N) epilogue32<EPI>(v, row, col0, g);
+        if (row < g.M && col0 < g.N &&
+            MC_DCHECK(col0 + 32 <= g.N && g.N <= g.ldc && row >= 0, g.status, kSiteGemmEpilogue))
+          epilogue32<EPI>(v, row, col0, g);
       }
       tc_fence_before();
       if constexpr (kDuoMode) {

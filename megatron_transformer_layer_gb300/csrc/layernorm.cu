@@ -67,7 +67,8 @@ __global__ void __launch_bounds__(kLnThreads) ln_fwd_kernel(const float* __restr
                                                             const uint16_t* __restrict__ beta,
                                                             uint16_t* __restrict__ out,
                                                             float* __restrict__ mean_out,
-                                                            float* __restrict__ rstd_out, int h) {
+                                                            float* __restrict__ rstd_out, int h,
+                                                            int64_t rows, int* status) {
   pdl_wait();  // the previous kernel on the stream has completed
   pdl_launch();
   __shared__ float red[2 * kLnThreads / 32];
@@ -105,7 +106,8 @@ __global__ void __launch_bounds__(kLnThreads) ln_fwd_kernel(const float* __restr
       o.y = (v[i].y - mean) * rstd * g.y + b.y;
       o.z = (v[i].z - mean) * rstd * g.z + b.z;
       o.w = (v[i].w - mean) * rstd * g.w + b.w;
-      store_bf16x4(out + row * h + 4 * c, o);
+      if (MC_DCHECK(row < rows && 4 * c + 4 <= h, status, kSiteLayerNorm))
+        store_bf16x4(out + row * h + 4 * c, o);
     }
   }
   if (threadIdx.x == 0) {
@@ -125,7 +127,7 @@ __global__ void __launch_bounds__(kLnBwdThreads) ln_bwd_kernel(
     const float* __restrict__ dout, const float* __restrict__ x, const float* __restrict__ mean,
     const float* __restrict__ rstd, const uint16_t* __restrict__ gamma,
     const float* resid, float* dx, uint16_t* __restrict__ dx_bf16,
-    float* __restrict__ partials, int64_t rows, int h, int want_colsum_dx) {
+    float* __restrict__ partials, int64_t rows, int h, int want_colsum_dx, int* status) {
   pdl_wait();  // the previous kernel on the stream has completed
   pdl_launch();
   extern __shared__ float colacc[];  // [3][h]
@@ -179,8 +181,10 @@ __global__ void __launch_bounds__(kLnBwdThreads) ln_bwd_kernel(
         o.y = rs * (gg.y - m1 - xh[i].y * m2) + rv[i].y;
         o.z = rs * (gg.z - m1 - xh[i].z * m2) + rv[i].z;
         o.w = rs * (gg.w - m1 - xh[i].w * m2) + rv[i].w;
-        reinterpret_cast<float4*>(dx + row * h)[c] = o;
-        if (dx_bf16) store_bf16x4(dx_bf16 + row * h + 4 * c, o);
+        if (MC_DCHECK(row < rows && 4 * c + 4 <= h, status, kSiteLayerNorm)) {
+          reinterpret_cast<float4*>(dx + row * h)[c] = o;
+          if (dx_bf16) store_bf16x4(dx_bf16 + row * h + 4 * c, o);
+        }
         float4* cg = reinterpret_cast<float4*>(colacc) + c;
         float4* cb = reinterpret_cast<float4*>(colacc + h) + c;
         float4 a = *cg, b = *cb;
@@ -302,9 +306,9 @@ __global__ void colsum_partial_kernel(const void* __restrict__ in, int64_t rows,
 
 template <int VPT>
 int ln_fwd_launch(const float* x, const uint16_t* g, const uint16_t* b, uint16_t* out,
-                  float* mean, float* rstd, int64_t rows, int h, cudaStream_t st) {
+                  float* mean, float* rstd, int64_t rows, int h, int* status, cudaStream_t st) {
   launch_kernel(ln_fwd_kernel<VPT>, dim3(static_cast<unsigned>(rows)), dim3(kLnThreads), 0, st, 1,
-                x, g, b, out, mean, rstd, h);
+                x, g, b, out, mean, rstd, h, rows, status);
   return cudaGetLastError() == cudaSuccess ? MC_OK : MC_ERR_CUDA;
 }
 
@@ -316,7 +320,7 @@ template <int VPT>
 int ln_bwd_launch(const float* dout, const float* x, const float* mean, const float* rstd,
                   const uint16_t* gamma, const float* resid, float* dx, uint16_t* dx_bf16,
                   float* partials, int64_t rows, int h, int want_colsum_dx, int* grid_out,
-                  cudaStream_t st) {
+                  int* status, cudaStream_t st) {
   const size_t smem = 3 * static_cast<size_t>(h) * sizeof(float);
   auto kern = ln_bwd_kernel<VPT>;
   // Opt in once per device to the largest column-partial buffer (h = kMaxLayerNormHidden);
@@ -338,7 +342,7 @@ int ln_bwd_launch(const float* dout, const float* x, const float* mean, const fl
   if (resident > 0 && grid > resident) grid = resident;
   *grid_out = static_cast<int>(grid);
   launch_kernel(kern, dim3(static_cast<unsigned>(grid)), dim3(kLnBwdThreads), smem, st, 1, dout, x,
-                mean, rstd, gamma, resid, dx, dx_bf16, partials, rows, h, want_colsum_dx);
+                mean, rstd, gamma, resid, dx, dx_bf16, partials, rows, h, want_colsum_dx, status);
   return cudaGetLastError() == cudaSuccess ? MC_OK : MC_ERR_CUDA;
 }
 
@@ -356,7 +360,6 @@ bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 int launch_layernorm_forward(const float* x, const uint16_t* gamma, const uint16_t* beta,
                              uint16_t* out, float* mean, float* rstd, int64_t rows, int h,
                              int* status, cudaStream_t st) {
-  (void)status;
   if (rows < 1 || h < 8 || h % 8 || h > kMaxLayerNormHidden) return MC_ERR_UNSUPPORTED;
   if (rows > 0x7fffffff) return MC_ERR_UNSUPPORTED;
   if (!x || !gamma || !beta || !out) return MC_ERR_NULLPTR;
@@ -364,12 +367,12 @@ int launch_layernorm_forward(const float* x, const uint16_t* gamma, const uint16
       (reinterpret_cast<uintptr_t>(beta) & 7u))
     return MC_ERR_ALIGN;
   switch (vpt_for(h)) {
-    case 1: return ln_fwd_launch<1>(x, gamma, beta, out, mean, rstd, rows, h, st);
-    case 2: return ln_fwd_launch<2>(x, gamma, beta, out, mean, rstd, rows, h, st);
-    case 4: return ln_fwd_launch<4>(x, gamma, beta, out, mean, rstd, rows, h, st);
-    case 8: return ln_fwd_launch<8>(x, gamma, beta, out, mean, rstd, rows, h, st);
-    case 16: return ln_fwd_launch<16>(x, gamma, beta, out, mean, rstd, rows, h, st);
-    case 32: return ln_fwd_launch<32>(x, gamma, beta, out, mean, rstd, rows, h, st);
+    case 1: return ln_fwd_launch<1>(x, gamma, beta, out, mean, rstd, rows, h, status, st);
+    case 2: return ln_fwd_launch<2>(x, gamma, beta, out, mean, rstd, rows, h, status, st);
+    case 4: return ln_fwd_launch<4>(x, gamma, beta, out, mean, rstd, rows, h, status, st);
+    case 8: return ln_fwd_launch<8>(x, gamma, beta, out, mean, rstd, rows, h, status, st);
+    case 16: return ln_fwd_launch<16>(x, gamma, beta, out, mean, rstd, rows, h, status, st);
+    case 32: return ln_fwd_launch<32>(x, gamma, beta, out, mean, rstd, rows, h, status, st);
     default: return MC_ERR_UNSUPPORTED;
   }
 }
@@ -384,7 +387,6 @@ int launch_layernorm_backward(const float* dout, const float* x, const float* me
                               float* dx, uint16_t* dx_bf16, float* dgamma, float* dbeta,
                               float* colsum_dx, int accumulate, float* partials, int64_t rows,
                               int h, int* status, cudaStream_t st) {
-  (void)status;
   if (rows < 1 || h < 8 || h % 8 || h > kMaxLayerNormHidden) return MC_ERR_UNSUPPORTED;
   if (!dout || !x || !mean || !rstd || !gamma || !dx || !partials || !dgamma || !dbeta)
     return MC_ERR_NULLPTR;
@@ -396,11 +398,11 @@ int launch_layernorm_backward(const float* dout, const float* x, const float* me
   const int want = colsum_dx != nullptr;
   int rc;
   switch (vpt_for(h, kLnBwdThreads)) {
-    case 1: rc = ln_bwd_launch<1>(dout, x, mean, rstd, gamma, resid, dx, dx_bf16, partials, rows, h, want, &grid, st); break;
-    case 2: rc = ln_bwd_launch<2>(dout, x, mean, rstd, gamma, resid, dx, dx_bf16, partials, rows, h, want, &grid, st); break;
-    case 4: rc = ln_bwd_launch<4>(dout, x, mean, rstd, gamma, resid, dx, dx_bf16, partials, rows, h, want, &grid, st); break;
-    case 8: rc = ln_bwd_launch<8>(dout, x, mean, rstd, gamma, resid, dx, dx_bf16, partials, rows, h, want, &grid, st); break;
-    case 16: rc = ln_bwd_launch<16>(dout, x, mean, rstd, gamma, resid, dx, dx_bf16, partials, rows, h, want, &grid, st); break;
+    case 1: rc = ln_bwd_launch<1>(dout, x, mean, rstd, gamma, resid, dx, dx_bf16, partials, rows, h, want, &grid, status, st); break;
+    case 2: rc = ln_bwd_launch<2>(dout, x, mean, rstd, gamma, resid, dx, dx_bf16, partials, rows, h, want, &grid, status, st); break;
+    case 4: rc = ln_bwd_launch<4>(dout, x, mean, rstd, gamma, resid, dx, dx_bf16, partials, rows, h, want, &grid, status, st); break;
+    case 8: rc = ln_bwd_launch<8>(dout, x, mean, rstd, gamma, resid, dx, dx_bf16, partials, rows, h, want, &grid, status, st); break;
+    case 16: rc = ln_bwd_launch<16>(dout, x, mean, rstd, gamma, resid, dx, dx_bf16, partials, rows, h, want, &grid, status, st); break;
     default: return MC_ERR_UNSUPPORTED;
   }
   if (rc != MC_OK) return rc;

@@ -52,6 +52,23 @@ __device__ __forceinline__ int peek_status(const int* status) {
   return status ? *reinterpret_cast<const volatile int*>(status) : 0;
 }
 
+// ---------------------------------------------------------------- index checks
+// A debug build (-DMC_DEBUG) checks, before every global store of its
+// kernels, that the indices lie inside the extents the kernel was given; a
+// failed check records MC_ERR_DEVICE_BOUNDS and where in the status word and
+// the store is skipped.  Other builds compile the checks out (MC_DCHECK is
+// then `true`); check_index itself is always available (the bounds
+// self-test calls it directly).
+__device__ __forceinline__ bool check_index(bool in_range, int* status, int where) {
+  if (!in_range) record_error(status, MC_ERR_DEVICE_BOUNDS, where);
+  return in_range;
+}
+#ifdef MC_DEBUG
+#define MC_DCHECK(cond, status, where) ::mc::check_index((cond), (status), (where))
+#else
+#define MC_DCHECK(cond, status, where) true
+#endif
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));

@@ -193,3 +193,13 @@ def test_fp8_quantize_2d_rejects_on_the_host():
                                       None) == L.MC_ERR_NULLPTR
     assert L.lib().mc_fp8_quantize_2d(0x10000, 1, 16, 64, 2, 0x10000, None, 0x10000, 0x10000,
                                       None) == L.MC_ERR_ARGUMENT
+
+
+def test_debug_library_exports_the_same_symbols():
+    """libmclayer_debug.so (-DMC_DEBUG) is the same ABI."""
+    from megatron_transformer_layer_gb300 import build
+    if not os.path.exists(build.DEBUG_LIB_PATH):
+        pytest.skip("debug library not built")
+    dbg = ctypes.CDLL(build.DEBUG_LIB_PATH)
+    for n in declared_functions():
+        assert hasattr(dbg, n), n
