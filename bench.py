@@ -55,12 +55,15 @@ WORKLOAD_NAMES = {
 LAUNCHES_PER_STEP = 7 + 21
 
 
-def launches_per_step(t_shards: int, recompute: bool) -> int:
+def launches_per_step(t_shards: int, recompute: bool, fp8: bool = False) -> int:
     """Kernel launches of one layer step; in sequence-parallel mode the
     per-token kernels and the reduce-scattered GEMMs run once per shard
-    (forward 4t + 3, backward 8t + 13; t = 1 gives the 7 + 21 above)."""
-    fwd = 4 * t_shards + 3
-    return fwd + 8 * t_shards + 13 + (fwd if recompute else 0)
+    (forward 4t + 3, backward 8t + 13; t = 1 gives the 7 + 21 above).  The
+    FP8 mode adds 3 launches per quantised tensor (amax, scale, cast): 8 in
+    the forward (the 4 weights, ln1, O, ln2, g), 4 in the backward (dy, dhp,
+    dx1, dQ|dK|dV)."""
+    fwd = 4 * t_shards + 3 + (24 if fp8 else 0)
+    return fwd + 8 * t_shards + 13 + (12 if fp8 else 0) + (fwd if recompute else 0)
 
 
 def dims(w):
@@ -729,8 +732,8 @@ def run_ours(args, world, rank, local):
                 "pipeline": "step i+1's inputs uploaded and step i's results read back on two "
                             "copy streams while step i computes (double-buffered)",
                 "serial_value": e2e_serial_value},
-        "gpu_launches": launches_per_step(w["tp_parts"] if args.sp else 1, args.recompute)
-        * n_layers * args.steps,
+        "gpu_launches": launches_per_step(w["tp_parts"] if args.sp else 1, args.recompute,
+                                          args.fp8) * n_layers * args.steps,
         "memory": {"saved_bytes_per_layer": layer.saved_bytes,
                    "workspace_bytes_per_layer": layer.ws_bytes,
                    "workspace_shared_by_stack": bool(args.recompute)},
