@@ -110,7 +110,7 @@ int launch_attention_forward(const uint16_t* qkv, uint16_t* o, float* lse, int b
   if (H > 65535 || b > 65535) return MC_ERR_UNSUPPORTED;
   if (!qkv || !o || !lse) return MC_ERR_NULLPTR;
   if (!al16(qkv) || !al16(o)) return MC_ERR_ALIGN;
-  return launch_attention_forward_tc(qkv, o, lse, b, s, H, d, status, st);
+  return launch_attention_forward_wide(qkv, o, lse, b, s, H, d, status, st);
 }
 
 int launch_attention_backward(const uint16_t* qkv, const uint16_t* o, const float* lse,

@@ -1,6 +1,10 @@
-// Causal flash attention forward on the sm_103a tensor cores (tcgen05).
+// Causal flash attention on the sm_103a tensor cores (tcgen05): the forward
+// over rectangles of the score matrix that the context-parallel path
+// combines, and the backward kernels (whole matrix or rectangles).  The
+// whole-sequence forward, with 256-key blocks, is attention_fwd_wide.cu.
 //
-// One CTA per (128-query tile, head, batch), heaviest tiles first:
+// Rectangle forward: one CTA per (128-query tile, head, batch), heaviest
+// tiles first:
 //   warp 0      TMA: the Q tile once, then K/V tiles of 128 keys into a
 //               2-deep ring (3-D tensor map over Q|K|V [b, s, 3a]: rows past
 //               the sequence read zeros)
@@ -11,7 +15,8 @@
 //   warps 2..5  one thread per query row: load the S row from TMEM, mask,
 //               online softmax (running max and sum, exp2 with log2(e)/sqrt(d)
 //               folded in), write P back into the S buffer as bf16 pairs;
-//               at the end normalise O and store O and the log-sum-exp.
+//               at the end normalise O and store the fp32 partial O and its
+//               log-sum-exp.
 // O is rescaled in TMEM only when a row's running max grows by more than 8
 // (log2 units); otherwise P is formed against the stale max (values <= 2^8),
 // which is exact because the final normalisation divides by the sum taken
@@ -63,10 +68,10 @@ struct FwdCfg {
   static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
 };
 
-template <int D, bool PART>
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, uint16_t* __restrict__ out,
-                       float* __restrict__ lse, int s, int H, int* status, const AttnPart part) {
+    attn_fwd_part_kernel(const __grid_constant__ CUtensorMap tm, int s, int H, int* status,
+                         const AttnPart part) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -297,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(&p_full[st]);
     }
-    if (PART && ok && mbar_wait_warp(o_final, 0, status, kSiteAttention)) {
+    if (ok && mbar_wait_warp(o_final, 0, status, kSiteAttention)) {
       // fp32 partial O (normalised over this rectangle's keys) and its lse
       tc_fence_after();
       const float inv = 1.f / l;
@@ -317,28 +322,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (q < s) part.lse[(static_cast<int64_t>(bi) * H + hh) * part.len + qr] = (m + log2f(l)) * kLn2;
-    } else if (!PART && ok && mbar_wait_warp(o_final, 0, status, kSiteAttention)) {
-      tc_fence_after();
-      const float inv = 1.f / l;
-      uint16_t* orow = out + (static_cast<int64_t>(bi) * s + q) * a + hh * D;
-#pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        float v[32];
-        tmem_ld_32x32b_x32(tO + lane_off + c * 32, v);
-        if (q < s && MC_DCHECK(q >= 0 && hh * D + c * 32 + 32 <= a, status, kSiteAttention)) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            uint4 wv;
-            wv.x = pack_bf16x2(v[8 * i + 0] * inv, v[8 * i + 1] * inv);
-            wv.y = pack_bf16x2(v[8 * i + 2] * inv, v[8 * i + 3] * inv);
-            wv.z = pack_bf16x2(v[8 * i + 4] * inv, v[8 * i + 5] * inv);
-            wv.w = pack_bf16x2(v[8 * i + 6] * inv, v[8 * i + 7] * inv);
-            dst[i] = wv;
-          }
-        }
-      }
-      if (q < s) lse[(static_cast<int64_t>(bi) * H + hh) * s + q] = (m + log2f(l)) * kLn2;
     }
   }
 
@@ -986,9 +969,9 @@ int launch_bwd_tc(const uint16_t* qkv, const float* lse, const uint16_t* dout, u
   return launch_bwd_dq_tc<D, false>(tq, td, lse, delta, dqkv, b, s, H, status, st, kWhole);
 }
 
-template <int D, bool PART>
-int launch_fwd_tc(const uint16_t* qkv, uint16_t* o, float* lse, int b, int s, int H, int* status,
-                  cudaStream_t st, const AttnPart& part) {
+template <int D>
+int launch_fwd_part(const uint16_t* qkv, int b, int s, int H, int* status, cudaStream_t st,
+                    const AttnPart& part) {
   using C = FwdCfg<D>;
   const uint64_t a3 = 3ull * H * D;
   CUtensorMap tm;
@@ -996,14 +979,14 @@ int launch_fwd_tc(const uint16_t* qkv, uint16_t* o, float* lse, int b, int s, in
   const uint64_t strides[2] = {a3 * 2, a3 * 2 * static_cast<uint64_t>(s)};
   const uint32_t box[3] = {64, 128, 1};
   if (!make_tmap_bf16(&tm, qkv, 3, dims, strides, box)) return MC_ERR_CUDA;
-  auto kern = attn_fwd_tc_kernel<D, PART>;
+  auto kern = attn_fwd_part_kernel<D>;
   static PerDeviceInit init;
   const cudaError_t attr = once_per_device(init, [&](long long*) {
     return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   });
   if (attr != cudaSuccess) return MC_ERR_CUDA;
-  dim3 grid(PART ? part.len / BQ : (s + BQ - 1) / BQ, H, b);
-  launch_kernel(kern, dim3(grid), dim3(kThreads), C::kSmem, st, 1, tm, o, lse, s, H, status, part);
+  dim3 grid(part.len / BQ, H, b);
+  launch_kernel(kern, dim3(grid), dim3(kThreads), C::kSmem, st, 1, tm, s, H, status, part);
   return cudaGetLastError() == cudaSuccess ? MC_OK : MC_ERR_CUDA;
 }
 
@@ -1016,18 +999,12 @@ int launch_attention_backward_tc(const uint16_t* qkv, const float* lse, const ui
                  : launch_bwd_tc<128>(qkv, lse, dout, dqkv, delta, b, s, H, status, st);
 }
 
-int launch_attention_forward_tc(const uint16_t* qkv, uint16_t* o, float* lse, int b, int s, int H,
-                                int d, int* status, cudaStream_t st) {
-  return d == 64 ? launch_fwd_tc<64, false>(qkv, o, lse, b, s, H, status, st, kWhole)
-                 : launch_fwd_tc<128, false>(qkv, o, lse, b, s, H, status, st, kWhole);
-}
-
 int launch_attention_forward_part(const uint16_t* qkv, int b, int s, int H, int d, int q_base,
                                   int q_len, int kb_lo, int kb_hi, float* part_o, float* part_lse,
                                   int* status, cudaStream_t st) {
   const AttnPart part = {q_base, q_len, kb_lo, kb_hi, part_o, part_lse};
-  return d == 64 ? launch_fwd_tc<64, true>(qkv, nullptr, nullptr, b, s, H, status, st, part)
-                 : launch_fwd_tc<128, true>(qkv, nullptr, nullptr, b, s, H, status, st, part);
+  return d == 64 ? launch_fwd_part<64>(qkv, b, s, H, status, st, part)
+                 : launch_fwd_part<128>(qkv, b, s, H, status, st, part);
 }
 
 int launch_attention_dq_part(const uint16_t* qkv, const float* lse, const uint16_t* dout,

@@ -164,8 +164,10 @@ int launch_fp8_quantize_2d(const void* in, bool in_bf16, int64_t rows, int64_t c
 
 int launch_attention_forward(const uint16_t* qkv, uint16_t* o, float* lse, int b, int s, int H,
                              int d, int* status, cudaStream_t stream);
-int launch_attention_forward_tc(const uint16_t* qkv, uint16_t* o, float* lse, int b, int s, int H,
-                                int d, int* status, cudaStream_t stream);
+// The whole-sequence causal forward with 256-key blocks (one 128-query tile
+// per CTA, 320 threads).
+int launch_attention_forward_wide(const uint16_t* qkv, uint16_t* o, float* lse, int b, int s,
+                                  int H, int d, int* status, cudaStream_t stream);
 int launch_attention_backward_tc(const uint16_t* qkv, const float* lse, const uint16_t* dout,
                                  uint16_t* dqkv, const float* delta, int b, int s, int H, int d,
                                  int* status, cudaStream_t stream);
