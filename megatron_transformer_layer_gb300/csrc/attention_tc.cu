@@ -559,13 +559,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // Visible: query >= key, both within the sequence.
       const int q0 = c0 + half * 64;
       const bool edge = q0 < r0 + 127 || q0 + 64 > s;
+      const float2 sc2 = make_float2(scale2, scale2);
 #pragma unroll
       for (int e = 0; e < 64; e += 4) {
         const float4 lv = *reinterpret_cast<const float4*>(l2 + e);
-        p[e] = fast_exp2(fmaf(p[e], scale2, -lv.x));
-        p[e + 1] = fast_exp2(fmaf(p[e + 1], scale2, -lv.y));
-        p[e + 2] = fast_exp2(fmaf(p[e + 2], scale2, -lv.z));
-        p[e + 3] = fast_exp2(fmaf(p[e + 3], scale2, -lv.w));
+        const float2 y0 = __ffma2_rn(make_float2(p[e], p[e + 1]), sc2, make_float2(-lv.x, -lv.y));
+        const float2 y1 =
+            __ffma2_rn(make_float2(p[e + 2], p[e + 3]), sc2, make_float2(-lv.z, -lv.w));
+        p[e] = fast_exp2(y0.x);
+        p[e + 1] = fast_exp2(y0.y);
+        p[e + 2] = fast_exp2(y1.x);
+        p[e + 3] = fast_exp2(y1.y);
       }
       if (edge) {
 #pragma unroll
@@ -579,19 +583,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         break;
       }
       tc_fence_after();
+      // All 64 dP^T columns in one round trip.
+      float dv[64];
+      tmem_ld_32x32b_x32_nowait(tdP + my_cols, dv);
+      tmem_ld_32x32b_x32_nowait(tdP + my_cols + 32, dv + 32);
+      tmem_ld_wait();
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
-        float dv[16];
-        tmem_ld_32x32b_x16(tdP + my_cols + g * 16, dv);
         uint32_t w[16];  // [P of the 16 queries | dS of the 16 queries]
 #pragma unroll
         for (int e = 0; e < 16; e += 4) {
           const float4 dlv = *reinterpret_cast<const float4*>(dl + g * 16 + e);
           const float* pp = p + g * 16 + e;
+          const float* dd = dv + g * 16 + e;
+          const float2 d0 = __fmul2_rn(make_float2(pp[0], pp[1]),
+                                       __fadd2_rn(make_float2(dd[0], dd[1]),
+                                                  make_float2(-dlv.x, -dlv.y)));
+          const float2 d1 = __fmul2_rn(make_float2(pp[2], pp[3]),
+                                       __fadd2_rn(make_float2(dd[2], dd[3]),
+                                                  make_float2(-dlv.z, -dlv.w)));
           w[e / 2] = pack_bf16x2(pp[0], pp[1]);
           w[e / 2 + 1] = pack_bf16x2(pp[2], pp[3]);
-          w[8 + e / 2] = pack_bf16x2(pp[0] * (dv[e] - dlv.x), pp[1] * (dv[e + 1] - dlv.y));
-          w[8 + e / 2 + 1] = pack_bf16x2(pp[2] * (dv[e + 2] - dlv.z), pp[3] * (dv[e + 3] - dlv.w));
+          w[8 + e / 2] = pack_bf16x2(d0.x, d0.y);
+          w[8 + e / 2 + 1] = pack_bf16x2(d1.x, d1.y);
         }
         // over this thread's own dP^T columns, already in registers
         tmem_st_32x32b_x16(tdP + my_cols + g * 16, w);
@@ -842,19 +856,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int c0 = (kb0 + j) * 128 + half * 64;
       const bool edge = c0 + 63 > q0 || c0 + 64 > s;
       uint32_t dw[32];
+      const float2 sc2 = make_float2(scale2, scale2), nl2 = make_float2(-my_l2, -my_l2);
+      const float2 nd2 = make_float2(-my_d, -my_d);
 #pragma unroll
       for (int e = 0; e < 64; e += 2) {
-        float ds[2];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          float pv = fast_exp2(fmaf(sv[e + u], scale2, -my_l2));
-          if (edge) {
-            const int col = c0 + e + u;
-            pv = (col <= r && col < s) ? pv : 0.f;
-          }
-          ds[u] = pv * (dv[e + u] - my_d);
+        const float2 y = __ffma2_rn(make_float2(sv[e], sv[e + 1]), sc2, nl2);
+        float2 pv = make_float2(fast_exp2(y.x), fast_exp2(y.y));
+        if (edge) {
+          const int col = c0 + e;
+          pv.x = (col <= r && col < s) ? pv.x : 0.f;
+          pv.y = (col + 1 <= r && col + 1 < s) ? pv.y : 0.f;
         }
-        dw[e / 2] = pack_bf16x2(ds[0], ds[1]);
+        const float2 ds = __fmul2_rn(pv, __fadd2_rn(make_float2(dv[e], dv[e + 1]), nd2));
+        dw[e / 2] = pack_bf16x2(ds.x, ds.y);
       }
       // dS_{j-1} must have been consumed by its dQ product.
       if (j > 0 && !mbar_wait_warp(ds_free, (j - 1) & 1, status, kSiteAttention)) {
