@@ -1,4 +1,6 @@
-// Causal flash attention forward with 256-key blocks (sm_103a, tcgen05).
+// Causal flash attention forward with 256-key blocks (sm_103a, tcgen05),
+// over the whole score matrix or over one rectangle of it (the
+// context-parallel path: fp32 partial O and its log-sum-exp, merged later).
 //
 // S_j = Q K_j^T runs as 128 x 256 x 16 MMAs, which keep the tensor pipe
 // busier per instruction than 128 x 128 ones (the shared-memory operand
@@ -29,6 +31,8 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+
+#include <climits>
 
 #include "mc_layer_internal.h"
 #include "ptx.cuh"
@@ -61,10 +65,23 @@ struct WideCfg {
   static constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;
 };
 
-template <int D>
+// A rectangle of the causal score matrix: query rows [base, base + len)
+// (whole 128-row tiles) against keys [key_lo, key_hi) (key_lo a multiple of
+// 128).  The whole matrix is {0, s, 0, INT_MAX} and writes bf16 O and the
+// fp32 log-sum-exp; a partial rectangle (the context-parallel path) writes
+// the fp32 O normalised over its own keys and that log-sum-exp, indexed by
+// the row within the rectangle: out [b, len, a], lse [b, H, len].
+struct WideRect {
+  int base, len;
+  int key_lo, key_hi;
+  float* out;
+  float* lse;
+};
+
+template <int D, bool PART>
 __global__ void __launch_bounds__(kWideThreads, 1)
     attn_fwd_wide_kernel(const __grid_constant__ CUtensorMap tm, uint16_t* __restrict__ out,
-                         float* __restrict__ lse, int s, int H, int* status) {
+                         float* __restrict__ lse, int s, int H, int* status, const WideRect rect) {
   using C = WideCfg<D>;
   constexpr int VS = C::kVSlots;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -93,10 +110,20 @@ __global__ void __launch_bounds__(kWideThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int a = H * D;
-  const int q_blk = static_cast<int>(gridDim.x - 1 - blockIdx.x);  // heaviest first
+  // heaviest first
+  const int q_blk =
+      (PART ? rect.base / 128 : 0) + static_cast<int>(gridDim.x - 1 - blockIdx.x);
   const int hh = blockIdx.y, bi = blockIdx.z;
   const int q0 = q_blk * 128;
-  const int n_kb = (min(q0 + 128, s) + kKeys - 1) / kKeys;  // 256-key blocks
+  // (the whole matrix: keys from 0, masked past s)
+  const int k_lo = PART ? rect.key_lo : 0;
+  const int k_end = PART ? min(s, rect.key_hi) : s;  // keys past it are masked
+  const int k_last = min(q0 + 128, k_end);           // no block starts at or after it
+  const int n_kb = (k_last - k_lo + kKeys - 1) / kKeys;   // 256-key blocks
+  if (n_kb < 1) {  // an empty rectangle: the caller's schedule never makes one
+    if (threadIdx.x == 0) record_error(status, MC_ERR_DEVICE_BOUNDS, kSiteAttention);
+    return;
+  }
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -150,7 +177,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
           mbar_arrive_expect_tx(&v_full[slot], C::kVHalf);
           for (int c = 0; c < C::kChunks; ++c)
             tma_load_3d(sV0 + slot * C::kVHalf + c * 16384, &tm, &v_full[slot],
-                        2 * a + hh * D + c * 64, jv * kKeys + h * 128, bi);
+                        2 * a + hh * D + c * 64, k_lo + jv * kKeys + h * 128, bi);
           ++v_issued;
         }
       };
@@ -162,7 +189,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
           for (int c = 0; c < C::kChunks; ++c)
             for (int h = 0; h < 2; ++h)
               tma_load_3d(sK[ks] + c * C::kChunkBytes + h * 16384, &tm, &k_full[ks],
-                          a + hh * D + c * 64, j * kKeys + h * 128, bi);
+                          a + hh * D + c * 64, k_lo + j * kKeys + h * 128, bi);
           ++k_issued;
         }
         if (j >= 1) load_v(j - 1);
@@ -266,9 +293,9 @@ __global__ void __launch_bounds__(kWideThreads, 1)
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(s_free);
-      const int key0 = j * kKeys + half * 128;
-      if (key0 + 127 > q0 || key0 + 128 > s) {  // diagonal or ragged: mask
-        const int lim = min(q + 1, s) - key0;   // keys [0, lim) of this half are visible
+      const int key0 = k_lo + j * kKeys + half * 128;
+      if (key0 + 127 > q0 || key0 + 128 > k_end) {  // diagonal, ragged or past the keys: mask
+        const int lim = min(q + 1, k_end) - key0;   // keys [0, lim) of this half are visible
 #pragma unroll
         for (int i = 0; i < 128; ++i) x[i] = i < lim ? x[i] : -INFINITY;
       }
@@ -338,25 +365,45 @@ __global__ void __launch_bounds__(kWideThreads, 1)
       tc_fence_after();
       l += exchange(l);  // both halves' sums, taken against the same max
       const float inv = 1.f / l;
-      uint16_t* orow = out + (static_cast<int64_t>(bi) * s + q) * a + hh * D;
+      if constexpr (PART) {
+        const int qr = q - rect.base;
+        float* orow = rect.out + (static_cast<int64_t>(bi) * rect.len + qr) * a + hh * D;
 #pragma unroll 1
-      for (int c = half * (D / 64); c < (half + 1) * (D / 64); ++c) {
-        float v[32];
-        tmem_ld_32x32b_x32(tO + lane_off + c * 32, v);
-        if (q < s && MC_DCHECK(q >= 0 && hh * D + c * 32 + 32 <= a, status, kSiteAttention)) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+        for (int c = half * (D / 64); c < (half + 1) * (D / 64); ++c) {
+          float v[32];
+          tmem_ld_32x32b_x32(tO + lane_off + c * 32, v);
+          if (q < s && MC_DCHECK(qr >= 0 && qr < rect.len && hh * D + c * 32 + 32 <= a, status,
+                                 kSiteAttention)) {
+            float4* dst = reinterpret_cast<float4*>(orow + c * 32);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            uint4 wv;
-            wv.x = pack_bf16x2(v[8 * i + 0] * inv, v[8 * i + 1] * inv);
-            wv.y = pack_bf16x2(v[8 * i + 2] * inv, v[8 * i + 3] * inv);
-            wv.z = pack_bf16x2(v[8 * i + 4] * inv, v[8 * i + 5] * inv);
-            wv.w = pack_bf16x2(v[8 * i + 6] * inv, v[8 * i + 7] * inv);
-            dst[i] = wv;
+            for (int i = 0; i < 8; ++i)
+              dst[i] = make_float4(v[4 * i] * inv, v[4 * i + 1] * inv, v[4 * i + 2] * inv,
+                                   v[4 * i + 3] * inv);
           }
         }
+        if (q < s && half == 0)
+          rect.lse[(static_cast<int64_t>(bi) * H + hh) * rect.len + qr] = (m + log2f(l)) * kLn2;
+      } else {
+        uint16_t* orow = out + (static_cast<int64_t>(bi) * s + q) * a + hh * D;
+#pragma unroll 1
+        for (int c = half * (D / 64); c < (half + 1) * (D / 64); ++c) {
+          float v[32];
+          tmem_ld_32x32b_x32(tO + lane_off + c * 32, v);
+          if (q < s && MC_DCHECK(q >= 0 && hh * D + c * 32 + 32 <= a, status, kSiteAttention)) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              uint4 wv;
+              wv.x = pack_bf16x2(v[8 * i + 0] * inv, v[8 * i + 1] * inv);
+              wv.y = pack_bf16x2(v[8 * i + 2] * inv, v[8 * i + 3] * inv);
+              wv.z = pack_bf16x2(v[8 * i + 4] * inv, v[8 * i + 5] * inv);
+              wv.w = pack_bf16x2(v[8 * i + 6] * inv, v[8 * i + 7] * inv);
+              dst[i] = wv;
+            }
+          }
+        }
+        if (q < s && half == 0) lse[(static_cast<int64_t>(bi) * H + hh) * s + q] = (m + log2f(l)) * kLn2;
       }
-      if (q < s && half == 0) lse[(static_cast<int64_t>(bi) * H + hh) * s + q] = (m + log2f(l)) * kLn2;
     }
   }
 
@@ -368,9 +415,9 @@ __global__ void __launch_bounds__(kWideThreads, 1)
   }
 }
 
-template <int D>
+template <int D, bool PART>
 int launch_wide(const uint16_t* qkv, uint16_t* o, float* lse, int b, int s, int H, int* status,
-                cudaStream_t st) {
+                cudaStream_t st, const WideRect& rect) {
   using C = WideCfg<D>;
   const uint64_t a3 = 3ull * H * D;
   CUtensorMap tm;
@@ -378,14 +425,14 @@ int launch_wide(const uint16_t* qkv, uint16_t* o, float* lse, int b, int s, int 
   const uint64_t strides[2] = {a3 * 2, a3 * 2 * static_cast<uint64_t>(s)};
   const uint32_t box[3] = {64, 128, 1};
   if (!make_tmap_bf16(&tm, qkv, 3, dims, strides, box)) return MC_ERR_CUDA;
-  auto kern = attn_fwd_wide_kernel<D>;
+  auto kern = attn_fwd_wide_kernel<D, PART>;
   static PerDeviceInit init;
   const cudaError_t attr = once_per_device(init, [&](long long*) {
     return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   });
   if (attr != cudaSuccess) return MC_ERR_CUDA;
-  dim3 grid((s + 127) / 128, H, b);
-  launch_kernel(kern, grid, dim3(kWideThreads), C::kSmem, st, 1, tm, o, lse, s, H, status);
+  dim3 grid(PART ? rect.len / 128 : (s + 127) / 128, H, b);
+  launch_kernel(kern, grid, dim3(kWideThreads), C::kSmem, st, 1, tm, o, lse, s, H, status, rect);
   return cudaGetLastError() == cudaSuccess ? MC_OK : MC_ERR_CUDA;
 }
 
@@ -393,8 +440,20 @@ int launch_wide(const uint16_t* qkv, uint16_t* o, float* lse, int b, int s, int 
 
 int launch_attention_forward_wide(const uint16_t* qkv, uint16_t* o, float* lse, int b, int s,
                                   int H, int d, int* status, cudaStream_t st) {
-  return d == 64 ? launch_wide<64>(qkv, o, lse, b, s, H, status, st)
-                 : launch_wide<128>(qkv, o, lse, b, s, H, status, st);
+  const WideRect whole = {0, s, 0, INT_MAX, nullptr, nullptr};
+  return d == 64 ? launch_wide<64, false>(qkv, o, lse, b, s, H, status, st, whole)
+                 : launch_wide<128, false>(qkv, o, lse, b, s, H, status, st, whole);
+}
+
+int launch_attention_forward_part(const uint16_t* qkv, int b, int s, int H, int d, int q_base,
+                                  int q_len, int kb_lo, int kb_hi, float* part_o, float* part_lse,
+                                  int* status, cudaStream_t st) {
+  if (q_base % 128 || q_len % 128 || q_len < 128 || kb_lo < 0 || kb_hi <= kb_lo)
+    return MC_ERR_ARGUMENT;
+  const WideRect rect = {q_base, q_len, kb_lo * 128,
+                         kb_hi > INT_MAX / 128 ? INT_MAX : kb_hi * 128, part_o, part_lse};
+  return d == 64 ? launch_wide<64, true>(qkv, nullptr, nullptr, b, s, H, status, st, rect)
+                 : launch_wide<128, true>(qkv, nullptr, nullptr, b, s, H, status, st, rect);
 }
 
 }  // namespace mc

@@ -1,26 +1,8 @@
-// Causal flash attention on the sm_103a tensor cores (tcgen05): the forward
-// over rectangles of the score matrix that the context-parallel path
-// combines, and the backward kernels (whole matrix or rectangles).  The
-// whole-sequence forward, with 256-key blocks, is attention_fwd_wide.cu.
-//
-// Rectangle forward: one CTA per (128-query tile, head, batch), heaviest
-// tiles first:
-//   warp 0      TMA: the Q tile once, then K/V tiles of 128 keys into a
-//               2-deep ring (3-D tensor map over Q|K|V [b, s, 3a]: rows past
-//               the sequence read zeros)
-//   warp 1      allocates 512 TMEM columns and issues tcgen05.mma from one
-//               thread: S_j = Q K_j^T (M = 128, N = 128, K = d) into one of
-//               two S buffers, then O += P_{j-1} V_{j-1} (M = 128, N = d,
-//               K = 128) with P read from tensor memory
-//   warps 2..5  one thread per query row: load the S row from TMEM, mask,
-//               online softmax (running max and sum, exp2 with log2(e)/sqrt(d)
-//               folded in), write P back into the S buffer as bf16 pairs;
-//               at the end normalise O and store the fp32 partial O and its
-//               log-sum-exp.
-// O is rescaled in TMEM only when a row's running max grows by more than 8
-// (log2 units); otherwise P is formed against the stale max (values <= 2^8),
-// which is exact because the final normalisation divides by the sum taken
-// against the same max.
+// Causal flash attention backward on the sm_103a tensor cores (tcgen05):
+// the dK/dV and dQ kernels, over the whole score matrix or over the
+// rectangles that the context-parallel path combines.  The forward (whole
+// matrix and rectangles) is attention_fwd_wide.cu; the delta pre-pass and
+// the argument checks are attention.cu.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -33,305 +15,22 @@
 namespace mc {
 namespace {
 
-constexpr int kThreads = 192;     // forward: producer, MMA, 4 softmax warps
-constexpr int kBwdThreads = 320;  // backward: producer, MMA, 8 compute warps
-constexpr int BQ = 128;   // query rows per CTA
-constexpr int BKV = 128;  // keys per block
+constexpr int kBwdThreads = 320;  // producer, MMA, 8 compute warps
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLn2 = 0.6931471805599453f;
-constexpr float kRescaleThreshold = 8.0f;
 
 // A rectangle of the causal score matrix, for the context-parallel path:
-// forward and dQ take query rows [base, base + len) against key blocks
-// [blk_lo, blk_hi); dK/dV take key rows [base, base + len) against query
-// blocks [blk_lo, blk_hi).  Results go to fp32 partials indexed by the row
-// within the rectangle: forward O [b, len, a] and lse [b, H, len]; dQ
-// [b, len, a]; dK | dV [b, len, 2a].  The fused kernels use the whole
-// matrix (base 0, len s, blocks [0, INT_MAX)) and ignore the partials.
+// dQ takes query rows [base, base + len) against key blocks [blk_lo, blk_hi);
+// dK/dV take key rows [base, base + len) against query blocks
+// [blk_lo, blk_hi).  Results go to fp32 partials indexed by the row within
+// the rectangle: dQ [b, len, a]; dK | dV [b, len, 2a].  The fused kernels
+// use the whole matrix (base 0, len s, blocks [0, INT_MAX)) and ignore the
+// partials.
 struct AttnPart {
   int base, len;
   int blk_lo, blk_hi;
   float* out;
   float* lse;
 };
-
-template <int D>
-struct FwdCfg {
-  static constexpr int kChunks = D / 64;              // 128-byte boxes per row
-  static constexpr int kTile = 128 * D * 2;           // [128 rows][D] bf16
-  static constexpr int kBarBytes = 18 * 8;
-  static constexpr int kUsed = 5 * kTile + kBarBytes + 1024;
-  // At least 116 KB so that two CTAs never share an SM (each holds all 512
-  // TMEM columns).
-  static constexpr int kSmem = kUsed > 116 * 1024 ? kUsed : 116 * 1024;
-  static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
-};
-
-template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
-    attn_fwd_part_kernel(const __grid_constant__ CUtensorMap tm, int s, int H, int* status,
-                         const AttnPart part) {
-  using C = FwdCfg<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
-  uint8_t* sQ = smem;
-  uint8_t* sK[2] = {smem + C::kTile, smem + 2 * C::kTile};
-  uint8_t* sV[2] = {smem + 3 * C::kTile, smem + 4 * C::kTile};
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 5 * C::kTile);
-  uint64_t* q_full = bars + 0;
-  uint64_t* k_full = bars + 1;    // [2]  K_j is released after S_j,
-  uint64_t* k_empty = bars + 3;   // [2]
-  uint64_t* s_full = bars + 5;    // [2]
-  uint64_t* p_full = bars + 7;    // [2]
-  uint64_t* o_ready = bars + 9;
-  uint64_t* drain = bars + 10;
-  uint64_t* v_full = bars + 11;   // [2]  V_j only after PV_j
-  uint64_t* v_empty = bars + 13;  // [2]
-  // Completes once, after the last PV: O is final.  (o_ready cannot serve:
-  // when the last S arrives only PV_{n-3} is known to be done, so a parity
-  // wait for PV_{n-1} could be satisfied by PV_{n-3}'s phase.)
-  uint64_t* o_final = bars + 15;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int a = H * D;
-  const int q_blk = part.base / BQ + static_cast<int>(gridDim.x - 1 - blockIdx.x);
-  const int hh = blockIdx.y, bi = blockIdx.z;
-  const int q0 = q_blk * BQ;
-  const int kb0 = part.blk_lo;  // first key block
-  const int n_kb = min((min(q0 + BQ, s) + BKV - 1) / BKV, part.blk_hi) - kb0;
-
-  if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&k_full[i], 1);
-      mbar_init(&k_empty[i], 1);
-      mbar_init(&v_full[i], 1);
-      mbar_init(&v_empty[i], 1);
-      mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], 128);
-    }
-    mbar_init(o_ready, 1);
-    mbar_init(o_final, 1);
-    mbar_init(drain, 1);
-    fence_mbar_init();
-    tma_prefetch_desc(&tm);
-  }
-  if (warp == 1) {
-    tmem_alloc(tmem_slot, C::kTmemCols);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  pdl_wait();  // the previous kernel on the stream has completed
-  const uint32_t tS[2] = {tmem + C::kColS0, tmem + C::kColS1};
-  const uint32_t tO = tmem + C::kColO;
-
-  if (warp == 0) {
-    if (lane == 0) {
-      // -------------------------------------------------------- producer
-      mbar_arrive_expect_tx(q_full, C::kTile);
-      for (int c = 0; c < C::kChunks; ++c)
-        tma_load_3d(sQ + c * 16384, &tm, q_full, hh * D + c * 64, q0, bi);
-      int k_issued = 0, v_issued = 0;
-      for (int j = 0; j < n_kb; ++j) {
-        const int st = j & 1;
-        const uint32_t ph = ((j >> 1) & 1) ^ 1u;
-        if (!mbar_wait(&k_empty[st], ph, status, kSiteAttention)) break;
-        mbar_arrive_expect_tx(&k_full[st], C::kTile);
-        for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d(sK[st] + c * 16384, &tm, &k_full[st], a + hh * D + c * 64, (kb0 + j) * BKV,
-                      bi);
-        ++k_issued;
-        if (!mbar_wait(&v_empty[st], ph, status, kSiteAttention)) break;
-        mbar_arrive_expect_tx(&v_full[st], C::kTile);
-        for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d(sV[st] + c * 16384, &tm, &v_full[st], 2 * a + hh * D + c * 64,
-                      (kb0 + j) * BKV, bi);
-        ++v_issued;
-      }
-      pdl_launch();  // every load of this CTA is issued
-      // Copies still in flight must land before the CTA exits.
-      mbar_wait(q_full, 0, status, kSiteAttention, 200000000ull, false);
-      for (int j = k_issued - 1; j >= 0 && j >= k_issued - 2; --j)
-        mbar_wait(&k_full[j & 1], (j >> 1) & 1, status, kSiteAttention, 200000000ull, false);
-      for (int j = v_issued - 1; j >= 0 && j >= v_issued - 2; --j)
-        mbar_wait(&v_full[j & 1], (j >> 1) & 1, status, kSiteAttention, 200000000ull, false);
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      // -------------------------------------------------------- MMA issuer
-      constexpr uint32_t kIdescQK = idesc_bf16_f32(128, BKV, false, false);
-      constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, false, true);
-      bool ok = mbar_wait(q_full, 0, status, kSiteAttention);
-      const uint32_t q_base = smem_u32(sQ);
-      for (int j = 0; ok && j <= n_kb; ++j) {
-        if (j < n_kb) {
-          const int st = j & 1;
-          if (!mbar_wait(&k_full[st], (j >> 1) & 1, status, kSiteAttention)) break;
-          // S buffer st was last read (as P) by PV_{j-2}.
-          if (j >= 2 && !mbar_wait(o_ready, (j - 2) & 1, status, kSiteAttention)) break;
-          tc_fence_after();
-          const uint32_t k_base = smem_u32(sK[st]);
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-            umma_bf16(tS[st], smem_desc_sw128(q_base + off, 16, 1024),
-                      smem_desc_sw128(k_base + off, 16, 1024), kIdescQK, kk > 0 ? 1u : 0u);
-          }
-          umma_commit(&s_full[st]);
-          umma_commit(&k_empty[st]);
-        }
-        if (j >= 1) {
-          const int pj = j - 1, pst = pj & 1;
-          if (!mbar_wait(&p_full[pst], (pj >> 1) & 1, status, kSiteAttention)) break;
-          if (!mbar_wait(&v_full[pst], (pj >> 1) & 1, status, kSiteAttention)) break;
-          tc_fence_after();
-          const uint32_t v_base = smem_u32(sV[pst]);
-#pragma unroll
-          for (int kk = 0; kk < BKV / 16; ++kk) {
-            // P: 16 keys = 8 packed columns; V (MN-major): 16 key rows of 128 B,
-            // 64-wide d chunks 16 KB apart.
-            umma_bf16_ts(tO, tS[pst] + kk * 8,
-                         smem_desc_sw128(v_base + kk * 2048, 16384, 1024), kIdescPV,
-                         (pj > 0 || kk > 0) ? 1u : 0u);
-          }
-          umma_commit(&v_empty[pst]);
-          umma_commit(o_ready);
-        }
-      }
-      umma_commit(o_final);
-      umma_commit(drain);
-      mbar_wait(drain, 0, status, kSiteAttention, 200000000ull, false);
-    }
-  } else {
-    // ---------------------------------------------------------- softmax
-    const int quarter = warp & 3;
-    const int row = quarter * 32 + lane;
-    const int q = q0 + row;
-    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const float scale = rsqrtf(static_cast<float>(D)) * kLog2e;
-    float m = -INFINITY, l = 0.f;
-    bool ok = true;
-    for (int j = 0; j < n_kb; ++j) {
-      const int st = j & 1;
-      if (!mbar_wait_warp(&s_full[st], (j >> 1) & 1, status, kSiteAttention)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      float x[BKV];
-      // Issue all four TMEM loads before the single wait.
-      tmem_ld_32x32b_x32_nowait(tS[st] + lane_off + 0, x + 0);
-      tmem_ld_32x32b_x32_nowait(tS[st] + lane_off + 32, x + 32);
-      tmem_ld_32x32b_x32_nowait(tS[st] + lane_off + 64, x + 64);
-      tmem_ld_32x32b_x32_nowait(tS[st] + lane_off + 96, x + 96);
-      tmem_ld_wait();
-      const int key0 = (kb0 + j) * BKV;
-      if (key0 + BKV - 1 > q0 || key0 + BKV > s) {  // diagonal or ragged block
-        const int lim = min(q + 1, s) - key0;       // keys [0, lim) are visible
-#pragma unroll
-        for (int i = 0; i < BKV; ++i) x[i] = i < lim ? x[i] : -INFINITY;
-      }
-      // Row maximum as eight independent chains, then a tree: one warp per
-      // scheduler has no other work to hide a 128-long dependent chain.
-      float mx8[8];
-#pragma unroll
-      for (int r = 0; r < 8; ++r) mx8[r] = x[r];
-#pragma unroll
-      for (int i = 8; i < BKV; i += 8) {
-#pragma unroll
-        for (int r = 0; r < 8; ++r) mx8[r] = fmaxf(mx8[r], x[i + r]);
-      }
-      float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-      mx *= scale;  // raw scores; scale > 0 commutes with max
-      const float m_new = fmaxf(m, mx);
-      const bool need = j > 0 && m_new > m + kRescaleThreshold;
-      if (j == 0) m = m_new;  // key 0 is visible to every row: m is finite
-      if (__any_sync(0xffffffffu, need)) {
-        const float alpha = need ? fast_exp2(m - m_new) : 1.f;
-        // S_j was issued after PV_{j-2} completed, so this parity can only
-        // name PV_{j-1}.
-        if (!mbar_wait_warp(o_ready, (j - 1) & 1, status, kSiteAttention)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          float v[32];
-          tmem_ld_32x32b_x32(tO + lane_off + c * 32, v);
-          uint32_t w[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(v[i] * alpha);
-          tmem_st_32x32b_x32(tO + lane_off + c * 32, w);
-        }
-        tmem_st_wait();
-        if (need) {
-          l *= alpha;
-          m = m_new;
-        }
-      }
-      uint32_t pk[BKV / 2];
-      float sm8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      const float neg_m = -m;
-#pragma unroll
-      for (int i = 0; i < BKV / 2; ++i) {
-        const float p0 = fast_exp2(fmaf(x[2 * i], scale, neg_m));
-        const float p1 = fast_exp2(fmaf(x[2 * i + 1], scale, neg_m));
-        sm8[(2 * i) & 7] += p0;
-        sm8[(2 * i + 1) & 7] += p1;
-        pk[i] = pack_bf16x2(p0, p1);
-      }
-      const float sum = ((sm8[0] + sm8[1]) + (sm8[2] + sm8[3])) +
-                        ((sm8[4] + sm8[5]) + (sm8[6] + sm8[7]));
-      l += sum;
-#pragma unroll
-      for (int c = 0; c < BKV / 64; ++c) {
-        uint32_t w[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) w[i] = pk[c * 32 + i];
-        tmem_st_32x32b_x32(tS[st] + lane_off + c * 32, w);
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&p_full[st]);
-    }
-    if (ok && mbar_wait_warp(o_final, 0, status, kSiteAttention)) {
-      // fp32 partial O (normalised over this rectangle's keys) and its lse
-      tc_fence_after();
-      const float inv = 1.f / l;
-      const int qr = q - part.base;
-      float* orow = part.out + (static_cast<int64_t>(bi) * part.len + qr) * a + hh * D;
-#pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        float v[32];
-        tmem_ld_32x32b_x32(tO + lane_off + c * 32, v);
-        if (q < s && MC_DCHECK(qr >= 0 && qr < part.len && hh * D + c * 32 + 32 <= a, status,
-                               kSiteAttention)) {
-          float4* dst = reinterpret_cast<float4*>(orow + c * 32);
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-            dst[i] = make_float4(v[4 * i] * inv, v[4 * i + 1] * inv, v[4 * i + 2] * inv,
-                                 v[4 * i + 3] * inv);
-        }
-      }
-      if (q < s) part.lse[(static_cast<int64_t>(bi) * H + hh) * part.len + qr] = (m + log2f(l)) * kLn2;
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, C::kTmemCols);
-  }
-}
 
 // ---------------------------------------------------------------- backward
 // Two kernels after the delta pre-pass, each keeping one 128-row operand
@@ -983,27 +682,6 @@ int launch_bwd_tc(const uint16_t* qkv, const float* lse, const uint16_t* dout, u
   return launch_bwd_dq_tc<D, false>(tq, td, lse, delta, dqkv, b, s, H, status, st, kWhole);
 }
 
-template <int D>
-int launch_fwd_part(const uint16_t* qkv, int b, int s, int H, int* status, cudaStream_t st,
-                    const AttnPart& part) {
-  using C = FwdCfg<D>;
-  const uint64_t a3 = 3ull * H * D;
-  CUtensorMap tm;
-  const uint64_t dims[3] = {a3, static_cast<uint64_t>(s), static_cast<uint64_t>(b)};
-  const uint64_t strides[2] = {a3 * 2, a3 * 2 * static_cast<uint64_t>(s)};
-  const uint32_t box[3] = {64, 128, 1};
-  if (!make_tmap_bf16(&tm, qkv, 3, dims, strides, box)) return MC_ERR_CUDA;
-  auto kern = attn_fwd_part_kernel<D>;
-  static PerDeviceInit init;
-  const cudaError_t attr = once_per_device(init, [&](long long*) {
-    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
-  });
-  if (attr != cudaSuccess) return MC_ERR_CUDA;
-  dim3 grid(part.len / BQ, H, b);
-  launch_kernel(kern, dim3(grid), dim3(kThreads), C::kSmem, st, 1, tm, s, H, status, part);
-  return cudaGetLastError() == cudaSuccess ? MC_OK : MC_ERR_CUDA;
-}
-
 }  // namespace
 
 int launch_attention_backward_tc(const uint16_t* qkv, const float* lse, const uint16_t* dout,
@@ -1011,14 +689,6 @@ int launch_attention_backward_tc(const uint16_t* qkv, const float* lse, const ui
                                  int* status, cudaStream_t st) {
   return d == 64 ? launch_bwd_tc<64>(qkv, lse, dout, dqkv, delta, b, s, H, status, st)
                  : launch_bwd_tc<128>(qkv, lse, dout, dqkv, delta, b, s, H, status, st);
-}
-
-int launch_attention_forward_part(const uint16_t* qkv, int b, int s, int H, int d, int q_base,
-                                  int q_len, int kb_lo, int kb_hi, float* part_o, float* part_lse,
-                                  int* status, cudaStream_t st) {
-  const AttnPart part = {q_base, q_len, kb_lo, kb_hi, part_o, part_lse};
-  return d == 64 ? launch_fwd_part<64>(qkv, b, s, H, status, st, part)
-                 : launch_fwd_part<128>(qkv, b, s, H, status, st, part);
 }
 
 int launch_attention_dq_part(const uint16_t* qkv, const float* lse, const uint16_t* dout,
