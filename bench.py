@@ -371,7 +371,7 @@ def stage_launcher(name, w, device, params=None, cp_parts=4):
             rc = L.mc_gemm(f, h, T, A, f, 1, B, h, 1, out, h, L.MC_EPI_STORE_F32, stream=st)
             assert rc == 0, L.mc_strerror(rc)
         return launch, 2.0 * T * h * f, "flop", "gemm_tcgen05 wgrad dW1 = dhp^T ln2 (MN-major A and B)"
-    if name in ("attn_fwd", "attn_bwd"):
+    if name in ("attn_fwd", "attn_bwd", "attn_bwd_recompute"):
         qkv, o = rnd(T, 3 * a), rnd(T, a)
         lse = torch.empty(b * H * s, device=device, dtype=torch.float32)
         dout, dqkv = rnd(T, a), rnd(T, 3 * a)
@@ -383,10 +383,20 @@ def stage_launcher(name, w, device, params=None, cp_parts=4):
                 assert L.mc_attention_forward(qkv, o, lse, b, s, H, d, stream=st) == 0
             return launch, causal, "flop", "causal attention forward"
 
+        if name == "attn_bwd_recompute":
+            def launch():
+                assert L.mc_attention_backward(qkv, o, lse, dout, dqkv, delta, b, s, H, d,
+                                               stream=st) == 0
+            return launch, 2.0 * causal, "flop", \
+                "causal attention backward (pre + dkdv + dq forming S, dP again)"
+        nbytes = L.mc_attention_backward_ws_bytes(b, s, H, d)
+        ds = torch.empty(nbytes, device=device, dtype=torch.uint8)
+
         def launch():
-            assert L.mc_attention_backward(qkv, o, lse, dout, dqkv, delta, b, s, H, d,
-                                           stream=st) == 0
-        return launch, 2.0 * causal, "flop", "causal attention backward (pre + dkdv + dq)"
+            assert L.mc_attention_backward_ws(qkv, o, lse, dout, dqkv, delta, b, s, H, d, ds,
+                                              nbytes, stream=st) == 0
+        return launch, 2.0 * causal, "flop", \
+            "causal attention backward (pre + dkdv writing dS + dQ = dS K)"
     if name in ("attn_fwd_cp", "attn_bwd_cp"):
         cp = cp_parts
         qkv, o = rnd(T, 3 * a), rnd(T, a)
@@ -780,6 +790,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="c4")
     ap.add_argument("--stage", choices=["gemm_fc1", "gemm_fc1_fp8", "gemm_wgrad", "attn_fwd",
+                                        "attn_bwd_recompute",
                                         "attn_bwd",
                                         "attn_fwd_cp", "attn_bwd_cp", "ln_bwd"],
                     default=None)

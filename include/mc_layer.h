@@ -169,7 +169,8 @@ int mc_layer_check_shape(const mc_layer_shape* shape);
 size_t mc_layer_saved_bytes(const mc_layer_shape* shape);
 
 /* Bytes of the `ws` scratch buffer, including the 256-byte device status
- * block at its start.  0 for an illegal shape. */
+ * block at its start and the attention backward's dS tiles
+ * (mc_attention_backward_ws_bytes).  0 for an illegal shape. */
 size_t mc_layer_workspace_bytes(const mc_layer_shape* shape);
 
 /* Forward pass.  x [T, h] fp32 in, y [T, h] fp32 out; fills `saved`.
@@ -266,6 +267,28 @@ int mc_attention_backward(const uint16_t* qkv, const uint16_t* o, const float* l
                           const uint16_t* dout, uint16_t* dqkv, float* delta, int32_t micro_batch,
                           int32_t seq_len, int32_t heads, int32_t head_dim, int* status,
                           void* stream);
+
+/* Bytes of the dS workspace of mc_attention_backward_ws: one 32 KB bf16
+ * tile per pair (query block i, key block j <= i) of 128 rows each, per head
+ * and batch: micro_batch * heads * n (n + 1) / 2 * 32768 with n =
+ * ceil(seq_len / 128) (1.1 GB at s = 4096 with 64 heads, 34.5 GB at
+ * s = 32768 with 32 heads).  0 for an invalid shape. */
+size_t mc_attention_backward_ws_bytes(int32_t micro_batch, int32_t seq_len, int32_t heads,
+                                      int32_t head_dim);
+
+/* mc_attention_backward with a dS workspace (device memory of
+ * mc_attention_backward_ws_bytes, 16-byte aligned; too small ->
+ * MC_ERR_WORKSPACE): the dK/dV kernel writes dS^T = P^T (dP^T - delta) as
+ * bf16 tiles there and dQ = dS K / sqrt(d) is a product over those tiles,
+ * instead of a kernel that forms S and dP a second time.  The backward the
+ * layer calls.  Same results as mc_attention_backward up to the summation
+ * order of S and dP inside the tensor core (dQ is formed from the dK/dV
+ * kernel's dS). */
+int mc_attention_backward_ws(const uint16_t* qkv, const uint16_t* o, const float* lse,
+                             const uint16_t* dout, uint16_t* dqkv, float* delta,
+                             int32_t micro_batch, int32_t seq_len, int32_t heads,
+                             int32_t head_dim, void* ds_workspace, size_t ds_workspace_bytes,
+                             int* status, void* stream);
 
 /* Allocation-free variant of mc_attention_backward.  The pages have no
  * counterpart to this entry point; it exists for callers that cannot allocate

@@ -93,6 +93,9 @@ _SIGNATURES = {
     "mc_attention_forward": (_INT, [_P, _P, _P, _I32, _I32, _I32, _I32, _P, _P]),
     "mc_attention_backward": (_INT, [_P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _P, _P]),
     "mc_attention_backward_noalloc": (_INT, [_P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _P, _P]),
+    "mc_attention_backward_ws_bytes": (_SZ, [_I32, _I32, _I32, _I32]),
+    "mc_attention_backward_ws": (_INT, [_P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _P, _SZ,
+                                        _P, _P]),
     "mc_selftest_wait_timeout": (_INT, [_I64, _P, _P]),
     "mc_selftest_bounds_check": (_INT, [_I64, _I64, _P, _P, _P]),
     "mc_fp8_scratch_floats": (_SZ, []),
@@ -225,6 +228,21 @@ def mc_attention_backward(qkv, o, lse, dout, dqkv, delta, micro_batch, seq_len, 
     return lib().mc_attention_backward(_ptr(qkv), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dqkv),
                                        _ptr(delta), micro_batch, seq_len, heads, head_dim,
                                        _ptr(status), _stream(stream))
+
+
+def mc_attention_backward_ws_bytes(micro_batch, seq_len, heads, head_dim) -> int:
+    return lib().mc_attention_backward_ws_bytes(micro_batch, seq_len, heads, head_dim)
+
+
+def mc_attention_backward_ws(qkv, o, lse, dout, dqkv, delta, micro_batch, seq_len, heads,
+                             head_dim, ds_workspace, ds_workspace_bytes, status=None,
+                             stream=None) -> int:
+    """mc_attention_backward whose dQ is formed from dS^T tiles written by the
+    dK/dV kernel into `ds_workspace` (uint8 device tensor)."""
+    return lib().mc_attention_backward_ws(_ptr(qkv), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dqkv),
+                                          _ptr(delta), micro_batch, seq_len, heads, head_dim,
+                                          _ptr(ds_workspace), ds_workspace_bytes, _ptr(status),
+                                          _stream(stream))
 
 
 def mc_attention_backward_noalloc(qkv, o, lse, dout, dqkv, micro_batch, seq_len, heads, head_dim,

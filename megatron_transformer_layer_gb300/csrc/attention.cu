@@ -73,13 +73,15 @@ __global__ void __launch_bounds__(kDeltaThreads)
 
 template <int D>
 int bwd_launch(const uint16_t* qkv, const uint16_t* o, const float* lse, const uint16_t* dout,
-               uint16_t* dqkv, float* delta, int b, int s, int H, int* status, cudaStream_t st) {
+               uint16_t* dqkv, float* delta, int b, int s, int H, int* status, cudaStream_t st,
+               uint8_t* ds_tiles) {
   const int64_t T = static_cast<int64_t>(b) * s;
   const int64_t blocks = (T * H + delta_rows_per_block<D>() - 1) / delta_rows_per_block<D>();
   launch_kernel(attn_bwd_pre_kernel<D>, dim3(static_cast<unsigned>(blocks)), dim3(kDeltaThreads),
                 0, st, 1, o, dout, delta, T, s, H);
   if (cudaGetLastError() != cudaSuccess) return MC_ERR_CUDA;
-  return launch_attention_backward_tc(qkv, lse, dout, dqkv, delta, b, s, H, D, status, st);
+  return launch_attention_backward_tc(qkv, lse, dout, dqkv, delta, b, s, H, D, status, st,
+                                      ds_tiles);
 }
 
 bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -115,15 +117,16 @@ int launch_attention_forward(const uint16_t* qkv, uint16_t* o, float* lse, int b
 
 int launch_attention_backward(const uint16_t* qkv, const uint16_t* o, const float* lse,
                               const uint16_t* dout, uint16_t* dqkv, float* delta, int b, int s,
-                              int H, int d, int* status, cudaStream_t st) {
+                              int H, int d, int* status, cudaStream_t st, uint8_t* ds_tiles) {
   (void)status;
   if (b < 1 || s < 1 || H < 1) return MC_ERR_SHAPE;
   if (d != 64 && d != 128) return MC_ERR_UNSUPPORTED;
   if (H > 65535 || b > 65535) return MC_ERR_UNSUPPORTED;
   if (!qkv || !o || !lse || !dout || !dqkv || !delta) return MC_ERR_NULLPTR;
-  if (!al16(qkv) || !al16(o) || !al16(dout) || !al16(dqkv)) return MC_ERR_ALIGN;
-  return d == 64 ? bwd_launch<64>(qkv, o, lse, dout, dqkv, delta, b, s, H, status, st)
-                 : bwd_launch<128>(qkv, o, lse, dout, dqkv, delta, b, s, H, status, st);
+  if (!al16(qkv) || !al16(o) || !al16(dout) || !al16(dqkv) || !al16(ds_tiles))
+    return MC_ERR_ALIGN;
+  return d == 64 ? bwd_launch<64>(qkv, o, lse, dout, dqkv, delta, b, s, H, status, st, ds_tiles)
+                 : bwd_launch<128>(qkv, o, lse, dout, dqkv, delta, b, s, H, status, st, ds_tiles);
 }
 
 // ---------------------------------------------------------------- no-alloc
@@ -174,5 +177,6 @@ extern "C" int mc_attention_backward_noalloc(const uint16_t* qkv, const uint16_t
   const int rc = mc::noalloc_scratch(&delta);
   if (rc != MC_OK) return rc;
   return mc::launch_attention_backward(qkv, o, lse, dout, dqkv, delta, micro_batch, seq_len, heads,
-                                       head_dim, status, static_cast<cudaStream_t>(stream));
+                                       head_dim, status, static_cast<cudaStream_t>(stream),
+                                       nullptr);
 }

@@ -17,6 +17,7 @@ namespace {
 
 constexpr int kBwdThreads = 320;  // producer, MMA, 8 compute warps
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int64_t kDsTileBytes = 128 * 128 * 2;  // one bf16 dS^T tile (128 keys x 128 queries)
 
 // A rectangle of the causal score matrix, for the context-parallel path:
 // dQ takes query rows [base, base + len) against key blocks [blk_lo, blk_hi);
@@ -41,8 +42,10 @@ template <int D>
 struct BwdCfg {
   static constexpr int kChunks = D / 64;
   static constexpr int kTile = 128 * D * 2;
-  // K, V, two (Q_i, dO_i) stages, lse/delta staging [2][2][128], barriers
-  static constexpr int kUsed = 6 * kTile + 4 * 128 * 4 + 24 * 8 + 1024;
+  // K, V, two (Q_i, dO_i) stages, the dS^T tile staged for its bulk store,
+  // lse/delta staging [2][2][128], barriers.  The dynamic shared memory
+  // starts 1024-byte aligned (checked at run time): no slack is reserved.
+  static constexpr int kUsed = 6 * kTile + static_cast<int>(kDsTileBytes) + 4 * 128 * 4 + 24 * 8;
   static constexpr int kSmem = kUsed > 116 * 1024 ? kUsed : 116 * 1024;
   static constexpr uint32_t kTmemCols = 512;
   static_assert(kUsed <= 227 * 1024, "dkdv kernel shared memory");
@@ -65,16 +68,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv,
                             const __grid_constant__ CUtensorMap tm_do, const float* __restrict__ lse,
                             const float* __restrict__ delta, uint16_t* __restrict__ dqkv, int s,
-                            int H, int* status, const AttnPart part) {
+                            int H, int* status, const AttnPart part,
+                            uint8_t* __restrict__ ds_tiles) {
   using C = BwdCfg<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+  extern __shared__ __align__(1024) uint8_t smem[];
+  if (smem_u32(smem) & 1023u) {  // the 128-byte swizzled tiles need 1024-byte alignment
+    if (threadIdx.x == 0) record_error(status, MC_ERR_DEVICE_BOUNDS, kSiteAttention);
+    return;
+  }
   uint8_t* sK = smem;
   uint8_t* sV = smem + C::kTile;
   uint8_t* sQ[2] = {smem + 2 * C::kTile, smem + 3 * C::kTile};
   uint8_t* sdO[2] = {smem + 4 * C::kTile, smem + 5 * C::kTile};
-  float* sL = reinterpret_cast<float*>(smem + 6 * C::kTile);  // [2][128] lse * log2(e)
+  uint8_t* sDs = smem + 6 * C::kTile;  // dS^T tile image (swizzled), 32 KB
+  float* sL = reinterpret_cast<float*>(sDs + kDsTileBytes);  // [2][128] lse * log2(e)
   float* sD = sL + 256;                                       // [2][128] delta
   uint64_t* bars = reinterpret_cast<uint64_t*>(sD + 256);
   uint64_t* r_full = bars + 0;
@@ -87,7 +94,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint64_t* acc_done = bars + 9;   // dV, dK products of block i complete
   uint64_t* drain = bars + 10;
   uint64_t* lse_ready = bars + 11;  // [2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 13);
+  uint64_t* ds_full = bars + 13;    // the dS^T tile of block i is in sDs (256 threads)
+  uint64_t* ds_free = bars + 14;    // its bulk store has read sDs
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int a = H * D;
@@ -112,6 +121,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(p_full, 256);
     mbar_init(acc_done, 1);
     mbar_init(drain, 1);
+    mbar_init(ds_full, 256);
+    mbar_init(ds_free, 1);
     fence_mbar_init();
     tma_prefetch_desc(&tm_qkv);
     tma_prefetch_desc(&tm_do);
@@ -282,29 +293,49 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         break;
       }
       tc_fence_after();
-      // All 64 dP^T columns in one round trip.
-      float dv[64];
-      tmem_ld_32x32b_x32_nowait(tdP + my_cols, dv);
-      tmem_ld_32x32b_x32_nowait(tdP + my_cols + 32, dv + 32);
-      tmem_ld_wait();
+      // dS^T of this (query block, key block) pair also goes to `ds_tiles`
+      // for the dQ product, as the 128-byte-swizzled shared-memory image of
+      // an MN-major A operand: query chunk `half` at 16 KB, key row t at
+      // 128 B, the 16-byte unit of queries [8u, 8u + 8) at unit u ^ (t & 7).
+      // It is assembled in sDs (conflict-free 16-byte writes) and leaves as
+      // one bulk store; the previous block's store must have read sDs first.
+      const bool store_ds = !PART && ds_tiles != nullptr;
+      uint8_t* ds_row = sDs + half * 16384 + t * 128;
+      if (store_ds && i > 0) {
+        if (threadIdx.x == 64) {
+          bulk_wait_read();
+          mbar_arrive(ds_free);
+        }
+        if (!mbar_wait_warp(ds_free, (i - 1) & 1, status, kSiteAttention)) {
+          ok = false;
+          break;
+        }
+      }
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
+        float dv[16];
+        tmem_ld_32x32b_x16(tdP + my_cols + g * 16, dv);
         uint32_t w[16];  // [P of the 16 queries | dS of the 16 queries]
 #pragma unroll
         for (int e = 0; e < 16; e += 4) {
           const float4 dlv = *reinterpret_cast<const float4*>(dl + g * 16 + e);
           const float* pp = p + g * 16 + e;
-          const float* dd = dv + g * 16 + e;
           const float2 d0 = __fmul2_rn(make_float2(pp[0], pp[1]),
-                                       __fadd2_rn(make_float2(dd[0], dd[1]),
+                                       __fadd2_rn(make_float2(dv[e], dv[e + 1]),
                                                   make_float2(-dlv.x, -dlv.y)));
           const float2 d1 = __fmul2_rn(make_float2(pp[2], pp[3]),
-                                       __fadd2_rn(make_float2(dd[2], dd[3]),
+                                       __fadd2_rn(make_float2(dv[e + 2], dv[e + 3]),
                                                   make_float2(-dlv.z, -dlv.w)));
           w[e / 2] = pack_bf16x2(pp[0], pp[1]);
           w[e / 2 + 1] = pack_bf16x2(pp[2], pp[3]);
           w[8 + e / 2] = pack_bf16x2(d0.x, d0.y);
           w[8 + e / 2 + 1] = pack_bf16x2(d1.x, d1.y);
+        }
+        if (store_ds) {
+          *reinterpret_cast<uint4*>(ds_row + (((2 * g) ^ (t & 7)) << 4)) =
+              make_uint4(w[8], w[9], w[10], w[11]);
+          *reinterpret_cast<uint4*>(ds_row + (((2 * g + 1) ^ (t & 7)) << 4)) =
+              make_uint4(w[12], w[13], w[14], w[15]);
         }
         // over this thread's own dP^T columns, already in registers
         tmem_st_32x32b_x16(tdP + my_cols + g * 16, w);
@@ -312,7 +343,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(p_full);
+      if (store_ds) {
+        fence_proxy_async_smem();  // sDs writes visible to the bulk copy
+        mbar_arrive(ds_full);
+        if (warp == 2) {
+          // one thread stores the assembled tile
+          if (!mbar_wait_warp(ds_full, i & 1, status, kSiteAttention)) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) {
+            const int qb = qb0 + i;
+            const int64_t tile =
+                (static_cast<int64_t>(bi) * H + hh) * (static_cast<int64_t>(nblk) * (nblk + 1) / 2) +
+                static_cast<int64_t>(qb) * (qb + 1) / 2 + kb;
+            if (MC_DCHECK(kb <= qb && qb < nblk, status, kSiteAttention)) {
+              bulk_store(ds_tiles + tile * kDsTileBytes, sDs, static_cast<uint32_t>(kDsTileBytes));
+              bulk_commit();
+            }
+          }
+        }
+      }
     }
+    // the tile stores must be complete (and done with sDs) before exit
+    if (!PART && ds_tiles && threadIdx.x == 64) bulk_wait_all();
     if (ok && mbar_wait_warp(acc_done, (count - 1) & 1, status, kSiteAttention)) {
       tc_fence_after();
       const float scale = rsqrtf(static_cast<float>(D));
@@ -644,7 +698,7 @@ int launch_bwd_dq_tc(const CUtensorMap& tq, const CUtensorMap& td, const float* 
 template <int D, bool PART>
 int launch_bwd_dkdv_tc(const CUtensorMap& tq, const CUtensorMap& td, const float* lse,
                        const float* delta, uint16_t* dqkv, int b, int s, int H, int* status,
-                       cudaStream_t st, const AttnPart& part) {
+                       cudaStream_t st, const AttnPart& part, uint8_t* ds_tiles = nullptr) {
   using C = BwdCfg<D>;
   auto kern = attn_bwd_dkdv_tc_kernel<D, PART>;
   static PerDeviceInit init;
@@ -654,7 +708,175 @@ int launch_bwd_dkdv_tc(const CUtensorMap& tq, const CUtensorMap& td, const float
   if (attr != cudaSuccess) return MC_ERR_CUDA;
   dim3 grid(PART ? part.len / 128 : (s + 127) / 128, H, b);
   launch_kernel(kern, dim3(grid), dim3(kBwdThreads), C::kSmem, st, 1, tq, td, lse, delta, dqkv, s,
-                H, status, part);
+                H, status, part, ds_tiles);
+  return cudaGetLastError() == cudaSuccess ? MC_OK : MC_ERR_CUDA;
+}
+
+// dQ from the dS^T tiles that the dK/dV kernel wrote: dQ_i = sum_{j <= i}
+// dS_ij K_j, without forming S and dP again.  One CTA per (128-query block,
+// head, batch), heaviest first; 192 threads:
+//   warp 0      producer: per key block j the 32 KB dS^T tile (one bulk copy
+//               of its swizzled image) and K_j (TMA) into a 3-deep ring
+//   warp 1      TMEM (d columns) and the MMA thread: dQ += dS_ij K_j with A =
+//               dS (queries contiguous: MN-major) and B = K_j (MN-major)
+//   warps 2..5  epilogue: dQ / sqrt(d) as bf16 into the dQ columns of dqkv
+// The tiles are read once from HBM; the kernel is bound by that stream, not
+// by the 128 x 128 products.
+template <int D>
+struct DqGemmCfg {
+  static constexpr int kChunks = D / 64;
+  static constexpr int kKTile = 128 * D * 2;
+  static constexpr int kStage = static_cast<int>(kDsTileBytes) + kKTile;
+  static constexpr int kStages = 3;
+  static constexpr int kUsed = kStages * kStage + 16 * 8;
+  static constexpr int kSmem = kUsed + 1024;  // + alignment slack
+  static_assert(kSmem <= 227 * 1024, "dq gemm shared memory");
+  static constexpr uint32_t kTmemCols = D;  // 64 or 128
+};
+
+template <int D>
+__global__ void __launch_bounds__(192, 1)
+    attn_bwd_dq_gemm_kernel(const __grid_constant__ CUtensorMap tm_qkv,
+                            const uint8_t* __restrict__ ds_tiles, uint16_t* __restrict__ dqkv,
+                            int s, int H, int* status) {
+  using C = DqGemmCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStage);
+  uint64_t* full = bars + 0;   // [3]
+  uint64_t* empty = bars + 3;  // [3]
+  uint64_t* acc_full = bars + 6;
+  uint64_t* drain = bars + 7;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 8);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int a = H * D;
+  const int nb = (s + 127) / 128;
+  const int qb = nb - 1 - static_cast<int>(blockIdx.x);  // heaviest first
+  const int hh = blockIdx.y, bi = blockIdx.z;
+  const int count = qb + 1;  // key blocks 0 .. qb
+  const int64_t tile0 = (static_cast<int64_t>(bi) * H + hh) * (static_cast<int64_t>(nb) * (nb + 1) / 2) +
+                        static_cast<int64_t>(qb) * (qb + 1) / 2;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::kStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(drain, 1);
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_qkv);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  pdl_wait();  // the dK/dV kernel (the dS^T tiles) has completed
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // -------------------------------------------------------- producer
+      int issued = 0;
+      for (int j = 0; j < count; ++j) {
+        const int st = j % C::kStages;
+        if (!mbar_wait(&empty[st], ((j / C::kStages) & 1) ^ 1u, status, kSiteAttention)) break;
+        uint8_t* dst = smem + st * C::kStage;
+        mbar_arrive_expect_tx(&full[st], C::kStage);
+        bulk_load(dst, ds_tiles + (tile0 + j) * kDsTileBytes, static_cast<uint32_t>(kDsTileBytes),
+                  &full[st]);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(dst + kDsTileBytes + c * 16384, &tm_qkv, &full[st], a + hh * D + c * 64,
+                      j * 128, bi);
+        ++issued;
+      }
+      pdl_launch();  // every load of this CTA is issued
+      for (int j = issued - 1; j >= 0 && j >= issued - C::kStages; --j)
+        mbar_wait(&full[j % C::kStages], (j / C::kStages) & 1, status, kSiteAttention, 200000000ull,
+                  false);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // -------------------------------------------------------- MMA issuer
+      constexpr uint32_t kIdesc = idesc_bf16_f32(128, D, true, true);
+      bool ok = true;
+      for (int j = 0; j < count; ++j) {
+        const int st = j % C::kStages;
+        if (!mbar_wait(&full[st], (j / C::kStages) & 1, status, kSiteAttention)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t ab = smem_u32(smem + st * C::kStage);
+        const uint32_t kbase = ab + static_cast<uint32_t>(kDsTileBytes);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          // 16 keys per step: 16 rows of 128 B in both MN-major operands;
+          // 64-wide query (A) or d (B) chunks 16 KB apart
+          umma_bf16(tmem, smem_desc_sw128(ab + kk * 2048, 16384, 1024),
+                    smem_desc_sw128(kbase + kk * 2048, 16384, 1024), kIdesc,
+                    (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(&empty[st]);
+      }
+      if (ok) umma_commit(acc_full);
+      umma_commit(drain);
+      mbar_wait(drain, 0, status, kSiteAttention, 200000000ull, false);
+    }
+  } else {
+    // ---------------------------------------------------------- epilogue
+    const int quarter = warp & 3;
+    const int r = qb * 128 + quarter * 32 + lane;  // this thread's query row
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    if (mbar_wait_warp(acc_full, 0, status, kSiteAttention)) {
+      tc_fence_after();
+      const float scale = rsqrtf(static_cast<float>(D));
+      const int64_t base = (static_cast<int64_t>(bi) * s + r) * 3 * static_cast<int64_t>(a);
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        float v[32];
+        tmem_ld_32x32b_x32(tmem + lane_off + c * 32, v);
+        if (r < s && MC_DCHECK(r >= 0 && hh * D + c * 32 + 32 <= a, status, kSiteAttention)) {
+          uint4* dst = reinterpret_cast<uint4*>(dqkv + base + hh * D + c * 32);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            uint4 wv;
+            wv.x = pack_bf16x2(v[8 * k + 0] * scale, v[8 * k + 1] * scale);
+            wv.y = pack_bf16x2(v[8 * k + 2] * scale, v[8 * k + 3] * scale);
+            wv.z = pack_bf16x2(v[8 * k + 4] * scale, v[8 * k + 5] * scale);
+            wv.w = pack_bf16x2(v[8 * k + 6] * scale, v[8 * k + 7] * scale);
+            dst[k] = wv;
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <int D>
+int launch_bwd_dq_gemm(const CUtensorMap& tq, const uint8_t* ds_tiles, uint16_t* dqkv, int b,
+                       int s, int H, int* status, cudaStream_t st) {
+  using C = DqGemmCfg<D>;
+  auto kern = attn_bwd_dq_gemm_kernel<D>;
+  static PerDeviceInit init;
+  const cudaError_t attr = once_per_device(init, [&](long long*) {
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  });
+  if (attr != cudaSuccess) return MC_ERR_CUDA;
+  dim3 grid((s + 127) / 128, H, b);
+  launch_kernel(kern, grid, dim3(192), C::kSmem, st, 1, tq, ds_tiles, dqkv, s, H, status);
   return cudaGetLastError() == cudaSuccess ? MC_OK : MC_ERR_CUDA;
 }
 
@@ -672,23 +894,34 @@ bool make_bwd_maps(CUtensorMap* tq, CUtensorMap* td, const uint16_t* qkv, const 
 
 constexpr AttnPart kWhole = {0, 0, 0, 0x7fffffff, nullptr, nullptr};
 
+// With `ds_tiles` (attention_ds_workspace_bytes of device memory) the dK/dV
+// kernel also writes dS^T and dQ is its product with K; without, the dQ
+// kernel forms S and dP again.
 template <int D>
 int launch_bwd_tc(const uint16_t* qkv, const float* lse, const uint16_t* dout, uint16_t* dqkv,
-                  const float* delta, int b, int s, int H, int* status, cudaStream_t st) {
+                  const float* delta, int b, int s, int H, int* status, cudaStream_t st,
+                  uint8_t* ds_tiles) {
   CUtensorMap tq, td;
   if (!make_bwd_maps(&tq, &td, qkv, dout, b, s, H * D)) return MC_ERR_CUDA;
-  int rc = launch_bwd_dkdv_tc<D, false>(tq, td, lse, delta, dqkv, b, s, H, status, st, kWhole);
+  int rc = launch_bwd_dkdv_tc<D, false>(tq, td, lse, delta, dqkv, b, s, H, status, st, kWhole,
+                                        ds_tiles);
   if (rc != MC_OK) return rc;
+  if (ds_tiles) return launch_bwd_dq_gemm<D>(tq, ds_tiles, dqkv, b, s, H, status, st);
   return launch_bwd_dq_tc<D, false>(tq, td, lse, delta, dqkv, b, s, H, status, st, kWhole);
 }
 
 }  // namespace
 
+int64_t attention_ds_workspace_bytes(int64_t b, int64_t s, int64_t H) {
+  const int64_t nb = (s + 127) / 128;
+  return b * H * (nb * (nb + 1) / 2) * kDsTileBytes;
+}
+
 int launch_attention_backward_tc(const uint16_t* qkv, const float* lse, const uint16_t* dout,
                                  uint16_t* dqkv, const float* delta, int b, int s, int H, int d,
-                                 int* status, cudaStream_t st) {
-  return d == 64 ? launch_bwd_tc<64>(qkv, lse, dout, dqkv, delta, b, s, H, status, st)
-                 : launch_bwd_tc<128>(qkv, lse, dout, dqkv, delta, b, s, H, status, st);
+                                 int* status, cudaStream_t st, uint8_t* ds_tiles) {
+  return d == 64 ? launch_bwd_tc<64>(qkv, lse, dout, dqkv, delta, b, s, H, status, st, ds_tiles)
+                 : launch_bwd_tc<128>(qkv, lse, dout, dqkv, delta, b, s, H, status, st, ds_tiles);
 }
 
 int launch_attention_dq_part(const uint16_t* qkv, const float* lse, const uint16_t* dout,

@@ -174,6 +174,7 @@ struct Work {
   int* status;
   uint16_t *dy16, *dhp, *dx1_16, *dO, *dqkv;
   float *dln, *dx1, *delta, *partials;
+  uint8_t* ds;  // the attention backward's dS^T tiles
   void* recompute_saved;  // activations region when they are recomputed
   // MC_FP8_HYBRID: the row-major 8-bit operands (forward: ln1, o, ln2, g and
   // the weights; backward: dy, dhp, dx1, dqkv), the backward operands'
@@ -199,6 +200,7 @@ Work plan_ws(const Dims& D, bool with_saved, void* p, size_t* bytes) {
   W.dO = c.take<uint16_t>(D.T * D.a);
   W.delta = c.take<float>(D.b * D.H * D.s);
   W.dqkv = c.take<uint16_t>(D.T * 3 * D.a);
+  W.ds = c.take<uint8_t>(attention_ds_workspace_bytes(D.b, D.s, D.H));
   const size_t ln_part = layernorm_backward_scratch_floats(D.T, static_cast<int>(D.h));
   int64_t widest = D.f > 3 * D.a ? D.f : 3 * D.a;
   if (D.h > widest) widest = D.h;
@@ -446,7 +448,7 @@ int enqueue_backward_fp8(const Dims& D, const mc_layer_weights* w, const float* 
   // B5  attention backward (bf16) -> dQ | dK | dV
   MC_TRY(launch_attention_backward(S.qkv, S.o, S.lse, W.dO, W.dqkv, W.delta, static_cast<int>(D.b),
                                    static_cast<int>(D.s), static_cast<int>(D.H),
-                                   static_cast<int>(D.d), W.status, st));
+                                   static_cast<int>(D.d), W.status, st, W.ds));
   // B6  QKV: db_qkv; dWqkv = dqkv^T ln1; dln1 = sum_p dqkv_p Wqkv_p
   MC_TRY(launch_colsum(W.dqkv, true, D.T, 3 * D.a, G.b_qkv, acc, nullptr, W.partials, W.status, st));
   MC_TRY(quant(W.dqkv, true, D.T, 3 * D.a, W.dqkv_q, W.dqkv_t, sb + 3));
@@ -559,7 +561,7 @@ int mc_layer_backward(const mc_layer_shape* shape, const mc_layer_weights* w, co
   // B5  attention backward -> dQ | dK | dV
   MC_TRY(launch_attention_backward(S.qkv, S.o, S.lse, W.dO, W.dqkv, W.delta, static_cast<int>(D.b),
                                    static_cast<int>(D.s), static_cast<int>(D.H),
-                                   static_cast<int>(D.d), W.status, st));
+                                   static_cast<int>(D.d), W.status, st, W.ds));
   // B6  QKV: db_qkv, dWqkv = dqkv^T ln1, dln1 = sum_p dqkv_p Wqkv_p (per
   //     shard in sequence-parallel mode)
   MC_TRY(launch_colsum(W.dqkv, true, D.T, 3 * D.a, G.b_qkv, acc, nullptr, W.partials, W.status, st));
@@ -652,6 +654,28 @@ int mc_attention_backward(const uint16_t* qkv, const uint16_t* o, const float* l
                           void* stream) {
   return launch_attention_backward(qkv, o, lse, dout, dqkv, delta, micro_batch, seq_len, heads,
                                    head_dim, status, static_cast<cudaStream_t>(stream));
+}
+
+size_t mc_attention_backward_ws_bytes(int32_t micro_batch, int32_t seq_len, int32_t heads,
+                                      int32_t head_dim) {
+  if (micro_batch < 1 || seq_len < 1 || heads < 1 || (head_dim != 64 && head_dim != 128))
+    return 0;
+  return static_cast<size_t>(attention_ds_workspace_bytes(micro_batch, seq_len, heads));
+}
+
+int mc_attention_backward_ws(const uint16_t* qkv, const uint16_t* o, const float* lse,
+                             const uint16_t* dout, uint16_t* dqkv, float* delta,
+                             int32_t micro_batch, int32_t seq_len, int32_t heads,
+                             int32_t head_dim, void* ds_workspace, size_t ds_workspace_bytes,
+                             int* status, void* stream) {
+  if (micro_batch < 1 || seq_len < 1 || heads < 1) return MC_ERR_SHAPE;
+  if (!ds_workspace) return MC_ERR_NULLPTR;
+  if (ds_workspace_bytes <
+      static_cast<size_t>(attention_ds_workspace_bytes(micro_batch, seq_len, heads)))
+    return MC_ERR_WORKSPACE;
+  return launch_attention_backward(qkv, o, lse, dout, dqkv, delta, micro_batch, seq_len, heads,
+                                   head_dim, status, static_cast<cudaStream_t>(stream),
+                                   static_cast<uint8_t*>(ds_workspace));
 }
 
 }  // extern "C"

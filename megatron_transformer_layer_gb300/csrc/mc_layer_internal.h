@@ -168,12 +168,19 @@ int launch_attention_forward(const uint16_t* qkv, uint16_t* o, float* lse, int b
 // per CTA, 320 threads).
 int launch_attention_forward_wide(const uint16_t* qkv, uint16_t* o, float* lse, int b, int s,
                                   int H, int d, int* status, cudaStream_t stream);
+// Bytes of the dS^T tile workspace of the attention backward: one 32 KB
+// bf16 tile per (query block, key block <= it) pair, per head and batch.
+int64_t attention_ds_workspace_bytes(int64_t b, int64_t s, int64_t H);
+// `ds_tiles` (16-byte aligned, attention_ds_workspace_bytes) selects the
+// backward whose dK/dV kernel writes dS^T and whose dQ is dS K; NULL selects
+// the one whose dQ kernel forms S and dP again.
 int launch_attention_backward_tc(const uint16_t* qkv, const float* lse, const uint16_t* dout,
                                  uint16_t* dqkv, const float* delta, int b, int s, int H, int d,
-                                 int* status, cudaStream_t stream);
+                                 int* status, cudaStream_t stream, uint8_t* ds_tiles);
 int launch_attention_backward(const uint16_t* qkv, const uint16_t* o, const float* lse,
                               const uint16_t* dout, uint16_t* dqkv, float* delta, int b, int s,
-                              int H, int d, int* status, cudaStream_t stream);
+                              int H, int d, int* status, cudaStream_t stream,
+                              uint8_t* ds_tiles = nullptr);
 
 // delta[b, h, i] = rowsum(dO * O) for head h of token i (the backward's pre-pass).
 int launch_attention_delta(const uint16_t* o, const uint16_t* dout, float* delta, int b, int s,

@@ -185,6 +185,24 @@ def test_fp8_hybrid_contract():
     assert L.mc_layer_workspace_bytes(ok) > L.mc_layer_workspace_bytes(L.make_shape(*base, 0))
 
 
+def test_attention_ds_workspace_contract():
+    # one 32 KB tile per (query block, key block <= it) pair, per head and batch
+    assert L.mc_attention_backward_ws_bytes(1, 4096, 64, 128) == 64 * 32 * 33 // 2 * 32768
+    assert L.mc_attention_backward_ws_bytes(2, 129, 3, 64) == 2 * 3 * 3 * 32768
+    assert L.mc_attention_backward_ws_bytes(1, 128, 1, 96) == 0
+    assert L.mc_attention_backward_ws_bytes(0, 128, 1, 128) == 0
+    g = L.lib().mc_attention_backward_ws
+    p = 0x10000
+    assert g(p, p, p, p, p, p, 1, 256, 2, 128, None, 1 << 30, None, None) == L.MC_ERR_NULLPTR
+    assert g(p, p, p, p, p, p, 1, 256, 2, 128, p, 100, None, None) == L.MC_ERR_WORKSPACE
+    assert g(p, p, p, p, p, p, 0, 256, 2, 128, p, 1 << 30, None, None) == L.MC_ERR_SHAPE
+
+
+def test_layer_workspace_holds_the_attention_ds_tiles():
+    base = L.mc_layer_workspace_bytes(L.make_shape(1, 512, 1024, 8, 4096, 2))
+    assert base >= L.mc_attention_backward_ws_bytes(1, 512, 8, 128)
+
+
 def test_fp8_quantize_2d_rejects_on_the_host():
     # rows / cols not multiples of 16, or no output: rejected before any launch
     assert L.lib().mc_fp8_quantize_2d(0x10000, 1, 10, 64, 0, 0x10000, None, 0x10000, 0x10000,

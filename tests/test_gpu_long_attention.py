@@ -78,6 +78,30 @@ def test_fused_attention_full_length_every_element(case):
     _compare("fused s32768", *first, ref)
 
 
+def test_ds_tile_backward_full_length_every_element(case):
+    """The backward the layer calls (dQ from the dK/dV kernel's dS tiles,
+    256 x 257 / 2 tiles per head, 2.1 GB here) at s = 32768: every element
+    against the oracle, bitwise repeatable, dK and dV equal to the
+    two-kernel path's."""
+    qb, dob, ref = case
+    qkv, dout = dev_bf16(qb), dev_bf16(dob)
+    o, lse, base = _fused(qkv, dout)
+    nbytes = L.mc_attention_backward_ws_bytes(B, S, H, D)
+    ws = torch.full((nbytes,), 0xFF, dtype=torch.uint8, device=DEV)
+    delta = torch.empty(B * H * S, dtype=torch.float32, device=DEV)
+    st = status()
+    runs = []
+    for _ in range(2):
+        dqkv = torch.full((B * S * 3 * A,), float("nan"), dtype=torch.bfloat16, device=DEV)
+        assert L.mc_attention_backward_ws(qkv, o, lse, dout, dqkv, delta, B, S, H, D, ws, nbytes,
+                                          st) == 0
+        check_status(st)
+        runs.append(dqkv)
+    assert torch.equal(runs[0], runs[1])
+    assert torch.equal(runs[0].view(S, 3 * A)[:, A:], base.view(S, 3 * A)[:, A:])
+    _compare("dS tiles s32768", o, lse, runs[0], ref)
+
+
 def test_context_parallel_attention_full_length(case):
     qb, dob, ref = case
     cp = 4

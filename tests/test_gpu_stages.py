@@ -207,6 +207,22 @@ def test_attention_forward_backward(b, s, H, d):
     got = to_f64(dqkv).reshape(b, s, 3 * a)
     for name, sl in (("dq", slice(0, a)), ("dk", slice(a, 2 * a)), ("dv", slice(2 * a, 3 * a))):
         assert_close(name, got[:, :, sl], g_ref[:, :, sl])
+    # the backward the layer calls: dQ from the dK/dV kernel's dS tiles.  The
+    # workspace starts as all-NaN bytes, so a tile read before it was written
+    # would poison dQ.
+    nbytes = L.mc_attention_backward_ws_bytes(b, s, H, d)
+    nb = (s + 127) // 128
+    assert nbytes == b * H * nb * (nb + 1) // 2 * 128 * 128 * 2
+    ws = torch.full((nbytes,), 0xFF, dtype=torch.uint8, device=DEV)
+    dqkv2 = torch.full((b * s * 3 * a,), float("nan"), dtype=torch.bfloat16, device=DEV)
+    assert L.mc_attention_backward_ws(qkv, o, lse, dev_bf16(dob), dqkv2, delta, b, s, H, d, ws,
+                                      nbytes, st) == 0
+    check_status(st)
+    got2 = to_f64(dqkv2).reshape(b, s, 3 * a)
+    for name, sl in (("dq", slice(0, a)), ("dk", slice(a, 2 * a)), ("dv", slice(2 * a, 3 * a))):
+        assert_close(name + " (dS tiles)", got2[:, :, sl], g_ref[:, :, sl])
+    # dK, dV come from the same kernel either way
+    assert torch.equal(dqkv2.view(b, s, 3 * a)[:, :, a:], dqkv.view(b, s, 3 * a)[:, :, a:])
 
 
 def test_attention_long_sequence_many_heads():
