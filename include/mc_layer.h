@@ -130,6 +130,15 @@ extern "C" {
  * mc_layer_workspace_bytes include the 8-bit copies. */
 #define MC_FP8_HYBRID 8u
 
+/* Attention backward without the dS tile workspace: the dQ kernel forms S
+ * and dP a second time (seven 128 x 128 products per causal block pair
+ * instead of five) and mc_layer_workspace_bytes leaves out the
+ * mc_attention_backward_ws_bytes tiles, which grow as seq_len^2 (34.5 GB at
+ * s = 32768 with 32 heads; ~550 GB at s = 131072).  For long sequences whose
+ * tiles do not fit.  Results as the default mode up to the summation order
+ * of S and dP inside the tensor core. */
+#define MC_ATTN_DQ_RECOMPUTE 16u
+
 typedef struct mc_layer_shape {
   int32_t micro_batch; /* b  (--micro-batch-size)               */
   int32_t seq_len;     /* s  (--seq-length), any value >= 1      */
@@ -140,7 +149,8 @@ typedef struct mc_layer_shape {
   int32_t head_dim;    /* 0 => hidden / heads; > 0 decouples a = heads * head_dim
                           from hidden (one tensor-parallel rank's shard run alone) */
   uint32_t flags;      /* MC_ACCUMULATE_GRADS | MC_RECOMPUTE_ACTIVATIONS |
-                          MC_SEQUENCE_PARALLEL | MC_FP8_HYBRID, or 0 */
+                          MC_SEQUENCE_PARALLEL | MC_FP8_HYBRID |
+                          MC_ATTN_DQ_RECOMPUTE, or 0 */
 } mc_layer_shape;
 
 /* bf16 parameters (uint16_t bit patterns), device pointers. */
@@ -169,8 +179,9 @@ int mc_layer_check_shape(const mc_layer_shape* shape);
 size_t mc_layer_saved_bytes(const mc_layer_shape* shape);
 
 /* Bytes of the `ws` scratch buffer, including the 256-byte device status
- * block at its start and the attention backward's dS tiles
- * (mc_attention_backward_ws_bytes).  0 for an illegal shape. */
+ * block at its start and (unless MC_ATTN_DQ_RECOMPUTE) the attention
+ * backward's dS tiles (mc_attention_backward_ws_bytes).  0 for an illegal
+ * shape. */
 size_t mc_layer_workspace_bytes(const mc_layer_shape* shape);
 
 /* Forward pass.  x [T, h] fp32 in, y [T, h] fp32 out; fills `saved`.

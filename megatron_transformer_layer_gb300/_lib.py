@@ -32,6 +32,7 @@ MC_ACCUMULATE_GRADS = 1
 MC_RECOMPUTE_ACTIVATIONS = 2
 MC_SEQUENCE_PARALLEL = 4
 MC_FP8_HYBRID = 8
+MC_ATTN_DQ_RECOMPUTE = 16
 
 MC_EPI_STORE_F32 = 0
 MC_EPI_STORE_BF16 = 1

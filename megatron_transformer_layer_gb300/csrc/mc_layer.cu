@@ -65,7 +65,8 @@ namespace {
 
 struct Dims {
   int64_t b, s, T, h, H, d, a, f, t;
-  bool fp8;  // MC_FP8_HYBRID
+  bool fp8;       // MC_FP8_HYBRID
+  bool ds_tiles;  // the attention backward's dS tiles (not MC_ATTN_DQ_RECOMPUTE)
 };
 
 Dims dims_of(const mc_layer_shape& sh) {
@@ -80,6 +81,7 @@ Dims dims_of(const mc_layer_shape& sh) {
   D.f = sh.ffn_hidden;
   D.t = sh.tp_parts;
   D.fp8 = (sh.flags & MC_FP8_HYBRID) != 0;
+  D.ds_tiles = (sh.flags & MC_ATTN_DQ_RECOMPUTE) == 0;
   return D;
 }
 
@@ -89,7 +91,7 @@ int check_shape(const mc_layer_shape* sh) {
       sh->ffn_hidden <= 0 || sh->tp_parts <= 0 || sh->head_dim < 0)
     return MC_ERR_SHAPE;
   if ((sh->flags & ~(MC_ACCUMULATE_GRADS | MC_RECOMPUTE_ACTIVATIONS | MC_SEQUENCE_PARALLEL |
-                     MC_FP8_HYBRID)) != 0)
+                     MC_FP8_HYBRID | MC_ATTN_DQ_RECOMPUTE)) != 0)
     return MC_ERR_ARGUMENT;
   if ((sh->flags & MC_FP8_HYBRID) && (sh->flags & MC_SEQUENCE_PARALLEL)) return MC_ERR_ARGUMENT;
   const int t = sh->tp_parts;
@@ -200,7 +202,7 @@ Work plan_ws(const Dims& D, bool with_saved, void* p, size_t* bytes) {
   W.dO = c.take<uint16_t>(D.T * D.a);
   W.delta = c.take<float>(D.b * D.H * D.s);
   W.dqkv = c.take<uint16_t>(D.T * 3 * D.a);
-  W.ds = c.take<uint8_t>(attention_ds_workspace_bytes(D.b, D.s, D.H));
+  W.ds = D.ds_tiles ? c.take<uint8_t>(attention_ds_workspace_bytes(D.b, D.s, D.H)) : nullptr;
   const size_t ln_part = layernorm_backward_scratch_floats(D.T, static_cast<int>(D.h));
   int64_t widest = D.f > 3 * D.a ? D.f : 3 * D.a;
   if (D.h > widest) widest = D.h;

@@ -27,11 +27,14 @@ class TransformerLayer:
 
     def __init__(self, micro_batch, seq_len, hidden, heads, ffn_hidden, tp_parts=1, head_dim=0,
                  params=None, device="cuda", accumulate_grads=False, recompute=False,
-                 workspace=None, sequence_parallel=False, fp8=False):
+                 workspace=None, sequence_parallel=False, fp8=False, attn_dq_recompute=False):
+        # attn_dq_recompute: the attention backward forms S and dP again for
+        # dQ instead of keeping dS tiles (whose workspace grows as seq_len^2)
         flags = (L.MC_ACCUMULATE_GRADS if accumulate_grads else 0) | \
             (L.MC_RECOMPUTE_ACTIVATIONS if recompute else 0) | \
             (L.MC_SEQUENCE_PARALLEL if sequence_parallel else 0) | \
-            (L.MC_FP8_HYBRID if fp8 else 0)
+            (L.MC_FP8_HYBRID if fp8 else 0) | \
+            (L.MC_ATTN_DQ_RECOMPUTE if attn_dq_recompute else 0)
         self.shape = L.make_shape(micro_batch, seq_len, hidden, heads, ffn_hidden, tp_parts,
                                   head_dim, flags)
         _check(L.mc_layer_check_shape(self.shape), "mc_layer_check_shape")

@@ -64,7 +64,7 @@ def test_saved_bytes_cover_the_activations():
 
 
 def test_unknown_flag_rejected():
-    assert L.mc_layer_check_shape(L.make_shape(1, 8, 768, 12, 3072, 1, 0, 16)) == L.MC_ERR_ARGUMENT
+    assert L.mc_layer_check_shape(L.make_shape(1, 8, 768, 12, 3072, 1, 0, 32)) == L.MC_ERR_ARGUMENT
 
 
 def test_strerror_covers_all_codes():
@@ -200,7 +200,14 @@ def test_attention_ds_workspace_contract():
 
 def test_layer_workspace_holds_the_attention_ds_tiles():
     base = L.mc_layer_workspace_bytes(L.make_shape(1, 512, 1024, 8, 4096, 2))
-    assert base >= L.mc_attention_backward_ws_bytes(1, 512, 8, 128)
+    tiles = L.mc_attention_backward_ws_bytes(1, 512, 8, 128)
+    assert base >= tiles
+    # MC_ATTN_DQ_RECOMPUTE leaves the tiles out (up to the 256-byte carving)
+    lean = L.mc_layer_workspace_bytes(L.make_shape(1, 512, 1024, 8, 4096, 2, 0,
+                                                   L.MC_ATTN_DQ_RECOMPUTE))
+    assert lean > 0 and base - tiles - 256 <= lean <= base - tiles
+    assert L.mc_layer_check_shape(L.make_shape(1, 512, 1024, 8, 4096, 2, 0,
+                                               L.MC_ATTN_DQ_RECOMPUTE | L.MC_FP8_HYBRID)) == 0
 
 
 def test_fp8_quantize_2d_rejects_on_the_host():

@@ -22,8 +22,8 @@ def _oracle(inp, t):
     return O.layer_forward_backward(sh, inp.params_f64(), inp.f64("x"), inp.f64("dy"))
 
 
-def _check_layer(inp, t, label):
-    _, y, dx, G = run_layer(inp, t)
+def _check_layer(inp, t, label, layer=None):
+    _, y, dx, G = run_layer(inp, t, layer=layer)
     y_o, dx_o, G_o = _oracle(inp, t)
     floor = floor_norm_rel(inp.shape.with_tp(1), inp.params_f64(), inp.f64("x"), inp.f64("dy"),
                            exact=(y_o, dx_o, G_o))
@@ -140,6 +140,21 @@ def test_config2_stack_of_12_layers():
 def test_config3(t):
     """b8 s1024 h2048 H16 (d128) f8192."""
     _check_layer(make_layer_inputs(LayerShape(8, 1024, 2048, 16, 8192, t)), t, f"c3 t={t}")
+
+
+def test_attn_dq_recompute_flag_matches_oracle():
+    """MC_ATTN_DQ_RECOMPUTE: the attention backward without the dS tile
+    workspace (its dQ kernel forms S and dP again) -- both gates against the
+    oracle, the forward bitwise equal to the default mode, a workspace
+    smaller by the tiles."""
+    from megatron_transformer_layer_gb300.layer import TransformerLayer
+    shape = LayerShape(2, 129, 1024, 8, 4096, 2)
+    inp = make_layer_inputs(shape, seed=1, init=NONTRIVIAL_INIT)
+    lean = TransformerLayer(2, 129, 1024, 8, 4096, 2, attn_dq_recompute=True)
+    default, y0, _, _ = run_layer(inp)
+    assert lean.ws_bytes < default.ws_bytes
+    y1, _, _ = _check_layer(inp, 2, "attn dq recompute", layer=lean)
+    assert np.array_equal(y0, y1)
 
 
 def test_activation_recomputation_matches_default_mode():
