@@ -201,6 +201,15 @@ int mc_layer_backward(const mc_layer_shape* shape, const mc_layer_weights* w, co
  * MC_ERR_DEVICE_BOUNDS (or MC_ERR_CUDA if the synchronisation fails). */
 int mc_layer_device_status(const void* ws, void* stream);
 
+/* What this build of the library was compiled with, a bit mask:
+ * MC_BUILD_DEBUG (1) -- the -DMC_DEBUG index checks before every global
+ * store; MC_BUILD_NVTX (2) -- NVTX ranges around the layer's calls and
+ * each of their stages (F1..F7, B1..B7), for a profiler's timeline or its
+ * range filters. */
+#define MC_BUILD_DEBUG 1
+#define MC_BUILD_NVTX 2
+int mc_build_features(void);
+
 /* Static, human-readable text for a status code. */
 const char* mc_strerror(int code);
 

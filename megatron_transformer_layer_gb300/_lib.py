@@ -33,6 +33,8 @@ MC_RECOMPUTE_ACTIVATIONS = 2
 MC_SEQUENCE_PARALLEL = 4
 MC_FP8_HYBRID = 8
 MC_ATTN_DQ_RECOMPUTE = 16
+MC_BUILD_DEBUG = 1
+MC_BUILD_NVTX = 2
 
 MC_EPI_STORE_F32 = 0
 MC_EPI_STORE_BF16 = 1
@@ -95,6 +97,7 @@ _SIGNATURES = {
     "mc_attention_backward": (_INT, [_P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _P, _P]),
     "mc_attention_backward_noalloc": (_INT, [_P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _P, _P]),
     "mc_attention_backward_ws_bytes": (_SZ, [_I32, _I32, _I32, _I32]),
+    "mc_build_features": (_INT, []),
     "mc_attention_backward_ws": (_INT, [_P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _P, _SZ,
                                         _P, _P]),
     "mc_selftest_wait_timeout": (_INT, [_I64, _P, _P]),

@@ -6,7 +6,12 @@ megatron_transformer_layer_gb300.build`` (or ``build()``).  ``build(debug=True)`
 builds ``libmclayer_debug.so`` from the same sources with ``-DMC_DEBUG``: its
 kernels check the indices of every global store against their extents and
 record MC_ERR_DEVICE_BOUNDS instead of storing out of range (the binding
-loads it when MC_LAYER_DEBUG=1 is set).
+loads it when MC_LAYER_DEBUG=1 is set).  Both are compiled with
+``-DMC_NVTX``: the layer's calls open one NVTX range per stage (F1..F7,
+B1..B7, nested in ``mc_layer_forward`` / ``mc_layer_backward``), which a
+profiler can show or filter on (``ncu --nvtx --nvtx-include ...``);
+``build(nvtx=False)`` leaves them out.  NVTX v3 is header-only and costs a
+pointer test per range when no tool is attached.
 """
 from __future__ import annotations
 
@@ -49,7 +54,8 @@ def _compile(nvcc: str, src: str, extra: list[str], build_dir: str) -> str:
     return obj
 
 
-def build(verbose: bool = False, extra_flags: list[str] | None = None, debug: bool = False) -> str:
+def build(verbose: bool = False, extra_flags: list[str] | None = None, debug: bool = False,
+          nvtx: bool = True) -> str:
     """Compile and link the library (the debug variant with `debug`);
     returns its path."""
     nvcc = _nvcc()
@@ -57,7 +63,8 @@ def build(verbose: bool = False, extra_flags: list[str] | None = None, debug: bo
     lib_path = DEBUG_LIB_PATH if debug else LIB_PATH
     os.makedirs(build_dir, exist_ok=True)
     srcs = sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
-    extra = list(extra_flags or []) + (["-DMC_DEBUG"] if debug else [])
+    extra = list(extra_flags or []) + (["-DMC_DEBUG"] if debug else []) + \
+        (["-DMC_NVTX"] if nvtx else [])
     with concurrent.futures.ThreadPoolExecutor(max_workers=min(len(srcs), os.cpu_count() or 4)) as ex:
         objs = list(ex.map(lambda s: _compile(nvcc, s, extra, build_dir), srcs))
     libdir = _cuda_lib_dir(nvcc)

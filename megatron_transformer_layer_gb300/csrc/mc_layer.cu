@@ -324,6 +324,7 @@ constexpr int kE4M3 = 0, kE5M2 = 1;
 // pass -- and the GEMM's epilogue multiplies by the two inverse scales.
 int enqueue_forward_fp8(const Dims& D, const mc_layer_weights* w, const float* x, float* y,
                         const Saved& S, const Work& W, cudaStream_t st) {
+  StageRanges R("mc_layer_forward (fp8)");
   const int t = static_cast<int>(D.t);
   const int h = static_cast<int>(D.h);
   float* si = S.scale_inv;  // [ln1, o, ln2, g, w_qkv, w_o, w_fc1, w_fc2]
@@ -332,33 +333,41 @@ int enqueue_forward_fp8(const Dims& D, const mc_layer_weights* w, const float* x
     return launch_fp8_quantize_2d(in, bf16, rows, cols, kE4M3, out, out_t, sinv, W.partials, st);
   };
   // the weights, [out, in] as stored and transposed for the input gradients
+  R.next("F0 weights to E4M3");
   MC_TRY(quant(w->w_qkv, true, 3 * D.a, D.h, W.wqkv_q, S.wqkv_t, si + 4));
   MC_TRY(quant(w->w_o, true, D.h, D.a, W.wo_q, S.wo_t, si + 5));
   MC_TRY(quant(w->w_fc1, true, D.f, D.h, W.w1_q, S.w1_t, si + 6));
   MC_TRY(quant(w->w_fc2, true, D.h, D.f, W.w2_q, S.w2_t, si + 7));
   // F1  LN1, quantised
+  R.next("F1 LN1");
   MC_TRY(launch_layernorm_forward(x, w->ln1_g, w->ln1_b, S.ln1, S.mu1, S.rs1, D.T, h, W.status, st));
   MC_TRY(quant(S.ln1, true, D.T, D.h, W.ln1_q, S.ln1_t, si + 0));
   // F2  QKV
+  R.next("F2 QKV");
   MC_TRY(launch_gemm_fp8(D.T, 3 * D.a, D.h, W.ln1_q, D.h, kE4M3, W.wqkv_q, D.h, kE4M3, si + 0,
                          si + 4, S.qkv, 3 * D.a, MC_EPI_BIAS_BF16, w->b_qkv, nullptr, 0, 0, 1,
                          W.status, st));
   // F3  causal attention (bf16), O quantised
+  R.next("F3 causal attention");
   MC_TRY(launch_attention_forward(S.qkv, S.o, S.lse, static_cast<int>(D.b), static_cast<int>(D.s),
                                   static_cast<int>(D.H), static_cast<int>(D.d), W.status, st));
   MC_TRY(quant(S.o, true, D.T, D.a, W.o_q, S.o_t, si + 1));
   // F4  out-projection: partition partials summed in the accumulator, + b_o + x
+  R.next("F4 out-projection");
   MC_TRY(launch_gemm_fp8(D.T, D.h, D.a, W.o_q, D.a, kE4M3, W.wo_q, D.a, kE4M3, si + 1, si + 5,
                          S.x1, D.h, MC_EPI_BIAS_RESID_F32, w->b_o, x, D.h, 0, t, W.status, st));
   // F5  LN2, quantised
+  R.next("F5 LN2");
   MC_TRY(launch_layernorm_forward(S.x1, w->ln2_g, w->ln2_b, S.ln2, S.mu2, S.rs2, D.T, h, W.status,
                                   st));
   MC_TRY(quant(S.ln2, true, D.T, D.h, W.ln2_q, S.ln2_t, si + 2));
   // F6  fc1 + bias + GeLU; g quantised
+  R.next("F6 fc1");
   MC_TRY(launch_gemm_fp8(D.T, D.f, D.h, W.ln2_q, D.h, kE4M3, W.w1_q, D.h, kE4M3, si + 2, si + 6,
                          S.g, D.f, MC_EPI_BIAS_GELU, w->b_fc1, S.hp, D.f, 0, 1, W.status, st));
   MC_TRY(quant(S.g, true, D.T, D.f, W.g_q, S.g_t, si + 3));
   // F7  fc2: partials summed, + b_fc2 + x1
+  R.next("F7 fc2");
   MC_TRY(launch_gemm_fp8(D.T, D.h, D.f, W.g_q, D.f, kE4M3, W.w2_q, D.f, kE4M3, si + 3, si + 7, y,
                          D.h, MC_EPI_BIAS_RESID_F32, w->b_fc2, S.x1, D.h, 0, t, W.status, st));
   return MC_OK;
@@ -367,22 +376,27 @@ int enqueue_forward_fp8(const Dims& D, const mc_layer_weights* w, const float* x
 int enqueue_forward(const Dims& D, const mc_layer_weights* w, const float* x, float* y,
                     const Saved& S, const Work& W, bool sp, cudaStream_t st) {
   if (D.fp8) return enqueue_forward_fp8(D, w, x, y, S, W, st);
+  StageRanges R("mc_layer_forward");
   const int t = static_cast<int>(D.t);
   const int h = static_cast<int>(D.h);
   const Shards sh = shards_of(D, sp);
   // F1  LN1 (per shard)
+  R.next("F1 LN1");
   for (int64_t p = 0; p < sh.n; ++p) {
     const int64_t r0 = p * sh.rows;
     MC_TRY(launch_layernorm_forward(x + r0 * D.h, w->ln1_g, w->ln1_b, S.ln1 + r0 * D.h, S.mu1 + r0,
                                     S.rs1 + r0, sh.rows, h, W.status, st));
   }
   // F2  QKV (column-parallel: every partition's heads are output columns)
+  R.next("F2 QKV");
   MC_TRY(launch_gemm(D.T, 3 * D.a, D.h, S.ln1, D.h, 0, w->w_qkv, D.h, 0, S.qkv, 3 * D.a,
                      MC_EPI_BIAS_BF16, w->b_qkv, nullptr, 0, 0, 1, W.status, st));
   // F3  causal attention, local per head
+  R.next("F3 causal attention");
   MC_TRY(launch_attention_forward(S.qkv, S.o, S.lse, static_cast<int>(D.b), static_cast<int>(D.s),
                                   static_cast<int>(D.H), static_cast<int>(D.d), W.status, st));
   // F4  out-projection, row-parallel: partition partials summed in the
+  R.next("F4 out-projection");
   //     accumulator, then + b_o + x (per shard)
   for (int64_t p = 0; p < sh.n; ++p) {
     const int64_t r0 = p * sh.rows;
@@ -390,15 +404,18 @@ int enqueue_forward(const Dims& D, const mc_layer_weights* w, const float* x, fl
                        D.h, MC_EPI_BIAS_RESID_F32, w->b_o, x + r0 * D.h, D.h, 0, t, W.status, st));
   }
   // F5  LN2 (per shard)
+  R.next("F5 LN2");
   for (int64_t p = 0; p < sh.n; ++p) {
     const int64_t r0 = p * sh.rows;
     MC_TRY(launch_layernorm_forward(S.x1 + r0 * D.h, w->ln2_g, w->ln2_b, S.ln2 + r0 * D.h,
                                     S.mu2 + r0, S.rs2 + r0, sh.rows, h, W.status, st));
   }
   // F6  fc1 + bias + GeLU (column-parallel)
+  R.next("F6 fc1");
   MC_TRY(launch_gemm(D.T, D.f, D.h, S.ln2, D.h, 0, w->w_fc1, D.h, 0, S.g, D.f, MC_EPI_BIAS_GELU,
                      w->b_fc1, S.hp, D.f, 0, 1, W.status, st));
   // F7  fc2, row-parallel: partials summed, + b_fc2 + x1 (per shard)
+  R.next("F7 fc2");
   for (int64_t p = 0; p < sh.n; ++p) {
     const int64_t r0 = p * sh.rows;
     MC_TRY(launch_gemm(sh.rows, D.h, D.f, S.g + r0 * D.f, D.f, 0, w->w_fc2, D.f, 0, y + r0 * D.h,
@@ -414,6 +431,7 @@ int enqueue_forward(const Dims& D, const mc_layer_weights* w, const float* x, fl
 int enqueue_backward_fp8(const Dims& D, const mc_layer_weights* w, const float* x,
                          const float* dy, float* dx, const mc_layer_grads& G, const Saved& S,
                          const Work& W, int acc, cudaStream_t st) {
+  StageRanges R("mc_layer_backward (fp8)");
   const int t = static_cast<int>(D.t);
   const int h = static_cast<int>(D.h);
   const float* sf = S.scale_inv;  // [ln1, o, ln2, g, w_qkv, w_o, w_fc1, w_fc2]
@@ -423,6 +441,7 @@ int enqueue_backward_fp8(const Dims& D, const mc_layer_weights* w, const float* 
     return launch_fp8_quantize_2d(in, bf16, rows, cols, kE5M2, out, out_t, sinv, W.partials, st);
   };
   // B1  fc2: db2 = colsum(dy); dW2 = dy^T g; dhp = (dy W2) * gelu'(hp)
+  R.next("B1 fc2");
   MC_TRY(launch_colsum(dy, false, D.T, D.h, G.b_fc2, acc, nullptr, W.partials, W.status, st));
   MC_TRY(quant(dy, false, D.T, D.h, W.dy_q, W.dy_t, sb + 0));
   MC_TRY(launch_gemm_fp8(D.h, D.f, D.T, W.dy_t, D.T, kE5M2, S.g_t, D.T, kE4M3, sb + 0, sf + 3,
@@ -431,6 +450,7 @@ int enqueue_backward_fp8(const Dims& D, const mc_layer_weights* w, const float* 
   MC_TRY(launch_gemm_fp8(D.T, D.f, D.h, W.dy_q, D.h, kE5M2, S.w2_t, D.h, kE4M3, sb + 0, sf + 7,
                          W.dhp, D.f, MC_EPI_GELU_BWD, nullptr, S.hp, D.f, 0, 1, W.status, st));
   // B2  fc1: db1; dW1 = dhp^T ln2; dln2 = sum_p dhp_p W1_p
+  R.next("B2 fc1");
   MC_TRY(launch_colsum(W.dhp, true, D.T, D.f, G.b_fc1, acc, nullptr, W.partials, W.status, st));
   MC_TRY(quant(W.dhp, true, D.T, D.f, W.dhp_q, W.dhp_t, sb + 1));
   MC_TRY(launch_gemm_fp8(D.f, D.h, D.T, W.dhp_t, D.T, kE5M2, S.ln2_t, D.T, kE4M3, sb + 1, sf + 2,
@@ -439,19 +459,23 @@ int enqueue_backward_fp8(const Dims& D, const mc_layer_weights* w, const float* 
   MC_TRY(launch_gemm_fp8(D.T, D.h, D.f, W.dhp_q, D.f, kE5M2, S.w1_t, D.f, kE4M3, sb + 1, sf + 6,
                          W.dln, D.h, MC_EPI_STORE_F32, nullptr, nullptr, 0, 0, t, W.status, st));
   // B3  LN2 backward: dx1 = dy + LN2^T(dln2); dgamma2, dbeta2; db_o
+  R.next("B3 LN2 backward");
   MC_TRY(launch_layernorm_backward(W.dln, S.x1, S.mu2, S.rs2, w->ln2_g, dy, W.dx1, nullptr,
                                    G.ln2_g, G.ln2_b, G.b_o, acc, W.partials, D.T, h, W.status, st));
   MC_TRY(quant(W.dx1, false, D.T, D.h, W.dx1_q, W.dx1_t, sb + 2));
   // B4  out-projection: dWo = dx1^T O; dO = dx1 Wo
+  R.next("B4 out-projection");
   MC_TRY(launch_gemm_fp8(D.h, D.a, D.T, W.dx1_t, D.T, kE5M2, S.o_t, D.T, kE4M3, sb + 2, sf + 1,
                          G.w_o, D.a, MC_EPI_STORE_F32, nullptr, nullptr, 0, acc, 1, W.status, st));
   MC_TRY(launch_gemm_fp8(D.T, D.a, D.h, W.dx1_q, D.h, kE5M2, S.wo_t, D.h, kE4M3, sb + 2, sf + 5,
                          W.dO, D.a, MC_EPI_STORE_BF16, nullptr, nullptr, 0, 0, 1, W.status, st));
   // B5  attention backward (bf16) -> dQ | dK | dV
+  R.next("B5 attention backward");
   MC_TRY(launch_attention_backward(S.qkv, S.o, S.lse, W.dO, W.dqkv, W.delta, static_cast<int>(D.b),
                                    static_cast<int>(D.s), static_cast<int>(D.H),
                                    static_cast<int>(D.d), W.status, st, W.ds));
   // B6  QKV: db_qkv; dWqkv = dqkv^T ln1; dln1 = sum_p dqkv_p Wqkv_p
+  R.next("B6 QKV");
   MC_TRY(launch_colsum(W.dqkv, true, D.T, 3 * D.a, G.b_qkv, acc, nullptr, W.partials, W.status, st));
   MC_TRY(quant(W.dqkv, true, D.T, 3 * D.a, W.dqkv_q, W.dqkv_t, sb + 3));
   MC_TRY(launch_gemm_fp8(3 * D.a, D.h, D.T, W.dqkv_t, D.T, kE5M2, S.ln1_t, D.T, kE4M3, sb + 3,
@@ -461,6 +485,7 @@ int enqueue_backward_fp8(const Dims& D, const mc_layer_weights* w, const float* 
                          sb + 3, sf + 4, W.dln, D.h, MC_EPI_STORE_F32, nullptr, nullptr, 0, 0, t,
                          W.status, st));
   // B7  LN1 backward: dx = dx1 + LN1^T(dln1); dgamma1, dbeta1
+  R.next("B7 LN1 backward");
   MC_TRY(launch_layernorm_backward(W.dln, x, S.mu1, S.rs1, w->ln1_g, W.dx1, dx, nullptr, G.ln1_g,
                                    G.ln1_b, nullptr, acc, W.partials, D.T, h, W.status, st));
   return MC_OK;
@@ -522,10 +547,12 @@ int mc_layer_backward(const mc_layer_shape* shape, const mc_layer_weights* w, co
   // rest add).  Weight gradients and the column-parallel products read all
   // shards' rows, which lie side by side: the all-gather.
   if (D.fp8) return enqueue_backward_fp8(D, w, x, dy, dx, G, S, W, acc, st);
+  StageRanges R("mc_layer_backward");
   const Shards sh = shards_of(D, seq_parallel(*shape));
   auto shard_acc = [&](int64_t p) { return p == 0 ? acc : 1; };
 
   // B1  fc2: db2 = colsum(dy) (+ bf16 copy of dy as a GEMM operand),
+  R.next("B1 fc2");
   //     dW2 = dy^T g, dhp = (dy W2) * gelu'(hp)
   for (int64_t p = 0; p < sh.n; ++p) {
     const int64_t r0 = p * sh.rows;
@@ -537,6 +564,7 @@ int mc_layer_backward(const mc_layer_shape* shape, const mc_layer_weights* w, co
   MC_TRY(launch_gemm(D.T, D.f, D.h, W.dy16, D.h, 0, w->w_fc2, D.f, 1, W.dhp, D.f, MC_EPI_GELU_BWD,
                      nullptr, S.hp, D.f, 0, 1, W.status, st));
   // B2  fc1: db1, dW1 = dhp^T ln2, dln2 = sum_p dhp_p W1_p (partition sum in
+  R.next("B2 fc1");
   //     the accumulator; per shard in sequence-parallel mode)
   MC_TRY(launch_colsum(W.dhp, true, D.T, D.f, G.b_fc1, acc, nullptr, W.partials, W.status, st));
   MC_TRY(launch_gemm(D.f, D.h, D.T, W.dhp, D.f, 1, S.ln2, D.h, 1, G.w_fc1, D.h, MC_EPI_STORE_F32,
@@ -548,6 +576,7 @@ int mc_layer_backward(const mc_layer_shape* shape, const mc_layer_weights* w, co
                        st));
   }
   // B3  LN2 backward: dx1 = dy + LN2^T(dln2); dgamma2, dbeta2; db_o = colsum(dx1)
+  R.next("B3 LN2 backward");
   for (int64_t p = 0; p < sh.n; ++p) {
     const int64_t r0 = p * sh.rows;
     MC_TRY(launch_layernorm_backward(W.dln + r0 * D.h, S.x1 + r0 * D.h, S.mu2 + r0, S.rs2 + r0,
@@ -556,15 +585,18 @@ int mc_layer_backward(const mc_layer_shape* shape, const mc_layer_weights* w, co
                                      W.partials, sh.rows, h, W.status, st));
   }
   // B4  out-projection: dWo = dx1^T O, dO = dx1 Wo
+  R.next("B4 out-projection");
   MC_TRY(launch_gemm(D.h, D.a, D.T, W.dx1_16, D.h, 1, S.o, D.a, 1, G.w_o, D.a, MC_EPI_STORE_F32,
                      nullptr, nullptr, 0, acc, 1, W.status, st));
   MC_TRY(launch_gemm(D.T, D.a, D.h, W.dx1_16, D.h, 0, w->w_o, D.a, 1, W.dO, D.a, MC_EPI_STORE_BF16,
                      nullptr, nullptr, 0, 0, 1, W.status, st));
   // B5  attention backward -> dQ | dK | dV
+  R.next("B5 attention backward");
   MC_TRY(launch_attention_backward(S.qkv, S.o, S.lse, W.dO, W.dqkv, W.delta, static_cast<int>(D.b),
                                    static_cast<int>(D.s), static_cast<int>(D.H),
                                    static_cast<int>(D.d), W.status, st, W.ds));
   // B6  QKV: db_qkv, dWqkv = dqkv^T ln1, dln1 = sum_p dqkv_p Wqkv_p (per
+  R.next("B6 QKV");
   //     shard in sequence-parallel mode)
   MC_TRY(launch_colsum(W.dqkv, true, D.T, 3 * D.a, G.b_qkv, acc, nullptr, W.partials, W.status, st));
   MC_TRY(launch_gemm(3 * D.a, D.h, D.T, W.dqkv, 3 * D.a, 1, S.ln1, D.h, 1, G.w_qkv, D.h,
@@ -576,6 +608,7 @@ int mc_layer_backward(const mc_layer_shape* shape, const mc_layer_weights* w, co
                        W.status, st));
   }
   // B7  LN1 backward: dx = dx1 + LN1^T(dln1); dgamma1, dbeta1
+  R.next("B7 LN1 backward");
   for (int64_t p = 0; p < sh.n; ++p) {
     const int64_t r0 = p * sh.rows;
     MC_TRY(launch_layernorm_backward(W.dln + r0 * D.h, x + r0 * D.h, S.mu1 + r0, S.rs1 + r0,
@@ -656,6 +689,17 @@ int mc_attention_backward(const uint16_t* qkv, const uint16_t* o, const float* l
                           void* stream) {
   return launch_attention_backward(qkv, o, lse, dout, dqkv, delta, micro_batch, seq_len, heads,
                                    head_dim, status, static_cast<cudaStream_t>(stream));
+}
+
+int mc_build_features(void) {
+  int f = 0;
+#ifdef MC_DEBUG
+  f |= MC_BUILD_DEBUG;
+#endif
+#ifdef MC_NVTX
+  f |= MC_BUILD_NVTX;
+#endif
+  return f;
 }
 
 size_t mc_attention_backward_ws_bytes(int32_t micro_batch, int32_t seq_len, int32_t heads,

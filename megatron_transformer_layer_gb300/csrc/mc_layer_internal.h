@@ -11,6 +11,9 @@
 #endif
 
 #include <mutex>
+#ifdef MC_NVTX
+#include <nvtx3/nvToolsExt.h>
+#endif
 
 namespace mc {
 
@@ -110,6 +113,40 @@ inline cudaError_t once_per_device(PerDeviceInit& s, F&& init, long long* value 
   return s.err[dev];
 }
 #endif
+
+// NVTX ranges of the layer's launch sequence (compiled in with -DMC_NVTX):
+// one range for the call and, inside it, one per stage, each closing when
+// the next opens.  Host-side only; no effect on what is enqueued.
+class StageRanges {
+ public:
+  explicit StageRanges(const char* call) {
+#ifdef MC_NVTX
+    nvtxRangePushA(call);
+#else
+    (void)call;
+#endif
+  }
+  void next(const char* stage) {
+#ifdef MC_NVTX
+    if (open_) nvtxRangePop();
+    nvtxRangePushA(stage);
+    open_ = true;
+#else
+    (void)stage;
+#endif
+  }
+  ~StageRanges() {
+#ifdef MC_NVTX
+    if (open_) nvtxRangePop();
+    nvtxRangePop();
+#endif
+  }
+  StageRanges(const StageRanges&) = delete;
+  StageRanges& operator=(const StageRanges&) = delete;
+
+ private:
+  bool open_ = false;
+};
 
 #ifdef __CUDACC__
 // bf16 tensor map with 128-byte swizzle and zero fill; strides_bytes has

@@ -220,6 +220,19 @@ def test_fp8_quantize_2d_rejects_on_the_host():
                                       None) == L.MC_ERR_ARGUMENT
 
 
+def test_build_features():
+    """The release library carries the NVTX stage ranges and no index
+    checks; the debug library (if built) carries both."""
+    from megatron_transformer_layer_gb300 import build
+    f = L.lib().mc_build_features()
+    assert f & L.MC_BUILD_NVTX
+    if os.environ.get("MC_LAYER_DEBUG") != "1":
+        assert not f & L.MC_BUILD_DEBUG
+    if os.path.exists(build.DEBUG_LIB_PATH):
+        dbg = ctypes.CDLL(build.DEBUG_LIB_PATH)
+        assert dbg.mc_build_features() == L.MC_BUILD_DEBUG | L.MC_BUILD_NVTX
+
+
 def test_debug_library_exports_the_same_symbols():
     """libmclayer_debug.so (-DMC_DEBUG) is the same ABI."""
     from megatron_transformer_layer_gb300 import build
