@@ -250,6 +250,22 @@ def test_attention_long_sequence_many_heads():
     for o, lse, dqkv in runs[1:]:
         assert torch.equal(o, runs[0][0]) and torch.equal(lse, runs[0][1])
         assert torch.equal(dqkv, runs[0][2])
+    # the layer's backward (dQ from dS tiles): repeatable, dK and dV equal to
+    # the two-kernel path's, dQ checked on the sampled heads below
+    nbytes = L.mc_attention_backward_ws_bytes(b, s, H, d)
+    ws = torch.full((nbytes,), 0xFF, dtype=torch.uint8, device=DEV)
+    tiled = []
+    for _ in range(2):
+        dq2 = torch.full((b * s * 3 * a,), float("nan"), dtype=torch.bfloat16, device=DEV)
+        delta = torch.empty(b * H * s, dtype=torch.float32, device=DEV)
+        st = status()
+        assert L.mc_attention_backward_ws(qkv, runs[0][0], runs[0][1], dout, dq2, delta, b, s, H,
+                                          d, ws, nbytes, st) == 0
+        check_status(st)
+        tiled.append(dq2)
+    assert torch.equal(tiled[0], tiled[1])
+    assert torch.equal(tiled[0].view(s, 3 * a)[:, a:], runs[0][2].view(s, 3 * a)[:, a:])
+    g2 = to_f64(tiled[0]).reshape(s, 3 * a)
     o = to_f64(runs[0][0]).reshape(s, a)
     g = to_f64(runs[0][2]).reshape(s, 3 * a)
     do64 = bf16_bits_to_f64(dob).reshape(s, a)
@@ -261,6 +277,7 @@ def test_attention_long_sequence_many_heads():
         assert_close(f"attn_o head {hh}", o[:, c], o_ref)
         dq, dk, dv = O.causal_attention_backward(q, k, v, o_ref, lse_ref, do64[:, c])
         assert_close(f"dq head {hh}", g[:, c], dq)
+        assert_close(f"dq head {hh} (dS tiles)", g2[:, c], dq)
         assert_close(f"dk head {hh}", g[:, ck], dk)
         assert_close(f"dv head {hh}", g[:, cv], dv)
 
