@@ -34,10 +34,13 @@ struct AttnPart {
 };
 
 // ---------------------------------------------------------------- backward
-// Two kernels after the delta pre-pass, each keeping one 128-row operand
-// block resident and streaming the other side through TMA rings:
-//   dkdv: rows = keys (K, V resident; Q_i, dO_i streamed), accumulates dV, dK.
-//   dq:   rows = queries (Q, dO resident; K_j, V_j streamed), accumulates dQ.
+// Two kernels after the delta pre-pass:
+//   dkdv: rows = keys (K, V resident; Q_i, dO_i streamed), accumulates dV,
+//         dK and, given a dS workspace, writes each block pair's dS^T tile.
+//   dq:   rows = queries.  With the tiles, dQ = dS K streams them and K_j
+//         (attn_bwd_dq_gemm_kernel); without, Q and dO stay resident, K_j
+//         and V_j stream in, and S and dP are formed again
+//         (attn_bwd_dq_tc_kernel; also the context-parallel rectangles).
 template <int D>
 struct BwdCfg {
   static constexpr int kChunks = D / 64;
@@ -57,7 +60,9 @@ struct BwdCfg {
 //            registers), then dV += P^T_{i-1} dO_{i-1}, dK += dS^T_{i-1} Q_{i-1},
 //            then (those done) dP^T_i = V dO_i^T.
 //   compute  load S^T_i, release it; P^T = exp2(S^T c - lse2) while the MMAs
-//            above run; then load dP^T_i and form dS^T = P^T (dP^T - delta).
+//            above run; then load dP^T_i and form dS^T = P^T (dP^T - delta);
+//            with a dS workspace, also into the shared-memory tile image
+//            that one thread then sends out with a bulk store.
 // Each compute thread owns one key row and 64 query columns of dP^T, and
 // writes its P^T and dS^T (bf16 pairs) back over exactly those columns: the
 // 16 queries of group g (dP^T columns [16g, 16g + 16)) leave P at columns
