@@ -718,13 +718,18 @@ int launch_bwd_dkdv_tc(const CUtensorMap& tq, const CUtensorMap& td, const float
 }
 
 // dQ from the dS^T tiles that the dK/dV kernel wrote: dQ_i = sum_{j <= i}
-// dS_ij K_j, without forming S and dP again.  One CTA per (128-query block,
-// head, batch), heaviest first; 192 threads:
+// dS_ij K_j, without forming S and dP again.  Persistent: one CTA per SM
+// walks a share of the (128-query block, head, batch) items -- each head's
+// blocks heaviest first, handed out in a snake over the CTAs -- with its
+// ring and accumulators carried across items.  192 threads:
 //   warp 0      producer: per key block j the 32 KB dS^T tile (one bulk copy
-//               of its swizzled image) and K_j (TMA) into a 3-deep ring
-//   warp 1      TMEM (d columns) and the MMA thread: dQ += dS_ij K_j with A =
-//               dS (queries contiguous: MN-major) and B = K_j (MN-major)
-//   warps 2..5  epilogue: dQ / sqrt(d) as bf16 into the dQ columns of dqkv
+//               of its swizzled image) and K_j (TMA) into a 3-deep ring,
+//               running on into the next item's tiles without a gap
+//   warp 1      TMEM (two accumulators of 128 columns) and the MMA thread:
+//               dQ += dS_ij K_j with A = dS (queries contiguous: MN-major)
+//               and B = K_j (MN-major), the items alternating accumulators
+//   warps 2..5  epilogue: dQ / sqrt(d) as bf16 into the dQ columns of dqkv,
+//               while the next item accumulates into the other accumulator
 // The tiles are read once from HBM; the kernel is bound by that stream, not
 // by the 128 x 128 products.
 template <int D>
@@ -736,40 +741,54 @@ struct DqGemmCfg {
   static constexpr int kUsed = kStages * kStage + 16 * 8;
   static constexpr int kSmem = kUsed + 1024;  // + alignment slack
   static_assert(kSmem <= 227 * 1024, "dq gemm shared memory");
-  static constexpr uint32_t kTmemCols = D;  // 64 or 128
+  static constexpr uint32_t kTmemCols = 256;  // two accumulators of 128 columns
 };
+
+// Item r of CTA blockIdx.x (snake over the dispatch order): query block,
+// head and batch; false once the CTA's share is done.
+__device__ __forceinline__ bool dq_item(int r, int nb, int H, int n_items, int& qb, int& hh,
+                                        int& bi) {
+  const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+  const int64_t k = static_cast<int64_t>(r) * G + ((r & 1) ? G - 1 - c : c);
+  if (k >= n_items) return false;
+  qb = nb - 1 - static_cast<int>(k % nb);  // heaviest first within a head
+  const int rest = static_cast<int>(k / nb);
+  hh = rest % H;
+  bi = rest / H;
+  return true;
+}
 
 template <int D>
 __global__ void __launch_bounds__(192, 1)
     attn_bwd_dq_gemm_kernel(const __grid_constant__ CUtensorMap tm_qkv,
                             const uint8_t* __restrict__ ds_tiles, uint16_t* __restrict__ dqkv,
-                            int s, int H, int* status) {
+                            int s, int H, int n_items, int* status) {
   using C = DqGemmCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStage);
-  uint64_t* full = bars + 0;   // [3]
-  uint64_t* empty = bars + 3;  // [3]
-  uint64_t* acc_full = bars + 6;
-  uint64_t* drain = bars + 7;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 8);
+  uint64_t* full = bars + 0;       // [3]
+  uint64_t* empty = bars + 3;      // [3]
+  uint64_t* acc_full = bars + 6;   // [2]  an item's dQ is complete in accumulator a
+  uint64_t* acc_empty = bars + 8;  // [2]  the epilogue has read accumulator a (128 threads)
+  uint64_t* drain = bars + 10;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 11);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int a = H * D;
   const int nb = (s + 127) / 128;
-  const int qb = nb - 1 - static_cast<int>(blockIdx.x);  // heaviest first
-  const int hh = blockIdx.y, bi = blockIdx.z;
-  const int count = qb + 1;  // key blocks 0 .. qb
-  const int64_t tile0 = (static_cast<int64_t>(bi) * H + hh) * (static_cast<int64_t>(nb) * (nb + 1) / 2) +
-                        static_cast<int64_t>(qb) * (qb + 1) / 2;
+  const int64_t ntri = static_cast<int64_t>(nb) * (nb + 1) / 2;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kStages; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
     }
-    mbar_init(acc_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], 128);
+    }
     mbar_init(drain, 1);
     fence_mbar_init();
     tma_prefetch_desc(&tm_qkv);
@@ -787,66 +806,85 @@ __global__ void __launch_bounds__(192, 1)
   if (warp == 0) {
     if (lane == 0) {
       // -------------------------------------------------------- producer
-      int issued = 0;
-      for (int j = 0; j < count; ++j) {
-        const int st = j % C::kStages;
-        if (!mbar_wait(&empty[st], ((j / C::kStages) & 1) ^ 1u, status, kSiteAttention)) break;
-        uint8_t* dst = smem + st * C::kStage;
-        mbar_arrive_expect_tx(&full[st], C::kStage);
-        bulk_load(dst, ds_tiles + (tile0 + j) * kDsTileBytes, static_cast<uint32_t>(kDsTileBytes),
-                  &full[st]);
-        for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d(dst + kDsTileBytes + c * 16384, &tm_qkv, &full[st], a + hh * D + c * 64,
-                      j * 128, bi);
-        ++issued;
+      int gt = 0;  // tiles issued, across items
+      bool ok = true;
+      int qb, hh, bi;
+      for (int r = 0; ok && dq_item(r, nb, H, n_items, qb, hh, bi); ++r) {
+        const int64_t tile0 = (static_cast<int64_t>(bi) * H + hh) * ntri +
+                              static_cast<int64_t>(qb) * (qb + 1) / 2;
+        for (int j = 0; j <= qb; ++j, ++gt) {
+          const int st = gt % C::kStages;
+          if (!mbar_wait(&empty[st], ((gt / C::kStages) & 1) ^ 1u, status, kSiteAttention)) {
+            ok = false;
+            break;
+          }
+          uint8_t* dst = smem + st * C::kStage;
+          mbar_arrive_expect_tx(&full[st], C::kStage);
+          bulk_load(dst, ds_tiles + (tile0 + j) * kDsTileBytes,
+                    static_cast<uint32_t>(kDsTileBytes), &full[st]);
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_load_3d(dst + kDsTileBytes + c * 16384, &tm_qkv, &full[st], a + hh * D + c * 64,
+                        j * 128, bi);
+        }
       }
       pdl_launch();  // every load of this CTA is issued
-      for (int j = issued - 1; j >= 0 && j >= issued - C::kStages; --j)
-        mbar_wait(&full[j % C::kStages], (j / C::kStages) & 1, status, kSiteAttention, 200000000ull,
-                  false);
+      for (int g = gt - 1; g >= 0 && g >= gt - C::kStages; --g)
+        mbar_wait(&full[g % C::kStages], (g / C::kStages) & 1, status, kSiteAttention,
+                  200000000ull, false);
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // -------------------------------------------------------- MMA issuer
       constexpr uint32_t kIdesc = idesc_bf16_f32(128, D, true, true);
       bool ok = true;
-      for (int j = 0; j < count; ++j) {
-        const int st = j % C::kStages;
-        if (!mbar_wait(&full[st], (j / C::kStages) & 1, status, kSiteAttention)) {
-          ok = false;
-          break;
-        }
+      int gt = 0, qb, hh, bi;
+      for (int r = 0; ok && dq_item(r, nb, H, n_items, qb, hh, bi); ++r) {
+        const int acc = r & 1;
+        // the epilogue of item r - 2 has read this accumulator
+        if (!mbar_wait(&acc_empty[acc], ((r >> 1) & 1) ^ 1u, status, kSiteAttention)) break;
         tc_fence_after();
-        const uint32_t ab = smem_u32(smem + st * C::kStage);
-        const uint32_t kbase = ab + static_cast<uint32_t>(kDsTileBytes);
+        const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * 128);
+        for (int j = 0; j <= qb; ++j, ++gt) {
+          const int st = gt % C::kStages;
+          if (!mbar_wait(&full[st], (gt / C::kStages) & 1, status, kSiteAttention)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t ab = smem_u32(smem + st * C::kStage);
+          const uint32_t kbase = ab + static_cast<uint32_t>(kDsTileBytes);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          // 16 keys per step: 16 rows of 128 B in both MN-major operands;
-          // 64-wide query (A) or d (B) chunks 16 KB apart
-          umma_bf16(tmem, smem_desc_sw128(ab + kk * 2048, 16384, 1024),
-                    smem_desc_sw128(kbase + kk * 2048, 16384, 1024), kIdesc,
-                    (j > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < 8; ++kk) {
+            // 16 keys per step: 16 rows of 128 B in both MN-major operands;
+            // 64-wide query (A) or d (B) chunks 16 KB apart
+            umma_bf16(d_tmem, smem_desc_sw128(ab + kk * 2048, 16384, 1024),
+                      smem_desc_sw128(kbase + kk * 2048, 16384, 1024), kIdesc,
+                      (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(&empty[st]);
         }
-        umma_commit(&empty[st]);
+        if (ok) umma_commit(&acc_full[acc]);
       }
-      if (ok) umma_commit(acc_full);
       umma_commit(drain);
       mbar_wait(drain, 0, status, kSiteAttention, 200000000ull, false);
     }
   } else {
     // ---------------------------------------------------------- epilogue
     const int quarter = warp & 3;
-    const int r = qb * 128 + quarter * 32 + lane;  // this thread's query row
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    if (mbar_wait_warp(acc_full, 0, status, kSiteAttention)) {
+    const float scale = rsqrtf(static_cast<float>(D));
+    int qb, hh, bi;
+    for (int r = 0; dq_item(r, nb, H, n_items, qb, hh, bi); ++r) {
+      const int acc = r & 1;
+      if (!mbar_wait_warp(&acc_full[acc], (r >> 1) & 1, status, kSiteAttention)) break;
       tc_fence_after();
-      const float scale = rsqrtf(static_cast<float>(D));
-      const int64_t base = (static_cast<int64_t>(bi) * s + r) * 3 * static_cast<int64_t>(a);
+      const int row = qb * 128 + quarter * 32 + lane;  // this thread's query row
+      const int64_t base = (static_cast<int64_t>(bi) * s + row) * 3 * static_cast<int64_t>(a);
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         float v[32];
-        tmem_ld_32x32b_x32(tmem + lane_off + c * 32, v);
-        if (r < s && MC_DCHECK(r >= 0 && hh * D + c * 32 + 32 <= a, status, kSiteAttention)) {
+        tmem_ld_32x32b_x32(tmem + static_cast<uint32_t>(acc * 128) + lane_off + c * 32, v);
+        if (row < s && MC_DCHECK(row >= 0 && hh * D + c * 32 + 32 <= a, status, kSiteAttention)) {
           uint4* dst = reinterpret_cast<uint4*>(dqkv + base + hh * D + c * 32);
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
@@ -859,6 +897,8 @@ __global__ void __launch_bounds__(192, 1)
           }
         }
       }
+      tc_fence_before();
+      mbar_arrive(&acc_empty[acc]);  // the accumulator may take the item after next
     }
   }
 
@@ -880,8 +920,11 @@ int launch_bwd_dq_gemm(const CUtensorMap& tq, const uint8_t* ds_tiles, uint16_t*
     return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   });
   if (attr != cudaSuccess) return MC_ERR_CUDA;
-  dim3 grid((s + 127) / 128, H, b);
-  launch_kernel(kern, grid, dim3(192), C::kSmem, st, 1, tq, ds_tiles, dqkv, s, H, status);
+  const int64_t n_items = static_cast<int64_t>((s + 127) / 128) * H * b;
+  if (n_items > 0x7fffffff) return MC_ERR_UNSUPPORTED;
+  const int grid = static_cast<int>(n_items < num_sms() ? n_items : num_sms());
+  launch_kernel(kern, dim3(grid), dim3(192), C::kSmem, st, 1, tq, ds_tiles, dqkv, s, H,
+                static_cast<int>(n_items), status);
   return cudaGetLastError() == cudaSuccess ? MC_OK : MC_ERR_CUDA;
 }
 
