@@ -6,7 +6,7 @@
 // 1 when amax is 0), q = round-to-nearest-even of x * scale (fp32 product),
 // saturated to +-fmax (E4M3: 448, E5M2: 57344), and scale_inv = 1 / scale for
 // the GEMM epilogue.
-//   amax_partial_kernel  grid-stride |x| maxima, one per block
+//   amax_partial_kernel  grid-stride |x| maxima (16-byte loads), one per block
 //   fp8_scale_kernel     one block: the maximum of the partials, scale, scale_inv
 //   fp8_cast_kernel      x * scale -> 8-bit, 8 elements per thread step
 // The maximum is order-independent, so the result is deterministic.
@@ -28,15 +28,45 @@ __device__ __forceinline__ float load_elem(const void* in, bool bf16, int64_t i)
               : static_cast<const float*>(in)[i];
 }
 
+// |x| maximum of one 16-byte vector: 8 bf16 or 4 fp32 values.
+template <bool BF16>
+__device__ __forceinline__ float vec_absmax(uint4 v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  float m = 0.f;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    if constexpr (BF16) {
+      m = fmaxf(m, fmaxf(fabsf(bf16_lo(w[k])), fabsf(bf16_hi(w[k]))));
+    } else {
+      m = fmaxf(m, fabsf(__uint_as_float(w[k])));
+    }
+  }
+  return m;
+}
+
+// Grid-stride |x| maxima, one per block: 16-byte loads, four in flight per
+// thread, then the n % (elements per vector) tail element by element.
 template <bool BF16>
 __global__ void amax_partial_kernel(const void* __restrict__ in, int64_t n,
                                     float* __restrict__ partials) {
   pdl_wait();  // the previous kernel on the stream has completed
   pdl_launch();
-  float m = 0.f;
+  constexpr int kPerVec = BF16 ? 8 : 4;
+  const uint4* __restrict__ vin = static_cast<const uint4*>(in);
+  const int64_t nv = n / kPerVec;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n; i += stride)
-    m = fmaxf(m, fabsf(load_elem(in, BF16, i)));
+  int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+  float m = 0.f;
+  for (; i + 3 * stride < nv; i += 4 * stride) {
+    const uint4 a = __ldg(vin + i), b = __ldg(vin + i + stride), c = __ldg(vin + i + 2 * stride),
+                d = __ldg(vin + i + 3 * stride);
+    m = fmaxf(m, fmaxf(fmaxf(vec_absmax<BF16>(a), vec_absmax<BF16>(b)),
+                       fmaxf(vec_absmax<BF16>(c), vec_absmax<BF16>(d))));
+  }
+  for (; i < nv; i += stride) m = fmaxf(m, vec_absmax<BF16>(__ldg(vin + i)));
+  for (int64_t j = nv * kPerVec + blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+       j < n; j += stride)
+    m = fmaxf(m, fabsf(load_elem(in, BF16, j)));
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
   __shared__ float wm[kThreadsPerBlock / 32];
