@@ -404,18 +404,25 @@ int mc_gemm_fp8(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_t lda, 
  * gives every rank the same causal work.  In ring step t rank r holds the K/V
  * chunks of rank (r - t) mod cp_parts and computes, for each of its query
  * chunks i and each held key chunk j <= i, the partial attention of chunk i
- * over chunk j (causal mask inside the diagonal pair); the partials of a
- * query chunk are merged with the log-sum-exp rule.  On one GPU the K/V
- * exchange is the read of the other chunk's rows, and all ranks' partials of
- * a step run as kernels on `stream` in schedule order.  Results equal
- * mc_attention_forward / _backward up to fp32 rounding of the merge.
+ * over chunk j (causal mask inside the diagonal pair).  Each partial is
+ * folded into running fp32 results as soon as it is computed: a query
+ * chunk's O and log-sum-exp by the log-sum-exp rule, its dQ and a key
+ * chunk's dK, dV by addition; a chunk's last pair writes the bf16 result.
+ * On one GPU the K/V exchange is the read of the other chunk's rows, and
+ * all ranks' partials of a step run as kernels on `stream` in schedule
+ * order.  Results equal mc_attention_forward / _backward up to the fp32
+ * rounding of the merges and sums (to the bit for a chunk with one pair:
+ * O, lse and dQ of chunk 0, dK and dV of the last chunk).
  *
  * Requirements: cp_parts >= 1, seq_len a multiple of 256 * cp_parts,
  * head_dim 64 or 128; the caller-owned workspace of
- * mc_attention_cp_workspace_bytes bytes (16-byte aligned) holds the fp32
- * partials (chunk pairs x micro_batch x c x 3a floats plus the partial lse).
- * Errors as mc_attention_forward, plus MC_ERR_SHAPE for an unsupported
- * seq_len / cp_parts pair and MC_ERR_WORKSPACE for a short workspace. */
+ * mc_attention_cp_workspace_bytes bytes (16-byte aligned) holds the running
+ * sums (micro_batch x seq_len x 3a floats) and one chunk pair's bf16 dS^T
+ * tiles (micro_batch x heads x (c / 128)^2 tiles of 128 x 128); its size
+ * does not grow with cp_parts.  Forward and backward may share it; it must
+ * not be shared with a concurrent call.  Errors as mc_attention_forward,
+ * plus MC_ERR_SHAPE for an unsupported seq_len / cp_parts pair and
+ * MC_ERR_WORKSPACE for a short workspace. */
 
 /* The pairs (query chunk, key chunk) that virtual rank `rank` computes in
  * ring step `step`: writes up to 4 pairs as pairs[2k] = query chunk,
@@ -434,8 +441,8 @@ int mc_attention_forward_cp(const uint16_t* qkv, uint16_t* o, float* lse, int32_
 
 /* Same results and layouts as mc_attention_backward: each pair's dQ, dK, dV
  * use the merged lse and delta = rowsum(dO * O); a chunk's dQ is the sum of
- * its pairs' (key chunks in order), a chunk's dK and dV the sum over the
- * query chunks that saw it (in order), each summed in fp32. */
+ * its pairs', a chunk's dK and dV the sum over the query chunks that saw it,
+ * each summed in fp32 in schedule order (deterministic). */
 int mc_attention_backward_cp(const uint16_t* qkv, const uint16_t* o, const float* lse,
                              const uint16_t* dout, uint16_t* dqkv, float* delta,
                              int32_t micro_batch, int32_t seq_len, int32_t heads,

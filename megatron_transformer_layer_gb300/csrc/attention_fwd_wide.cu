@@ -1,6 +1,7 @@
 // Causal flash attention forward with 256-key blocks (sm_103a, tcgen05),
 // over the whole score matrix or over one rectangle of it (the
-// context-parallel path: fp32 partial O and its log-sum-exp, merged later).
+// context-parallel path: each rectangle merges its O and log-sum-exp into
+// the rows' running fp32 result).
 //
 // S_j = Q K_j^T runs as 128 x 256 x 16 MMAs, which keep the tensor pipe
 // busier per instruction than 128 x 128 ones (the shared-memory operand
@@ -68,14 +69,18 @@ struct WideCfg {
 // A rectangle of the causal score matrix: query rows [base, base + len)
 // (whole 128-row tiles) against keys [key_lo, key_hi) (key_lo a multiple of
 // 128).  The whole matrix is {0, s, 0, INT_MAX} and writes bf16 O and the
-// fp32 log-sum-exp; a partial rectangle (the context-parallel path) writes
-// the fp32 O normalised over its own keys and that log-sum-exp, indexed by
-// the row within the rectangle: out [b, len, a], lse [b, H, len].
+// fp32 log-sum-exp.  A partial rectangle (the context-parallel path) merges
+// its O and log-sum-exp into the rows' running ones by the log-sum-exp rule:
+// `out` [b, s, a] holds O normalised over the keys seen so far, `lse2`
+// [b, H, s] their log2-sum-exp (indexed by the absolute row).  Without
+// kCpAccMerge in `mode` there is nothing to merge with; with kCpAccFinal
+// the merged result goes to the kernel's bf16 O and natural-log lse.
 struct WideRect {
   int base, len;
   int key_lo, key_hi;
   float* out;
-  float* lse;
+  float* lse2;
+  int mode;
 };
 
 template <int D, bool PART>
@@ -363,26 +368,41 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     }
     if (__all_sync(0xffffffffu, ok) && mbar_wait_warp(o_final, 0, status, kSiteAttention)) {
       tc_fence_after();
+      float run_l2 = 0.f;  // the rows' running log2-sum-exp
+      const bool merge = PART && (rect.mode & kCpAccMerge);
+      const int64_t lrow = (static_cast<int64_t>(bi) * H + hh) * s + q;
+      // Both halves read it before either passes the exchange below, after
+      // which half 0 may overwrite it.
+      if (merge && q < s) run_l2 = rect.lse2[lrow];
       l += exchange(l);  // both halves' sums, taken against the same max
       const float inv = 1.f / l;
       if constexpr (PART) {
-        const int qr = q - rect.base;
-        float* orow = rect.out + (static_cast<int64_t>(bi) * rect.len + qr) * a + hh * D;
+        // this rectangle's log2-sum-exp m + log2(l), merged with the running one
+        float l2 = m + log2f(l), c_new = inv, c_old = 0.f;
+        if (merge) {
+          const float mx = fmaxf(run_l2, l2);
+          l2 = mx + log2f(fast_exp2(run_l2 - mx) + fast_exp2(l2 - mx));
+          c_old = fast_exp2(run_l2 - l2);
+          c_new = fast_exp2(m - l2);  // = exp2(this rectangle's l2 - merged l2) / l
+        }
+        const bool final = rect.mode & kCpAccFinal;
+        const int64_t row_off = (static_cast<int64_t>(bi) * s + q) * a + hh * D;
 #pragma unroll 1
         for (int c = half * (D / 64); c < (half + 1) * (D / 64); ++c) {
           float v[32];
           tmem_ld_32x32b_x32(tO + lane_off + c * 32, v);
-          if (q < s && MC_DCHECK(qr >= 0 && qr < rect.len && hh * D + c * 32 + 32 <= a, status,
-                                 kSiteAttention)) {
-            float4* dst = reinterpret_cast<float4*>(orow + c * 32);
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-              dst[i] = make_float4(v[4 * i] * inv, v[4 * i + 1] * inv, v[4 * i + 2] * inv,
-                                   v[4 * i + 3] * inv);
-          }
+          if (q < s && MC_DCHECK(q - rect.base >= 0 && q - rect.base < rect.len &&
+                                     hh * D + c * 32 + 32 <= a,
+                                 status, kSiteAttention))
+            accumulate_row32(v, c_new, c_old, rect.out + row_off + c * 32,
+                             out + row_off + c * 32, merge, final);
         }
-        if (q < s && half == 0)
-          rect.lse[(static_cast<int64_t>(bi) * H + hh) * rect.len + qr] = (m + log2f(l)) * kLn2;
+        if (q < s && half == 0) {
+          if (final)
+            lse[lrow] = l2 * kLn2;
+          else
+            rect.lse2[lrow] = l2;
+        }
       } else {
         uint16_t* orow = out + (static_cast<int64_t>(bi) * s + q) * a + hh * D;
 #pragma unroll 1
@@ -440,20 +460,23 @@ int launch_wide(const uint16_t* qkv, uint16_t* o, float* lse, int b, int s, int 
 
 int launch_attention_forward_wide(const uint16_t* qkv, uint16_t* o, float* lse, int b, int s,
                                   int H, int d, int* status, cudaStream_t st) {
-  const WideRect whole = {0, s, 0, INT_MAX, nullptr, nullptr};
+  const WideRect whole = {0, s, 0, INT_MAX, nullptr, nullptr, 0};
   return d == 64 ? launch_wide<64, false>(qkv, o, lse, b, s, H, status, st, whole)
                  : launch_wide<128, false>(qkv, o, lse, b, s, H, status, st, whole);
 }
 
-int launch_attention_forward_part(const uint16_t* qkv, int b, int s, int H, int d, int q_base,
-                                  int q_len, int kb_lo, int kb_hi, float* part_o, float* part_lse,
-                                  int* status, cudaStream_t st) {
-  if (q_base % 128 || q_len % 128 || q_len < 128 || kb_lo < 0 || kb_hi <= kb_lo)
+int launch_attention_forward_part(const uint16_t* qkv, uint16_t* o, float* lse, int b, int s,
+                                  int H, int d, int q_base, int q_len, int kb_lo, int kb_hi,
+                                  float* acc_o, float* acc_lse2, int mode, int* status,
+                                  cudaStream_t st) {
+  // Every query tile must see at least one key block: kb_lo * 128 <= q_base.
+  if (q_base % 128 || q_len % 128 || q_len < 128 || q_base + q_len > s || kb_lo < 0 ||
+      kb_hi <= kb_lo || static_cast<int64_t>(kb_lo) * 128 > q_base)
     return MC_ERR_ARGUMENT;
   const WideRect rect = {q_base, q_len, kb_lo * 128,
-                         kb_hi > INT_MAX / 128 ? INT_MAX : kb_hi * 128, part_o, part_lse};
-  return d == 64 ? launch_wide<64, true>(qkv, nullptr, nullptr, b, s, H, status, st, rect)
-                 : launch_wide<128, true>(qkv, nullptr, nullptr, b, s, H, status, st, rect);
+                         kb_hi > INT_MAX / 128 ? INT_MAX : kb_hi * 128, acc_o, acc_lse2, mode};
+  return d == 64 ? launch_wide<64, true>(qkv, o, lse, b, s, H, status, st, rect)
+                 : launch_wide<128, true>(qkv, o, lse, b, s, H, status, st, rect);
 }
 
 }  // namespace mc

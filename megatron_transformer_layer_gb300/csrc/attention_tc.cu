@@ -22,15 +22,16 @@ constexpr int64_t kDsTileBytes = 128 * 128 * 2;  // one bf16 dS^T tile (128 keys
 // A rectangle of the causal score matrix, for the context-parallel path:
 // dQ takes query rows [base, base + len) against key blocks [blk_lo, blk_hi);
 // dK/dV take key rows [base, base + len) against query blocks
-// [blk_lo, blk_hi).  Results go to fp32 partials indexed by the row within
-// the rectangle: dQ [b, len, a]; dK | dV [b, len, 2a].  The fused kernels
-// use the whole matrix (base 0, len s, blocks [0, INT_MAX)) and ignore the
-// partials.
+// [blk_lo, blk_hi).  Results are added to running fp32 sums indexed by the
+// absolute row, `acc`: dQ [b, s, a]; dK | dV [b, s, 2a].  Without
+// kCpAccMerge in `mode` there is no earlier sum to add; with kCpAccFinal the
+// sum goes to dqkv as bf16 instead.  The fused kernels use the whole matrix
+// (base 0, len s, blocks [0, INT_MAX)) and no sums.
 struct AttnPart {
   int base, len;
   int blk_lo, blk_hi;
-  float* out;
-  float* lse;
+  float* acc;
+  int mode;
 };
 
 // ---------------------------------------------------------------- backward
@@ -38,9 +39,9 @@ struct AttnPart {
 //   dkdv: rows = keys (K, V resident; Q_i, dO_i streamed), accumulates dV,
 //         dK and, given a dS workspace, writes each block pair's dS^T tile.
 //   dq:   rows = queries.  With the tiles, dQ = dS K streams them and K_j
-//         (attn_bwd_dq_gemm_kernel); without, Q and dO stay resident, K_j
-//         and V_j stream in, and S and dP are formed again
-//         (attn_bwd_dq_tc_kernel; also the context-parallel rectangles).
+//         (attn_bwd_dq_gemm_kernel; also the context-parallel rectangles);
+//         without, Q and dO stay resident, K_j and V_j stream in, and S and
+//         dP are formed again (attn_bwd_dq_tc_kernel).
 template <int D>
 struct BwdCfg {
   static constexpr int kChunks = D / 64;
@@ -304,7 +305,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // 128 B, the 16-byte unit of queries [8u, 8u + 8) at unit u ^ (t & 7).
       // It is assembled in sDs (conflict-free 16-byte writes) and leaves as
       // one bulk store; the previous block's store must have read sDs first.
-      const bool store_ds = !PART && ds_tiles != nullptr;
+      const bool store_ds = ds_tiles != nullptr;
       uint8_t* ds_row = sDs + half * 16384 + t * 128;
       if (store_ds && i > 0) {
         if (threadIdx.x == 64) {
@@ -358,11 +359,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             break;
           }
           if (lane == 0) {
+            // the whole matrix: the lower triangle of (query block, key block)
+            // pairs per head; a rectangle: its nq x nk pairs per head
             const int qb = qb0 + i;
+            const int nq = part.blk_hi - part.blk_lo, nk = part.len / 128;
+            const int kr = kb - part.base / 128;
             const int64_t tile =
-                (static_cast<int64_t>(bi) * H + hh) * (static_cast<int64_t>(nblk) * (nblk + 1) / 2) +
-                static_cast<int64_t>(qb) * (qb + 1) / 2 + kb;
-            if (MC_DCHECK(kb <= qb && qb < nblk, status, kSiteAttention)) {
+                PART ? ((static_cast<int64_t>(bi) * H + hh) * nq + (qb - part.blk_lo)) * nk + kr
+                     : (static_cast<int64_t>(bi) * H + hh) *
+                               (static_cast<int64_t>(nblk) * (nblk + 1) / 2) +
+                           static_cast<int64_t>(qb) * (qb + 1) / 2 + kb;
+            const bool in_rect =
+                PART ? qb >= part.blk_lo && qb < part.blk_hi && kr >= 0 && kr < nk : true;
+            if (MC_DCHECK(kb <= qb && qb < nblk && in_rect, status, kSiteAttention)) {
               bulk_store(ds_tiles + tile * kDsTileBytes, sDs, static_cast<uint32_t>(kDsTileBytes));
               bulk_commit();
             }
@@ -371,7 +380,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
     }
     // the tile stores must be complete (and done with sDs) before exit
-    if (!PART && ds_tiles && threadIdx.x == 64) bulk_wait_all();
+    if (ds_tiles && threadIdx.x == 64) bulk_wait_all();
     if (ok && mbar_wait_warp(acc_done, (count - 1) & 1, status, kSiteAttention)) {
       tc_fence_after();
       const float scale = rsqrtf(static_cast<float>(D));
@@ -390,14 +399,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               r >= 0 && col + c * 32 + 32 <= 3 * a && (!PART || r - part.base < part.len), status,
               kSiteAttention);
           if (PART && r < s && in_range) {
-            // fp32 partials of this rectangle: dK at [0, a), dV at [a, 2a)
-            float4* dst = reinterpret_cast<float4*>(
-                part.out + (static_cast<int64_t>(bi) * part.len + (r - part.base)) * 2 * a +
-                (w == 0 ? a : 0) + hh * D + c * 32);
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-              dst[k] = make_float4(v[4 * k] * mul, v[4 * k + 1] * mul, v[4 * k + 2] * mul,
-                                   v[4 * k + 3] * mul);
+            // the running sums: dK at [0, a), dV at [a, 2a) of the key's row
+            float* run = part.acc + (static_cast<int64_t>(bi) * s + r) * 2 * a +
+                         (w == 0 ? a : 0) + hh * D + c * 32;
+            accumulate_row32(v, mul, 1.f, run, dqkv + base + col + c * 32,
+                             part.mode & kCpAccMerge, part.mode & kCpAccFinal);
           } else if (!PART && r < s && in_range) {
             uint4* dst = reinterpret_cast<uint4*>(dqkv + base + col + c * 32);
 #pragma unroll
@@ -440,12 +446,12 @@ struct DqCfg {
 // (s_free), so S_{j+1} = Q K_{j+1}^T and dP_{j+1} = dO V_{j+1}^T run while
 // dS_j is formed; dQ += dS_j K_j follows when dS_j is in TMEM (ds_full), and
 // its completion (ds_free) lets dS_{j+1} be written.
-template <int D, bool PART>
+template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv,
                           const __grid_constant__ CUtensorMap tm_do, const float* __restrict__ lse,
                           const float* __restrict__ delta, uint16_t* __restrict__ dqkv, int s,
-                          int H, int* status, const AttnPart part) {
+                          int H, int* status) {
   using C = DqCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -472,11 +478,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int a = H * D;
   const int hh = blockIdx.y, bi = blockIdx.z;
-  // heaviest first; fused: query blocks 0 .. nblk - 1 against key blocks 0 .. qb
-  const int qb = part.base / 128 + static_cast<int>(gridDim.x - 1 - blockIdx.x);
+  // heaviest first: query blocks 0 .. nblk - 1 against key blocks 0 .. qb
+  const int qb = static_cast<int>(gridDim.x - 1 - blockIdx.x);
   const int q0 = qb * 128;
-  const int kb0 = part.blk_lo;
-  const int count = min(qb + 1, part.blk_hi) - kb0;  // key blocks kb0 .. kb0 + count - 1
+  const int count = qb + 1;  // key blocks 0 .. qb
 
   if (threadIdx.x == 0) {
     mbar_init(r_full, 1);
@@ -523,13 +528,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_arrive_expect_tx(&k_full[ks], C::kTile);
         for (int c = 0; c < C::kChunks; ++c)
           tma_load_3d(sK[ks] + c * 16384, &tm_qkv, &k_full[ks], a + hh * D + c * 64,
-                      (kb0 + j) * 128, bi);
+                      j * 128, bi);
         ++k_issued;
         if (!mbar_wait(&v_empty[vs], vph ^ 1u, status, kSiteAttention)) break;
         mbar_arrive_expect_tx(&v_full[vs], C::kTile);
         for (int c = 0; c < C::kChunks; ++c)
           tma_load_3d(sV[vs] + c * 16384, &tm_qkv, &v_full[vs], 2 * a + hh * D + c * 64,
-                      (kb0 + j) * 128,
+                      j * 128,
                       bi);
         ++v_issued;
       }
@@ -611,7 +616,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(s_free);
-      const int c0 = (kb0 + j) * 128 + half * 64;
+      const int c0 = j * 128 + half * 64;
       const bool edge = c0 + 63 > q0 || c0 + 64 > s;
       uint32_t dw[32];
       const float2 sc2 = make_float2(scale2, scale2), nl2 = make_float2(-my_l2, -my_l2);
@@ -648,18 +653,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         float v[32];
         tmem_ld_32x32b_x32(tdQ + lane_off + c * 32, v);
         const bool in_range =
-            MC_DCHECK(r >= 0 && hh * D + c * 32 + 32 <= a && (!PART || r - part.base < part.len),
-                      status, kSiteAttention);
-        if (PART && r < s && in_range) {
-          // fp32 partial dQ of this rectangle
-          float4* dst = reinterpret_cast<float4*>(
-              part.out + (static_cast<int64_t>(bi) * part.len + (r - part.base)) * a + hh * D +
-              c * 32);
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            dst[k] = make_float4(v[4 * k] * scale, v[4 * k + 1] * scale, v[4 * k + 2] * scale,
-                                 v[4 * k + 3] * scale);
-        } else if (!PART && r < s && in_range) {
+            MC_DCHECK(r >= 0 && hh * D + c * 32 + 32 <= a, status, kSiteAttention);
+        if (r < s && in_range) {
           uint4* dst = reinterpret_cast<uint4*>(dqkv + base + hh * D + c * 32);
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
@@ -683,20 +678,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 }
 
-template <int D, bool PART>
+template <int D>
 int launch_bwd_dq_tc(const CUtensorMap& tq, const CUtensorMap& td, const float* lse,
                      const float* delta, uint16_t* dqkv, int b, int s, int H, int* status,
-                     cudaStream_t st, const AttnPart& part) {
+                     cudaStream_t st) {
   using C = DqCfg<D>;
-  auto kern = attn_bwd_dq_tc_kernel<D, PART>;
+  auto kern = attn_bwd_dq_tc_kernel<D>;
   static PerDeviceInit init;
   const cudaError_t attr = once_per_device(init, [&](long long*) {
     return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   });
   if (attr != cudaSuccess) return MC_ERR_CUDA;
-  dim3 grid(PART ? part.len / 128 : (s + 127) / 128, H, b);
+  dim3 grid((s + 127) / 128, H, b);
   launch_kernel(kern, dim3(grid), dim3(kBwdThreads), C::kSmem, st, 1, tq, td, lse, delta, dqkv, s,
-                H, status, part);
+                H, status);
   return cudaGetLastError() == cudaSuccess ? MC_OK : MC_ERR_CUDA;
 }
 
@@ -731,7 +726,9 @@ int launch_bwd_dkdv_tc(const CUtensorMap& tq, const CUtensorMap& td, const float
 //   warps 2..5  epilogue: dQ / sqrt(d) as bf16 into the dQ columns of dqkv,
 //               while the next item accumulates into the other accumulator
 // The tiles are read once from HBM; the kernel is bound by that stream, not
-// by the 128 x 128 products.
+// by the 128 x 128 products.  The whole matrix reads each head's lower
+// triangle of tiles; a context-parallel rectangle (PART) the nq x nk tiles
+// that the dK/dV kernel wrote for it, adding dQ to the running fp32 sums.
 template <int D>
 struct DqGemmCfg {
   static constexpr int kChunks = D / 64;
@@ -744,25 +741,34 @@ struct DqGemmCfg {
   static constexpr uint32_t kTmemCols = 256;  // two accumulators of 128 columns
 };
 
-// Item r of CTA blockIdx.x (snake over the dispatch order): query block,
-// head and batch; false once the CTA's share is done.
-__device__ __forceinline__ bool dq_item(int r, int nb, int H, int n_items, int& qb, int& hh,
+// Query blocks [q_lo, q_lo + nq) against key blocks [k_lo, k_lo + nk)
+// (key blocks past a query block are not visible); `acc` and `mode` as in
+// AttnPart.  The whole matrix is {0, nb, 0, nb}.
+struct DqRect {
+  int q_lo, nq, k_lo, nk;
+  float* acc;
+  int mode;
+};
+
+// Item r of CTA blockIdx.x (snake over the dispatch order): query block
+// (rectangle-relative), head and batch; false once the CTA's share is done.
+__device__ __forceinline__ bool dq_item(int r, int nq, int H, int n_items, int& qr, int& hh,
                                         int& bi) {
   const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
   const int64_t k = static_cast<int64_t>(r) * G + ((r & 1) ? G - 1 - c : c);
   if (k >= n_items) return false;
-  qb = nb - 1 - static_cast<int>(k % nb);  // heaviest first within a head
-  const int rest = static_cast<int>(k / nb);
+  qr = nq - 1 - static_cast<int>(k % nq);  // heaviest first within a head
+  const int rest = static_cast<int>(k / nq);
   hh = rest % H;
   bi = rest / H;
   return true;
 }
 
-template <int D>
+template <int D, bool PART>
 __global__ void __launch_bounds__(192, 1)
     attn_bwd_dq_gemm_kernel(const __grid_constant__ CUtensorMap tm_qkv,
                             const uint8_t* __restrict__ ds_tiles, uint16_t* __restrict__ dqkv,
-                            int s, int H, int n_items, int* status) {
+                            int s, int H, int n_items, int* status, const DqRect rect) {
   using C = DqGemmCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -779,6 +785,14 @@ __global__ void __launch_bounds__(192, 1)
   const int a = H * D;
   const int nb = (s + 127) / 128;
   const int64_t ntri = static_cast<int64_t>(nb) * (nb + 1) / 2;
+  const int nq = rect.nq;
+  // key blocks rect.k_lo .. + n_keys(qb) - 1 and the first tile of an item
+  auto n_keys = [&](int qb) { return PART ? min(rect.nk, qb + 1 - rect.k_lo) : qb + 1; };
+  auto first_tile = [&](int qr, int hh, int bi) {
+    const int qb = rect.q_lo + qr;
+    return PART ? ((static_cast<int64_t>(bi) * H + hh) * nq + qr) * rect.nk
+                : (static_cast<int64_t>(bi) * H + hh) * ntri + static_cast<int64_t>(qb) * (qb + 1) / 2;
+  };
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kStages; ++i) {
@@ -808,11 +822,11 @@ __global__ void __launch_bounds__(192, 1)
       // -------------------------------------------------------- producer
       int gt = 0;  // tiles issued, across items
       bool ok = true;
-      int qb, hh, bi;
-      for (int r = 0; ok && dq_item(r, nb, H, n_items, qb, hh, bi); ++r) {
-        const int64_t tile0 = (static_cast<int64_t>(bi) * H + hh) * ntri +
-                              static_cast<int64_t>(qb) * (qb + 1) / 2;
-        for (int j = 0; j <= qb; ++j, ++gt) {
+      int qr, hh, bi;
+      for (int r = 0; ok && dq_item(r, nq, H, n_items, qr, hh, bi); ++r) {
+        const int64_t tile0 = first_tile(qr, hh, bi);
+        const int nj = n_keys(rect.q_lo + qr);
+        for (int j = 0; j < nj; ++j, ++gt) {
           const int st = gt % C::kStages;
           if (!mbar_wait(&empty[st], ((gt / C::kStages) & 1) ^ 1u, status, kSiteAttention)) {
             ok = false;
@@ -824,7 +838,7 @@ __global__ void __launch_bounds__(192, 1)
                     static_cast<uint32_t>(kDsTileBytes), &full[st]);
           for (int c = 0; c < C::kChunks; ++c)
             tma_load_3d(dst + kDsTileBytes + c * 16384, &tm_qkv, &full[st], a + hh * D + c * 64,
-                        j * 128, bi);
+                        (rect.k_lo + j) * 128, bi);
         }
       }
       pdl_launch();  // every load of this CTA is issued
@@ -837,14 +851,15 @@ __global__ void __launch_bounds__(192, 1)
       // -------------------------------------------------------- MMA issuer
       constexpr uint32_t kIdesc = idesc_bf16_f32(128, D, true, true);
       bool ok = true;
-      int gt = 0, qb, hh, bi;
-      for (int r = 0; ok && dq_item(r, nb, H, n_items, qb, hh, bi); ++r) {
+      int gt = 0, qr, hh, bi;
+      for (int r = 0; ok && dq_item(r, nq, H, n_items, qr, hh, bi); ++r) {
+        const int nj = n_keys(rect.q_lo + qr);
         const int acc = r & 1;
         // the epilogue of item r - 2 has read this accumulator
         if (!mbar_wait(&acc_empty[acc], ((r >> 1) & 1) ^ 1u, status, kSiteAttention)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * 128);
-        for (int j = 0; j <= qb; ++j, ++gt) {
+        for (int j = 0; j < nj; ++j, ++gt) {
           const int st = gt % C::kStages;
           if (!mbar_wait(&full[st], (gt / C::kStages) & 1, status, kSiteAttention)) {
             ok = false;
@@ -873,27 +888,33 @@ __global__ void __launch_bounds__(192, 1)
     const int quarter = warp & 3;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const float scale = rsqrtf(static_cast<float>(D));
-    int qb, hh, bi;
-    for (int r = 0; dq_item(r, nb, H, n_items, qb, hh, bi); ++r) {
+    int qr, hh, bi;
+    for (int r = 0; dq_item(r, nq, H, n_items, qr, hh, bi); ++r) {
       const int acc = r & 1;
       if (!mbar_wait_warp(&acc_full[acc], (r >> 1) & 1, status, kSiteAttention)) break;
       tc_fence_after();
-      const int row = qb * 128 + quarter * 32 + lane;  // this thread's query row
+      const int row = (rect.q_lo + qr) * 128 + quarter * 32 + lane;  // this thread's query row
       const int64_t base = (static_cast<int64_t>(bi) * s + row) * 3 * static_cast<int64_t>(a);
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         float v[32];
         tmem_ld_32x32b_x32(tmem + static_cast<uint32_t>(acc * 128) + lane_off + c * 32, v);
         if (row < s && MC_DCHECK(row >= 0 && hh * D + c * 32 + 32 <= a, status, kSiteAttention)) {
-          uint4* dst = reinterpret_cast<uint4*>(dqkv + base + hh * D + c * 32);
+          if constexpr (PART) {
+            float* run = rect.acc + (static_cast<int64_t>(bi) * s + row) * a + hh * D + c * 32;
+            accumulate_row32(v, scale, 1.f, run, dqkv + base + hh * D + c * 32,
+                             rect.mode & kCpAccMerge, rect.mode & kCpAccFinal);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(dqkv + base + hh * D + c * 32);
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            uint4 wv;
-            wv.x = pack_bf16x2(v[8 * k + 0] * scale, v[8 * k + 1] * scale);
-            wv.y = pack_bf16x2(v[8 * k + 2] * scale, v[8 * k + 3] * scale);
-            wv.z = pack_bf16x2(v[8 * k + 4] * scale, v[8 * k + 5] * scale);
-            wv.w = pack_bf16x2(v[8 * k + 6] * scale, v[8 * k + 7] * scale);
-            dst[k] = wv;
+            for (int k = 0; k < 4; ++k) {
+              uint4 wv;
+              wv.x = pack_bf16x2(v[8 * k + 0] * scale, v[8 * k + 1] * scale);
+              wv.y = pack_bf16x2(v[8 * k + 2] * scale, v[8 * k + 3] * scale);
+              wv.z = pack_bf16x2(v[8 * k + 4] * scale, v[8 * k + 5] * scale);
+              wv.w = pack_bf16x2(v[8 * k + 6] * scale, v[8 * k + 7] * scale);
+              dst[k] = wv;
+            }
           }
         }
       }
@@ -910,37 +931,43 @@ __global__ void __launch_bounds__(192, 1)
   }
 }
 
-template <int D>
+template <int D, bool PART>
 int launch_bwd_dq_gemm(const CUtensorMap& tq, const uint8_t* ds_tiles, uint16_t* dqkv, int b,
-                       int s, int H, int* status, cudaStream_t st) {
+                       int s, int H, const DqRect& rect, int* status, cudaStream_t st) {
   using C = DqGemmCfg<D>;
-  auto kern = attn_bwd_dq_gemm_kernel<D>;
+  auto kern = attn_bwd_dq_gemm_kernel<D, PART>;
   static PerDeviceInit init;
   const cudaError_t attr = once_per_device(init, [&](long long*) {
     return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   });
   if (attr != cudaSuccess) return MC_ERR_CUDA;
-  const int64_t n_items = static_cast<int64_t>((s + 127) / 128) * H * b;
+  const int64_t n_items = static_cast<int64_t>(rect.nq) * H * b;
   if (n_items > 0x7fffffff) return MC_ERR_UNSUPPORTED;
   const int grid = static_cast<int>(n_items < num_sms() ? n_items : num_sms());
   launch_kernel(kern, dim3(grid), dim3(192), C::kSmem, st, 1, tq, ds_tiles, dqkv, s, H,
-                static_cast<int>(n_items), status);
+                static_cast<int>(n_items), status, rect);
   return cudaGetLastError() == cudaSuccess ? MC_OK : MC_ERR_CUDA;
 }
 
 // Tensor maps over Q|K|V [b, s, 3a] and dO [b, s, a] with 64 x 128 boxes.
-bool make_bwd_maps(CUtensorMap* tq, CUtensorMap* td, const uint16_t* qkv, const uint16_t* dout,
-                   int b, int s, int a_) {
+bool make_qkv_map(CUtensorMap* tq, const uint16_t* qkv, int b, int s, int a_) {
   const uint64_t a = static_cast<uint64_t>(a_);
   const uint32_t box[3] = {64, 128, 1};
   const uint64_t dq[3] = {3 * a, static_cast<uint64_t>(s), static_cast<uint64_t>(b)};
   const uint64_t sq[2] = {3 * a * 2, 3 * a * 2 * static_cast<uint64_t>(s)};
-  const uint64_t dd[3] = {a, static_cast<uint64_t>(s), static_cast<uint64_t>(b)};
-  const uint64_t sd[2] = {a * 2, a * 2 * static_cast<uint64_t>(s)};
-  return make_tmap_bf16(tq, qkv, 3, dq, sq, box) && make_tmap_bf16(td, dout, 3, dd, sd, box);
+  return make_tmap_bf16(tq, qkv, 3, dq, sq, box);
 }
 
-constexpr AttnPart kWhole = {0, 0, 0, 0x7fffffff, nullptr, nullptr};
+bool make_bwd_maps(CUtensorMap* tq, CUtensorMap* td, const uint16_t* qkv, const uint16_t* dout,
+                   int b, int s, int a_) {
+  const uint64_t a = static_cast<uint64_t>(a_);
+  const uint32_t box[3] = {64, 128, 1};
+  const uint64_t dd[3] = {a, static_cast<uint64_t>(s), static_cast<uint64_t>(b)};
+  const uint64_t sd[2] = {a * 2, a * 2 * static_cast<uint64_t>(s)};
+  return make_qkv_map(tq, qkv, b, s, a_) && make_tmap_bf16(td, dout, 3, dd, sd, box);
+}
+
+constexpr AttnPart kWhole = {0, 0, 0, 0x7fffffff, nullptr, 0};
 
 // With `ds_tiles` (attention_ds_workspace_bytes of device memory) the dK/dV
 // kernel also writes dS^T and dQ is its product with K; without, the dQ
@@ -954,8 +981,12 @@ int launch_bwd_tc(const uint16_t* qkv, const float* lse, const uint16_t* dout, u
   int rc = launch_bwd_dkdv_tc<D, false>(tq, td, lse, delta, dqkv, b, s, H, status, st, kWhole,
                                         ds_tiles);
   if (rc != MC_OK) return rc;
-  if (ds_tiles) return launch_bwd_dq_gemm<D>(tq, ds_tiles, dqkv, b, s, H, status, st);
-  return launch_bwd_dq_tc<D, false>(tq, td, lse, delta, dqkv, b, s, H, status, st, kWhole);
+  if (ds_tiles) {
+    const int nb = (s + 127) / 128;
+    const DqRect whole = {0, nb, 0, nb, nullptr, 0};
+    return launch_bwd_dq_gemm<D, false>(tq, ds_tiles, dqkv, b, s, H, whole, status, st);
+  }
+  return launch_bwd_dq_tc<D>(tq, td, lse, delta, dqkv, b, s, H, status, st);
 }
 
 }  // namespace
@@ -972,26 +1003,41 @@ int launch_attention_backward_tc(const uint16_t* qkv, const float* lse, const ui
                  : launch_bwd_tc<128>(qkv, lse, dout, dqkv, delta, b, s, H, status, st, ds_tiles);
 }
 
-int launch_attention_dq_part(const uint16_t* qkv, const float* lse, const uint16_t* dout,
-                             const float* delta, int b, int s, int H, int d, int q_base, int q_len,
-                             int kb_lo, int kb_hi, float* part_dq, int* status, cudaStream_t st) {
-  CUtensorMap tq, td;
-  if (!make_bwd_maps(&tq, &td, qkv, dout, b, s, H * d)) return MC_ERR_CUDA;
-  const AttnPart part = {q_base, q_len, kb_lo, kb_hi, part_dq, nullptr};
-  return d == 64 ? launch_bwd_dq_tc<64, true>(tq, td, lse, delta, nullptr, b, s, H, status, st, part)
-                 : launch_bwd_dq_tc<128, true>(tq, td, lse, delta, nullptr, b, s, H, status, st, part);
+int64_t attention_cp_tile_bytes(int64_t b, int64_t H, int64_t nq, int64_t nk) {
+  return b * H * nq * nk * kDsTileBytes;
 }
 
 int launch_attention_dkdv_part(const uint16_t* qkv, const float* lse, const uint16_t* dout,
-                               const float* delta, int b, int s, int H, int d, int k_base,
-                               int k_len, int qb_lo, int qb_hi, float* part_dkv, int* status,
-                               cudaStream_t st) {
+                               const float* delta, uint16_t* dqkv, int b, int s, int H, int d,
+                               int k_base, int k_len, int qb_lo, int qb_hi, float* acc_dkv,
+                               uint8_t* ds_tiles, int mode, int* status, cudaStream_t st) {
+  // whole 128-row key blocks inside the sequence; every key block sees at
+  // least one query block (qb_lo * 128 >= k_base)
+  if (k_base % 128 || k_len % 128 || k_len < 128 || k_base + k_len > s || qb_lo < 0 ||
+      qb_hi <= qb_lo || static_cast<int64_t>(qb_hi) * 128 > s ||
+      static_cast<int64_t>(qb_lo) * 128 < k_base)
+    return MC_ERR_ARGUMENT;
   CUtensorMap tq, td;
   if (!make_bwd_maps(&tq, &td, qkv, dout, b, s, H * d)) return MC_ERR_CUDA;
-  const AttnPart part = {k_base, k_len, qb_lo, qb_hi, part_dkv, nullptr};
-  return d == 64
-             ? launch_bwd_dkdv_tc<64, true>(tq, td, lse, delta, nullptr, b, s, H, status, st, part)
-             : launch_bwd_dkdv_tc<128, true>(tq, td, lse, delta, nullptr, b, s, H, status, st, part);
+  const AttnPart part = {k_base, k_len, qb_lo, qb_hi, acc_dkv, mode};
+  return d == 64 ? launch_bwd_dkdv_tc<64, true>(tq, td, lse, delta, dqkv, b, s, H, status, st,
+                                                part, ds_tiles)
+                 : launch_bwd_dkdv_tc<128, true>(tq, td, lse, delta, dqkv, b, s, H, status, st,
+                                                 part, ds_tiles);
+}
+
+int launch_attention_dq_part(const uint16_t* qkv, const uint8_t* ds_tiles, uint16_t* dqkv, int b,
+                             int s, int H, int d, int qb_lo, int nq, int kb_lo, int nk,
+                             float* acc_dq, int mode, int* status, cudaStream_t st) {
+  // every query block sees at least one key block (qb_lo >= kb_lo)
+  if (qb_lo < 0 || nq < 1 || kb_lo < 0 || nk < 1 || qb_lo < kb_lo ||
+      static_cast<int64_t>(qb_lo + nq) * 128 > s || static_cast<int64_t>(kb_lo + nk) * 128 > s)
+    return MC_ERR_ARGUMENT;
+  CUtensorMap tq;
+  if (!make_qkv_map(&tq, qkv, b, s, H * d)) return MC_ERR_CUDA;
+  const DqRect rect = {qb_lo, nq, kb_lo, nk, acc_dq, mode};
+  return d == 64 ? launch_bwd_dq_gemm<64, true>(tq, ds_tiles, dqkv, b, s, H, rect, status, st)
+                 : launch_bwd_dq_gemm<128, true>(tq, ds_tiles, dqkv, b, s, H, rect, status, st);
 }
 
 }  // namespace mc

@@ -510,6 +510,44 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// 32 values of one row added to a running fp32 sum (the context-parallel
+// rectangles): x = c_new v + (merge ? c_old run : 0), written back to `run`,
+// or, for the row's last share (`final`), as bf16 to `out` instead.  `run`
+// and `out` are 16-byte aligned.
+__device__ __forceinline__ void accumulate_row32(const float* v, float c_new, float c_old,
+                                                 float* run, uint16_t* out, bool merge,
+                                                 bool final) {
+  float x[32];
+  if (merge) {
+    const float4* src = reinterpret_cast<const float4*>(run);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float4 o = src[k];
+      x[4 * k + 0] = fmaf(c_old, o.x, c_new * v[4 * k + 0]);
+      x[4 * k + 1] = fmaf(c_old, o.y, c_new * v[4 * k + 1]);
+      x[4 * k + 2] = fmaf(c_old, o.z, c_new * v[4 * k + 2]);
+      x[4 * k + 3] = fmaf(c_old, o.w, c_new * v[4 * k + 3]);
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 32; ++k) x[k] = c_new * v[k];
+  }
+  if (final) {
+    uint4* dst = reinterpret_cast<uint4*>(out);
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      dst[k] = make_uint4(pack_bf16x2(x[8 * k + 0], x[8 * k + 1]),
+                          pack_bf16x2(x[8 * k + 2], x[8 * k + 3]),
+                          pack_bf16x2(x[8 * k + 4], x[8 * k + 5]),
+                          pack_bf16x2(x[8 * k + 6], x[8 * k + 7]));
+  } else {
+    float4* dst = reinterpret_cast<float4*>(run);
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      dst[k] = make_float4(x[4 * k + 0], x[4 * k + 1], x[4 * k + 2], x[4 * k + 3]);
+  }
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 

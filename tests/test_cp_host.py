@@ -51,10 +51,15 @@ def test_schedule_rejects_bad_arguments():
 
 
 def test_workspace_bytes():
+    """Running fp32 sums for the whole sequence ([b, s, 3a]) plus one chunk
+    pair's bf16 dS^T tiles ([b, H, c/128, c/128] x 128 x 128): the size does
+    not grow with the number of CP partitions."""
     b, s, H, d, cp = 2, 2048, 4, 128, 4
-    C, c, a = 2 * cp, s // (2 * cp), H * d
-    pairs = C * (C + 1) // 2
-    assert L.mc_attention_cp_workspace_bytes(b, s, H, d, cp) == pairs * b * c * 3 * a * 4
+    c, a = s // (2 * cp), H * d
+    tiles = b * H * (c // 128) ** 2 * 128 * 128 * 2
+    assert L.mc_attention_cp_workspace_bytes(b, s, H, d, cp) == b * s * 3 * a * 4 + tiles
+    sizes = [L.mc_attention_cp_workspace_bytes(1, 8192, 8, 128, k) for k in (1, 2, 4, 8)]
+    assert sizes == sorted(sizes, reverse=True)
     assert L.mc_attention_cp_workspace_bytes(b, 2048 + 128, H, d, cp) == 0  # chunk not whole tiles
     assert L.mc_attention_cp_workspace_bytes(b, s, H, 96, cp) == 0
     assert L.mc_attention_cp_workspace_bytes(b, s, H, d, 0) == 0

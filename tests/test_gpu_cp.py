@@ -100,3 +100,35 @@ def test_cp_attention_long_sequence_against_fused_and_oracle():
         assert_close(f"cp o head {hh}", og[:, :, cs[0]], o_ref[:, :, cs[0]])
         for name, c in zip(("dq", "dk", "dv"), cs):
             assert_close(f"cp {name} head {hh}", gg[:, :, c], g_ref[:, :, c])
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_cp_single_pair_chunks_equal_fused_bitwise(d):
+    """A chunk whose result comes from one chunk pair is computed by the same
+    blocks in the same order as in the fused kernels, so it matches them bit
+    for bit: O and LSE of chunk 0 (its only pair is the diagonal one), and,
+    given the same O and LSE, dQ of chunk 0 and dK, dV of the last chunk."""
+    b, s, H, cp = 1, 2048, 3, 2
+    a, c = H * d, s // (2 * cp)
+    qb = bits(b * s * 3 * a, 44, std=1.8)
+    dob = bits(b * s * a, 45)
+    o, lse, dqkv = _run_cp(qb, dob, b, s, H, d, cp)
+    qkv, dout = dev_bf16(qb), dev_bf16(dob)
+    of, lf = torch.empty_like(o), torch.empty_like(lse)
+    st = status()
+    assert L.mc_attention_forward(qkv, of, lf, b, s, H, d, st) == 0
+    nbytes = L.mc_attention_backward_ws_bytes(b, s, H, d)
+    ds = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+    gf = torch.full_like(dqkv, float("nan"))
+    delta = torch.empty_like(lse)
+    # the fused backward from the context-parallel forward's O and LSE
+    assert L.mc_attention_backward_ws(qkv, o, lse, dout, gf, delta, b, s, H, d, ds, nbytes,
+                                      st) == 0
+    check_status(st)
+    assert torch.equal(o.view(s, a)[:c], of.view(s, a)[:c])
+    assert torch.equal(lse.view(H, s)[:, :c], lf.view(H, s)[:, :c])
+    g, gfv = dqkv.view(s, 3 * a), gf.view(s, 3 * a)
+    assert torch.equal(g[:c, :a], gfv[:c, :a])
+    assert torch.equal(g[s - c:, a:], gfv[s - c:, a:])
+    # and the rest agrees to rounding
+    assert_close("cp vs fused dqkv", to_f64(dqkv), to_f64(gf))
