@@ -19,8 +19,10 @@ namespace {
 // ---------------------------------------------------------------- backward
 // delta[b, h, i] = sum_c dO[i, h*D + c] * O[i, h*D + c].  D/8 threads share a
 // (token, head) row, each loading 16 bytes of O and of dO; rows are taken
-// head-major (token fastest), so a block's delta stores are contiguous, and
-// each thread handles kDeltaPasses rows with all their loads issued first.
+// token-major (head fastest), so row r starts at element r * D of both
+// [T, a] arrays and a block streams one contiguous range of each (the
+// scattered 4-byte delta stores are 1/(2D) of the traffic and merge in L2),
+// and each thread handles kDeltaPasses rows with all their loads issued first.
 constexpr int kDeltaThreads = 256;
 constexpr int kDeltaPasses = 4;
 
@@ -39,16 +41,15 @@ __global__ void __launch_bounds__(kDeltaThreads)
   constexpr int RPP = kDeltaThreads / TPR;    // rows per pass of the block
   const int sub = static_cast<int>(threadIdx.x) % TPR;
   const int64_t rows = T * H;
-  const int64_t a = static_cast<int64_t>(H) * D;
   const int64_t r0 = blockIdx.x * delta_rows_per_block<D>() + threadIdx.x / TPR;
   uint4 xo[kDeltaPasses], xd[kDeltaPasses];
 #pragma unroll
   for (int p = 0; p < kDeltaPasses; ++p) {
-    const int64_t r = r0 + p * RPP;  // r = head * T + token
+    const int64_t r = r0 + p * RPP;  // r = token * H + head
     xo[p] = make_uint4(0u, 0u, 0u, 0u);
     xd[p] = make_uint4(0u, 0u, 0u, 0u);
     if (r < rows) {
-      const int64_t off = (r % T) * a + (r / T) * D + sub * 8;
+      const int64_t off = r * D + sub * 8;  // = token * a + head * D + sub * 8
       xo[p] = __ldg(reinterpret_cast<const uint4*>(o + off));
       xd[p] = __ldg(reinterpret_cast<const uint4*>(dout + off));
     }
@@ -64,7 +65,7 @@ __global__ void __launch_bounds__(kDeltaThreads)
     for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     const int64_t r = r0 + p * RPP;
     if (sub == 0 && r < rows) {
-      const int64_t hh = r / T, tok = r % T;
+      const int64_t hh = r % H, tok = r / H;
       const int64_t bi = tok / s, i = tok % s;
       delta[(bi * H + hh) * s + i] = acc;
     }
