@@ -409,17 +409,17 @@ int mc_gemm_fp8(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_t lda, 
  * chunk's O and log-sum-exp by the log-sum-exp rule, its dQ and a key
  * chunk's dK, dV by addition; a chunk's last pair writes the bf16 result.
  * On one GPU the K/V exchange is the read of the other chunk's rows, and
- * all ranks' partials of a step run as kernels on `stream` in schedule
- * order.  Results equal mc_attention_forward / _backward up to the fp32
+ * the ranks of a ring step run together: one launch per sub-step (every
+ * rank's k-th pair of the step), on `stream`, in schedule order.  Results equal mc_attention_forward / _backward up to the fp32
  * rounding of the merges and sums (to the bit for a chunk with one pair:
  * O, lse and dQ of chunk 0, dK and dV of the last chunk).
  *
  * Requirements: cp_parts >= 1, seq_len a multiple of 256 * cp_parts,
  * head_dim 64 or 128; the caller-owned workspace of
  * mc_attention_cp_workspace_bytes bytes (16-byte aligned) holds the running
- * sums (micro_batch x seq_len x 3a floats) and one chunk pair's bf16 dS^T
- * tiles (micro_batch x heads x (c / 128)^2 tiles of 128 x 128); its size
- * does not grow with cp_parts.  Forward and backward may share it; it must
+ * sums (micro_batch x seq_len x 3a floats) and the bf16 dS^T tiles of one
+ * sub-step (up to cp_parts chunk pairs of micro_batch x heads x (c / 128)^2
+ * tiles of 128 x 128); its size does not grow with cp_parts.  Forward and backward may share it; it must
  * not be shared with a concurrent call.  Errors as mc_attention_forward,
  * plus MC_ERR_SHAPE for an unsupported seq_len / cp_parts pair and
  * MC_ERR_WORKSPACE for a short workspace. */

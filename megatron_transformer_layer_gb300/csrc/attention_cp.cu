@@ -10,8 +10,10 @@
 // work (every rank computes 2 cp - 1 full chunk pairs and 2 diagonal ones).
 // In ring step t rank r holds the K/V chunks of rank (r - t) mod cp and
 // computes the partial attention of each of its query chunks i over each
-// held key chunk j <= i.  As a ring implementation does, each partial is
-// folded into running fp32 results at once, in schedule order:
+// held key chunk j <= i.  The ranks of a ring step run together: sub-step k
+// of step t is one launch of every rank's k-th pair (no two of which share a
+// query chunk or a key chunk).  As a ring implementation does, each partial
+// is folded into running fp32 results at once, in schedule order:
 //   forward  chunk i's O and log-sum-exp merged with the pair's by the
 //            log-sum-exp rule;
 //   backward the pair's dK, dV added to key chunk j's sums (the ones a ring
@@ -41,44 +43,84 @@ int check_cp(int b, int s, int H, int d, int cp) {
   return MC_OK;
 }
 
-// Workspace: the running sums, [b, s, 3a] fp32 (forward: O at [0, a) per
-// row and the log2-sum-exp [b, H, s] after it; backward: dQ [b, s, a] then
-// dK | dV [b, s, 2a]), followed by one chunk pair's dS^T tiles.
-size_t cp_workspace_bytes(int b, int s, int H, int d, int cp) {
-  const int64_t a = static_cast<int64_t>(H) * d, cb = s / (2 * cp) / 128;
-  return static_cast<size_t>(static_cast<int64_t>(b) * s * 3 * a * 4 +
-                             attention_cp_tile_bytes(b, H, cb, cb));
-}
-
-// The pairs in launch order (ring step, rank, the rank's pairs), each with
-// the accumulation mode of its query chunk i (total i + 1 pairs) and of its
-// key chunk j (total C - j pairs).
-struct CpPair {
-  int i, j, mode_q, mode_k;
-};
-
-std::vector<CpPair> cp_pairs(int cp) {
+// The launches in order: ring step t, sub-step k = the k-th pair of every
+// rank in step t (ranks in order, at most kCpMaxRects to a launch).  Each
+// pair is the rectangle of its query chunk i and key chunk j with the
+// accumulation modes of both: chunk i has i + 1 pairs, key chunk j has
+// C - j.  A rank's pairs of a step keep their order in the sub-steps, and a
+// chunk's pairs all come from one rank within a step, so every chunk sees
+// its pairs in schedule order.
+std::vector<std::vector<CpRect>> cp_launches(int cp, int c) {
   const int C = 2 * cp;
-  std::vector<int> seen_q(C, 0), seen_k(C, 0);
-  std::vector<CpPair> out;
-  for (int t = 0; t < cp; ++t)
+  std::vector<int> seen_q(C, 0), seen_k(C, 0), np(cp);
+  std::vector<int32_t> pairs(static_cast<size_t>(cp) * 8);
+  std::vector<std::vector<CpRect>> out;
+  for (int t = 0; t < cp; ++t) {
+    int kmax = 0;
     for (int r = 0; r < cp; ++r) {
-      int32_t pairs[8];
-      const int n = mc_cp_schedule(cp, r, t, pairs);
-      for (int k = 0; k < n; ++k) {
-        const int i = pairs[2 * k], j = pairs[2 * k + 1];
-        CpPair p = {i, j, 0, 0};
+      np[r] = mc_cp_schedule(cp, r, t, &pairs[static_cast<size_t>(r) * 8]);
+      kmax = np[r] > kmax ? np[r] : kmax;
+    }
+    for (int k = 0; k < kmax; ++k) {
+      std::vector<CpRect> launch;
+      for (int r = 0; r < cp; ++r) {
+        if (k >= np[r]) continue;
+        const int i = pairs[static_cast<size_t>(r) * 8 + 2 * k];
+        const int j = pairs[static_cast<size_t>(r) * 8 + 2 * k + 1];
+        CpRect p = {i * c, c, j * c, c, 0, 0};
         p.mode_q = (seen_q[i] > 0 ? kCpAccMerge : 0) | (seen_q[i] == i ? kCpAccFinal : 0);
         p.mode_k = (seen_k[j] > 0 ? kCpAccMerge : 0) | (seen_k[j] == C - 1 - j ? kCpAccFinal : 0);
         ++seen_q[i];
         ++seen_k[j];
-        out.push_back(p);
+        launch.push_back(p);
+        if (static_cast<int>(launch.size()) == kCpMaxRects) {
+          out.push_back(launch);
+          launch.clear();
+        }
       }
+      if (!launch.empty()) out.push_back(launch);
     }
+  }
   return out;
 }
 
+// Workspace: the running sums, [b, s, 3a] fp32 (forward: O at [0, a) per
+// row and the log2-sum-exp [b, H, s] after it; backward: dQ [b, s, a] then
+// dK | dV [b, s, 2a]), followed by the dS^T tiles of the largest launch
+// (at most cp pairs).
+size_t cp_workspace_bytes(int b, int s, int H, int d, int cp) {
+  const int64_t a = static_cast<int64_t>(H) * d;
+  int64_t tiles = 0;
+  for (const auto& l : cp_launches(cp, s / (2 * cp))) {
+    const int64_t t = attention_cp_tile_bytes(l.data(), static_cast<int>(l.size()), b, H);
+    tiles = t > tiles ? t : tiles;
+  }
+  return static_cast<size_t>(static_cast<int64_t>(b) * s * 3 * a * 4 + tiles);
+}
+
 }  // namespace
+
+int check_cp_rects(const CpRect* rects, int n, int s) {
+  if (!rects || n < 1 || n > kCpMaxRects) return MC_ERR_ARGUMENT;
+  for (int i = 0; i < n; ++i) {
+    const CpRect& r = rects[i];
+    // whole 128-row blocks inside the sequence; every query block sees at
+    // least one key block and every key block at least one query block
+    if (r.q_base < 0 || r.k_base < 0 || r.q_len < 128 || r.k_len < 128 || r.q_base % 128 ||
+        r.k_base % 128 || r.q_len % 128 || r.k_len % 128 ||
+        static_cast<int64_t>(r.q_base) + r.q_len > s ||
+        static_cast<int64_t>(r.k_base) + r.k_len > s || r.k_base > r.q_base ||
+        r.k_base + r.k_len > r.q_base + r.q_len)
+      return MC_ERR_ARGUMENT;
+    for (int j = 0; j < i; ++j) {  // no running sum touched twice in one launch
+      const CpRect& o = rects[j];
+      if (r.q_base < o.q_base + o.q_len && o.q_base < r.q_base + r.q_len) return MC_ERR_ARGUMENT;
+      if (r.k_base < o.k_base + o.k_len && o.k_base < r.k_base + r.k_len) return MC_ERR_ARGUMENT;
+    }
+  }
+  return MC_OK;
+}
+
 }  // namespace mc
 
 using namespace mc;
@@ -118,13 +160,13 @@ int mc_attention_forward_cp(const uint16_t* qkv, uint16_t* o, float* lse, int32_
   if (!al16(qkv) || !al16(o) || !al16(workspace)) return MC_ERR_ALIGN;
   if (workspace_bytes < cp_workspace_bytes(b, s, H, d, cp)) return MC_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int c = s / (2 * cp), cb = c / 128;
+  const int c = s / (2 * cp);
   const int64_t a = static_cast<int64_t>(H) * d;
   float* acc_o = static_cast<float*>(workspace);
   float* acc_lse2 = acc_o + static_cast<int64_t>(b) * s * a;
-  for (const CpPair& p : cp_pairs(cp)) {
-    rc = launch_attention_forward_part(qkv, o, lse, b, s, H, d, p.i * c, c, p.j * cb,
-                                       (p.j + 1) * cb, acc_o, acc_lse2, p.mode_q, status, st);
+  for (const auto& l : cp_launches(cp, c)) {
+    rc = launch_attention_forward_parts(qkv, o, lse, b, s, H, d, l.data(), static_cast<int>(l.size()),
+                                        acc_o, acc_lse2, status, st);
     if (rc != MC_OK) return rc;
   }
   return MC_OK;
@@ -143,21 +185,21 @@ int mc_attention_backward_cp(const uint16_t* qkv, const uint16_t* o, const float
     return MC_ERR_ALIGN;
   if (workspace_bytes < cp_workspace_bytes(b, s, H, d, cp)) return MC_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int c = s / (2 * cp), cb = c / 128;
+  const int c = s / (2 * cp);
   const int64_t a = static_cast<int64_t>(H) * d;
   float* acc_dq = static_cast<float*>(workspace);
   float* acc_dkv = acc_dq + static_cast<int64_t>(b) * s * a;
   uint8_t* tiles = reinterpret_cast<uint8_t*>(acc_dkv + static_cast<int64_t>(b) * s * 2 * a);
   rc = launch_attention_delta(o, dout, delta, b, s, H, d, st);
   if (rc != MC_OK) return rc;
-  for (const CpPair& p : cp_pairs(cp)) {
+  for (const auto& l : cp_launches(cp, c)) {
+    const int n = static_cast<int>(l.size());
     // key rows of chunk j against the query blocks of chunk i: dK, dV and dS^T
-    rc = launch_attention_dkdv_part(qkv, lse, dout, delta, dqkv, b, s, H, d, p.j * c, c,
-                                    p.i * cb, (p.i + 1) * cb, acc_dkv, tiles, p.mode_k, status, st);
+    rc = launch_attention_dkdv_parts(qkv, lse, dout, delta, dqkv, b, s, H, d, l.data(), n, acc_dkv,
+                                     tiles, status, st);
     if (rc != MC_OK) return rc;
     // dQ of chunk i from those tiles and K of chunk j
-    rc = launch_attention_dq_part(qkv, tiles, dqkv, b, s, H, d, p.i * cb, cb, p.j * cb, cb, acc_dq,
-                                  p.mode_q, status, st);
+    rc = launch_attention_dq_parts(qkv, tiles, dqkv, b, s, H, d, l.data(), n, acc_dq, status, st);
     if (rc != MC_OK) return rc;
   }
   return MC_OK;

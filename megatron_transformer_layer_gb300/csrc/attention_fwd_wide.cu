@@ -78,15 +78,25 @@ struct WideCfg {
 struct WideRect {
   int base, len;
   int key_lo, key_hi;
+  int mode;
+};
+
+// The rectangles of one launch (disjoint query rows): CTAs
+// [cta_end[i - 1], cta_end[i]) take the 128-row query tiles of rectangle i,
+// heaviest first.
+struct WideRects {
+  int n;
+  int cta_end[kCpMaxRects];
+  WideRect r[kCpMaxRects];
   float* out;
   float* lse2;
-  int mode;
 };
 
 template <int D, bool PART>
 __global__ void __launch_bounds__(kWideThreads, 1)
     attn_fwd_wide_kernel(const __grid_constant__ CUtensorMap tm, uint16_t* __restrict__ out,
-                         float* __restrict__ lse, int s, int H, int* status, const WideRect rect) {
+                         float* __restrict__ lse, int s, int H, int* status,
+                         const __grid_constant__ WideRects rects) {
   using C = WideCfg<D>;
   constexpr int VS = C::kVSlots;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -115,9 +125,15 @@ __global__ void __launch_bounds__(kWideThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int a = H * D;
-  // heaviest first
+  // this CTA's rectangle (the whole matrix: one) and query tile, heaviest first
+  int ri = 0;
+  if constexpr (PART)
+    while (ri + 1 < rects.n && static_cast<int>(blockIdx.x) >= rects.cta_end[ri]) ++ri;
+  const WideRect rect = rects.r[ri];
+  const int cta0 = ri > 0 ? rects.cta_end[ri - 1] : 0;
   const int q_blk =
-      (PART ? rect.base / 128 : 0) + static_cast<int>(gridDim.x - 1 - blockIdx.x);
+      PART ? rect.base / 128 + (rect.len / 128 - 1 - (static_cast<int>(blockIdx.x) - cta0))
+           : static_cast<int>(gridDim.x - 1 - blockIdx.x);
   const int hh = blockIdx.y, bi = blockIdx.z;
   const int q0 = q_blk * 128;
   // (the whole matrix: keys from 0, masked past s)
@@ -286,6 +302,10 @@ __global__ void __launch_bounds__(kWideThreads, 1)
       return peer;
     };
     for (int j = 0; ok && j < n_kb; ++j) {
+      if (PART && (rect.mode & kCpAccMerge) && j == max(n_kb - 3, 0) && q < s)
+        // the running O that this thread merges into at the end: into L2 now
+        bulk_prefetch_l2(rects.out + (static_cast<int64_t>(bi) * s + q) * a + hh * D + half * (D / 2),
+                         D * 2);
       if (!mbar_wait_warp(s_full, j & 1, status, kSiteAttention)) {
         ok = false;
         break;
@@ -373,7 +393,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
       const int64_t lrow = (static_cast<int64_t>(bi) * H + hh) * s + q;
       // Both halves read it before either passes the exchange below, after
       // which half 0 may overwrite it.
-      if (merge && q < s) run_l2 = rect.lse2[lrow];
+      if (merge && q < s) run_l2 = rects.lse2[lrow];
       l += exchange(l);  // both halves' sums, taken against the same max
       const float inv = 1.f / l;
       if constexpr (PART) {
@@ -394,14 +414,14 @@ __global__ void __launch_bounds__(kWideThreads, 1)
           if (q < s && MC_DCHECK(q - rect.base >= 0 && q - rect.base < rect.len &&
                                      hh * D + c * 32 + 32 <= a,
                                  status, kSiteAttention))
-            accumulate_row32(v, c_new, c_old, rect.out + row_off + c * 32,
+            accumulate_row32(v, c_new, c_old, rects.out + row_off + c * 32,
                              out + row_off + c * 32, merge, final);
         }
         if (q < s && half == 0) {
           if (final)
             lse[lrow] = l2 * kLn2;
           else
-            rect.lse2[lrow] = l2;
+            rects.lse2[lrow] = l2;
         }
       } else {
         uint16_t* orow = out + (static_cast<int64_t>(bi) * s + q) * a + hh * D;
@@ -437,7 +457,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
 
 template <int D, bool PART>
 int launch_wide(const uint16_t* qkv, uint16_t* o, float* lse, int b, int s, int H, int* status,
-                cudaStream_t st, const WideRect& rect) {
+                cudaStream_t st, const WideRects& rects) {
   using C = WideCfg<D>;
   const uint64_t a3 = 3ull * H * D;
   CUtensorMap tm;
@@ -451,8 +471,8 @@ int launch_wide(const uint16_t* qkv, uint16_t* o, float* lse, int b, int s, int 
     return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   });
   if (attr != cudaSuccess) return MC_ERR_CUDA;
-  dim3 grid(PART ? rect.len / 128 : (s + 127) / 128, H, b);
-  launch_kernel(kern, grid, dim3(kWideThreads), C::kSmem, st, 1, tm, o, lse, s, H, status, rect);
+  dim3 grid(PART ? rects.cta_end[rects.n - 1] : (s + 127) / 128, H, b);
+  launch_kernel(kern, grid, dim3(kWideThreads), C::kSmem, st, 1, tm, o, lse, s, H, status, rects);
   return cudaGetLastError() == cudaSuccess ? MC_OK : MC_ERR_CUDA;
 }
 
@@ -460,23 +480,33 @@ int launch_wide(const uint16_t* qkv, uint16_t* o, float* lse, int b, int s, int 
 
 int launch_attention_forward_wide(const uint16_t* qkv, uint16_t* o, float* lse, int b, int s,
                                   int H, int d, int* status, cudaStream_t st) {
-  const WideRect whole = {0, s, 0, INT_MAX, nullptr, nullptr, 0};
+  WideRects whole = {};
+  whole.n = 1;
+  whole.cta_end[0] = (s + 127) / 128;
+  whole.r[0] = {0, s, 0, INT_MAX, 0};
   return d == 64 ? launch_wide<64, false>(qkv, o, lse, b, s, H, status, st, whole)
                  : launch_wide<128, false>(qkv, o, lse, b, s, H, status, st, whole);
 }
 
-int launch_attention_forward_part(const uint16_t* qkv, uint16_t* o, float* lse, int b, int s,
-                                  int H, int d, int q_base, int q_len, int kb_lo, int kb_hi,
-                                  float* acc_o, float* acc_lse2, int mode, int* status,
-                                  cudaStream_t st) {
-  // Every query tile must see at least one key block: kb_lo * 128 <= q_base.
-  if (q_base % 128 || q_len % 128 || q_len < 128 || q_base + q_len > s || kb_lo < 0 ||
-      kb_hi <= kb_lo || static_cast<int64_t>(kb_lo) * 128 > q_base)
-    return MC_ERR_ARGUMENT;
-  const WideRect rect = {q_base, q_len, kb_lo * 128,
-                         kb_hi > INT_MAX / 128 ? INT_MAX : kb_hi * 128, acc_o, acc_lse2, mode};
-  return d == 64 ? launch_wide<64, true>(qkv, o, lse, b, s, H, status, st, rect)
-                 : launch_wide<128, true>(qkv, o, lse, b, s, H, status, st, rect);
+int launch_attention_forward_parts(const uint16_t* qkv, uint16_t* o, float* lse, int b, int s,
+                                   int H, int d, const CpRect* rects, int n, float* acc_o,
+                                   float* acc_lse2, int* status, cudaStream_t st) {
+  if (check_cp_rects(rects, n, s) != MC_OK) return MC_ERR_ARGUMENT;
+  // Rectangles off the diagonal (every tile the same length) first, then the
+  // diagonal ones, whose tiles the kernel takes heaviest first.
+  WideRects w = {};
+  w.out = acc_o;
+  w.lse2 = acc_lse2;
+  for (int pass = 0; pass < 2; ++pass)
+    for (int i = 0; i < n; ++i) {
+      const CpRect& r = rects[i];
+      if ((r.q_base == r.k_base) != (pass == 1)) continue;
+      w.r[w.n] = {r.q_base, r.q_len, r.k_base, r.k_base + r.k_len, r.mode_q};
+      w.cta_end[w.n] = (w.n > 0 ? w.cta_end[w.n - 1] : 0) + r.q_len / 128;
+      ++w.n;
+    }
+  return d == 64 ? launch_wide<64, true>(qkv, o, lse, b, s, H, status, st, w)
+                 : launch_wide<128, true>(qkv, o, lse, b, s, H, status, st, w);
 }
 
 }  // namespace mc

@@ -20,18 +20,27 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr int64_t kDsTileBytes = 128 * 128 * 2;  // one bf16 dS^T tile (128 keys x 128 queries)
 
 // A rectangle of the causal score matrix, for the context-parallel path:
-// dQ takes query rows [base, base + len) against key blocks [blk_lo, blk_hi);
 // dK/dV take key rows [base, base + len) against query blocks
-// [blk_lo, blk_hi).  Results are added to running fp32 sums indexed by the
-// absolute row, `acc`: dQ [b, s, a]; dK | dV [b, s, 2a].  Without
-// kCpAccMerge in `mode` there is no earlier sum to add; with kCpAccFinal the
-// sum goes to dqkv as bf16 instead.  The fused kernels use the whole matrix
-// (base 0, len s, blocks [0, INT_MAX)) and no sums.
+// [blk_lo, blk_hi).  Results are added to running fp32 sums dK | dV
+// [b, s, 2a] indexed by the absolute row.  Without kCpAccMerge in `mode`
+// there is no earlier sum to add; with kCpAccFinal the sum goes to dqkv as
+// bf16 instead.  The rectangle's dS^T tiles start at tile `tile0` of the
+// workspace.  The fused kernel uses the whole matrix (base 0, blocks
+// [0, INT_MAX)) and no sums.
 struct AttnPart {
   int base, len;
   int blk_lo, blk_hi;
-  float* acc;
   int mode;
+  int64_t tile0;
+};
+
+// The rectangles of one launch (disjoint key rows): CTAs
+// [cta_end[i - 1], cta_end[i]) take the 128-key blocks of rectangle i.
+struct AttnParts {
+  int n;
+  int cta_end[kCpMaxRects];
+  AttnPart r[kCpMaxRects];
+  float* acc;
 };
 
 // ---------------------------------------------------------------- backward
@@ -74,7 +83,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv,
                             const __grid_constant__ CUtensorMap tm_do, const float* __restrict__ lse,
                             const float* __restrict__ delta, uint16_t* __restrict__ dqkv, int s,
-                            int H, int* status, const AttnPart part,
+                            int H, int* status, const __grid_constant__ AttnParts parts,
                             uint8_t* __restrict__ ds_tiles) {
   using C = BwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -108,7 +117,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int a = H * D;
   const int hh = blockIdx.y, bi = blockIdx.z;
   const int nblk = (s + 127) / 128;
-  const int kb = part.base / 128 + static_cast<int>(blockIdx.x);  // this CTA's key block
+  // this CTA's rectangle (the whole matrix: one) and key block
+  int ri = 0;
+  if constexpr (PART)
+    while (ri + 1 < parts.n && static_cast<int>(blockIdx.x) >= parts.cta_end[ri]) ++ri;
+  const AttnPart part = parts.r[ri];
+  const int cta0 = ri > 0 ? parts.cta_end[ri - 1] : 0;
+  const int kb = part.base / 128 + static_cast<int>(blockIdx.x) - cta0;
   const int r0 = kb * 128;
   // query blocks qb0 .. qb0 + count - 1 (fused: kb .. nblk - 1)
   const int qb0 = max(kb, part.blk_lo);
@@ -365,7 +380,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const int nq = part.blk_hi - part.blk_lo, nk = part.len / 128;
             const int kr = kb - part.base / 128;
             const int64_t tile =
-                PART ? ((static_cast<int64_t>(bi) * H + hh) * nq + (qb - part.blk_lo)) * nk + kr
+                PART ? part.tile0 + ((static_cast<int64_t>(bi) * H + hh) * nq + (qb - part.blk_lo)) * nk + kr
                      : (static_cast<int64_t>(bi) * H + hh) *
                                (static_cast<int64_t>(nblk) * (nblk + 1) / 2) +
                            static_cast<int64_t>(qb) * (qb + 1) / 2 + kb;
@@ -400,7 +415,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               kSiteAttention);
           if (PART && r < s && in_range) {
             // the running sums: dK at [0, a), dV at [a, 2a) of the key's row
-            float* run = part.acc + (static_cast<int64_t>(bi) * s + r) * 2 * a +
+            float* run = parts.acc + (static_cast<int64_t>(bi) * s + r) * 2 * a +
                          (w == 0 ? a : 0) + hh * D + c * 32;
             accumulate_row32(v, mul, 1.f, run, dqkv + base + col + c * 32,
                              part.mode & kCpAccMerge, part.mode & kCpAccFinal);
@@ -698,7 +713,7 @@ int launch_bwd_dq_tc(const CUtensorMap& tq, const CUtensorMap& td, const float* 
 template <int D, bool PART>
 int launch_bwd_dkdv_tc(const CUtensorMap& tq, const CUtensorMap& td, const float* lse,
                        const float* delta, uint16_t* dqkv, int b, int s, int H, int* status,
-                       cudaStream_t st, const AttnPart& part, uint8_t* ds_tiles = nullptr) {
+                       cudaStream_t st, const AttnParts& parts, uint8_t* ds_tiles = nullptr) {
   using C = BwdCfg<D>;
   auto kern = attn_bwd_dkdv_tc_kernel<D, PART>;
   static PerDeviceInit init;
@@ -706,9 +721,9 @@ int launch_bwd_dkdv_tc(const CUtensorMap& tq, const CUtensorMap& td, const float
     return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   });
   if (attr != cudaSuccess) return MC_ERR_CUDA;
-  dim3 grid(PART ? part.len / 128 : (s + 127) / 128, H, b);
+  dim3 grid(PART ? parts.cta_end[parts.n - 1] : (s + 127) / 128, H, b);
   launch_kernel(kern, dim3(grid), dim3(kBwdThreads), C::kSmem, st, 1, tq, td, lse, delta, dqkv, s,
-                H, status, part, ds_tiles);
+                H, status, parts, ds_tiles);
   return cudaGetLastError() == cudaSuccess ? MC_OK : MC_ERR_CUDA;
 }
 
@@ -742,23 +757,37 @@ struct DqGemmCfg {
 };
 
 // Query blocks [q_lo, q_lo + nq) against key blocks [k_lo, k_lo + nk)
-// (key blocks past a query block are not visible); `acc` and `mode` as in
-// AttnPart.  The whole matrix is {0, nb, 0, nb}.
+// (key blocks past a query block are not visible); its dS^T tiles start at
+// tile `tile0`; `mode` as in AttnPart.  The whole matrix is {0, nb, 0, nb}.
 struct DqRect {
   int q_lo, nq, k_lo, nk;
-  float* acc;
   int mode;
+  int64_t tile0;
 };
 
-// Item r of CTA blockIdx.x (snake over the dispatch order): query block
-// (rectangle-relative), head and batch; false once the CTA's share is done.
-__device__ __forceinline__ bool dq_item(int r, int nq, int H, int n_items, int& qr, int& hh,
-                                        int& bi) {
+// The rectangles of one launch (disjoint query rows): items
+// [item_end[i - 1], item_end[i]) are rectangle i's (query block, head,
+// batch) triples; `acc` holds the running dQ sums [b, s, a].
+struct DqRects {
+  int n;
+  int item_end[kCpMaxRects];
+  DqRect r[kCpMaxRects];
+  float* acc;
+};
+
+// Item r of CTA blockIdx.x (snake over the dispatch order): rectangle,
+// query block within it, head and batch; false once the CTA's share is done.
+__device__ __forceinline__ bool dq_item(int r, const DqRects& rects, int H, int& ri, int& qr,
+                                        int& hh, int& bi) {
   const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
   const int64_t k = static_cast<int64_t>(r) * G + ((r & 1) ? G - 1 - c : c);
-  if (k >= n_items) return false;
-  qr = nq - 1 - static_cast<int>(k % nq);  // heaviest first within a head
-  const int rest = static_cast<int>(k / nq);
+  if (k >= rects.item_end[rects.n - 1]) return false;
+  ri = 0;
+  while (ri + 1 < rects.n && k >= rects.item_end[ri]) ++ri;
+  const int kr = static_cast<int>(k - (ri > 0 ? rects.item_end[ri - 1] : 0));
+  const int nq = rects.r[ri].nq;
+  qr = nq - 1 - kr % nq;  // heaviest first within a head
+  const int rest = kr / nq;
   hh = rest % H;
   bi = rest / H;
   return true;
@@ -768,7 +797,7 @@ template <int D, bool PART>
 __global__ void __launch_bounds__(192, 1)
     attn_bwd_dq_gemm_kernel(const __grid_constant__ CUtensorMap tm_qkv,
                             const uint8_t* __restrict__ ds_tiles, uint16_t* __restrict__ dqkv,
-                            int s, int H, int n_items, int* status, const DqRect rect) {
+                            int s, int H, int* status, const __grid_constant__ DqRects rects) {
   using C = DqGemmCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -785,12 +814,11 @@ __global__ void __launch_bounds__(192, 1)
   const int a = H * D;
   const int nb = (s + 127) / 128;
   const int64_t ntri = static_cast<int64_t>(nb) * (nb + 1) / 2;
-  const int nq = rect.nq;
-  // key blocks rect.k_lo .. + n_keys(qb) - 1 and the first tile of an item
-  auto n_keys = [&](int qb) { return PART ? min(rect.nk, qb + 1 - rect.k_lo) : qb + 1; };
-  auto first_tile = [&](int qr, int hh, int bi) {
-    const int qb = rect.q_lo + qr;
-    return PART ? ((static_cast<int64_t>(bi) * H + hh) * nq + qr) * rect.nk
+  // key blocks R.k_lo .. + n_keys(R, qb) - 1 and the first tile of an item
+  auto n_keys = [&](const DqRect& R, int qb) { return PART ? min(R.nk, qb + 1 - R.k_lo) : qb + 1; };
+  auto first_tile = [&](const DqRect& R, int qr, int hh, int bi) {
+    const int qb = R.q_lo + qr;
+    return PART ? R.tile0 + ((static_cast<int64_t>(bi) * H + hh) * R.nq + qr) * R.nk
                 : (static_cast<int64_t>(bi) * H + hh) * ntri + static_cast<int64_t>(qb) * (qb + 1) / 2;
   };
 
@@ -822,10 +850,11 @@ __global__ void __launch_bounds__(192, 1)
       // -------------------------------------------------------- producer
       int gt = 0;  // tiles issued, across items
       bool ok = true;
-      int qr, hh, bi;
-      for (int r = 0; ok && dq_item(r, nq, H, n_items, qr, hh, bi); ++r) {
-        const int64_t tile0 = first_tile(qr, hh, bi);
-        const int nj = n_keys(rect.q_lo + qr);
+      int ri, qr, hh, bi;
+      for (int r = 0; ok && dq_item(r, rects, H, ri, qr, hh, bi); ++r) {
+        const DqRect& R = rects.r[ri];
+        const int64_t tile0 = first_tile(R, qr, hh, bi);
+        const int nj = n_keys(R, R.q_lo + qr);
         for (int j = 0; j < nj; ++j, ++gt) {
           const int st = gt % C::kStages;
           if (!mbar_wait(&empty[st], ((gt / C::kStages) & 1) ^ 1u, status, kSiteAttention)) {
@@ -838,7 +867,7 @@ __global__ void __launch_bounds__(192, 1)
                     static_cast<uint32_t>(kDsTileBytes), &full[st]);
           for (int c = 0; c < C::kChunks; ++c)
             tma_load_3d(dst + kDsTileBytes + c * 16384, &tm_qkv, &full[st], a + hh * D + c * 64,
-                        (rect.k_lo + j) * 128, bi);
+                        (R.k_lo + j) * 128, bi);
         }
       }
       pdl_launch();  // every load of this CTA is issued
@@ -851,9 +880,9 @@ __global__ void __launch_bounds__(192, 1)
       // -------------------------------------------------------- MMA issuer
       constexpr uint32_t kIdesc = idesc_bf16_f32(128, D, true, true);
       bool ok = true;
-      int gt = 0, qr, hh, bi;
-      for (int r = 0; ok && dq_item(r, nq, H, n_items, qr, hh, bi); ++r) {
-        const int nj = n_keys(rect.q_lo + qr);
+      int gt = 0, ri, qr, hh, bi;
+      for (int r = 0; ok && dq_item(r, rects, H, ri, qr, hh, bi); ++r) {
+        const int nj = n_keys(rects.r[ri], rects.r[ri].q_lo + qr);
         const int acc = r & 1;
         // the epilogue of item r - 2 has read this accumulator
         if (!mbar_wait(&acc_empty[acc], ((r >> 1) & 1) ^ 1u, status, kSiteAttention)) break;
@@ -888,12 +917,13 @@ __global__ void __launch_bounds__(192, 1)
     const int quarter = warp & 3;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const float scale = rsqrtf(static_cast<float>(D));
-    int qr, hh, bi;
-    for (int r = 0; dq_item(r, nq, H, n_items, qr, hh, bi); ++r) {
+    int ri, qr, hh, bi;
+    for (int r = 0; dq_item(r, rects, H, ri, qr, hh, bi); ++r) {
       const int acc = r & 1;
+      const DqRect& R = rects.r[ri];
+      const int row = (R.q_lo + qr) * 128 + quarter * 32 + lane;  // this thread's query row
       if (!mbar_wait_warp(&acc_full[acc], (r >> 1) & 1, status, kSiteAttention)) break;
       tc_fence_after();
-      const int row = (rect.q_lo + qr) * 128 + quarter * 32 + lane;  // this thread's query row
       const int64_t base = (static_cast<int64_t>(bi) * s + row) * 3 * static_cast<int64_t>(a);
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
@@ -901,9 +931,9 @@ __global__ void __launch_bounds__(192, 1)
         tmem_ld_32x32b_x32(tmem + static_cast<uint32_t>(acc * 128) + lane_off + c * 32, v);
         if (row < s && MC_DCHECK(row >= 0 && hh * D + c * 32 + 32 <= a, status, kSiteAttention)) {
           if constexpr (PART) {
-            float* run = rect.acc + (static_cast<int64_t>(bi) * s + row) * a + hh * D + c * 32;
+            float* run = rects.acc + (static_cast<int64_t>(bi) * s + row) * a + hh * D + c * 32;
             accumulate_row32(v, scale, 1.f, run, dqkv + base + hh * D + c * 32,
-                             rect.mode & kCpAccMerge, rect.mode & kCpAccFinal);
+                             R.mode & kCpAccMerge, R.mode & kCpAccFinal);
           } else {
             uint4* dst = reinterpret_cast<uint4*>(dqkv + base + hh * D + c * 32);
 #pragma unroll
@@ -933,7 +963,7 @@ __global__ void __launch_bounds__(192, 1)
 
 template <int D, bool PART>
 int launch_bwd_dq_gemm(const CUtensorMap& tq, const uint8_t* ds_tiles, uint16_t* dqkv, int b,
-                       int s, int H, const DqRect& rect, int* status, cudaStream_t st) {
+                       int s, int H, const DqRects& rects, int* status, cudaStream_t st) {
   using C = DqGemmCfg<D>;
   auto kern = attn_bwd_dq_gemm_kernel<D, PART>;
   static PerDeviceInit init;
@@ -941,11 +971,10 @@ int launch_bwd_dq_gemm(const CUtensorMap& tq, const uint8_t* ds_tiles, uint16_t*
     return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   });
   if (attr != cudaSuccess) return MC_ERR_CUDA;
-  const int64_t n_items = static_cast<int64_t>(rect.nq) * H * b;
-  if (n_items > 0x7fffffff) return MC_ERR_UNSUPPORTED;
-  const int grid = static_cast<int>(n_items < num_sms() ? n_items : num_sms());
-  launch_kernel(kern, dim3(grid), dim3(192), C::kSmem, st, 1, tq, ds_tiles, dqkv, s, H,
-                static_cast<int>(n_items), status, rect);
+  const int n_items = rects.item_end[rects.n - 1];
+  const int grid = n_items < num_sms() ? n_items : num_sms();
+  launch_kernel(kern, dim3(grid), dim3(192), C::kSmem, st, 1, tq, ds_tiles, dqkv, s, H, status,
+                rects);
   return cudaGetLastError() == cudaSuccess ? MC_OK : MC_ERR_CUDA;
 }
 
@@ -967,7 +996,6 @@ bool make_bwd_maps(CUtensorMap* tq, CUtensorMap* td, const uint16_t* qkv, const 
   return make_qkv_map(tq, qkv, b, s, a_) && make_tmap_bf16(td, dout, 3, dd, sd, box);
 }
 
-constexpr AttnPart kWhole = {0, 0, 0, 0x7fffffff, nullptr, 0};
 
 // With `ds_tiles` (attention_ds_workspace_bytes of device memory) the dK/dV
 // kernel also writes dS^T and dQ is its product with K; without, the dQ
@@ -978,13 +1006,22 @@ int launch_bwd_tc(const uint16_t* qkv, const float* lse, const uint16_t* dout, u
                   uint8_t* ds_tiles) {
   CUtensorMap tq, td;
   if (!make_bwd_maps(&tq, &td, qkv, dout, b, s, H * D)) return MC_ERR_CUDA;
-  int rc = launch_bwd_dkdv_tc<D, false>(tq, td, lse, delta, dqkv, b, s, H, status, st, kWhole,
+  const int nb = (s + 127) / 128;
+  AttnParts whole = {};
+  whole.n = 1;
+  whole.cta_end[0] = nb;
+  whole.r[0] = {0, s, 0, 0x7fffffff, 0, 0};
+  int rc = launch_bwd_dkdv_tc<D, false>(tq, td, lse, delta, dqkv, b, s, H, status, st, whole,
                                         ds_tiles);
   if (rc != MC_OK) return rc;
   if (ds_tiles) {
-    const int nb = (s + 127) / 128;
-    const DqRect whole = {0, nb, 0, nb, nullptr, 0};
-    return launch_bwd_dq_gemm<D, false>(tq, ds_tiles, dqkv, b, s, H, whole, status, st);
+    const int64_t n_items = static_cast<int64_t>(nb) * H * b;
+    if (n_items > 0x7fffffff) return MC_ERR_UNSUPPORTED;
+    DqRects dq = {};
+    dq.n = 1;
+    dq.item_end[0] = static_cast<int>(n_items);
+    dq.r[0] = {0, nb, 0, nb, 0, 0};
+    return launch_bwd_dq_gemm<D, false>(tq, ds_tiles, dqkv, b, s, H, dq, status, st);
   }
   return launch_bwd_dq_tc<D>(tq, td, lse, delta, dqkv, b, s, H, status, st);
 }
@@ -1003,41 +1040,77 @@ int launch_attention_backward_tc(const uint16_t* qkv, const float* lse, const ui
                  : launch_bwd_tc<128>(qkv, lse, dout, dqkv, delta, b, s, H, status, st, ds_tiles);
 }
 
-int64_t attention_cp_tile_bytes(int64_t b, int64_t H, int64_t nq, int64_t nk) {
-  return b * H * nq * nk * kDsTileBytes;
+int64_t attention_cp_tile_bytes(const CpRect* rects, int n, int64_t b, int64_t H) {
+  int64_t tiles = 0;
+  for (int i = 0; i < n; ++i)
+    tiles += b * H * (rects[i].q_len / 128) * static_cast<int64_t>(rects[i].k_len / 128);
+  return tiles * kDsTileBytes;
 }
 
-int launch_attention_dkdv_part(const uint16_t* qkv, const float* lse, const uint16_t* dout,
-                               const float* delta, uint16_t* dqkv, int b, int s, int H, int d,
-                               int k_base, int k_len, int qb_lo, int qb_hi, float* acc_dkv,
-                               uint8_t* ds_tiles, int mode, int* status, cudaStream_t st) {
-  // whole 128-row key blocks inside the sequence; every key block sees at
-  // least one query block (qb_lo * 128 >= k_base)
-  if (k_base % 128 || k_len % 128 || k_len < 128 || k_base + k_len > s || qb_lo < 0 ||
-      qb_hi <= qb_lo || static_cast<int64_t>(qb_hi) * 128 > s ||
-      static_cast<int64_t>(qb_lo) * 128 < k_base)
-    return MC_ERR_ARGUMENT;
+namespace {
+// Rectangles off the diagonal (every CTA or item the same length) go first
+// in a launch, the diagonal ones (heaviest first inside) after them; the
+// dS^T tiles keep the order given.
+template <typename F>
+void for_each_rect_heavy_first(const CpRect* rects, int n, F&& f) {
+  for (int pass = 0; pass < 2; ++pass)
+    for (int i = 0; i < n; ++i)
+      if ((rects[i].q_base == rects[i].k_base) == (pass == 1)) f(i);
+}
+
+void rect_tile_offsets(const CpRect* rects, int n, int64_t b, int64_t H, int64_t* tile0) {
+  int64_t t0 = 0;
+  for (int i = 0; i < n; ++i) {
+    tile0[i] = t0;
+    t0 += b * H * (rects[i].q_len / 128) * static_cast<int64_t>(rects[i].k_len / 128);
+  }
+}
+}  // namespace
+
+int launch_attention_dkdv_parts(const uint16_t* qkv, const float* lse, const uint16_t* dout,
+                                const float* delta, uint16_t* dqkv, int b, int s, int H, int d,
+                                const CpRect* rects, int n, float* acc_dkv, uint8_t* ds_tiles,
+                                int* status, cudaStream_t st) {
+  if (check_cp_rects(rects, n, s) != MC_OK || !ds_tiles) return MC_ERR_ARGUMENT;
   CUtensorMap tq, td;
   if (!make_bwd_maps(&tq, &td, qkv, dout, b, s, H * d)) return MC_ERR_CUDA;
-  const AttnPart part = {k_base, k_len, qb_lo, qb_hi, acc_dkv, mode};
-  return d == 64 ? launch_bwd_dkdv_tc<64, true>(tq, td, lse, delta, dqkv, b, s, H, status, st,
-                                                part, ds_tiles)
-                 : launch_bwd_dkdv_tc<128, true>(tq, td, lse, delta, dqkv, b, s, H, status, st,
-                                                 part, ds_tiles);
+  int64_t tile0[kCpMaxRects];
+  rect_tile_offsets(rects, n, b, H, tile0);
+  AttnParts p = {};
+  p.acc = acc_dkv;
+  for_each_rect_heavy_first(rects, n, [&](int i) {
+    const CpRect& r = rects[i];
+    p.r[p.n] = {r.k_base, r.k_len, r.q_base / 128, (r.q_base + r.q_len) / 128, r.mode_k, tile0[i]};
+    p.cta_end[p.n] = (p.n > 0 ? p.cta_end[p.n - 1] : 0) + r.k_len / 128;
+    ++p.n;
+  });
+  return d == 64 ? launch_bwd_dkdv_tc<64, true>(tq, td, lse, delta, dqkv, b, s, H, status, st, p,
+                                                ds_tiles)
+                 : launch_bwd_dkdv_tc<128, true>(tq, td, lse, delta, dqkv, b, s, H, status, st, p,
+                                                 ds_tiles);
 }
 
-int launch_attention_dq_part(const uint16_t* qkv, const uint8_t* ds_tiles, uint16_t* dqkv, int b,
-                             int s, int H, int d, int qb_lo, int nq, int kb_lo, int nk,
-                             float* acc_dq, int mode, int* status, cudaStream_t st) {
-  // every query block sees at least one key block (qb_lo >= kb_lo)
-  if (qb_lo < 0 || nq < 1 || kb_lo < 0 || nk < 1 || qb_lo < kb_lo ||
-      static_cast<int64_t>(qb_lo + nq) * 128 > s || static_cast<int64_t>(kb_lo + nk) * 128 > s)
-    return MC_ERR_ARGUMENT;
+int launch_attention_dq_parts(const uint16_t* qkv, const uint8_t* ds_tiles, uint16_t* dqkv, int b,
+                              int s, int H, int d, const CpRect* rects, int n, float* acc_dq,
+                              int* status, cudaStream_t st) {
+  if (check_cp_rects(rects, n, s) != MC_OK || !ds_tiles) return MC_ERR_ARGUMENT;
   CUtensorMap tq;
   if (!make_qkv_map(&tq, qkv, b, s, H * d)) return MC_ERR_CUDA;
-  const DqRect rect = {qb_lo, nq, kb_lo, nk, acc_dq, mode};
-  return d == 64 ? launch_bwd_dq_gemm<64, true>(tq, ds_tiles, dqkv, b, s, H, rect, status, st)
-                 : launch_bwd_dq_gemm<128, true>(tq, ds_tiles, dqkv, b, s, H, rect, status, st);
+  int64_t tile0[kCpMaxRects];
+  rect_tile_offsets(rects, n, b, H, tile0);
+  DqRects q = {};
+  q.acc = acc_dq;
+  int64_t items = 0;
+  for_each_rect_heavy_first(rects, n, [&](int i) {
+    const CpRect& r = rects[i];
+    q.r[q.n] = {r.q_base / 128, r.q_len / 128, r.k_base / 128, r.k_len / 128, r.mode_q, tile0[i]};
+    items += static_cast<int64_t>(r.q_len / 128) * H * b;
+    q.item_end[q.n] = static_cast<int>(items < 0x7fffffff ? items : 0x7fffffff);
+    ++q.n;
+  });
+  if (items > 0x7fffffff) return MC_ERR_UNSUPPORTED;
+  return d == 64 ? launch_bwd_dq_gemm<64, true>(tq, ds_tiles, dqkv, b, s, H, q, status, st)
+                 : launch_bwd_dq_gemm<128, true>(tq, ds_tiles, dqkv, b, s, H, q, status, st);
 }
 
 }  // namespace mc

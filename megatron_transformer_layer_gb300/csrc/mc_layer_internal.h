@@ -223,35 +223,47 @@ int launch_attention_backward(const uint16_t* qkv, const uint16_t* o, const floa
 int launch_attention_delta(const uint16_t* o, const uint16_t* dout, float* delta, int b, int s,
                            int H, int d, cudaStream_t stream);
 
-// Rectangles of the causal score matrix for the context-parallel path
-// (query or key rows [base, base + len), 128-row blocks of the other side
-// in [blk_lo, blk_hi)).  Each rectangle adds its share to a running fp32
-// sum indexed by the absolute row; `mode` says whether an earlier rectangle
-// left one (kCpAccMerge) and whether this is the rows' last rectangle
-// (kCpAccFinal), which writes the bf16 result instead.
+// Rectangles of the causal score matrix for the context-parallel path: one
+// chunk pair (query rows [q_base, q_base + q_len) against key rows
+// [k_base, k_base + k_len), all multiples of 128, k_base <= q_base), and the
+// accumulation modes of its query chunk (mode_q) and key chunk (mode_k).
+// Each rectangle adds its share to running fp32 sums indexed by the
+// absolute row; a mode says whether an earlier rectangle left one
+// (kCpAccMerge) and whether this is the rows' last rectangle (kCpAccFinal),
+// which writes the bf16 result instead.  One launch takes up to
+// kCpMaxRects rectangles, no two of which share a query chunk (forward, dQ)
+// or a key chunk (dK/dV), so that no running sum is touched twice:
 //   forward: O [b, s, a] over the keys seen so far and its log2-sum-exp
 //            [b, H, s], merged by the log-sum-exp rule; final: o and the
 //            natural-log lse;
 //   dkdv:    dK | dV [b, s, 2a] (dK scaled by 1/sqrt(d)) using the full lse
 //            and delta; final: the dK, dV columns of dqkv.  It also writes
-//            the rectangle's dS^T tiles, [b, H, nq, nk] x 32 KB (nq query
-//            blocks of the rectangle, nk key blocks), for
-//   dq:      dQ [b, s, a] += dS K_j / sqrt(d) over the tiles; final: the dQ
-//            columns of dqkv.
+//            each rectangle's dS^T tiles to `ds_tiles`, rectangle after
+//            rectangle in the order given, [b, H, nq, nk] x 32 KB each (nq
+//            query blocks, nk key blocks), for
+//   dq:      dQ [b, s, a] += dS K_j / sqrt(d) over those tiles (the same
+//            rectangles in the same order); final: the dQ columns of dqkv.
 constexpr int kCpAccMerge = 1;
 constexpr int kCpAccFinal = 2;
-int64_t attention_cp_tile_bytes(int64_t b, int64_t H, int64_t nq, int64_t nk);
-int launch_attention_forward_part(const uint16_t* qkv, uint16_t* o, float* lse, int b, int s,
-                                  int H, int d, int q_base, int q_len, int kb_lo, int kb_hi,
-                                  float* acc_o, float* acc_lse2, int mode, int* status,
-                                  cudaStream_t stream);
-int launch_attention_dkdv_part(const uint16_t* qkv, const float* lse, const uint16_t* dout,
-                               const float* delta, uint16_t* dqkv, int b, int s, int H, int d,
-                               int k_base, int k_len, int qb_lo, int qb_hi, float* acc_dkv,
-                               uint8_t* ds_tiles, int mode, int* status, cudaStream_t stream);
-int launch_attention_dq_part(const uint16_t* qkv, const uint8_t* ds_tiles, uint16_t* dqkv, int b,
-                             int s, int H, int d, int qb_lo, int nq, int kb_lo, int nk,
-                             float* acc_dq, int mode, int* status, cudaStream_t stream);
+constexpr int kCpMaxRects = 16;
+struct CpRect {
+  int q_base, q_len, k_base, k_len;
+  int mode_q, mode_k;
+};
+// The dS^T tile bytes of rectangles[0, n).
+int64_t attention_cp_tile_bytes(const CpRect* rects, int n, int64_t b, int64_t H);
+int launch_attention_forward_parts(const uint16_t* qkv, uint16_t* o, float* lse, int b, int s,
+                                   int H, int d, const CpRect* rects, int n, float* acc_o,
+                                   float* acc_lse2, int* status, cudaStream_t stream);
+int launch_attention_dkdv_parts(const uint16_t* qkv, const float* lse, const uint16_t* dout,
+                                const float* delta, uint16_t* dqkv, int b, int s, int H, int d,
+                                const CpRect* rects, int n, float* acc_dkv, uint8_t* ds_tiles,
+                                int* status, cudaStream_t stream);
+int launch_attention_dq_parts(const uint16_t* qkv, const uint8_t* ds_tiles, uint16_t* dqkv, int b,
+                              int s, int H, int d, const CpRect* rects, int n, float* acc_dq,
+                              int* status, cudaStream_t stream);
+// Checks a launch's rectangles against the sequence (MC_OK or MC_ERR_ARGUMENT).
+int check_cp_rects(const CpRect* rects, int n, int s);
 #endif
 
 }  // namespace mc

@@ -200,6 +200,14 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 // every committed copy has read its source, bulk_wait_all until it is
 // complete).  Generic-proxy writes of the source must be made visible first
 // (fence_proxy_async_smem by the writing threads, before they signal).
+// A hint: bring `bytes` (a multiple of 16, 16-byte aligned) of global memory
+// into L2 without waiting for it.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)),
+               "r"(bytes)
+               : "memory");
+}
+
 __device__ __forceinline__ void bulk_store(void* gdst, const void* ssrc, uint32_t bytes) {
   asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
                    reinterpret_cast<uint64_t>(gdst)),

@@ -51,12 +51,13 @@ def test_schedule_rejects_bad_arguments():
 
 
 def test_workspace_bytes():
-    """Running fp32 sums for the whole sequence ([b, s, 3a]) plus one chunk
-    pair's bf16 dS^T tiles ([b, H, c/128, c/128] x 128 x 128): the size does
-    not grow with the number of CP partitions."""
+    """Running fp32 sums for the whole sequence ([b, s, 3a]) plus the bf16
+    dS^T tiles of one launch: up to one chunk pair per rank, [b, H, c/128,
+    c/128] x 128 x 128 each.  The size does not grow with the number of CP
+    partitions."""
     b, s, H, d, cp = 2, 2048, 4, 128, 4
     c, a = s // (2 * cp), H * d
-    tiles = b * H * (c // 128) ** 2 * 128 * 128 * 2
+    tiles = cp * b * H * (c // 128) ** 2 * 128 * 128 * 2
     assert L.mc_attention_cp_workspace_bytes(b, s, H, d, cp) == b * s * 3 * a * 4 + tiles
     sizes = [L.mc_attention_cp_workspace_bytes(1, 8192, 8, 128, k) for k in (1, 2, 4, 8)]
     assert sizes == sorted(sizes, reverse=True)
