@@ -10,6 +10,8 @@
 //               epilogue, store to global memory; two warps per TMEM lane
 //               quarter, each taking half of the tile's columns; the second
 //               accumulator lets the next tile's main loop run underneath.
+//               Each warp's 32 x 32 blocks pass through shared memory so
+//               that its global accesses cover whole rows (coalesced).
 //
 // Operands may be K-major ([rows, K] in memory) or MN-major ([K, rows] in
 // memory); the latter is how the dgrad (W used as [K, N]) and wgrad
@@ -66,7 +68,7 @@ struct GemmArgs {
 //           of a 128 x 256 tile, which is what keeps the tensor pipe fed from L2.
 constexpr int kSolo = 0, kDuo = 1;
 
-template <int BN, int MODE>
+template <int BN, int MODE, int EPI>
 struct GemmCfg {
   static constexpr int kABytes = BM * BK * 2;
   // B bytes held per CTA and stage
@@ -79,7 +81,11 @@ struct GemmCfg {
   static constexpr int kTmemCols = 2 * BN;
   // ring + barriers (full, empty, acc_full x2, acc_empty x2, drain) + tmem slot
   static constexpr int kBarrierBytes = (2 * kStages + 5) * 8 + 8;
-  static constexpr int kSmemBytes = kStages * kStageBytes + kBarrierBytes + 1024;  // +align
+  // the epilogue's 32 x 33-float block per epilogue warp
+  static constexpr int kEpiBytes = kEpilogueWarps * 32 * 33 * 4;
+  static constexpr int kSmemBytes =
+      kStages * kStageBytes + kBarrierBytes + kEpiBytes + 1024;  // +align
+  static_assert(kSmemBytes <= 227 * 1024, "gemm shared memory");
 };
 
 __device__ __forceinline__ void tile_coords(int tile, int m_tiles, int n_tiles, int& mb, int& nb) {
@@ -106,89 +112,128 @@ __device__ __forceinline__ float gelu_tanh_grad(float x) {
   return 0.5f * (1.0f + th) + 0.5f * x * (1.0f - th * th) * c * fmaf(3.0f * 0.044715f, x2, 1.0f);
 }
 
-__device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* p, float (&v)[32]) {
-  const uint4* q = reinterpret_cast<const uint4*>(p);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint4 w = q[i];
-    v[8 * i + 0] = bf16_lo(w.x);
-    v[8 * i + 1] = bf16_hi(w.x);
-    v[8 * i + 2] = bf16_lo(w.y);
-    v[8 * i + 3] = bf16_hi(w.y);
-    v[8 * i + 4] = bf16_lo(w.z);
-    v[8 * i + 5] = bf16_hi(w.z);
-    v[8 * i + 6] = bf16_lo(w.w);
-    v[8 * i + 7] = bf16_hi(w.w);
-  }
+// 8 bf16 values (16 bytes) <-> 8 floats.
+__device__ __forceinline__ void unpack_bf16x8(const uint4 w, float (&v)[8]) {
+  v[0] = bf16_lo(w.x);
+  v[1] = bf16_hi(w.x);
+  v[2] = bf16_lo(w.y);
+  v[3] = bf16_hi(w.y);
+  v[4] = bf16_lo(w.z);
+  v[5] = bf16_hi(w.z);
+  v[6] = bf16_lo(w.w);
+  v[7] = bf16_hi(w.w);
 }
 
-__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* p, const float (&v)[32]) {
-  uint4* q = reinterpret_cast<uint4*>(p);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    uint4 w;
-    w.x = pack_bf16x2(v[8 * i + 0], v[8 * i + 1]);
-    w.y = pack_bf16x2(v[8 * i + 2], v[8 * i + 3]);
-    w.z = pack_bf16x2(v[8 * i + 4], v[8 * i + 5]);
-    w.w = pack_bf16x2(v[8 * i + 6], v[8 * i + 7]);
-    q[i] = w;
-  }
+__device__ __forceinline__ uint4 pack_bf16x8(const float (&v)[8]) {
+  return make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                    pack_bf16x2(v[6], v[7]));
 }
 
-// Applies the epilogue to 32 consecutive columns [col0, col0 + 32) of `row`.
+// The fused epilogue of one warp's 32 x 32 block of the accumulator: rows
+// r0 + [0, 32), columns col0 + [0, 32).  tcgen05.ld leaves one row per lane
+// (v); the block goes through shared memory (`blk`, rows padded to 33
+// floats, so that both phases are free of bank conflicts) and comes back
+// with several lanes on one row, so that each 16-byte global access of the
+// warp touches 4 (fp32) or 8 (bf16) rows instead of 32.  Every global read
+// of the epilogue (residual, pre-activation, the output added to) is issued
+// before the first store, which could alias it.
 template <int EPI>
-__device__ __forceinline__ void epilogue32(float (&v)[32], int row, int col0, const GemmArgs& g) {
-  if constexpr (EPI == MC_EPI_STORE_F32) {
-    float4* o = reinterpret_cast<float4*>(static_cast<float*>(g.out) + (int64_t)row * g.ldc + col0);
+__device__ __forceinline__ void epilogue_block(const float (&v)[32], float* blk, int lane, int r0,
+                                               int col0, const GemmArgs& g) {
+  auto stage = [&] {
+#pragma unroll
+    for (int k = 0; k < 32; ++k) blk[lane * 33 + k] = v[k];
+    __syncwarp();
+  };
+  const bool cols_ok =
+      col0 < g.N && MC_DCHECK(col0 + 32 <= g.N && g.N <= g.ldc && r0 >= 0, g.status,
+                              kSiteGemmEpilogue);
+  if constexpr (EPI == MC_EPI_STORE_F32 || EPI == MC_EPI_BIAS_RESID_F32) {
+    // fp32: 8 lanes per row, 4 columns each; rows 4 i + lane / 8
+    stage();
+    const int sub = lane & 7;
+    constexpr bool kResid = EPI == MC_EPI_BIAS_RESID_F32;
+    const bool reads = kResid || g.accumulate;
+    float4 bias4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    if constexpr (kResid) {
+      const uint2 bw = *reinterpret_cast<const uint2*>(g.bias + col0 + 4 * sub);
+      bias4 = make_float4(bf16_lo(bw.x), bf16_hi(bw.x), bf16_lo(bw.y), bf16_hi(bw.y));
+    }
+    float4 x[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      float4 w = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-      if (g.accumulate) {
-        const float4 old = o[i];
-        w.x += old.x;
-        w.y += old.y;
-        w.z += old.z;
-        w.w += old.w;
+      const int grow = r0 + 4 * i + (lane >> 3);
+      x[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (reads && cols_ok && grow < g.M) {
+        const float* base = kResid ? static_cast<const float*>(g.aux) + (int64_t)grow * g.ldaux
+                                   : static_cast<const float*>(g.out) + (int64_t)grow * g.ldc;
+        x[i] = *reinterpret_cast<const float4*>(base + col0 + 4 * sub);
       }
-      o[i] = w;
     }
-  } else if constexpr (EPI == MC_EPI_STORE_BF16) {
-    store_bf16x32(static_cast<__nv_bfloat16*>(g.out) + (int64_t)row * g.ldc + col0, v);
-  } else if constexpr (EPI == MC_EPI_BIAS_BF16) {
-    float b[32];
-    load_bf16x32(g.bias + col0, b);
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] += b[i];
-    store_bf16x32(static_cast<__nv_bfloat16*>(g.out) + (int64_t)row * g.ldc + col0, v);
-  } else if constexpr (EPI == MC_EPI_BIAS_GELU) {
-    float b[32];
-    load_bf16x32(g.bias + col0, b);
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] += b[i];
-    store_bf16x32(static_cast<__nv_bfloat16*>(const_cast<void*>(g.aux)) + (int64_t)row * g.ldaux +
-                      col0,
-                  v);
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = gelu_tanh(v[i]);
-    store_bf16x32(static_cast<__nv_bfloat16*>(g.out) + (int64_t)row * g.ldc + col0, v);
-  } else if constexpr (EPI == MC_EPI_BIAS_RESID_F32) {
-    float b[32];
-    load_bf16x32(g.bias + col0, b);
-    const float4* r =
-        reinterpret_cast<const float4*>(static_cast<const float*>(g.aux) + (int64_t)row * g.ldaux + col0);
-    float4* o = reinterpret_cast<float4*>(static_cast<float*>(g.out) + (int64_t)row * g.ldc + col0);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const float4 rr = r[i];
-      o[i] = make_float4(v[4 * i] + b[4 * i] + rr.x, v[4 * i + 1] + b[4 * i + 1] + rr.y,
-                         v[4 * i + 2] + b[4 * i + 2] + rr.z, v[4 * i + 3] + b[4 * i + 3] + rr.w);
+      const int lr = 4 * i + (lane >> 3);
+      const int grow = r0 + lr;
+      const float* src = blk + lr * 33 + 4 * sub;
+      float4 w = make_float4(src[0], src[1], src[2], src[3]);
+      if (cols_ok && grow < g.M) {
+        if constexpr (kResid)  // (acc + bias) + residual
+          w = make_float4(w.x + bias4.x + x[i].x, w.y + bias4.y + x[i].y, w.z + bias4.z + x[i].z,
+                          w.w + bias4.w + x[i].w);
+        else if (g.accumulate)
+          w = make_float4(w.x + x[i].x, w.y + x[i].y, w.z + x[i].z, w.w + x[i].w);
+        *reinterpret_cast<float4*>(static_cast<float*>(g.out) + (int64_t)grow * g.ldc + col0 +
+                                   4 * sub) = w;
+      }
     }
-  } else if constexpr (EPI == MC_EPI_GELU_BWD) {
-    float hp[32];
-    load_bf16x32(static_cast<const __nv_bfloat16*>(g.aux) + (int64_t)row * g.ldaux + col0, hp);
+    __syncwarp();  // the block is read before the next chunk overwrites it
+  } else {
+    // bf16: 4 lanes per row, 8 columns each; rows 8 i + lane / 4
+    stage();
+    const int sub = lane & 3;
+    float b[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if constexpr (EPI == MC_EPI_BIAS_BF16 || EPI == MC_EPI_BIAS_GELU)
+      unpack_bf16x8(*reinterpret_cast<const uint4*>(g.bias + col0 + 8 * sub), b);
+    uint4 hp[4];  // GELU_BWD: the pre-activation
+    if constexpr (EPI == MC_EPI_GELU_BWD) {
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] *= gelu_tanh_grad(hp[i]);
-    store_bf16x32(static_cast<__nv_bfloat16*>(g.out) + (int64_t)row * g.ldc + col0, v);
+      for (int i = 0; i < 4; ++i) {
+        const int grow = r0 + 8 * i + (lane >> 2);
+        hp[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (cols_ok && grow < g.M)
+          hp[i] = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(g.aux) +
+                                                  (int64_t)grow * g.ldaux + col0 + 8 * sub);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int lr = 8 * i + (lane >> 2);
+      const int grow = r0 + lr;
+      float x[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) x[k] = blk[lr * 33 + 8 * sub + k];
+      if (!cols_ok || grow >= g.M) continue;
+      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(g.out) + (int64_t)grow * g.ldc + col0 + 8 * sub;
+      if constexpr (EPI == MC_EPI_BIAS_BF16 || EPI == MC_EPI_BIAS_GELU) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) x[k] += b[k];
+      }
+      if constexpr (EPI == MC_EPI_BIAS_GELU) {
+        // the pre-activation for the backward, then the activation
+        *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(const_cast<void*>(g.aux)) +
+                                  (int64_t)grow * g.ldaux + col0 + 8 * sub) = pack_bf16x8(x);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) x[k] = gelu_tanh(x[k]);
+      }
+      if constexpr (EPI == MC_EPI_GELU_BWD) {
+        float h[8];
+        unpack_bf16x8(hp[i], h);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) x[k] *= gelu_tanh_grad(h[k]);
+      }
+      *reinterpret_cast<uint4*>(out) = pack_bf16x8(x);
+    }
+    __syncwarp();  // the block is read before the next chunk overwrites it
   }
 }
 
@@ -207,7 +252,7 @@ template <bool A_MN, bool B_MN, int BN, int EPI, int MODE, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB, const GemmArgs g) {
-  using Cfg = GemmCfg<BN, MODE>;
+  using Cfg = GemmCfg<BN, MODE, EPI>;
   constexpr int S = Cfg::kStages;
   constexpr bool kDuoMode = MODE == kDuo;
   static_assert(!F8 || (!A_MN && !B_MN), "8-bit operands are K-major");
@@ -225,6 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* drain = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  float* epi_stage = reinterpret_cast<float*>(smem + S * Cfg::kStageBytes + Cfg::kBarrierBytes);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -438,7 +484,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       unit_coords(u, mb, nb);
       if (!mbar_wait_warp(&acc_full[acc], acc_phase, g.status, kSiteGemmEpilogue)) break;
       tc_fence_after();
-      const int row = mb * BM + quarter * 32 + lane;
+      const int r0 = mb * BM + quarter * 32;  // the warp's 32 rows
+      float* blk = epi_stage + (warp - 2) * (32 * 33);
       const uint32_t t_row = tmem_base + static_cast<uint32_t>(acc * BN) +
                              (static_cast<uint32_t>(quarter * 32) << 16);
 #pragma unroll 1
@@ -450,9 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] *= dq;
         }
-        if (row < g.M && col0 < g.N &&
-            MC_DCHECK(col0 + 32 <= g.N && g.N <= g.ldc && row >= 0, g.status, kSiteGemmEpilogue))
-          epilogue32<EPI>(v, row, col0, g);
+        epilogue_block<EPI>(v, blk, lane, r0, col0, g);
       }
       tc_fence_before();
       if constexpr (kDuoMode) {
@@ -520,7 +565,7 @@ bool make_tmap(CUtensorMap* map, const void* base, uint64_t inner, uint64_t oute
 template <bool A_MN, bool B_MN, int BN, int EPI, int MODE, bool F8 = false>
 int launch_variant(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& g,
                    cudaStream_t stream) {
-  using Cfg = GemmCfg<BN, MODE>;
+  using Cfg = GemmCfg<BN, MODE, EPI>;
   constexpr bool PAIR = MODE == kDuo;
   auto kern = gemm_tcgen05_kernel<A_MN, B_MN, BN, EPI, MODE, F8>;
   static PerDeviceInit init;
