@@ -90,6 +90,7 @@ struct WideRects {
   WideRect r[kCpMaxRects];
   float* out;
   float* lse2;
+  int head_major;  // the whole matrix: the grid order (attention_cta)
 };
 
 template <int D, bool PART>
@@ -131,10 +132,11 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     while (ri + 1 < rects.n && static_cast<int>(blockIdx.x) >= rects.cta_end[ri]) ++ri;
   const WideRect rect = rects.r[ri];
   const int cta0 = ri > 0 ? rects.cta_end[ri - 1] : 0;
+  int t_heavy, hh, bi;
+  attention_cta(!PART && rects.head_major, H, t_heavy, hh, bi);
   const int q_blk =
       PART ? rect.base / 128 + (rect.len / 128 - 1 - (static_cast<int>(blockIdx.x) - cta0))
-           : static_cast<int>(gridDim.x - 1 - blockIdx.x);
-  const int hh = blockIdx.y, bi = blockIdx.z;
+           : (s + 127) / 128 - 1 - t_heavy;
   const int q0 = q_blk * 128;
   // (the whole matrix: keys from 0, masked past s)
   const int k_lo = PART ? rect.key_lo : 0;
@@ -471,7 +473,8 @@ int launch_wide(const uint16_t* qkv, uint16_t* o, float* lse, int b, int s, int 
     return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   });
   if (attr != cudaSuccess) return MC_ERR_CUDA;
-  dim3 grid(PART ? rects.cta_end[rects.n - 1] : (s + 127) / 128, H, b);
+  const dim3 grid = PART ? dim3(rects.cta_end[rects.n - 1], H, b)
+                         : attention_grid(rects.head_major, (s + 127) / 128, H, b);
   launch_kernel(kern, grid, dim3(kWideThreads), C::kSmem, st, 1, tm, o, lse, s, H, status, rects);
   return cudaGetLastError() == cudaSuccess ? MC_OK : MC_ERR_CUDA;
 }
@@ -484,6 +487,7 @@ int launch_attention_forward_wide(const uint16_t* qkv, uint16_t* o, float* lse, 
   whole.n = 1;
   whole.cta_end[0] = (s + 127) / 128;
   whole.r[0] = {0, s, 0, INT_MAX, 0};
+  whole.head_major = attention_head_major((s + 127) / 128, H, b) ? 1 : 0;
   return d == 64 ? launch_wide<64, false>(qkv, o, lse, b, s, H, status, st, whole)
                  : launch_wide<128, false>(qkv, o, lse, b, s, H, status, st, whole);
 }

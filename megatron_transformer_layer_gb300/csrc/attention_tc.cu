@@ -41,6 +41,7 @@ struct AttnParts {
   int cta_end[kCpMaxRects];
   AttnPart r[kCpMaxRects];
   float* acc;
+  int head_major;  // the whole matrix: the grid order (attention_cta)
 };
 
 // ---------------------------------------------------------------- backward
@@ -115,15 +116,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int a = H * D;
-  const int hh = blockIdx.y, bi = blockIdx.z;
   const int nblk = (s + 127) / 128;
-  // this CTA's rectangle (the whole matrix: one) and key block
+  // this CTA's rectangle (the whole matrix: one) and key block (heaviest:
+  // the first of a head's)
+  int t_heavy, hh, bi;
+  attention_cta(!PART && parts.head_major, H, t_heavy, hh, bi);
   int ri = 0;
   if constexpr (PART)
     while (ri + 1 < parts.n && static_cast<int>(blockIdx.x) >= parts.cta_end[ri]) ++ri;
   const AttnPart part = parts.r[ri];
   const int cta0 = ri > 0 ? parts.cta_end[ri - 1] : 0;
-  const int kb = part.base / 128 + static_cast<int>(blockIdx.x) - cta0;
+  const int kb = PART ? part.base / 128 + static_cast<int>(blockIdx.x) - cta0 : t_heavy;
   const int r0 = kb * 128;
   // query blocks qb0 .. qb0 + count - 1 (fused: kb .. nblk - 1)
   const int qb0 = max(kb, part.blk_lo);
@@ -466,7 +469,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv,
                           const __grid_constant__ CUtensorMap tm_do, const float* __restrict__ lse,
                           const float* __restrict__ delta, uint16_t* __restrict__ dqkv, int s,
-                          int H, int* status) {
+                          int H, int* status, int head_major) {
   using C = DqCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -492,9 +495,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int a = H * D;
-  const int hh = blockIdx.y, bi = blockIdx.z;
   // heaviest first: query blocks 0 .. nblk - 1 against key blocks 0 .. qb
-  const int qb = static_cast<int>(gridDim.x - 1 - blockIdx.x);
+  int t_heavy, hh, bi;
+  attention_cta(head_major != 0, H, t_heavy, hh, bi);
+  const int qb = (s + 127) / 128 - 1 - t_heavy;
   const int q0 = qb * 128;
   const int count = qb + 1;  // key blocks 0 .. qb
 
@@ -704,9 +708,10 @@ int launch_bwd_dq_tc(const CUtensorMap& tq, const CUtensorMap& td, const float* 
     return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   });
   if (attr != cudaSuccess) return MC_ERR_CUDA;
-  dim3 grid((s + 127) / 128, H, b);
-  launch_kernel(kern, dim3(grid), dim3(kBwdThreads), C::kSmem, st, 1, tq, td, lse, delta, dqkv, s,
-                H, status);
+  const int nb = (s + 127) / 128;
+  const bool hm = attention_head_major(nb, H, b);
+  launch_kernel(kern, attention_grid(hm, nb, H, b), dim3(kBwdThreads), C::kSmem, st, 1, tq, td, lse,
+                delta, dqkv, s, H, status, hm ? 1 : 0);
   return cudaGetLastError() == cudaSuccess ? MC_OK : MC_ERR_CUDA;
 }
 
@@ -721,9 +726,10 @@ int launch_bwd_dkdv_tc(const CUtensorMap& tq, const CUtensorMap& td, const float
     return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   });
   if (attr != cudaSuccess) return MC_ERR_CUDA;
-  dim3 grid(PART ? parts.cta_end[parts.n - 1] : (s + 127) / 128, H, b);
-  launch_kernel(kern, dim3(grid), dim3(kBwdThreads), C::kSmem, st, 1, tq, td, lse, delta, dqkv, s,
-                H, status, parts, ds_tiles);
+  const dim3 grid = PART ? dim3(parts.cta_end[parts.n - 1], H, b)
+                         : attention_grid(parts.head_major, (s + 127) / 128, H, b);
+  launch_kernel(kern, grid, dim3(kBwdThreads), C::kSmem, st, 1, tq, td, lse, delta, dqkv, s, H,
+                status, parts, ds_tiles);
   return cudaGetLastError() == cudaSuccess ? MC_OK : MC_ERR_CUDA;
 }
 
@@ -773,6 +779,7 @@ struct DqRects {
   int item_end[kCpMaxRects];
   DqRect r[kCpMaxRects];
   float* acc;
+  int head_major;  // the whole matrix: every head's heaviest query block first
 };
 
 // Item r of CTA blockIdx.x (snake over the dispatch order): rectangle,
@@ -786,10 +793,17 @@ __device__ __forceinline__ bool dq_item(int r, const DqRects& rects, int H, int&
   while (ri + 1 < rects.n && k >= rects.item_end[ri]) ++ri;
   const int kr = static_cast<int>(k - (ri > 0 ? rects.item_end[ri - 1] : 0));
   const int nq = rects.r[ri].nq;
-  qr = nq - 1 - kr % nq;  // heaviest first within a head
-  const int rest = kr / nq;
-  hh = rest % H;
-  bi = rest / H;
+  int hb;
+  if (rects.head_major) {  // (the whole matrix: one rectangle)
+    const int n_hb = rects.item_end[0] / nq;
+    hb = kr % n_hb;
+    qr = nq - 1 - kr / n_hb;
+  } else {
+    qr = nq - 1 - kr % nq;  // heaviest first within a head
+    hb = kr / nq;
+  }
+  hh = hb % H;
+  bi = hb / H;
   return true;
 }
 
@@ -1011,6 +1025,7 @@ int launch_bwd_tc(const uint16_t* qkv, const float* lse, const uint16_t* dout, u
   whole.n = 1;
   whole.cta_end[0] = nb;
   whole.r[0] = {0, s, 0, 0x7fffffff, 0, 0};
+  whole.head_major = attention_head_major(nb, H, b) ? 1 : 0;
   int rc = launch_bwd_dkdv_tc<D, false>(tq, td, lse, delta, dqkv, b, s, H, status, st, whole,
                                         ds_tiles);
   if (rc != MC_OK) return rc;
@@ -1021,6 +1036,7 @@ int launch_bwd_tc(const uint16_t* qkv, const float* lse, const uint16_t* dout, u
     dq.n = 1;
     dq.item_end[0] = static_cast<int>(n_items);
     dq.r[0] = {0, nb, 0, nb, 0, 0};
+    dq.head_major = attention_head_major(nb, H, b) ? 1 : 0;
     return launch_bwd_dq_gemm<D, false>(tq, ds_tiles, dqkv, b, s, H, dq, status, st);
   }
   return launch_bwd_dq_tc<D>(tq, td, lse, delta, dqkv, b, s, H, status, st);

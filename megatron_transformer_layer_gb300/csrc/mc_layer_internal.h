@@ -77,6 +77,18 @@ constexpr int kColsumMaxSplits = 512;
 
 int num_sms();  // SM count of the current device (cached per device)
 
+// Whole-matrix attention grids of at most four waves (tiles x heads x batch
+// CTAs against the SMs) take every head's heaviest tiles first
+// (attention_cta in ptx.cuh); the grid for either order.
+inline bool attention_head_major(int64_t tiles, int64_t H, int64_t b) {
+  return tiles * H * b <= 4ll * num_sms();
+}
+inline dim3 attention_grid(bool head_major, int tiles, int H, int b) {
+  return head_major ? dim3(static_cast<unsigned>(H * b), static_cast<unsigned>(tiles), 1u)
+                    : dim3(static_cast<unsigned>(tiles), static_cast<unsigned>(H),
+                           static_cast<unsigned>(b));
+}
+
 #ifdef __CUDACC__
 // Identity of the current device's context: (device ordinal, context id).
 // The context id changes when the context is destroyed and re-created (e.g.

@@ -518,6 +518,25 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// The (tile, head, batch) of a whole-matrix attention CTA, tile t counted
+// from the heaviest.  The grid is (tiles, H, b): each head's tiles heaviest
+// first, head after head, so that the CTAs running together share one or
+// two heads' K and V in L2; or, with `head_major`, (H b, tiles): every
+// head's heaviest tile first, for grids of a few waves, whose time is set by
+// when their heaviest CTAs start.
+__device__ __forceinline__ void attention_cta(bool head_major, int H, int& t, int& hh, int& bi) {
+  if (head_major) {
+    const int hb = static_cast<int>(blockIdx.x);
+    hh = hb % H;
+    bi = hb / H;
+    t = static_cast<int>(blockIdx.y);
+  } else {
+    t = static_cast<int>(blockIdx.x);
+    hh = static_cast<int>(blockIdx.y);
+    bi = static_cast<int>(blockIdx.z);
+  }
+}
+
 // 32 values of one row added to a running fp32 sum (the context-parallel
 // rectangles): x = c_new v + (merge ? c_old run : 0), written back to `run`,
 // or, for the row's last share (`final`), as bf16 to `out` instead.  `run`
