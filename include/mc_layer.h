@@ -414,7 +414,8 @@ int mc_gemm_fp8(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_t lda, 
  * rounding of the merges and sums (to the bit for a chunk with one pair:
  * O, lse and dQ of chunk 0, dK and dV of the last chunk).
  *
- * Requirements: cp_parts >= 1, seq_len a multiple of 256 * cp_parts,
+ * Requirements: 1 <= cp_parts <= 256 (MC_ERR_UNSUPPORTED above), seq_len a
+ * multiple of 256 * cp_parts,
  * head_dim 64 or 128; the caller-owned workspace of
  * mc_attention_cp_workspace_bytes bytes (16-byte aligned) holds the running
  * sums (micro_batch x seq_len x 3a floats) and the bf16 dS^T tiles of one
@@ -430,6 +431,18 @@ int mc_gemm_fp8(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_t lda, 
  * Host only; every pair j <= i of the 2 cp_parts chunks occurs exactly once
  * over all ranks and steps. */
 int mc_cp_schedule(int32_t cp_parts, int32_t rank, int32_t step, int32_t* pairs);
+
+/* The launch plan of mc_attention_forward_cp / _backward_cp.  Host only.
+ * Every chunk pair of the schedule in launch order: sub-step k of ring
+ * step t is one launch of every rank's k-th pair of that step.  Each pair
+ * writes five entries: the index of its launch, its query chunk i, its key
+ * chunk j, and the accumulation modes of i and j (bit 0: add to a running
+ * sum left by an earlier pair of that chunk; bit 1: the chunk's last pair,
+ * which writes the result).  No launch holds two pairs of one query chunk
+ * or of one key chunk.  Returns the number of pairs, cp_parts (2 cp_parts
+ * + 1); MC_ERR_ARGUMENT for cp_parts outside [1, 256] or a null `entries`;
+ * MC_ERR_WORKSPACE when max_pairs is smaller. */
+int mc_cp_launch_plan(int32_t cp_parts, int32_t* entries, int32_t max_pairs);
 
 size_t mc_attention_cp_workspace_bytes(int32_t micro_batch, int32_t seq_len, int32_t heads,
                                        int32_t head_dim, int32_t cp_parts);

@@ -108,6 +108,7 @@ _SIGNATURES = {
     "mc_gemm_fp8": (_INT, [_I64, _I64, _I64, _P, _I64, _I32, _P, _I64, _I32, _P, _P, _P, _I64,
                            _I32, _P, _P, _I64, _I32, _I32, _P, _P]),
     "mc_cp_schedule": (_INT, [_I32, _I32, _I32, ctypes.POINTER(_I32)]),
+    "mc_cp_launch_plan": (_INT, [_I32, ctypes.POINTER(_I32), _I32]),
     "mc_attention_cp_workspace_bytes": (_SZ, [_I32, _I32, _I32, _I32, _I32]),
     "mc_attention_forward_cp": (_INT, [_P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P, _SZ, _P, _P]),
     "mc_attention_backward_cp": (_INT, [_P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P,
@@ -265,6 +266,18 @@ def mc_cp_schedule(cp_parts, rank, step):
     if n < 0:
         raise ValueError(mc_strerror(n))
     return [(buf[2 * k], buf[2 * k + 1]) for k in range(n)]
+
+
+def mc_cp_launch_plan(cp_parts):
+    """The context-parallel launch plan (host only): one tuple (launch,
+    query chunk, key chunk, mode of the query chunk, mode of the key chunk)
+    per chunk pair, in launch order; raises on an invalid argument."""
+    n_pairs = cp_parts * (2 * cp_parts + 1) if cp_parts > 0 else 1
+    buf = (_I32 * (5 * n_pairs))()
+    n = lib().mc_cp_launch_plan(cp_parts, buf, n_pairs)
+    if n < 0:
+        raise ValueError(mc_strerror(n))
+    return [tuple(buf[5 * k + e] for e in range(5)) for k in range(n)]
 
 
 def mc_attention_cp_workspace_bytes(micro_batch, seq_len, heads, head_dim, cp_parts) -> int:

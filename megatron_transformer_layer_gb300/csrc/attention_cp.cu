@@ -26,8 +26,6 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
-#include <vector>
-
 #include "mc_layer_internal.h"
 
 namespace mc {
@@ -35,8 +33,11 @@ namespace {
 
 bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+constexpr int kCpMaxParts = 256;  // the launch plan's fixed arrays
+
 int check_cp(int b, int s, int H, int d, int cp) {
   if (b < 1 || s < 1 || H < 1 || cp < 1) return MC_ERR_SHAPE;
+  if (cp > kCpMaxParts) return MC_ERR_UNSUPPORTED;
   if (d != 64 && d != 128) return MC_ERR_UNSUPPORTED;
   if (H > 65535 || b > 65535) return MC_ERR_UNSUPPORTED;
   if (s % (256 * cp) != 0) return MC_ERR_SHAPE;  // chunks of a whole number of 128-token tiles
@@ -45,43 +46,51 @@ int check_cp(int b, int s, int H, int d, int cp) {
 
 // The launches in order: ring step t, sub-step k = the k-th pair of every
 // rank in step t (ranks in order, at most kCpMaxRects to a launch).  Each
-// pair is the rectangle of its query chunk i and key chunk j with the
-// accumulation modes of both: chunk i has i + 1 pairs, key chunk j has
-// C - j.  A rank's pairs of a step keep their order in the sub-steps, and a
-// chunk's pairs all come from one rank within a step, so every chunk sees
-// its pairs in schedule order.
-std::vector<std::vector<CpRect>> cp_launches(int cp, int c) {
+// pair is the rectangle of its query chunk i and key chunk j (chunks of c
+// rows) with the accumulation modes of both: chunk i has i + 1 pairs, key
+// chunk j has C - j.  A rank's pairs of a step keep their order in the
+// sub-steps, and a chunk's pairs all come from one rank within a step, so
+// every chunk sees its pairs in schedule order.  Calls f(rects, n) for each
+// launch and stops at the first code other than MC_OK that f returns; no
+// heap memory (cp <= kCpMaxParts).
+template <typename F>
+int for_each_cp_launch(int cp, int c, F&& f) {
   const int C = 2 * cp;
-  std::vector<int> seen_q(C, 0), seen_k(C, 0), np(cp);
-  std::vector<int32_t> pairs(static_cast<size_t>(cp) * 8);
-  std::vector<std::vector<CpRect>> out;
+  int seen_q[2 * kCpMaxParts] = {}, seen_k[2 * kCpMaxParts] = {};
+  int32_t pairs[kCpMaxParts][8];
+  int np[kCpMaxParts];
   for (int t = 0; t < cp; ++t) {
     int kmax = 0;
     for (int r = 0; r < cp; ++r) {
-      np[r] = mc_cp_schedule(cp, r, t, &pairs[static_cast<size_t>(r) * 8]);
+      np[r] = mc_cp_schedule(cp, r, t, pairs[r]);
+      if (np[r] < 0) return np[r];
       kmax = np[r] > kmax ? np[r] : kmax;
     }
     for (int k = 0; k < kmax; ++k) {
-      std::vector<CpRect> launch;
+      CpRect launch[kCpMaxRects];
+      int n = 0;
       for (int r = 0; r < cp; ++r) {
         if (k >= np[r]) continue;
-        const int i = pairs[static_cast<size_t>(r) * 8 + 2 * k];
-        const int j = pairs[static_cast<size_t>(r) * 8 + 2 * k + 1];
+        const int i = pairs[r][2 * k], j = pairs[r][2 * k + 1];
         CpRect p = {i * c, c, j * c, c, 0, 0};
         p.mode_q = (seen_q[i] > 0 ? kCpAccMerge : 0) | (seen_q[i] == i ? kCpAccFinal : 0);
         p.mode_k = (seen_k[j] > 0 ? kCpAccMerge : 0) | (seen_k[j] == C - 1 - j ? kCpAccFinal : 0);
         ++seen_q[i];
         ++seen_k[j];
-        launch.push_back(p);
-        if (static_cast<int>(launch.size()) == kCpMaxRects) {
-          out.push_back(launch);
-          launch.clear();
+        launch[n++] = p;
+        if (n == kCpMaxRects) {
+          const int rc = f(launch, n);
+          if (rc != MC_OK) return rc;
+          n = 0;
         }
       }
-      if (!launch.empty()) out.push_back(launch);
+      if (n > 0) {
+        const int rc = f(launch, n);
+        if (rc != MC_OK) return rc;
+      }
     }
   }
-  return out;
+  return MC_OK;
 }
 
 // Workspace: the running sums, [b, s, 3a] fp32 (forward: O at [0, a) per
@@ -91,10 +100,11 @@ std::vector<std::vector<CpRect>> cp_launches(int cp, int c) {
 size_t cp_workspace_bytes(int b, int s, int H, int d, int cp) {
   const int64_t a = static_cast<int64_t>(H) * d;
   int64_t tiles = 0;
-  for (const auto& l : cp_launches(cp, s / (2 * cp))) {
-    const int64_t t = attention_cp_tile_bytes(l.data(), static_cast<int>(l.size()), b, H);
+  for_each_cp_launch(cp, s / (2 * cp), [&](const CpRect* rects, int n) {
+    const int64_t t = attention_cp_tile_bytes(rects, n, b, H);
     tiles = t > tiles ? t : tiles;
-  }
+    return MC_OK;
+  });
   return static_cast<size_t>(static_cast<int64_t>(b) * s * 3 * a * 4 + tiles);
 }
 
@@ -144,6 +154,26 @@ int mc_cp_schedule(int32_t cp_parts, int32_t rank, int32_t step, int32_t* pairs)
   return n;
 }
 
+int mc_cp_launch_plan(int32_t cp_parts, int32_t* entries, int32_t max_pairs) {
+  if (cp_parts < 1 || cp_parts > kCpMaxParts || !entries) return MC_ERR_ARGUMENT;
+  const int64_t pairs = static_cast<int64_t>(cp_parts) * (2 * cp_parts + 1);
+  if (max_pairs < pairs) return MC_ERR_WORKSPACE;
+  int launch = 0, k = 0;
+  const int rc = for_each_cp_launch(cp_parts, 1, [&](const CpRect* rects, int n) {
+    for (int i = 0; i < n; ++i, ++k) {
+      int32_t* e = entries + 5 * static_cast<int64_t>(k);
+      e[0] = launch;
+      e[1] = rects[i].q_base;  // chunks of one row: the chunk index
+      e[2] = rects[i].k_base;
+      e[3] = rects[i].mode_q;
+      e[4] = rects[i].mode_k;
+    }
+    ++launch;
+    return MC_OK;
+  });
+  return rc != MC_OK ? rc : k;
+}
+
 size_t mc_attention_cp_workspace_bytes(int32_t micro_batch, int32_t seq_len, int32_t heads,
                                        int32_t head_dim, int32_t cp_parts) {
   if (check_cp(micro_batch, seq_len, heads, head_dim, cp_parts) != MC_OK) return 0;
@@ -164,12 +194,10 @@ int mc_attention_forward_cp(const uint16_t* qkv, uint16_t* o, float* lse, int32_
   const int64_t a = static_cast<int64_t>(H) * d;
   float* acc_o = static_cast<float*>(workspace);
   float* acc_lse2 = acc_o + static_cast<int64_t>(b) * s * a;
-  for (const auto& l : cp_launches(cp, c)) {
-    rc = launch_attention_forward_parts(qkv, o, lse, b, s, H, d, l.data(), static_cast<int>(l.size()),
-                                        acc_o, acc_lse2, status, st);
-    if (rc != MC_OK) return rc;
-  }
-  return MC_OK;
+  return for_each_cp_launch(cp, c, [&](const CpRect* rects, int n) {
+    return launch_attention_forward_parts(qkv, o, lse, b, s, H, d, rects, n, acc_o, acc_lse2,
+                                          status, st);
+  });
 }
 
 int mc_attention_backward_cp(const uint16_t* qkv, const uint16_t* o, const float* lse,
@@ -192,17 +220,14 @@ int mc_attention_backward_cp(const uint16_t* qkv, const uint16_t* o, const float
   uint8_t* tiles = reinterpret_cast<uint8_t*>(acc_dkv + static_cast<int64_t>(b) * s * 2 * a);
   rc = launch_attention_delta(o, dout, delta, b, s, H, d, st);
   if (rc != MC_OK) return rc;
-  for (const auto& l : cp_launches(cp, c)) {
-    const int n = static_cast<int>(l.size());
+  return for_each_cp_launch(cp, c, [&](const CpRect* rects, int n) {
     // key rows of chunk j against the query blocks of chunk i: dK, dV and dS^T
-    rc = launch_attention_dkdv_parts(qkv, lse, dout, delta, dqkv, b, s, H, d, l.data(), n, acc_dkv,
-                                     tiles, status, st);
-    if (rc != MC_OK) return rc;
+    const int r = launch_attention_dkdv_parts(qkv, lse, dout, delta, dqkv, b, s, H, d, rects, n,
+                                              acc_dkv, tiles, status, st);
+    if (r != MC_OK) return r;
     // dQ of chunk i from those tiles and K of chunk j
-    rc = launch_attention_dq_parts(qkv, tiles, dqkv, b, s, H, d, l.data(), n, acc_dq, status, st);
-    if (rc != MC_OK) return rc;
-  }
-  return MC_OK;
+    return launch_attention_dq_parts(qkv, tiles, dqkv, b, s, H, d, rects, n, acc_dq, status, st);
+  });
 }
 
 }  // extern "C"

@@ -123,3 +123,57 @@ def test_chunk_pair_partials_merge_to_causal_attention(cp):
         lse[i * c:(i + 1) * c] = l
     np.testing.assert_allclose(o, o_ref, rtol=1e-12, atol=1e-12)
     np.testing.assert_allclose(lse, lse_ref, rtol=1e-12, atol=1e-12)
+
+
+MERGE, FINAL = 1, 2
+
+
+@pytest.mark.parametrize("cp", [1, 2, 3, 4, 8, 17, 40])
+def test_launch_plan_covers_the_schedule_without_conflicts(cp):
+    """The plan the CP entry points launch: every pair j <= i exactly once;
+    no launch holds two pairs of one query chunk or of one key chunk (each
+    would touch a running sum twice) nor more than 16 pairs; each rank's
+    pairs in the order of its ring steps."""
+    plan = L.mc_cp_launch_plan(cp)
+    C = 2 * cp
+    assert sorted((i, j) for _, i, j, _, _ in plan) == [(i, j) for i in range(C) for j in range(i + 1)]
+    launches = [entry[0] for entry in plan]
+    assert launches == sorted(launches) and launches[0] == 0
+    assert sorted(set(launches)) == list(range(launches[-1] + 1))
+    by_launch = {}
+    for l, i, j, _, _ in plan:
+        by_launch.setdefault(l, []).append((i, j))
+    for pairs in by_launch.values():
+        qs, ks = [i for i, _ in pairs], [j for _, j in pairs]
+        assert len(set(qs)) == len(qs) and len(set(ks)) == len(ks) and len(pairs) <= 16
+    for r in range(cp):
+        mine = [(i, j) for _, i, j, _, _ in plan if i in (r, C - 1 - r)]
+        assert mine == [p for t in range(cp) for p in L.mc_cp_schedule(cp, r, t)]
+
+
+@pytest.mark.parametrize("cp", [1, 2, 3, 4, 8, 17])
+def test_launch_plan_accumulation_modes(cp):
+    """A chunk's first pair writes its running sum, the later ones add to
+    it, its last writes the result: query chunk i has i + 1 pairs, key chunk
+    j has 2 cp - j."""
+    plan = L.mc_cp_launch_plan(cp)
+    C = 2 * cp
+    for chunk in range(C):
+        for pos, mpos, n in ((1, 3, chunk + 1), (2, 4, C - chunk)):
+            modes = [e[mpos] for e in plan if e[pos] == chunk]
+            assert len(modes) == n
+            want = [FINAL] if n == 1 else [0] + [MERGE] * (n - 2) + [MERGE | FINAL]
+            assert modes == want
+
+
+def test_launch_plan_limits():
+    assert len(L.mc_cp_launch_plan(256)) == 256 * 513
+    for bad in (0, 257, -1):
+        with pytest.raises(ValueError):
+            L.mc_cp_launch_plan(bad)
+    buf = (L.ctypes.c_int32 * 50)()
+    assert L.lib().mc_cp_launch_plan(2, buf, 9) == L.MC_ERR_WORKSPACE
+    assert L.lib().mc_cp_launch_plan(2, None, 10) == L.MC_ERR_ARGUMENT
+    assert L.lib().mc_cp_launch_plan(2, buf, 10) == 10
+    # 257 parts is beyond the plan's fixed arrays: the entry points refuse it
+    assert L.mc_attention_cp_workspace_bytes(1, 256 * 257, 1, 128, 257) == 0
