@@ -177,3 +177,59 @@ def test_launch_plan_limits():
     assert L.lib().mc_cp_launch_plan(2, buf, 10) == 10
     # 257 parts is beyond the plan's fixed arrays: the entry points refuse it
     assert L.mc_attention_cp_workspace_bytes(1, 256 * 257, 1, 128, 257) == 0
+
+
+@pytest.mark.parametrize("cp", [1, 2, 3])
+def test_running_sums_in_launch_order_give_causal_attention(cp):
+    """What the context-parallel kernels compute, walked in the plan's launch
+    order with its modes: each pair's O and log-sum-exp (log2 units) merged
+    into its query chunk's running ones as the forward epilogue does, and
+    each pair's dQ, dK, dV (from the merged LSE and delta) added to running
+    sums, a chunk's last pair writing the result.  fp64: equal to the
+    oracle's causal attention forward and backward to 1e-12."""
+    rng = np.random.default_rng(4)
+    C, c, d = 2 * cp, 8, 16
+    s = C * c
+    q, k, v, do = (rng.standard_normal((s, d)) * 1.5 for _ in range(4))
+    o_ref, lse_ref = O.causal_attention_forward(q, k, v)
+    dq_ref, dk_ref, dv_ref = O.causal_attention_backward(q, k, v, o_ref, lse_ref, do)
+    plan = L.mc_cp_launch_plan(cp)
+    rows = lambda i: slice(i * c, (i + 1) * c)  # noqa: E731
+    # forward
+    run_o, run_l2, o, lse = {}, {}, np.full_like(o_ref, np.nan), np.full_like(lse_ref, np.nan)
+    for _, i, j, mq, _ in plan:
+        o_p, lse_p = _partial(q[rows(i)], k[rows(j)], v[rows(j)], i * c, j * c, i == j)
+        l2_p = lse_p / np.log(2.0)
+        if mq & MERGE:
+            mx = np.maximum(run_l2[i], l2_p)
+            l2 = mx + np.log2(np.exp2(run_l2[i] - mx) + np.exp2(l2_p - mx))
+            o_m = np.exp2(run_l2[i] - l2)[:, None] * run_o[i] + np.exp2(l2_p - l2)[:, None] * o_p
+        else:
+            l2, o_m = l2_p, o_p
+        if mq & FINAL:
+            o[rows(i)], lse[rows(i)] = o_m, l2 * np.log(2.0)
+        else:
+            run_o[i], run_l2[i] = o_m, l2
+    np.testing.assert_allclose(o, o_ref, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(lse, lse_ref, rtol=1e-12, atol=1e-12)
+    # backward: every pair from the merged LSE and delta = rowsum(dO * O)
+    delta = (do * o).sum(axis=1)
+    out = {n: np.full_like(q, np.nan) for n in ("dq", "dk", "dv")}
+    run = {}
+    for _, i, j, mq, mk in plan:
+        qi, kj, vj, doi = q[rows(i)], k[rows(j)], v[rows(j)], do[rows(i)]
+        sc = qi @ kj.T / np.sqrt(d)
+        if i == j:
+            sc = np.where(np.tril(np.ones((c, c), bool)), sc, -np.inf)
+        p = np.exp(sc - lse[rows(i)][:, None])
+        ds = p * (doi @ vj.T - delta[rows(i)][:, None])
+        shares = (("dq", i, mq, ds @ kj / np.sqrt(d)), ("dk", j, mk, ds.T @ qi / np.sqrt(d)),
+                  ("dv", j, mk, p.T @ doi))
+        for name, chunk, mode, val in shares:
+            acc = run[(name, chunk)] + val if mode & MERGE else val
+            if mode & FINAL:
+                out[name][rows(chunk)] = acc
+            else:
+                run[(name, chunk)] = acc
+    for name, ref in (("dq", dq_ref), ("dk", dk_ref), ("dv", dv_ref)):
+        np.testing.assert_allclose(out[name], ref, rtol=1e-12, atol=1e-12, err_msg=name)
